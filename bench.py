@@ -1,0 +1,433 @@
+#!/usr/bin/env python3
+"""Throughput of the Llama decoder block forward on GB300, one JSON line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-decode]
+
+Headline workload: one Llama-3-8B-shaped block prefill, B=1, S=8192 (bf16, fp32 accumulation).
+A step is one llama_block_forward call over the 8192 tokens (RMSNorm, fused QKV+RoPE+KV write,
+causal GQA attention, O projection + residual, RMSNorm, gate/up + SiLU*mul, down + residual).
+`decode` reports the 32-layer batch-64 decode step against 8192 cached positions
+(llama_stack_decode_step, replayed as a CUDA graph).  Under torchrun every rank runs its own
+replica (the block has no exchange step); value = all ranks' tokens / max rank time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "block-forward tokens/s (prefill & decode) at 1 GB300; % of TC/HBM roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return p, "measured"
+    except Exception:
+        return FALLBACK_PEAKS, "fallback"
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+    def __init__(self, device: int):
+        import torch
+        self.proc = None
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200"]
+        try:
+            uuid = str(torch.cuda.get_device_properties(device).uuid)
+            cmd.insert(1, f"--id=GPU-{uuid}")
+        except Exception:
+            pass
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        sm, smax, reasons = [], [], set()
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(self.NAMES, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        hi = [s for s in sm if s >= 0.5 * max(sm)]   # samples under load
+        return {"sm_mhz": statistics.median(hi), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- helpers
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    import torch
+    torch.cuda.synchronize()
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+
+
+def max_over_ranks(world, v: float) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def prefill_flops(wl):
+    """Algorithmic FLOPs of one block forward: 2mnp for the seven projections, causal attention
+    (QK^T and PV over the visible keys only: 4 * n_q * hd * S(S+1)/2 per sequence)."""
+    T = wl.B * wl.S
+    hq, hkv = wl.n_q * wl.head_dim, wl.n_kv * wl.head_dim
+    return {
+        "gemm_tc_qkv": 2.0 * T * wl.d_model * (hq + 2 * hkv),
+        "gemm_tc_resid": 2.0 * T * (hq * wl.d_model + wl.d_ff * wl.d_model),
+        "gemm_tc_swiglu": 2.0 * T * wl.d_model * 2 * wl.d_ff,
+        "attn": 4.0 * wl.n_q * wl.head_dim * wl.B * wl.S * (wl.S + 1) / 2,
+    }
+
+
+def decode_bytes(wl, cap_unused=None):
+    """Algorithmic HBM bytes of one decode step (bf16): every cached K/V read once, every weight
+    read once, the new K/V written, inputs read and logits written."""
+    L, B, t = wl.n_layers, wl.B, wl.t_cache
+    row = wl.n_kv * wl.head_dim
+    kv_read = L * B * (t + 1) * row * 2 * 2
+    hq = wl.n_q * wl.head_dim
+    layer_w = (wl.d_model * (hq + 2 * row) + hq * wl.d_model + 3 * wl.d_model * wl.d_ff + 2 * wl.d_model) * 2
+    return {
+        "kv_read": kv_read,
+        "weights": L * layer_w,
+        "lm_head": wl.vocab * wl.d_model * 2 + wl.d_model * 2,
+        "kv_append": L * B * row * 2 * 2,
+        "logits": B * wl.vocab * 4,
+        "input": B * wl.d_model * 2,
+    }
+
+
+# ----------------------------------------------------------------------------- our arm
+def bench_prefill(args, world, rank):
+    import torch
+
+    import llama_decoder_block_fwd_gb300 as L
+    from synth import configs as C
+    from synth import workloads as W
+
+    wl = C.LLAMA3_8B_PREFILL
+    T = wl.B * wl.S
+    w = W.device_layer(wl)
+    x = W.device_x(wl).reshape(T, wl.d_model)
+    y = torch.empty_like(x)
+    ws = torch.empty(L.llama_workspace_bytes(L.OP_BLOCK_FORWARD, wl.dims, wl.dtype), dtype=torch.uint8,
+                     device="cuda")
+    bw = L.block_weights(w)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        L.llama_block_forward(wl.dims, wl.dtype, bw, x, y, 0, None, None, 0, ws, stream)
+
+    for _ in range(args.warmup):
+        step()
+    barrier(world)
+    if L.llama_get_device_status() != 0:
+        raise RuntimeError("device status word set during warm-up")
+    clocks = ClockSampler(torch.cuda.current_device())
+    L.llama_profile_read()            # clear
+    L.llama_profile_enable(True)
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    barrier(world)
+    L.llama_profile_enable(False)
+    clk = clocks.stop()
+    ms_total = max_over_ranks(world, e0.elapsed_time(e1))
+    prof = L.llama_profile_read()
+    if L.llama_get_device_status() != 0:
+        raise RuntimeError("device status word set during the timed region")
+
+    # end to end: pinned host x -> device, block, device y -> pinned host, every step
+    xh = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
+    xh.copy_(x)
+    yh = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+    xd = torch.empty_like(x)
+
+    def e2e_step():
+        xd.copy_(xh, non_blocking=True)
+        L.llama_block_forward(wl.dims, wl.dtype, bw, xd, y, 0, None, None, 0, ws, stream)
+        yh.copy_(y, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    barrier(world)
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    f1.record(stream)
+    barrier(world)
+    e2e_ms = max_over_ranks(world, f0.elapsed_time(f1))
+
+    pk, pk_src = peaks()
+    flops = prefill_flops(wl)
+    step_flops = sum(flops.values())
+    kernels = {}
+    launches = 0
+    for name, (n, ms) in prof.items():
+        kernels[name] = {"launches": n, "ms_per_step": ms / args.steps, "share": ms / max(sum(v[1] for v in prof.values()), 1e-9)}
+        launches += n
+    dom = max(prof.items(), key=lambda kv: kv[1][1])[0] if prof else None
+    dom_key = "attn" if dom and dom.startswith("attn") else dom
+    dom_flops = flops.get(dom_key, 0.0)
+    dom_ms = prof[dom][1] if dom else 0.0
+    timed_s = ms_total / 1e3
+    peak_tf = pk["bf16_tflops_sustained"] if timed_s > 1.0 else pk["bf16_tflops"]
+    achieved = dom_flops * args.steps / (dom_ms / 1e3) / 1e12 if dom_ms > 0 else 0.0
+    ms_step = ms_total / args.steps
+    out = {
+        "value": world * T / (ms_step / 1e3),
+        "ms_per_step": ms_step,
+        "clocks": clk,
+        "e2e": {"value": world * T / (e2e_ms / args.steps / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": x.numel() * x.element_size(),
+                "d2h_bytes_per_step": y.numel() * y.element_size()},
+        "gpu_launches": launches,
+        "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": achieved / peak_tf, "traffic": None,
+                     "peak_source": f"{pk_src} bf16 {'sustained' if timed_s > 1.0 else 'burst'}"},
+        "block_tc_frac": step_flops / (ms_step / 1e3) / 1e12 / peak_tf,
+        "block_tflops": step_flops / (ms_step / 1e3) / 1e12,
+        "kernels": kernels,
+        "config": {"workload": wl.name, "B": wl.B, "S": wl.S, "d_model": wl.d_model, "n_q": wl.n_q,
+                   "n_kv": wl.n_kv, "head_dim": wl.head_dim, "d_ff": wl.d_ff, "theta_base": wl.theta_base,
+                   "eps": wl.eps, "global_batch": world * wl.B, "seq_len": wl.S, "parallelism": f"replicas{world}",
+                   "l2": "inputs larger than L2 (436 MB of weights + 64 MB activations per step)",
+                   "flops_per_step": step_flops},
+    }
+    del w, x, y, ws, xh, yh, xd
+    torch.cuda.empty_cache()
+    return out
+
+
+def bench_decode(args, world, rank):
+    import torch
+
+    import llama_decoder_block_fwd_gb300 as L
+    from synth import configs as C
+    from synth import workloads as W
+
+    wl = C.LLAMA3_8B_DECODE
+    cap = wl.t_cache + 1
+    tensors = []
+    layers = []
+    for l in range(wl.n_layers):
+        t = W.device_layer(wl, l)
+        tensors.append(t)
+        layers.append(L.block_weights(t))
+    kc, vc = W.device_caches(wl, cap)
+    final_g, w_lm = W.device_final(wl)
+    x = W.device_x_emb(wl)
+    logits = torch.empty((wl.B, wl.vocab), dtype=torch.float32, device="cuda")
+    ws = torch.empty(L.llama_workspace_bytes(L.OP_STACK_DECODE_STEP, wl.dims, wl.dtype, wl.n_layers, wl.vocab, cap),
+                     dtype=torch.uint8, device="cuda")
+
+    def step(stream=None):
+        L.llama_stack_decode_step(wl.dims, wl.dtype, layers, final_g, w_lm, wl.vocab, x, kc, vc, cap, wl.t_cache,
+                                  logits, ws, stream)
+
+    # eager pass with per-launch events (per-kernel durations), then graph replay for the step time
+    step()
+    barrier(world)
+    L.llama_profile_read()
+    L.llama_profile_enable(True)
+    nprof = max(2, min(args.steps, 5))
+    for _ in range(nprof):
+        step()
+    L.llama_profile_enable(False)
+    prof = L.llama_profile_read()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for _ in range(args.warmup):
+        g.replay()
+    barrier(world)
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        g.replay()
+    e1.record(stream)
+    barrier(world)
+    if L.llama_get_device_status() != 0:
+        raise RuntimeError("device status word set during decode")
+    ms = max_over_ranks(world, e0.elapsed_time(e1)) / args.steps
+    pk, pk_src = peaks()
+    nb = decode_bytes(wl)
+    step_bytes = sum(nb.values())
+    kernels = {k: {"launches": n // nprof, "ms_per_step": t / nprof} for k, (n, t) in prof.items()}
+    attn = [k for k in prof if k.startswith("attn")]
+    dom = max(prof.items(), key=lambda kv: kv[1][1])[0]
+    out = {
+        "workload": wl.name, "value": world * wl.B / (ms / 1e3), "unit": "tokens/s", "ms_per_step": ms,
+        "bytes_per_step": step_bytes,
+        "hbm_frac_step": step_bytes / (ms / 1e3) / 1e9 / pk["hbm_gbs"],
+        "gpu_launches_per_step": sum(n for n, _ in prof.values()) // nprof,
+        "kernels": kernels, "dominant_kernel": dom,
+        "graph": "CUDA graph replay of one llama_stack_decode_step",
+        "l2": "inputs larger than L2 (69 GB KV cache + 15 GB weights)",
+    }
+    if attn:
+        a = attn[0]
+        n, t = prof[a]
+        per_launch_bytes = nb["kv_read"] / wl.n_layers
+        achieved = per_launch_bytes / (t / n / 1e3) / 1e9
+        out["roofline"] = {"bound": "hbm", "kernel": a, "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                           "frac": achieved / pk["hbm_gbs"], "traffic": None, "peak_source": f"{pk_src} hbm"}
+    del tensors, layers, kc, vc, final_g, w_lm, x, logits, ws, g
+    torch.cuda.empty_cache()
+    return out
+
+
+# ----------------------------------------------------------------------------- oracle legs
+def oracle_prefill_sample(S_sample: int):
+    """Time the fp64 oracle on one sequence of S_sample tokens of the 8B block (weights drawn
+    before the clock starts).  Returns (tokens/s, seconds, threads)."""
+    import numpy as np
+
+    import oracle as O
+    from synth import configs as C
+    from synth import workloads as W
+
+    wl = C.LLAMA3_8B_PREFILL
+    hw = O.BlockWeights(**W.host_layer(wl))
+    x = W.host_x(wl, 0)[:S_sample][None]
+    d = O.Dims(1, S_sample, wl.d_model, wl.n_q, wl.n_kv, wl.head_dim, wl.d_ff, wl.theta_base, wl.eps)
+    t0 = time.perf_counter()
+    O.block_forward(x, hw, d)
+    dt = time.perf_counter() - t0
+    threads = int(os.environ.get("OPENBLAS_NUM_THREADS", os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1)))
+    return S_sample / dt, dt, threads
+
+
+def run_reference(args, world):
+    from synth import configs as C
+    wl = C.LLAMA3_8B_PREFILL
+    S_sample = 512
+    for _ in range(args.warmup):
+        oracle_prefill_sample(S_sample)
+    times = []
+    for _ in range(args.steps):
+        _, dt, threads = oracle_prefill_sample(S_sample)
+        times.append(dt)
+    ms = 1e3 * sum(times) / len(times)
+    val = S_sample / (ms / 1e3)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "B": wl.B, "S": wl.S, "d_model": wl.d_model, "n_q": wl.n_q,
+                   "n_kv": wl.n_kv, "head_dim": wl.head_dim, "d_ff": wl.d_ff},
+        "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": f"one sequence of {S_sample} tokens of the 8B block per step (fp64 numpy)"},
+        "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    if args.impl == "reference":
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        if int(os.environ.get("RANK", "0")) == 0:
+            run_reference(args, world)
+        return
+
+    world, rank, local = dist_setup()
+    pre = bench_prefill(args, world, rank)
+    dec = None if args.no_decode else bench_decode(args, world, rank)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        S_sample = 1024
+        tps, dt, threads = oracle_prefill_sample(S_sample)
+        cpu = {"value": tps, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+               "sample": f"one sequence of {S_sample} tokens of the 8B block, fp64 numpy, {dt:.1f} s"}
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": pre["value"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": pre["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,0.02) weights, N(0,1) inputs)",
+            "config": pre["config"], "roofline": pre["roofline"], "cpu_baseline": cpu, "e2e": pre["e2e"],
+            "gpu_launches": pre["gpu_launches"], "clocks": pre["clocks"], "block_tc_frac": pre["block_tc_frac"],
+            "block_tflops": pre["block_tflops"], "kernels": pre["kernels"], "decode": dec,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,179 @@
+/*
+ * llama_block.h — C ABI of the GB300 (sm_103a) Llama decoder-block forward library.
+ *
+ * The block computed here (sources: "Llama Architecture: RMSNorm, SwiGLU, RoPE, GQA,
+ * and PyTorch Implementation", Mathematical Foundations 1-4 and Production PyTorch
+ * Implementation Steps 1-2; "LLaMA Architecture > Model Architecture", The Transformer
+ * Block; "LLaMA-3 8B 现代 LLM 架构、计算规模与能耗", sections 四, 五, 九, 十):
+ *
+ *     u = RMSNorm(x; g_attn)                 x * rsqrt(mean(x^2) + eps) * g
+ *     q = RoPE(u W_Q^T), k = RoPE(u W_K^T), v = u W_V^T
+ *     o = softmax(q k^T / sqrt(head_dim) + causal mask) v,  query head h reads KV head h / (n_q/n_kv)
+ *     h = x + o W_O^T
+ *     y = h + W_down (SiLU(W_gate RMSNorm(h; g_ffn)) * W_up RMSNorm(h; g_ffn))
+ *
+ * Conventions shared by every call
+ *   - All pointers are DEVICE pointers unless stated otherwise; the caller owns and allocates
+ *     all memory (tensors, caches, workspace).  The library never allocates device memory.
+ *   - All calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default stream).
+ *     Argument and shape errors are returned synchronously and nothing is launched.  Errors
+ *     found on the device (a wait that timed out) are latched in a device status word read by
+ *     llama_get_device_status().
+ *   - dtype: LLAMA_F32 or LLAMA_BF16 for activations, weights and gains alike.  Arithmetic
+ *     accumulates in fp32 for both.
+ *   - Weights are row-major [out, in] (the nn.Linear layout), so a projection is x W^T.
+ *   - Activations are token-major: x [B, S, d_model] = [B*S rows, d_model];
+ *     q [B, S, n_q, head_dim]; k, v [B, S, n_kv, head_dim]; caches [B, capacity, n_kv, head_dim].
+ *   - Positions are 0-based absolute positions; token s of a call sits at pos0 + s, and a query
+ *     at position m sees keys 0..m.  RoPE turns the interleaved pair (x_2k, x_2k+1) by
+ *     m * theta_base^(-2k/head_dim).  Positions must be < 2^24; the angle is reduced exactly for
+ *     positions below 2^19.
+ *   - Device pointers must be 16-byte aligned; row widths must keep every row 16-byte aligned.
+ *   - The bf16 path uses tcgen05 tensor cores and requires head_dim in {64, 128}, d_model,
+ *     n_q*head_dim, n_kv*head_dim and d_ff multiples of 128, and 128 % (n_q/n_kv) == 0.
+ *     Other bf16 shapes, and every f32 shape, run on CUDA-core kernels.
+ */
+#ifndef LLAMA_BLOCK_H
+#define LLAMA_BLOCK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The shape record every call takes.  Fields a call does not use must still be >= 0. */
+typedef struct llama_dims {
+  int64_t B;          /* batch (sequences) */
+  int64_t S;          /* tokens per sequence in this call */
+  int64_t d_model;    /* residual width */
+  int64_t n_q;        /* query heads */
+  int64_t n_kv;       /* key/value heads; n_q % n_kv == 0 */
+  int64_t head_dim;   /* per-head width; even */
+  int64_t d_ff;       /* SwiGLU hidden width */
+  double theta_base;  /* RoPE base (1e4, 5e5, ...) */
+  double eps;         /* RMSNorm epsilon, added inside the square root */
+} llama_dims;
+
+typedef enum llama_dtype { LLAMA_F32 = 0, LLAMA_BF16 = 1 } llama_dtype;
+
+typedef enum llama_status {
+  LLAMA_OK = 0,
+  LLAMA_ERR_INVALID_ARG = 1,   /* null pointer, negative or inconsistent size */
+  LLAMA_ERR_UNSUPPORTED = 2,   /* shape or dtype this library does not handle */
+  LLAMA_ERR_ALIGNMENT = 3,     /* pointer not 16-byte aligned */
+  LLAMA_ERR_WORKSPACE = 4,     /* workspace missing or smaller than llama_workspace_bytes() */
+  LLAMA_ERR_CUDA = 5,          /* a CUDA runtime call or launch failed */
+  LLAMA_ERR_TIMEOUT = 6        /* device side: a bounded wait ran out (kernel gave up cleanly) */
+} llama_status;
+
+/* One block's parameters (device pointers, dtype of the call):
+ *   attn_norm_g, ffn_norm_g [d_model]
+ *   wq [n_q*hd, d_model], wk, wv [n_kv*hd, d_model], wo [d_model, n_q*hd]
+ *   w_gate, w_up [d_ff, d_model], w_down [d_model, d_ff]                                     */
+typedef struct llama_block_weights {
+  const void* attn_norm_g;
+  const void* wq;
+  const void* wk;
+  const void* wv;
+  const void* wo;
+  const void* ffn_norm_g;
+  const void* w_gate;
+  const void* w_up;
+  const void* w_down;
+} llama_block_weights;
+
+/* Operation ids for llama_workspace_bytes. */
+typedef enum llama_op {
+  LLAMA_OP_RMSNORM = 0,
+  LLAMA_OP_ROPE = 1,
+  LLAMA_OP_GQA_ATTENTION = 2,
+  LLAMA_OP_SWIGLU_FFN = 3,
+  LLAMA_OP_BLOCK_FORWARD = 4,
+  LLAMA_OP_STACK_DECODE_STEP = 5
+} llama_op;
+
+/* RMSNorm over the feature axis ("Llama Architecture ...", Mathematical Foundations 1, with eps
+ * inside the root as in its Step 1 code; the RMSNorm study note, "How it works").
+ * x, y: [B*S, d_model]; g: [d_model].  y = x * rsqrt(mean(x^2) + eps) * g, fp32 accumulation,
+ * one rounding to dtype.  y may alias x.  Uses B, S, d_model, eps.                          */
+int llama_rmsnorm(const llama_dims* dims, int dtype, const void* x, const void* g, void* y,
+                  void* stream);
+
+/* RoPE in place ("Llama Architecture ...", Mathematical Foundations 3; "LLaMA-3 8B ...",
+ * section 四.3).  q: [B, S, n_q, hd], k: [B, S, n_kv, hd]; either may be NULL.  Token s of
+ * every sequence is at position pos0 + s.  Uses B, S, n_q, n_kv, head_dim, theta_base.       */
+int llama_rope(const llama_dims* dims, int dtype, void* q, void* k, int64_t pos0, void* stream);
+
+/* Causal grouped-query attention on post-RoPE inputs ("Llama Architecture ...", Mathematical
+ * Foundations 4; "LLaMA-3 8B ...", section 四.4 and its 8Q/2KV example).
+ *   q: [B, S, n_q, hd], queries at positions pos0 .. pos0+S-1
+ *   k, v: [B, kv_capacity, n_kv, hd], holding keys/values for positions 0 .. pos0+S-1
+ *   o: [B, S, n_q, hd]
+ * Query head h reads KV head h / (n_q/n_kv); a query at position m sees keys 0..m; scale
+ * 1/sqrt(hd).  Requires pos0 + S <= kv_capacity.  ws: scratch of llama_workspace_bytes(
+ * LLAMA_OP_GQA_ATTENTION, ...) bytes (may be 0; then ws may be NULL).                       */
+int llama_gqa_attention(const llama_dims* dims, int dtype, const void* q, const void* k,
+                        const void* v, int64_t kv_capacity, int64_t pos0, void* o, void* ws,
+                        size_t ws_bytes, void* stream);
+
+/* SwiGLU feed-forward ("Llama Architecture ...", Mathematical Foundations 2; "LLaMA-3 8B ...",
+ * section 五).  x, y: [B*S, d_model]; y = W_down(SiLU(W_gate x) * W_up x), no residual.
+ * ws holds the [B*S, d_ff] gated product.  y must not alias x.                              */
+int llama_swiglu_ffn(const llama_dims* dims, int dtype, const void* x, const void* w_gate,
+                     const void* w_up, const void* w_down, void* y, void* ws, size_t ws_bytes,
+                     void* stream);
+
+/* One decoder block over B sequences of S new tokens at positions pos0 .. pos0+S-1
+ * ("Llama Architecture ...", Step 2 LlamaTransformerBlock; "LLaMA Architecture > Model
+ * Architecture", The Transformer Block).  x, y: [B*S, d_model]; y must not alias x.
+ * k_cache, v_cache: [B, cache_capacity, n_kv, hd]; on entry they hold positions 0..pos0-1,
+ * and the call writes the rotated keys and the values of the new tokens at pos0..pos0+S-1.
+ * Both NULL: pos0 must be 0 and the block's K/V live in the workspace.                       */
+int llama_block_forward(const llama_dims* dims, int dtype, const llama_block_weights* w,
+                        const void* x, void* y, int64_t pos0, void* k_cache, void* v_cache,
+                        int64_t cache_capacity, void* ws, size_t ws_bytes, void* stream);
+
+/* One decode step of an n_layers stack, one new token per sequence, then the final RMSNorm
+ * and the untied LM head ("LLaMA-3 8B ...", sections 二, 九 and 十).  dims->S must be 1.
+ *   layers: HOST array of n_layers weight records (device pointers inside)
+ *   final_g [d_model]; w_lm [vocab, d_model]; x_emb [B, d_model] (the new tokens' embedding rows)
+ *   k_cache, v_cache: [n_layers, B, cache_capacity, n_kv, hd]; positions 0..t_cache-1 are read,
+ *   position t_cache of every layer is written (so t_cache < cache_capacity)
+ *   logits: [B, vocab] float32, whatever dtype is.
+ * The residual stream is kept in fp32 across layers (in ws).                                 */
+int llama_stack_decode_step(const llama_dims* dims, int dtype, int n_layers,
+                            const llama_block_weights* layers, const void* final_g,
+                            const void* w_lm, int64_t vocab, const void* x_emb, void* k_cache,
+                            void* v_cache, int64_t cache_capacity, int64_t t_cache, float* logits,
+                            void* ws, size_t ws_bytes, void* stream);
+
+/* Workspace bytes the call `op` needs for these arguments (0 if none).  kv_capacity is the
+ * cache capacity for attention/decode and is ignored otherwise.                              */
+size_t llama_workspace_bytes(int op, const llama_dims* dims, int dtype, int n_layers,
+                             int64_t vocab, int64_t kv_capacity);
+
+/* Synchronises `stream`, then reads and clears the device status word of the current device.
+ * *out receives LLAMA_OK or LLAMA_ERR_TIMEOUT (a kernel's bounded wait ran out and it exited).
+ * Returns LLAMA_OK, or LLAMA_ERR_CUDA if the synchronisation or the copy failed.             */
+int llama_get_device_status(int* out, void* stream);
+
+/* Benchmark timing.  While enabled, every kernel the library launches is bracketed by two CUDA
+ * events recorded on the launching stream (the events are created on first use and reused;
+ * no device memory is allocated).  Do not enable it while a stream is being captured. */
+int llama_profile_enable(int on);
+
+/* Synchronises the device, then reports the launches recorded since profiling was enabled or
+ * last read, aggregated by kernel role: names[i] (static strings), launches[i], total_ms[i] for
+ * i < *n_kinds (at most max_kinds).  Clears the record.                                      */
+int llama_profile_read(int max_kinds, const char** names, int* launches, double* total_ms, int* n_kinds);
+
+/* Static, human-readable name of a status code. */
+const char* llama_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LLAMA_BLOCK_H */

@@ -1,0 +1,203 @@
+"""Python binding of the C ABI in include/llama_block.h.
+
+Argument marshalling only: every step of the block runs in the CUDA kernels of
+libllama_block.so.  torch is used for device memory and streams; tensors are
+passed as raw device pointers.  If the library has not been built the first
+call raises: there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Sequence
+
+__all__ = [
+    "F32", "BF16", "LlamaError", "Dims", "BlockWeights", "lib", "dims_of",
+    "llama_rmsnorm", "llama_rope", "llama_gqa_attention", "llama_swiglu_ffn",
+    "llama_block_forward", "llama_stack_decode_step", "llama_workspace_bytes",
+    "llama_get_device_status", "llama_status_string", "llama_profile_enable", "llama_profile_read",
+    "OP_RMSNORM", "OP_ROPE", "OP_GQA_ATTENTION", "OP_SWIGLU_FFN", "OP_BLOCK_FORWARD",
+    "OP_STACK_DECODE_STEP",
+]
+
+F32, BF16 = 0, 1
+(OP_RMSNORM, OP_ROPE, OP_GQA_ATTENTION, OP_SWIGLU_FFN, OP_BLOCK_FORWARD,
+ OP_STACK_DECODE_STEP) = range(6)
+STATUS_NAMES = {0: "LLAMA_OK", 1: "LLAMA_ERR_INVALID_ARG", 2: "LLAMA_ERR_UNSUPPORTED",
+                3: "LLAMA_ERR_ALIGNMENT", 4: "LLAMA_ERR_WORKSPACE", 5: "LLAMA_ERR_CUDA",
+                6: "LLAMA_ERR_TIMEOUT"}
+
+_DIR = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_DIR, "libllama_block.so")
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int64), ("S", ctypes.c_int64), ("d_model", ctypes.c_int64),
+                ("n_q", ctypes.c_int64), ("n_kv", ctypes.c_int64), ("head_dim", ctypes.c_int64),
+                ("d_ff", ctypes.c_int64), ("theta_base", ctypes.c_double), ("eps", ctypes.c_double)]
+
+
+_WEIGHT_FIELDS = ["attn_norm_g", "wq", "wk", "wv", "wo", "ffn_norm_g", "w_gate", "w_up", "w_down"]
+
+
+class BlockWeights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in _WEIGHT_FIELDS]
+
+
+class LlamaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; raises if it was not built (no fallback exists)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build()")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+            pd = ctypes.POINTER(Dims)
+            sig = {
+                "llama_rmsnorm": [pd, i32, vp, vp, vp, vp],
+                "llama_rope": [pd, i32, vp, vp, i64, vp],
+                "llama_gqa_attention": [pd, i32, vp, vp, vp, i64, i64, vp, vp, sz, vp],
+                "llama_swiglu_ffn": [pd, i32, vp, vp, vp, vp, vp, vp, sz, vp],
+                "llama_block_forward": [pd, i32, ctypes.POINTER(BlockWeights), vp, vp, i64, vp, vp, i64,
+                                        vp, sz, vp],
+                "llama_stack_decode_step": [pd, i32, i32, ctypes.POINTER(BlockWeights), vp, vp, i64, vp,
+                                            vp, vp, i64, i64, vp, vp, sz, vp],
+                "llama_get_device_status": [ctypes.POINTER(ctypes.c_int), vp],
+            }
+            for name, args in sig.items():
+                fn = getattr(L, name)
+                fn.argtypes = args
+                fn.restype = ctypes.c_int
+            L.llama_workspace_bytes.argtypes = [i32, pd, i32, i32, i64, i64]
+            L.llama_workspace_bytes.restype = sz
+            L.llama_profile_enable.argtypes = [i32]
+            L.llama_profile_enable.restype = ctypes.c_int
+            L.llama_profile_read.argtypes = [i32, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_int),
+                                             ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]
+            L.llama_profile_read.restype = ctypes.c_int
+            L.llama_status_string.argtypes = [i32]
+            L.llama_status_string.restype = ctypes.c_char_p
+            _lib = L
+    return _lib
+
+
+def dims_of(B, S, d_model, n_q, n_kv, head_dim, d_ff, theta_base, eps) -> Dims:
+    return Dims(int(B), int(S), int(d_model), int(n_q), int(n_kv), int(head_dim), int(d_ff),
+                float(theta_base), float(eps))
+
+
+def _d(dims) -> Dims:
+    if isinstance(dims, Dims):
+        return dims
+    if isinstance(dims, Sequence):
+        return dims_of(*dims)
+    return dims_of(dims.B, dims.S, dims.d_model, dims.n_q, dims.n_kv, dims.head_dim, dims.d_ff,
+                   dims.theta_base, dims.eps)
+
+
+def _p(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _s(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != 0:
+        raise LlamaError(rc, where)
+
+
+def _nbytes(t) -> int:
+    return 0 if t is None else t.numel() * t.element_size()
+
+
+def block_weights(w) -> BlockWeights:
+    """BlockWeights from a mapping (or object) holding the nine device tensors."""
+    get = (lambda n: w[n]) if isinstance(w, dict) else (lambda n: getattr(w, n))
+    return BlockWeights(*[_p(get(n)) for n in _WEIGHT_FIELDS])
+
+
+def llama_rmsnorm(dims, dtype, x, g, y, stream=None):
+    _check(lib().llama_rmsnorm(ctypes.byref(_d(dims)), dtype, _p(x), _p(g), _p(y), _s(stream)), "llama_rmsnorm")
+
+
+def llama_rope(dims, dtype, q, k, pos0=0, stream=None):
+    _check(lib().llama_rope(ctypes.byref(_d(dims)), dtype, _p(q), _p(k), int(pos0), _s(stream)), "llama_rope")
+
+
+def llama_gqa_attention(dims, dtype, q, k, v, kv_capacity, pos0, o, ws=None, stream=None):
+    _check(lib().llama_gqa_attention(ctypes.byref(_d(dims)), dtype, _p(q), _p(k), _p(v), int(kv_capacity),
+                                     int(pos0), _p(o), _p(ws), _nbytes(ws), _s(stream)), "llama_gqa_attention")
+
+
+def llama_swiglu_ffn(dims, dtype, x, w_gate, w_up, w_down, y, ws, stream=None):
+    _check(lib().llama_swiglu_ffn(ctypes.byref(_d(dims)), dtype, _p(x), _p(w_gate), _p(w_up), _p(w_down),
+                                  _p(y), _p(ws), _nbytes(ws), _s(stream)), "llama_swiglu_ffn")
+
+
+def llama_block_forward(dims, dtype, weights, x, y, pos0=0, k_cache=None, v_cache=None, cache_capacity=0,
+                        ws=None, stream=None):
+    w = weights if isinstance(weights, BlockWeights) else block_weights(weights)
+    _check(lib().llama_block_forward(ctypes.byref(_d(dims)), dtype, ctypes.byref(w), _p(x), _p(y), int(pos0),
+                                     _p(k_cache), _p(v_cache), int(cache_capacity), _p(ws), _nbytes(ws),
+                                     _s(stream)), "llama_block_forward")
+
+
+def llama_stack_decode_step(dims, dtype, layers, final_g, w_lm, vocab, x_emb, k_cache, v_cache, cache_capacity,
+                            t_cache, logits, ws, stream=None):
+    n = len(layers)
+    arr = (BlockWeights * n)(*[lw if isinstance(lw, BlockWeights) else block_weights(lw) for lw in layers])
+    _check(lib().llama_stack_decode_step(ctypes.byref(_d(dims)), dtype, n, arr, _p(final_g), _p(w_lm), int(vocab),
+                                         _p(x_emb), _p(k_cache), _p(v_cache), int(cache_capacity), int(t_cache),
+                                         _p(logits), _p(ws), _nbytes(ws), _s(stream)), "llama_stack_decode_step")
+
+
+def llama_workspace_bytes(op, dims, dtype, n_layers=0, vocab=0, kv_capacity=0) -> int:
+    return int(lib().llama_workspace_bytes(int(op), ctypes.byref(_d(dims)), dtype, int(n_layers), int(vocab),
+                                           int(kv_capacity)))
+
+
+def llama_get_device_status(stream=None) -> int:
+    out = ctypes.c_int(-1)
+    _check(lib().llama_get_device_status(ctypes.byref(out), _s(stream)), "llama_get_device_status")
+    return out.value
+
+
+def llama_profile_enable(on: bool = True) -> None:
+    _check(lib().llama_profile_enable(1 if on else 0), "llama_profile_enable")
+
+
+def llama_profile_read(max_kinds: int = 32) -> dict:
+    """{kernel role: (launches, total_ms)} for the launches recorded since the last read."""
+    names = (ctypes.c_char_p * max_kinds)()
+    launches = (ctypes.c_int * max_kinds)()
+    ms = (ctypes.c_double * max_kinds)()
+    n = ctypes.c_int(0)
+    _check(lib().llama_profile_read(max_kinds, names, launches, ms, ctypes.byref(n)), "llama_profile_read")
+    return {names[i].decode(): (launches[i], ms[i]) for i in range(n.value)}
+
+
+def llama_status_string(status: int) -> str:
+    return lib().llama_status_string(int(status)).decode()

@@ -1,0 +1,612 @@
+// C ABI of the library (include/llama_block.h): argument validation, workspace planning,
+// RoPE frequency set-up, tensor-map encoding and kernel dispatch.  Nothing here allocates
+// device memory, synchronises a stream (except llama_get_device_status) or touches the host
+// copy of any tensor.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "kernels.h"
+
+namespace llama {
+
+// ------------------------------------------------------------------ device status word
+__device__ unsigned g_device_status;
+
+static unsigned* status_ptr() {
+  static unsigned* cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!cached[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+    cached[dev] = static_cast<unsigned*>(p);
+  }
+  return cached[dev];
+}
+
+static int num_sms() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!cached[dev]) {
+    int n = 0;
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    cached[dev] = n > 0 ? n : 148;
+  }
+  return cached[dev];
+}
+
+// ------------------------------------------------------------------ launch profiling
+namespace prof {
+struct Rec { const char* name; int a, b; };
+static std::mutex mu;
+static bool on = false;
+static std::vector<cudaEvent_t> pool;
+static size_t next = 0;
+static std::vector<Rec> recs;
+static int open_a = -1;
+static const char* open_name = nullptr;
+
+static int take() {
+  if (next == pool.size()) {
+    cudaEvent_t e;
+    if (cudaEventCreate(&e) != cudaSuccess) return -1;
+    pool.push_back(e);
+  }
+  return (int)next++;
+}
+static void begin(const char* name, cudaStream_t st) {
+  if (!on) return;
+  std::lock_guard<std::mutex> g(mu);
+  open_a = take();
+  open_name = name;
+  if (open_a >= 0) cudaEventRecord(pool[open_a], st);
+}
+static void end(cudaStream_t st) {
+  if (!on) return;
+  std::lock_guard<std::mutex> g(mu);
+  if (open_a < 0) return;
+  const int b = take();
+  if (b < 0) return;
+  cudaEventRecord(pool[b], st);
+  recs.push_back({open_name, open_a, b});
+  open_a = -1;
+}
+}  // namespace prof
+
+// ------------------------------------------------------------------ tensor maps
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool encode_tmap_2d_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+                         uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {row_stride_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_tmap_3d_bf16(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                         uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1, uint32_t b2) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {stride1_bytes, stride2_bytes};
+  cuuint32_t box[3] = {b0, b1, b2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_tmap_4d_bf16(CUtensorMap* m, const void* base, const uint64_t* dims, const uint64_t* strides_bytes,
+                         const uint32_t* box) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t d[4] = {dims[0], dims[1], dims[2], dims[3]};
+  cuuint64_t s[3] = {strides_bytes[0], strides_bytes[1], strides_bytes[2]};
+  cuuint32_t b[4] = {box[0], box[1], box[2], box[3]};
+  cuuint32_t e[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), d, s, b, e, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
+// ------------------------------------------------------------------ helpers
+namespace {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+inline size_t esize(int dtype) { return dtype == LLAMA_F32 ? 4 : 2; }
+inline size_t round256(size_t b) { return (b + 255) & ~size_t(255); }
+
+constexpr int64_t kMaxPos = (int64_t)1 << 24;
+
+int check_dtype(int dtype) { return (dtype == LLAMA_F32 || dtype == LLAMA_BF16) ? LLAMA_OK : LLAMA_ERR_UNSUPPORTED; }
+
+// Common shape checks; `need` selects which fields must be positive.
+enum : unsigned { NEED_ROWS = 1, NEED_D = 2, NEED_HEADS = 4, NEED_FF = 8 };
+int check_dims(const llama_dims* d, unsigned need) {
+  if (!d) return LLAMA_ERR_INVALID_ARG;
+  if (d->B < 0 || d->S < 0 || d->d_model < 0 || d->n_q < 0 || d->n_kv < 0 || d->head_dim < 0 || d->d_ff < 0)
+    return LLAMA_ERR_INVALID_ARG;
+  if ((need & NEED_D) && d->d_model <= 0) return LLAMA_ERR_INVALID_ARG;
+  if (need & NEED_HEADS) {
+    if (d->n_q <= 0 || d->n_kv <= 0 || d->head_dim <= 0 || d->n_q % d->n_kv != 0) return LLAMA_ERR_INVALID_ARG;
+    if (d->head_dim % 2 != 0) return LLAMA_ERR_INVALID_ARG;
+    if (d->head_dim > 2 * kMaxRopePairs) return LLAMA_ERR_UNSUPPORTED;
+    if (!(d->theta_base > 0.0) || !std::isfinite(d->theta_base)) return LLAMA_ERR_INVALID_ARG;
+  }
+  if ((need & NEED_FF) && d->d_ff <= 0) return LLAMA_ERR_INVALID_ARG;
+  if (!(d->eps >= 0.0) || !std::isfinite(d->eps)) return LLAMA_ERR_INVALID_ARG;
+  const int64_t big = (int64_t)1 << 31;
+  if (d->B * d->S >= big || d->d_model >= big || d->d_ff >= big) return LLAMA_ERR_UNSUPPORTED;
+  return LLAMA_OK;
+}
+
+// theta_k = theta_base^(-2k/head_dim), split into two floats (hi = fl(theta_k)).
+void rope_freqs(const llama_dims* d, RopeFreq* out) {
+  const int half = (int)(d->head_dim / 2);
+  for (int k = 0; k < half; ++k) {
+    const double th = std::pow(d->theta_base, -2.0 * (double)k / (double)d->head_dim);
+    const float hi = (float)th;
+    out[k].hi = hi;
+    out[k].lo = (float)(th - (double)hi);
+  }
+}
+
+int launch_status() {
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? LLAMA_OK : LLAMA_ERR_CUDA;
+}
+
+// GEMM dispatch: tcgen05 for the bf16 shapes it supports, CUDA cores otherwise.
+int run_gemm(const GemmDesc& g, const char* role, cudaStream_t st) {
+  static const char* const tc_names[] = {"gemm_tc_store", "gemm_tc_resid", "gemm_tc_swiglu", "gemm_tc_qkv",
+                                         "gemm_tc_atomic"};
+  static const char* const simt_names[] = {"gemm_simt_store", "gemm_simt_resid", "gemm_simt_swiglu",
+                                           "gemm_simt_qkv", "gemm_simt_atomic"};
+  (void)role;
+  const bool tc = gemm_tc_supported(g);
+  prof::begin(tc ? tc_names[g.epi.kind] : simt_names[g.epi.kind], st);
+  if (tc) {
+    unsigned* status = status_ptr();
+    if (!status) return LLAMA_ERR_CUDA;
+    if (launch_gemm_tc(g, num_sms(), status, st) != 0) return LLAMA_ERR_CUDA;
+  } else {
+    if (launch_gemm_simt(g, st) != 0) return LLAMA_ERR_CUDA;
+  }
+  prof::end(st);
+  return launch_status();
+}
+
+int run_attention(const AttnDesc& a, cudaStream_t st) {
+  const bool tc = attn_tc_supported(a);
+  prof::begin(tc ? "attn_tc" : "attn_simt", st);
+  if (tc) {
+    unsigned* status = status_ptr();
+    if (!status) return LLAMA_ERR_CUDA;
+    if (launch_attn_tc(a, num_sms(), status, st) != 0) return LLAMA_ERR_CUDA;
+  } else {
+    if (launch_attn_simt(a, st) != 0) return LLAMA_ERR_CUDA;
+  }
+  prof::end(st);
+  return launch_status();
+}
+
+int run_rmsnorm(int dtype, int x_f32, int y_f32, const void* x, const void* g, void* y, int64_t rows, int64_t d,
+                float eps, cudaStream_t st) {
+  prof::begin("rmsnorm", st);
+  if (launch_rmsnorm(dtype, x_f32, y_f32, x, g, y, rows, d, eps, st) != 0) return LLAMA_ERR_UNSUPPORTED;
+  prof::end(st);
+  return launch_status();
+}
+
+Epi make_epi(int kind, int out_f32, void* out, int64_t ldo) {
+  Epi e;
+  memset(&e, 0, sizeof(e));
+  e.kind = kind;
+  e.out_f32 = out_f32;
+  e.out = out;
+  e.ldo = ldo;
+  e.S = 1;
+  return e;
+}
+
+GemmDesc make_gemm(int dtype, int64_t M, const void* A, int64_t K) {
+  GemmDesc g;
+  memset(&g, 0, sizeof(g));
+  g.M = M;
+  g.K = K;
+  g.dtype = dtype;
+  g.A = A;
+  g.lda = K;
+  return g;
+}
+
+// Workspace carving: fixed-order, 256-byte aligned slices.
+struct Carver {
+  char* base;
+  size_t off = 0;
+  void* take(size_t bytes) {
+    void* p = base ? base + off : nullptr;
+    off += round256(bytes);
+    return p;
+  }
+};
+
+struct BlockWs {
+  void *u, *q, *o, *h, *m, *k, *v;
+  size_t bytes;
+};
+
+BlockWs plan_block(const llama_dims* d, int dtype, bool own_kv, void* base) {
+  const size_t es = esize(dtype);
+  const size_t T = (size_t)(d->B * d->S);
+  Carver c{static_cast<char*>(base)};
+  BlockWs w;
+  w.u = c.take(T * d->d_model * es);
+  w.q = c.take(T * d->n_q * d->head_dim * es);
+  w.o = c.take(T * d->n_q * d->head_dim * es);
+  w.h = c.take(T * d->d_model * 4);     // residual stream after attention, kept in fp32
+  w.m = c.take(T * d->d_ff * es);
+  w.k = own_kv ? c.take(T * d->n_kv * d->head_dim * es) : nullptr;
+  w.v = own_kv ? c.take(T * d->n_kv * d->head_dim * es) : nullptr;
+  w.bytes = c.off;
+  return w;
+}
+
+struct DecodeWs {
+  void *xres, *u, *q, *o, *m;
+  size_t bytes;
+};
+
+DecodeWs plan_decode(const llama_dims* d, int dtype, void* base) {
+  const size_t es = esize(dtype);
+  const size_t T = (size_t)d->B;
+  Carver c{static_cast<char*>(base)};
+  DecodeWs w;
+  w.xres = c.take(T * d->d_model * 4);
+  w.u = c.take(T * d->d_model * es);
+  w.q = c.take(T * d->n_q * d->head_dim * es);
+  w.o = c.take(T * d->n_q * d->head_dim * es);
+  w.m = c.take(T * d->d_ff * es);
+  w.bytes = c.off;
+  return w;
+}
+
+// The Q/K/V projection with RoPE on Q and K and the K/V write into [B, cap, n_kv*hd] caches.
+int run_qkv(const llama_dims* d, int dtype, const llama_block_weights* w, const void* u, void* q, void* kc,
+            void* vc, int64_t cap, int64_t pos0, cudaStream_t st) {
+  const int64_t T = d->B * d->S, hq = d->n_q * d->head_dim, hkv = d->n_kv * d->head_dim;
+  GemmDesc g = make_gemm(dtype, T, u, d->d_model);
+  g.nseg = 3;
+  g.B[0] = w->wq; g.nB[0] = hq;
+  g.B[1] = w->wk; g.nB[1] = hkv;
+  g.B[2] = w->wv; g.nB[2] = hkv;
+  g.N = hq + 2 * hkv;
+  g.epi = make_epi(EPI_QKV, dtype == LLAMA_F32, q, hq);
+  g.epi.k_out = kc;
+  g.epi.v_out = vc;
+  g.epi.nq_cols = hq;
+  g.epi.nkv_cols = hkv;
+  g.epi.S = d->S;
+  g.epi.cap = cap;
+  g.epi.pos0 = pos0;
+  g.epi.hd = (int)d->head_dim;
+  rope_freqs(d, g.epi.freq);
+  return run_gemm(g, nullptr, st);
+}
+
+// out = resid + A W^T  (W [N, K])
+int run_linear_resid(int dtype, int64_t M, const void* A, int64_t K, const void* W, int64_t N, const void* resid,
+                     int resid_f32, void* out, int out_f32, cudaStream_t st) {
+  GemmDesc g = make_gemm(dtype, M, A, K);
+  g.nseg = 1;
+  g.B[0] = W; g.nB[0] = N;
+  g.N = N;
+  g.epi = make_epi(resid ? EPI_RESID : EPI_STORE, out_f32, out, N);
+  g.epi.resid = resid;
+  g.epi.resid_f32 = resid_f32;
+  g.epi.ldr = N;
+  return run_gemm(g, nullptr, st);
+}
+
+int run_gate_up(int dtype, int64_t M, const void* A, int64_t K, const void* wg, const void* wu, int64_t dff,
+                void* m, cudaStream_t st) {
+  GemmDesc g = make_gemm(dtype, M, A, K);
+  g.nseg = 2;
+  g.B[0] = wg; g.nB[0] = dff;
+  g.B[1] = wu; g.nB[1] = dff;
+  g.N = 2 * dff;
+  g.epi = make_epi(EPI_SWIGLU, dtype == LLAMA_F32, m, dff);
+  return run_gemm(g, nullptr, st);
+}
+
+AttnDesc make_attn(const llama_dims* d, int dtype, const void* q, const void* k, const void* v, void* o, int64_t cap,
+                   int64_t pos0) {
+  AttnDesc a;
+  memset(&a, 0, sizeof(a));
+  a.dtype = dtype;
+  a.q = q; a.k = k; a.v = v; a.o = o;
+  a.B = d->B; a.S = d->S; a.n_q = d->n_q; a.n_kv = d->n_kv; a.hd = d->head_dim;
+  a.cap = cap;
+  a.pos0 = pos0;
+  a.scale = (float)(1.0 / std::sqrt((double)d->head_dim));
+  return a;
+}
+
+bool block_weights_ok(const llama_block_weights* w) {
+  if (!w) return false;
+  const void* ps[9] = {w->attn_norm_g, w->wq, w->wk, w->wv, w->wo, w->ffn_norm_g, w->w_gate, w->w_up, w->w_down};
+  for (const void* p : ps)
+    if (!p) return false;
+  return true;
+}
+bool block_weights_aligned(const llama_block_weights* w) {
+  const void* ps[9] = {w->attn_norm_g, w->wq, w->wk, w->wv, w->wo, w->ffn_norm_g, w->w_gate, w->w_up, w->w_down};
+  for (const void* p : ps)
+    if (!aligned16(p)) return false;
+  return true;
+}
+
+// One block on already-validated arguments (shared by block_forward and the decode stack).
+// x/y: dtype rows unless x_f32 (decode residual stream in fp32, updated in place: y == x).
+int block_body(const llama_dims* d, int dtype, const llama_block_weights* w, const void* x, int x_f32, void* y,
+               int64_t pos0, void* kc, void* vc, int64_t cap, const BlockWs& ws, cudaStream_t st) {
+  const int64_t T = d->B * d->S, D = d->d_model, hq = d->n_q * d->head_dim;
+  const int f32 = dtype == LLAMA_F32;
+  const float eps = (float)d->eps;
+  int rc;
+  // u = RMSNorm(x; g_attn)
+  if ((rc = run_rmsnorm(dtype, x_f32 || f32, f32, x, w->attn_norm_g, ws.u, T, D, eps, st)) != LLAMA_OK) return rc;
+  // q, k, v with RoPE; k, v written into the cache at pos0..pos0+S-1
+  if ((rc = run_qkv(d, dtype, w, ws.u, ws.q, kc, vc, cap, pos0, st)) != LLAMA_OK) return rc;
+  // o = causal GQA attention
+  AttnDesc a = make_attn(d, dtype, ws.q, kc, vc, ws.o, cap, pos0);
+  if ((rc = run_attention(a, st)) != LLAMA_OK) return rc;
+  // h = x + o W_O^T, kept in fp32 (decode: the fp32 stream is updated in place)
+  void* h = x_f32 ? y : ws.h;
+  if ((rc = run_linear_resid(dtype, T, ws.o, hq, w->wo, D, x, x_f32 || f32, h, 1, st)) != LLAMA_OK) return rc;
+  // w = RMSNorm(h; g_ffn)  (reuses u)
+  if ((rc = run_rmsnorm(dtype, 1, f32, h, w->ffn_norm_g, ws.u, T, D, eps, st)) != LLAMA_OK) return rc;
+  // m = SiLU(w W_gate^T) * (w W_up^T)
+  if ((rc = run_gate_up(dtype, T, ws.u, D, w->w_gate, w->w_up, d->d_ff, ws.m, st)) != LLAMA_OK) return rc;
+  // y = h + m W_down^T
+  return run_linear_resid(dtype, T, ws.m, d->d_ff, w->w_down, D, h, 1, y, x_f32 || f32, st);
+}
+
+}  // namespace
+}  // namespace llama
+
+using namespace llama;
+
+extern "C" {
+
+const char* llama_status_string(int status) {
+  switch (status) {
+    case LLAMA_OK: return "ok";
+    case LLAMA_ERR_INVALID_ARG: return "invalid argument";
+    case LLAMA_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case LLAMA_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    case LLAMA_ERR_WORKSPACE: return "workspace missing or too small";
+    case LLAMA_ERR_CUDA: return "CUDA error";
+    case LLAMA_ERR_TIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int llama_profile_enable(int on) {
+  std::lock_guard<std::mutex> g(prof::mu);
+  prof::on = on != 0;
+  return LLAMA_OK;
+}
+
+int llama_profile_read(int max_kinds, const char** names, int* launches, double* total_ms, int* n_kinds) {
+  if (!n_kinds || max_kinds < 0 || (max_kinds > 0 && (!names || !launches || !total_ms))) return LLAMA_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return LLAMA_ERR_CUDA;
+  std::lock_guard<std::mutex> g(prof::mu);
+  int n = 0;
+  for (const prof::Rec& r : prof::recs) {
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, prof::pool[r.a], prof::pool[r.b]) != cudaSuccess) return LLAMA_ERR_CUDA;
+    int i = 0;
+    while (i < n && std::strcmp(names[i], r.name) != 0) ++i;
+    if (i == n) {
+      if (n == max_kinds) continue;
+      names[n] = r.name; launches[n] = 0; total_ms[n] = 0.0; ++n;
+    }
+    launches[i] += 1;
+    total_ms[i] += ms;
+  }
+  prof::recs.clear();
+  prof::next = 0;
+  *n_kinds = n;
+  return LLAMA_OK;
+}
+
+int llama_get_device_status(int* out, void* stream) {
+  if (!out) return LLAMA_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return LLAMA_ERR_CUDA;
+  unsigned* p = status_ptr();
+  if (!p) return LLAMA_ERR_CUDA;
+  unsigned v = 0;
+  if (cudaMemcpy(&v, p, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return LLAMA_ERR_CUDA;
+  if (v != 0) {
+    const unsigned zero = 0;
+    if (cudaMemcpy(p, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return LLAMA_ERR_CUDA;
+  }
+  *out = (v & STATUS_TIMEOUT) ? LLAMA_ERR_TIMEOUT : LLAMA_OK;
+  return LLAMA_OK;
+}
+
+size_t llama_workspace_bytes(int op, const llama_dims* d, int dtype, int n_layers, int64_t vocab,
+                             int64_t kv_capacity) {
+  (void)n_layers; (void)vocab; (void)kv_capacity;
+  if (!d || check_dtype(dtype) != LLAMA_OK) return 0;
+  const size_t es = esize(dtype);
+  switch (op) {
+    case LLAMA_OP_SWIGLU_FFN: return round256((size_t)(d->B * d->S * d->d_ff) * es);
+    case LLAMA_OP_BLOCK_FORWARD: return plan_block(d, dtype, true, nullptr).bytes;
+    case LLAMA_OP_STACK_DECODE_STEP: return plan_decode(d, dtype, nullptr).bytes;
+    default: return 0;
+  }
+}
+
+int llama_rmsnorm(const llama_dims* d, int dtype, const void* x, const void* g, void* y, void* stream) {
+  int rc;
+  if ((rc = check_dtype(dtype)) != LLAMA_OK) return rc;
+  if ((rc = check_dims(d, NEED_D)) != LLAMA_OK) return rc;
+  const int64_t rows = d->B * d->S;
+  if (rows == 0) return LLAMA_OK;
+  if (!x || !g || !y) return LLAMA_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(g) || !aligned16(y)) return LLAMA_ERR_ALIGNMENT;
+  const int f32 = dtype == LLAMA_F32;
+  return run_rmsnorm(dtype, f32, f32, x, g, y, rows, d->d_model, (float)d->eps, static_cast<cudaStream_t>(stream));
+}
+
+int llama_rope(const llama_dims* d, int dtype, void* q, void* k, int64_t pos0, void* stream) {
+  int rc;
+  if ((rc = check_dtype(dtype)) != LLAMA_OK) return rc;
+  if ((rc = check_dims(d, NEED_HEADS)) != LLAMA_OK) return rc;
+  if (pos0 < 0 || pos0 + d->S > kMaxPos) return LLAMA_ERR_INVALID_ARG;
+  if (d->B * d->S == 0 || (!q && !k)) return LLAMA_OK;
+  if ((q && !aligned16(q)) || (k && !aligned16(k))) return LLAMA_ERR_ALIGNMENT;
+  RopeFreq f[kMaxRopePairs];
+  rope_freqs(d, f);
+  if (launch_rope(dtype, q, k, d->B, d->S, q ? d->n_q : 0, k ? d->n_kv : 0, (int)d->head_dim, pos0, f,
+                  static_cast<cudaStream_t>(stream)) != 0)
+    return LLAMA_ERR_CUDA;
+  return launch_status();
+}
+
+int llama_gqa_attention(const llama_dims* d, int dtype, const void* q, const void* k, const void* v,
+                        int64_t kv_capacity, int64_t pos0, void* o, void* ws, size_t ws_bytes, void* stream) {
+  (void)ws; (void)ws_bytes;
+  int rc;
+  if ((rc = check_dtype(dtype)) != LLAMA_OK) return rc;
+  if ((rc = check_dims(d, NEED_HEADS)) != LLAMA_OK) return rc;
+  if (pos0 < 0 || kv_capacity < 0 || pos0 + d->S > kv_capacity || pos0 + d->S > kMaxPos) return LLAMA_ERR_INVALID_ARG;
+  if (d->B * d->S == 0) return LLAMA_OK;
+  if (!q || !k || !v || !o) return LLAMA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return LLAMA_ERR_ALIGNMENT;
+  AttnDesc a = make_attn(d, dtype, q, k, v, o, kv_capacity, pos0);
+  return run_attention(a, static_cast<cudaStream_t>(stream));
+}
+
+int llama_swiglu_ffn(const llama_dims* d, int dtype, const void* x, const void* w_gate, const void* w_up,
+                     const void* w_down, void* y, void* ws, size_t ws_bytes, void* stream) {
+  int rc;
+  if ((rc = check_dtype(dtype)) != LLAMA_OK) return rc;
+  if ((rc = check_dims(d, NEED_D | NEED_FF)) != LLAMA_OK) return rc;
+  const int64_t T = d->B * d->S;
+  if (T == 0) return LLAMA_OK;
+  if (!x || !w_gate || !w_up || !w_down || !y || x == y) return LLAMA_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w_gate) || !aligned16(w_up) || !aligned16(w_down) || !aligned16(y))
+    return LLAMA_ERR_ALIGNMENT;
+  const size_t need = llama_workspace_bytes(LLAMA_OP_SWIGLU_FFN, d, dtype, 0, 0, 0);
+  if (!ws || ws_bytes < need) return LLAMA_ERR_WORKSPACE;
+  if (!aligned16(ws)) return LLAMA_ERR_ALIGNMENT;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if ((rc = run_gate_up(dtype, T, x, d->d_model, w_gate, w_up, d->d_ff, ws, st)) != LLAMA_OK) return rc;
+  return run_linear_resid(dtype, T, ws, d->d_ff, w_down, d->d_model, nullptr, 0, y, dtype == LLAMA_F32, st);
+}
+
+int llama_block_forward(const llama_dims* d, int dtype, const llama_block_weights* w, const void* x, void* y,
+                        int64_t pos0, void* k_cache, void* v_cache, int64_t cache_capacity, void* ws, size_t ws_bytes,
+                        void* stream) {
+  int rc;
+  if ((rc = check_dtype(dtype)) != LLAMA_OK) return rc;
+  if ((rc = check_dims(d, NEED_D | NEED_HEADS | NEED_FF)) != LLAMA_OK) return rc;
+  if (!block_weights_ok(w) || !x || !y || x == y) return LLAMA_ERR_INVALID_ARG;
+  const bool own_kv = !k_cache && !v_cache;
+  if (!own_kv && (!k_cache || !v_cache)) return LLAMA_ERR_INVALID_ARG;
+  if (own_kv) {
+    if (pos0 != 0) return LLAMA_ERR_INVALID_ARG;
+    cache_capacity = d->S;
+  }
+  if (pos0 < 0 || pos0 + d->S > cache_capacity || pos0 + d->S > kMaxPos) return LLAMA_ERR_INVALID_ARG;
+  if (d->B * d->S == 0) return LLAMA_OK;
+  if (!aligned16(x) || !aligned16(y) || !block_weights_aligned(w) || (k_cache && !aligned16(k_cache)) ||
+      (v_cache && !aligned16(v_cache)))
+    return LLAMA_ERR_ALIGNMENT;
+  const size_t need = plan_block(d, dtype, own_kv, nullptr).bytes;
+  if (!ws || ws_bytes < need) return LLAMA_ERR_WORKSPACE;
+  if (!aligned16(ws)) return LLAMA_ERR_ALIGNMENT;
+  BlockWs b = plan_block(d, dtype, own_kv, ws);
+  void* kc = own_kv ? b.k : k_cache;
+  void* vc = own_kv ? b.v : v_cache;
+  return block_body(d, dtype, w, x, 0, y, pos0, kc, vc, cache_capacity, b, static_cast<cudaStream_t>(stream));
+}
+
+int llama_stack_decode_step(const llama_dims* d, int dtype, int n_layers, const llama_block_weights* layers,
+                            const void* final_g, const void* w_lm, int64_t vocab, const void* x_emb, void* k_cache,
+                            void* v_cache, int64_t cache_capacity, int64_t t_cache, float* logits, void* ws,
+                            size_t ws_bytes, void* stream) {
+  int rc;
+  if ((rc = check_dtype(dtype)) != LLAMA_OK) return rc;
+  if ((rc = check_dims(d, NEED_D | NEED_HEADS | NEED_FF)) != LLAMA_OK) return rc;
+  if (d->S != 1 || n_layers <= 0 || vocab <= 0 || !layers || !final_g || !w_lm || !x_emb || !k_cache || !v_cache ||
+      !logits)
+    return LLAMA_ERR_INVALID_ARG;
+  if (t_cache < 0 || t_cache + 1 > cache_capacity || t_cache + 1 > kMaxPos) return LLAMA_ERR_INVALID_ARG;
+  for (int l = 0; l < n_layers; ++l)
+    if (!block_weights_ok(&layers[l])) return LLAMA_ERR_INVALID_ARG;
+  if (d->B == 0) return LLAMA_OK;
+  for (int l = 0; l < n_layers; ++l)
+    if (!block_weights_aligned(&layers[l])) return LLAMA_ERR_ALIGNMENT;
+  if (!aligned16(final_g) || !aligned16(w_lm) || !aligned16(x_emb) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      !aligned16(logits))
+    return LLAMA_ERR_ALIGNMENT;
+  const size_t need = plan_decode(d, dtype, nullptr).bytes;
+  if (!ws || ws_bytes < need) return LLAMA_ERR_WORKSPACE;
+  if (!aligned16(ws)) return LLAMA_ERR_ALIGNMENT;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  DecodeWs dw = plan_decode(d, dtype, ws);
+  const int64_t Bn = d->B, D = d->d_model;
+  const size_t es = esize(dtype);
+  // fp32 residual stream <- embedding rows
+  if (dtype == LLAMA_F32) {
+    if (cudaMemcpyAsync(dw.xres, x_emb, (size_t)(Bn * D) * 4, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+      return LLAMA_ERR_CUDA;
+  } else if (launch_widen_bf16(x_emb, static_cast<float*>(dw.xres), Bn * D, st) != 0) {
+    return LLAMA_ERR_CUDA;
+  }
+  const size_t layer_cache = (size_t)(Bn * cache_capacity * d->n_kv * d->head_dim) * es;
+  BlockWs b;
+  b.u = dw.u; b.q = dw.q; b.o = dw.o; b.h = nullptr; b.m = dw.m; b.k = nullptr; b.v = nullptr; b.bytes = 0;
+  for (int l = 0; l < n_layers; ++l) {
+    void* kc = static_cast<char*>(k_cache) + l * layer_cache;
+    void* vc = static_cast<char*>(v_cache) + l * layer_cache;
+    if ((rc = block_body(d, dtype, &layers[l], dw.xres, 1, dw.xres, t_cache, kc, vc, cache_capacity, b, st)) !=
+        LLAMA_OK)
+      return rc;
+  }
+  // z = RMSNorm(x; g_final); logits = z W_lm^T (fp32)
+  if ((rc = run_rmsnorm(dtype, 1, dtype == LLAMA_F32, dw.xres, final_g, dw.u, Bn, D, (float)d->eps, st)) != LLAMA_OK)
+    return rc;
+  return run_linear_resid(dtype, Bn, dw.u, D, w_lm, vocab, nullptr, 0, logits, 1, st);
+}
+
+}  // extern "C"

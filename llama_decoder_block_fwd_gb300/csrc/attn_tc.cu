@@ -1,0 +1,361 @@
+// tcgen05 causal GQA flash attention (prefill and chunked prefill against a cache).
+//
+// What it computes ("Llama Architecture ...", Mathematical Foundations 4; "LLaMA-3 8B ...",
+// section 四.4): for query head h at absolute position m and its KV head g = h / r,
+//     o = sum_j softmax_j(q . k_j / sqrt(hd)) v_j   over keys j <= m.
+// The softmax is taken blockwise over 128-key tiles with a running maximum and sum (the
+// FlashAttention reformulation the "LLaMA-3 8B" page describes in section 四.4): the result is
+// the same up to the order of floating-point additions.
+//
+// Layout of the work (sm_103a):
+//   * A CTA owns one Q tile of 128 rows = (128/r) consecutive tokens x the r query heads of one
+//     KV group, so every K/V tile staged in shared memory serves all r heads of the group.
+//     The tile is one 3-D TMA box of Q [B*S, n_q, hd]: rows are (token, head) pairs.
+//   * warp 0 (one thread): TMA loads of Q once and of K/V tiles (128 keys x hd) into a
+//     2-stage ring.  K/V use a 4-D tensor map whose position extent is the number of valid keys,
+//     so positions past the cached ones read as zeros.
+//   * warp 1 (one thread): tcgen05.mma S = Q K^T (M=128, N=128, K=hd) into one of two TMEM
+//     score buffers, then O += P V (M=128, N=hd, K=128; V is the MN-major operand).  S_{j+1}
+//     is issued before P_j V_j so scores are ready when the softmax warps need them.
+//   * warps 2-5 (one thread per row = TMEM lane): read S, mask, keep the running max m and sum
+//     l, write P = exp2(S*scale*log2e - m) as bf16 into shared memory (128B swizzle), and
+//     rescale O in TMEM only when the row max grew by more than 2^8 (the bound keeps P <= 256).
+//     At the end they divide O by l and store bf16 rows.
+#include <algorithm>
+#include <cstring>
+
+#include "kernels.h"
+
+namespace llama {
+namespace {
+
+constexpr int AT_THREADS = 192;
+constexpr uint32_t TMEM_COLS_ATTN = 512;
+constexpr float kRescaleLog2 = 8.0f;
+
+struct __align__(64) AttnParams {
+  CUtensorMap tmQ;   // [B*S, n_q, hd], box (64, r, 128/r)
+  CUtensorMap tmK;   // [B, kv_len, n_kv, hd], box (64, 1, 128, 1)
+  CUtensorMap tmV;
+  uint16_t* o;       // [B, S, n_q, hd]
+  int B, S, n_q, n_kv, hd, r, tokens_per_tile, t_blocks;
+  int pos0;
+  float scale_log2;  // log2(e) / sqrt(hd)
+  unsigned* status;
+};
+
+template <int HD>
+struct Smem {
+  static constexpr uint32_t Q = 128 * HD * 2;       // Q tile
+  static constexpr uint32_t KV = 128 * HD * 2;      // one K or V tile
+  static constexpr uint32_t P = 128 * 128 * 2;      // P tile (bf16)
+  static constexpr uint32_t OFF_Q = 0;
+  static constexpr uint32_t OFF_K = OFF_Q + Q;               // 2 stages
+  static constexpr uint32_t OFF_V = OFF_K + 2 * KV;          // 2 stages
+  static constexpr uint32_t OFF_P = OFF_V + 2 * KV;
+  static constexpr uint32_t OFF_BAR = OFF_P + P;
+  static constexpr uint32_t TOTAL = OFF_BAR + 256 + 1024;
+};
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* m, uint64_t* bar, int x, int y, int z,
+                                            int w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+template <int HD>
+__global__ void __launch_bounds__(AT_THREADS, 1) attn_tc_kernel(const __grid_constant__ AttnParams p) {
+  using L = Smem<HD>;
+  constexpr int HALVES = HD / 64;          // 64-wide (128-byte) column blocks of Q, K, V
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
+  uint64_t* q_full = bars + 0;
+  uint64_t* k_full = bars + 1;     // [2]
+  uint64_t* v_full = bars + 3;     // [2]
+  uint64_t* kv_empty = bars + 5;   // [2]
+  uint64_t* s_full = bars + 7;     // [2]
+  uint64_t* s_free = bars + 9;     // [2]
+  uint64_t* p_full = bars + 11;
+  uint64_t* o_done = bars + 12;
+  uint64_t* drain = bars + 13;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  // ---- which tile: longest (latest tokens) first for load balance
+  const int groups = p.B * p.n_kv;
+  const int tb = p.t_blocks - 1 - (int)(blockIdx.x / groups);
+  const int bg = (int)(blockIdx.x % groups);
+  const int b = bg / p.n_kv, g = bg % p.n_kv;
+  const int t0 = tb * p.tokens_per_tile;
+  const int t_end = min(t0 + p.tokens_per_tile, p.S);
+  const int last_key = p.pos0 + t_end - 1;               // largest position any valid row sees
+  const int n_tiles = last_key / 128 + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 14; ++i) mbar_init(&bars[i], (i == 9 || i == 10 || i == 11) ? 128 : 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&p.tmQ);
+    tma_prefetch_desc(&p.tmK);
+    tma_prefetch_desc(&p.tmV);
+  }
+  if (warp == 1) { tmem_alloc(tmem_slot, TMEM_COLS_ATTN); tmem_relinquish(); }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t tS = tmem;              // S buffers at columns 0 and 128
+  const uint32_t tO = tmem + 256;        // O at columns 256 .. 256+HD-1
+
+  if (warp == 0) {
+    if (lane == 0) {  // ------------------------------------------------ TMA producer
+      mbar_arrive_expect_tx(q_full, L::Q);
+      for (int hh = 0; hh < HALVES; ++hh)
+        tma_load_3d(sbase + L::OFF_Q + hh * 16384, &p.tmQ, q_full, hh * 64, g * p.r, b * p.S + t0);
+      for (int j = 0; j < n_tiles; ++j) {
+        const int st = j & 1;
+        const uint32_t ph = (j >> 1) & 1;
+        if (!mbar_wait(&kv_empty[st], ph ^ 1, abort_flag, p.status)) break;
+        mbar_arrive_expect_tx(&k_full[st], L::KV);
+        for (int hh = 0; hh < HALVES; ++hh)
+          tma_load_4d(sbase + L::OFF_K + st * L::KV + hh * 16384, &p.tmK, &k_full[st], hh * 64, g, j * 128, b);
+        mbar_arrive_expect_tx(&v_full[st], L::KV);
+        for (int hh = 0; hh < HALVES; ++hh)
+          tma_load_4d(sbase + L::OFF_V + st * L::KV + hh * 16384, &p.tmV, &v_full[st], hh * 64, g, j * 128, b);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // ------------------------------------------------ MMA issuer
+      const uint32_t idesc_s = idesc_bf16(128, 128);
+      const uint32_t idesc_o = idesc_bf16(128, HD, /*b_mn_major=*/true);
+      bool ok = mbar_wait(q_full, 0, abort_flag, p.status);
+      tc_fence_after();
+      auto issue_pv = [&](int i) -> bool {
+        const int st = i & 1;
+        if (!mbar_wait(p_full, i & 1, abort_flag, p.status)) return false;
+        if (!mbar_wait(&v_full[st], (i >> 1) & 1, abort_flag, p.status)) return false;
+        tc_fence_after();
+        const uint32_t pa = sbase + L::OFF_P;
+        const uint32_t va = sbase + L::OFF_V + st * L::KV;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {   // 16 keys per step
+          const uint64_t ad = sdesc_sw128(pa + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(va + k * 2048, 16384, 1024);
+          tc_mma(tO, ad, bd, idesc_o, (i > 0 || k > 0) ? 1u : 0u);
+        }
+        tc_commit(o_done);
+        tc_commit(&kv_empty[st]);
+        return true;
+      };
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        const int st = j & 1;
+        const uint32_t ph = (j >> 1) & 1;
+        if (!mbar_wait(&k_full[st], ph, abort_flag, p.status)) { ok = false; break; }
+        if (!mbar_wait(&s_free[st], ph ^ 1, abort_flag, p.status)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t ka = sbase + L::OFF_K + st * L::KV;
+        const uint32_t qa = sbase + L::OFF_Q;
+#pragma unroll
+        for (int k = 0; k < HD / 16; ++k) {
+          const uint64_t ad = sdesc_sw128(qa + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(ka + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
+          tc_mma(tS + st * 128, ad, bd, idesc_s, k > 0 ? 1u : 0u);
+        }
+        tc_commit(&s_full[st]);
+        if (j > 0 && !issue_pv(j - 1)) { ok = false; break; }
+      }
+      if (ok) issue_pv(n_tiles - 1);
+      int no_abort = 0;
+      tc_commit(drain);
+      mbar_wait(drain, 0, &no_abort, p.status);
+    }
+  } else {  // ------------------------------------------------------------ softmax warps 2..5
+    const int qw = warp & 3;
+    const int row = qw * 32 + lane;                     // TMEM lane = Q tile row
+    const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
+    const int tok = t0 + row / p.r;                     // token within the sequence
+    const int qpos = p.pos0 + tok;                      // absolute position of this row
+    const int full_tiles = (p.pos0 + t0 + 1) / 128;     // tiles entirely visible to every row
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    uint8_t* prow = smem + L::OFF_P + row * 128;
+    const int sw = row & 7;
+    for (int j = 0; j < n_tiles; ++j) {
+      const int st = j & 1;
+      const uint32_t ph = (j >> 1) & 1;
+      if (!mbar_wait(&s_full[st], ph, abort_flag, p.status)) { ok = false; break; }
+      tc_fence_after();
+      float s[128];
+      {
+        uint32_t v[32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          tmem_ld32(tS + st * 128 + lane_off + c * 32, v);
+          tc_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(v[i]);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&s_free[st]);
+      if (j >= full_tiles) {
+        const int kbase = j * 128;
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (kbase + c > qpos) s[c] = -INFINITY;
+      }
+      float mx = s[0];
+#pragma unroll
+      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
+      const float mt = mx * p.scale_log2;
+      // P_{j-1} V_{j-1} must be finished before O or the P buffer is touched.
+      if (j > 0) {
+        if (!mbar_wait(o_done, (j - 1) & 1, abort_flag, p.status)) { ok = false; break; }
+        tc_fence_after();
+      }
+      float alpha = 1.f;
+      bool resc = false;
+      if (j == 0) {
+        m_ref = mt;
+      } else if (mt > m_ref + kRescaleLog2) {
+        alpha = exp2f(m_ref - mt);
+        m_ref = mt;
+        resc = true;
+      }
+      if (j > 0 && __any_sync(0xffffffffu, resc)) {
+        l *= alpha;
+#pragma unroll 1
+        for (int c = 0; c < HD / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tO + lane_off + c * 32, v);
+          tc_wait_ld();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+          tmem_st32(tO + lane_off + c * 32, v);
+        }
+        tc_wait_st();
+      }
+      const float mb = m_ref;
+      float lsum = 0.f;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {      // 16 chunks of 8 keys
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float p0 = exp2f(fmaf(s[c * 8 + 2 * e], p.scale_log2, -mb));
+          const float p1 = exp2f(fmaf(s[c * 8 + 2 * e + 1], p.scale_log2, -mb));
+          w[e] = pack_bf16x2(p0, p1);
+          lsum += __uint_as_float(w[e] << 16) + __uint_as_float(w[e] & 0xFFFF0000u);
+        }
+        const int atom = c >> 3, chunk = (c & 7) ^ sw;
+        *reinterpret_cast<uint4*>(prow + atom * 16384 + chunk * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      l += lsum;
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(p_full);
+    }
+    if (ok && mbar_wait(o_done, (n_tiles - 1) & 1, abort_flag, p.status)) {
+      tc_fence_after();
+      const float inv = 1.f / l;
+      const bool live = tok < p.S;
+      const int h = g * p.r + row % p.r;
+      uint16_t* orow = p.o + (((int64_t)b * p.S + tok) * p.n_q + h) * HD;
+#pragma unroll 1
+      for (int c = 0; c < HD / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tO + lane_off + c * 32, v);
+        tc_wait_ld();
+        if (live) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 8) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(v[i]) * inv, __uint_as_float(v[i + 1]) * inv);
+            w.y = pack_bf16x2(__uint_as_float(v[i + 2]) * inv, __uint_as_float(v[i + 3]) * inv);
+            w.z = pack_bf16x2(__uint_as_float(v[i + 4]) * inv, __uint_as_float(v[i + 5]) * inv);
+            w.w = pack_bf16x2(__uint_as_float(v[i + 6]) * inv, __uint_as_float(v[i + 7]) * inv);
+            *reinterpret_cast<uint4*>(orow + c * 32 + i) = w;
+          }
+        }
+      }
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS_ATTN);
+  }
+}
+
+template <int HD>
+int launch_hd(const AttnDesc& a, unsigned* status, cudaStream_t st) {
+  AttnParams p;
+  memset(&p, 0, sizeof(p));
+  const int r = (int)(a.n_q / a.n_kv);
+  const int tpt = 128 / r;
+  const int64_t kv_len = a.pos0 + a.S;
+  if (!encode_tmap_3d_bf16(&p.tmQ, a.q, (uint64_t)HD, (uint64_t)a.n_q, (uint64_t)(a.B * a.S), HD * 2,
+                           (uint64_t)a.n_q * HD * 2, 64, (uint32_t)r, (uint32_t)tpt))
+    return -1;
+  // K/V: dims (hd, n_kv, kv_len, B), strides in bytes for dims 1..3
+  auto enc4 = [&](CUtensorMap* m, const void* base) -> bool {
+    const uint64_t dims[4] = {(uint64_t)HD, (uint64_t)a.n_kv, (uint64_t)kv_len, (uint64_t)a.B};
+    const uint64_t strides[3] = {(uint64_t)HD * 2, (uint64_t)a.n_kv * HD * 2, (uint64_t)a.cap * a.n_kv * HD * 2};
+    const uint32_t box[4] = {64, 1, 128, 1};
+    return encode_tmap_4d_bf16(m, base, dims, strides, box);
+  };
+  if (!enc4(&p.tmK, a.k) || !enc4(&p.tmV, a.v)) return -1;
+  p.o = static_cast<uint16_t*>(a.o);
+  p.B = (int)a.B; p.S = (int)a.S; p.n_q = (int)a.n_q; p.n_kv = (int)a.n_kv; p.hd = HD; p.r = r;
+  p.tokens_per_tile = tpt;
+  p.t_blocks = (int)((a.S + tpt - 1) / tpt);
+  p.pos0 = (int)a.pos0;
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.status = status;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  static bool attr_set[64] = {};
+  if (dev < 0 || dev >= 64) return -1;
+  if (!attr_set[dev]) {
+    if (cudaFuncSetAttribute(attn_tc_kernel<HD>, cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<HD>::TOTAL) !=
+        cudaSuccess)
+      return -1;
+    attr_set[dev] = true;
+  }
+  const int64_t grid = (int64_t)p.t_blocks * a.B * a.n_kv;
+  attn_tc_kernel<HD><<<(unsigned)grid, AT_THREADS, Smem<HD>::TOTAL, st>>>(p);
+  return 0;
+}
+
+}  // namespace
+
+bool attn_tc_supported(const AttnDesc& a) {
+  if (a.dtype != LLAMA_BF16 || (a.hd != 64 && a.hd != 128)) return false;
+  if (a.n_kv <= 0 || a.n_q % a.n_kv != 0) return false;
+  const int64_t r = a.n_q / a.n_kv;
+  if (r > 128 || 128 % r != 0) return false;
+  if (a.S < 16) return false;                         // one-token steps use the decode kernel
+  if (a.pos0 + a.S > ((int64_t)1 << 30) || a.B * a.S > ((int64_t)1 << 30)) return false;
+  const uintptr_t al = reinterpret_cast<uintptr_t>(a.q) | reinterpret_cast<uintptr_t>(a.k) |
+                       reinterpret_cast<uintptr_t>(a.v) | reinterpret_cast<uintptr_t>(a.o);
+  return (al & 15) == 0;
+}
+
+int launch_attn_tc(const AttnDesc& a, int, unsigned* status, cudaStream_t st) {
+  return a.hd == 128 ? launch_hd<128>(a, status, st) : launch_hd<64>(a, status, st);
+}
+
+}  // namespace llama

@@ -1,0 +1,149 @@
+// GEMM epilogues shared by the CUDA-core and tcgen05 GEMMs.
+//
+// RoPE ("Llama Architecture ...", Mathematical Foundations 3): the pair (x_2k, x_2k+1) of a
+// head turns by m*theta_k:  (x_2k c - x_2k+1 s,  x_2k s + x_2k+1 c),  c, s = cos, sin(m theta_k).
+// SwiGLU (same page, Mathematical Foundations 2): SiLU(g) * u with SiLU(z) = z / (1 + e^-z).
+#pragma once
+
+#include "kernels.h"
+
+namespace llama {
+
+__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
+
+// Store n consecutive values (c % n == 0 for vector paths) of row r into a [*, ld] matrix.
+template <int n>
+__device__ __forceinline__ void store_run(void* base, int is_f32, int64_t ld, int64_t r, int64_t c,
+                                          const float* v) {
+  if (is_f32) {
+    float* p = static_cast<float*>(base) + r * ld + c;
+    if constexpr (n % 4 == 0) {
+#pragma unroll
+      for (int i = 0; i < n; i += 4) *reinterpret_cast<float4*>(p + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < n; ++i) p[i] = v[i];
+    }
+  } else {
+    uint16_t* p = static_cast<uint16_t*>(base) + r * ld + c;
+    if constexpr (n % 8 == 0) {
+#pragma unroll
+      for (int i = 0; i < n; i += 8) {
+        uint4 w;
+        w.x = pack_bf2(v[i], v[i + 1]);
+        w.y = pack_bf2(v[i + 2], v[i + 3]);
+        w.z = pack_bf2(v[i + 4], v[i + 5]);
+        w.w = pack_bf2(v[i + 6], v[i + 7]);
+        *reinterpret_cast<uint4*>(p + i) = w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < n; ++i) p[i] = f2bf(v[i]);
+    }
+  }
+}
+
+template <int n>
+__device__ __forceinline__ void load_run(const void* base, int is_f32, int64_t ld, int64_t r, int64_t c,
+                                         float* v) {
+  if (is_f32) {
+    const float* p = static_cast<const float*>(base) + r * ld + c;
+    if constexpr (n % 4 == 0) {
+#pragma unroll
+      for (int i = 0; i < n; i += 4) {
+        float4 w = *reinterpret_cast<const float4*>(p + i);
+        v[i] = w.x; v[i + 1] = w.y; v[i + 2] = w.z; v[i + 3] = w.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < n; ++i) v[i] = p[i];
+    }
+  } else {
+    const uint16_t* p = static_cast<const uint16_t*>(base) + r * ld + c;
+    if constexpr (n % 8 == 0) {
+#pragma unroll
+      for (int i = 0; i < n; i += 8) {
+        uint4 w = *reinterpret_cast<const uint4*>(p + i);
+        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          v[i + 2 * j] = __uint_as_float(u[j] << 16);
+          v[i + 2 * j + 1] = __uint_as_float(u[j] & 0xFFFF0000u);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < n; ++i) v[i] = bf2f(p[i]);
+    }
+  }
+}
+
+// Rotate n/2 consecutive pairs starting at column c (c even) of a head-major row at position pos.
+template <int n>
+__device__ __forceinline__ void rope_run(const Epi& e, int64_t c_in_seg, float pos, float* v) {
+  static_assert(n % 2 == 0 || n == 1, "runs of pairs");
+  if constexpr (n == 1) return;   // a lone column never carries RoPE (head_dim is even)
+#pragma unroll
+  for (int i = 0; i + 1 < n; i += 2) {
+    const int k = (int)((c_in_seg + i) % e.hd) >> 1;
+    float s, co;
+    rope_sincos(pos, e.freq[k], s, co);
+    const float x0 = v[i], x1 = v[i + 1];
+    v[i] = x0 * co - x1 * s;
+    v[i + 1] = x0 * s + x1 * co;
+  }
+}
+
+// Apply the epilogue to n consecutive columns c .. c+n-1 of row r (n even; for EPI_QKV the run
+// lies inside one of the Q/K/V column ranges; for EPI_SWIGLU `v` holds gate values and `u` the
+// matching up values and c indexes the d_ff output).
+template <int n>
+__device__ __forceinline__ void epi_run(const Epi& e, int64_t r, int64_t c, float* v, const float* u) {
+  switch (e.kind) {
+    case EPI_STORE:
+      store_run<n>(e.out, e.out_f32, e.ldo, r, c, v);
+      break;
+    case EPI_RESID: {
+      float t[n];
+      load_run<n>(e.resid, e.resid_f32, e.ldr, r, c, t);
+#pragma unroll
+      for (int i = 0; i < n; ++i) v[i] += t[i];
+      store_run<n>(e.out, e.out_f32, e.ldo, r, c, v);
+      break;
+    }
+    case EPI_SWIGLU: {
+#pragma unroll
+      for (int i = 0; i < n; ++i) v[i] = silu_f(v[i]) * u[i];
+      store_run<n>(e.out, e.out_f32, e.ldo, r, c, v);
+      break;
+    }
+    case EPI_ATOMIC: {
+      float* p = static_cast<float*>(e.out) + r * e.ldo + c;
+#pragma unroll
+      for (int i = 0; i < n; ++i) atomicAdd(p + i, v[i]);
+      break;
+    }
+    case EPI_QKV: {
+      const int64_t s = r % e.S;
+      const float pos = (float)(e.pos0 + s);
+      if (c < e.nq_cols) {
+        rope_run<n>(e, c, pos, v);
+        store_run<n>(e.out, e.out_f32, e.nq_cols, r, c, v);
+      } else {
+        const int64_t krow = (r / e.S) * e.cap + e.pos0 + s;
+        if (c < e.nq_cols + e.nkv_cols) {
+          const int64_t cc = c - e.nq_cols;
+          rope_run<n>(e, cc, pos, v);
+          store_run<n>(e.k_out, e.out_f32, e.nkv_cols, krow, cc, v);
+        } else {
+          store_run<n>(e.v_out, e.out_f32, e.nkv_cols, krow, c - e.nq_cols - e.nkv_cols, v);
+        }
+      }
+      break;
+    }
+    default:
+      break;
+  }
+}
+
+}  // namespace llama

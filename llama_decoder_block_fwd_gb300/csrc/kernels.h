@@ -1,0 +1,87 @@
+// Internal interface between the C ABI (api.cu) and the kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "common.cuh"
+
+namespace llama {
+
+constexpr int kMaxRopePairs = 128;   // head_dim <= 256
+
+// What a GEMM does with its fp32 result D[r, c] (r < M, c < N).
+enum EpiKind : int {
+  EPI_STORE = 0,   // out[r, c] = D
+  EPI_RESID = 1,   // out[r, c] = resid[r, c] + D           (out may alias resid)
+  EPI_SWIGLU = 2,  // out[r, j] = SiLU(D_gate[r, j]) * D_up[r, j]; B = (gate, up)
+  EPI_QKV = 3,     // columns [0,nq) -> RoPE -> q; [nq, nq+nkv) -> RoPE -> k cache; rest -> v cache
+  EPI_ATOMIC = 4,  // out[r, c] += D  (fp32 out; partial sums of a split K range)
+};
+
+struct Epi {
+  int kind;
+  int out_f32;          // 1: out is float32, 0: bf16
+  void* out;            // STORE/RESID/SWIGLU/ATOMIC: [M, ldo]; QKV: q [M, nq_cols]
+  int64_t ldo;
+  const void* resid;
+  int resid_f32;
+  int64_t ldr;
+  // EPI_QKV: token r = b*S + s sits at position pos0 + s; its K/V row in the caches
+  // [B, cap, nkv_cols] is b*cap + pos0 + s.
+  void* k_out;
+  void* v_out;
+  int64_t nq_cols, nkv_cols;
+  int64_t S, cap, pos0;
+  int hd;
+  RopeFreq freq[kMaxRopePairs];
+};
+
+// D[M, N] = A[M, K] * B[N, K]^T with B the row-concatenation of nseg segments
+// (for EPI_SWIGLU: B[0] = W_gate, B[1] = W_up, N = 2 * d_ff, output width d_ff).
+struct GemmDesc {
+  int64_t M, N, K;
+  int dtype;            // LLAMA_F32 or LLAMA_BF16, for A and B
+  const void* A;
+  int64_t lda;          // elements
+  const void* B[3];
+  int64_t nB[3];        // rows of each segment
+  int nseg;
+  Epi epi;
+};
+
+struct AttnDesc {
+  int dtype;
+  const void* q;        // [B, S, n_q, hd]
+  const void* k;        // [B, cap, n_kv, hd]
+  const void* v;
+  void* o;              // [B, S, n_q, hd]
+  int64_t B, S, n_q, n_kv, hd, cap, pos0;
+  float scale;          // 1/sqrt(hd)
+};
+
+// rows x d RMSNorm; x_f32/y_f32 give the element types of x and y, g has type `dtype`.
+int launch_rmsnorm(int dtype, int x_f32, int y_f32, const void* x, const void* g, void* y, int64_t rows,
+                   int64_t d, float eps, cudaStream_t st);
+int launch_rope(int dtype, void* q, void* k, int64_t B, int64_t S, int64_t n_q, int64_t n_kv, int hd,
+                int64_t pos0, const RopeFreq* freq, cudaStream_t st);
+int launch_gemm_simt(const GemmDesc& g, cudaStream_t st);
+int launch_attn_simt(const AttnDesc& a, cudaStream_t st);
+int launch_widen_bf16(const void* src, float* dst, int64_t n, cudaStream_t st);
+
+// tensor-core paths (bf16 only)
+bool gemm_tc_supported(const GemmDesc& g);
+int launch_gemm_tc(const GemmDesc& g, int num_sms, unsigned* status, cudaStream_t st);
+bool attn_tc_supported(const AttnDesc& a);
+int launch_attn_tc(const AttnDesc& a, int num_sms, unsigned* status, cudaStream_t st);
+
+// tensor-map encoding (driver entry point resolved through the runtime)
+bool encode_tmap_2d_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+                         uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer);
+bool encode_tmap_4d_bf16(CUtensorMap* m, const void* base, const uint64_t* dims, const uint64_t* strides_bytes,
+                         const uint32_t* box);
+bool encode_tmap_3d_bf16(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                         uint64_t stride1_bytes, uint64_t stride2_bytes, uint32_t b0, uint32_t b1, uint32_t b2);
+
+}  // namespace llama

@@ -1,0 +1,381 @@
+// CUDA-core kernels: RMSNorm (the one used on every path), RoPE, and the generic GEMM and
+// attention used for float32 and for bf16 shapes the tcgen05 kernels do not take.
+#include <algorithm>
+
+#include "epilogue.cuh"
+#include "kernels.h"
+
+namespace llama {
+namespace {
+
+// ------------------------------------------------------------------------------------------
+// RMSNorm: y = x * rsqrt(mean(x^2) + eps) * g  ("Llama Architecture ...", Mathematical
+// Foundations 1 with eps inside the root as its Step 1 code has it; RMSNorm study note, "How
+// it works").  One warp per row, fp32 sum of squares, 128-bit loads; the row stays in
+// registers between the reduction and the scaling pass (CH 16-byte chunks per lane).
+// ------------------------------------------------------------------------------------------
+template <typename T> struct V16;
+template <> struct V16<float> {
+  static constexpr int N = 4;
+  static __device__ __forceinline__ void unpack(const uint4& w, float* f) {
+    f[0] = __uint_as_float(w.x); f[1] = __uint_as_float(w.y);
+    f[2] = __uint_as_float(w.z); f[3] = __uint_as_float(w.w);
+  }
+  static __device__ __forceinline__ uint4 pack(const float* f) {
+    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]), __float_as_uint(f[3]));
+  }
+};
+template <> struct V16<uint16_t> {
+  static constexpr int N = 8;
+  static __device__ __forceinline__ void unpack(const uint4& w, float* f) {
+    const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      f[2 * j] = __uint_as_float(u[j] << 16);
+      f[2 * j + 1] = __uint_as_float(u[j] & 0xFFFF0000u);
+    }
+  }
+  static __device__ __forceinline__ uint4 pack(const float* f) {
+    return make_uint4(pack_bf2(f[0], f[1]), pack_bf2(f[2], f[3]), pack_bf2(f[4], f[5]), pack_bf2(f[6], f[7]));
+  }
+};
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+template <typename T, int CH>
+__global__ void __launch_bounds__(256) rmsnorm_reg_kernel(const T* __restrict__ x, const T* __restrict__ g,
+                                                          T* __restrict__ y, int64_t rows, int d, float eps) {
+  constexpr int N = V16<T>::N;
+  const int lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const int nch = d / N;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + row * d);
+  uint4 buf[CH];
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < CH; ++i) {
+    const int c = lane + 32 * i;
+    if (c < nch) {
+      buf[i] = __ldcs(xr + c);   // streamed once: do not keep in L1
+      float f[N];
+      V16<T>::unpack(buf[i], f);
+#pragma unroll
+      for (int j = 0; j < N; ++j) ss = fmaf(f[j], f[j], ss);
+    }
+  }
+  ss = warp_sum(ss);
+  const float rs = rsqrtf(ss / (float)d + eps);
+  const uint4* gr = reinterpret_cast<const uint4*>(g);
+  uint4* yr = reinterpret_cast<uint4*>(y + row * d);
+#pragma unroll
+  for (int i = 0; i < CH; ++i) {
+    const int c = lane + 32 * i;
+    if (c < nch) {
+      float f[N], w[N];
+      V16<T>::unpack(buf[i], f);
+      V16<T>::unpack(__ldg(gr + c), w);
+#pragma unroll
+      for (int j = 0; j < N; ++j) f[j] = f[j] * rs * w[j];
+      __stcs(yr + c, V16<T>::pack(f));
+    }
+  }
+}
+
+// Any widths and any mix of x / y element types (the decode path normalises its fp32
+// residual stream into bf16).  Two passes over the row.
+template <typename TX, typename TG, typename TY>
+__global__ void __launch_bounds__(256) rmsnorm_generic_kernel(const TX* __restrict__ x, const TG* __restrict__ g,
+                                                              TY* __restrict__ y, int64_t rows, int64_t d,
+                                                              float eps) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  const TX* xr = x + row * d;
+  float ss = 0.f;
+  for (int64_t c = lane; c < d; c += 32) {
+    const float f = Elt<TX>::ld(xr + c);
+    ss = fmaf(f, f, ss);
+  }
+  ss = warp_sum(ss);
+  const float rs = rsqrtf(ss / (float)d + eps);
+  TY* yr = y + row * d;
+  for (int64_t c = lane; c < d; c += 32) Elt<TY>::st(yr + c, Elt<TX>::ld(xr + c) * rs * Elt<TG>::ld(g + c));
+}
+
+template <typename T>
+int rmsnorm_reg_dispatch(const T* x, const T* g, T* y, int64_t rows, int64_t d, float eps, cudaStream_t st) {
+  constexpr int N = V16<T>::N;
+  const int64_t nch = d / N;
+  const int64_t per_lane = (nch + 31) / 32;
+  const unsigned grid = (unsigned)((rows + 7) / 8);
+  if (per_lane <= 1) rmsnorm_reg_kernel<T, 1><<<grid, 256, 0, st>>>(x, g, y, rows, (int)d, eps);
+  else if (per_lane <= 2) rmsnorm_reg_kernel<T, 2><<<grid, 256, 0, st>>>(x, g, y, rows, (int)d, eps);
+  else if (per_lane <= 4) rmsnorm_reg_kernel<T, 4><<<grid, 256, 0, st>>>(x, g, y, rows, (int)d, eps);
+  else if (per_lane <= 8) rmsnorm_reg_kernel<T, 8><<<grid, 256, 0, st>>>(x, g, y, rows, (int)d, eps);
+  else if (per_lane <= 16) rmsnorm_reg_kernel<T, 16><<<grid, 256, 0, st>>>(x, g, y, rows, (int)d, eps);
+  else return -1;
+  return 0;
+}
+
+// ------------------------------------------------------------------------------------------
+// RoPE in place on q [B,S,n_q,hd] and k [B,S,n_kv,hd]; one thread per pair.
+// ------------------------------------------------------------------------------------------
+struct RopeParams {
+  void* q;
+  void* k;
+  int64_t B, S, n_q, n_kv, pos0;
+  int hd;
+  RopeFreq freq[kMaxRopePairs];
+};
+
+template <typename T>
+__global__ void rope_kernel(const __grid_constant__ RopeParams p) {
+  const int64_t half = p.hd / 2;
+  const int64_t nq_pairs = p.B * p.S * p.n_q * half;
+  const int64_t nk_pairs = p.B * p.S * p.n_kv * half;
+  const int64_t total = nq_pairs + (p.k ? nk_pairs : 0);
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    T* base;
+    int64_t idx, heads;
+    if (i < nq_pairs && p.q) { base = static_cast<T*>(p.q); idx = i; heads = p.n_q; }
+    else if (i >= nq_pairs) { base = static_cast<T*>(p.k); idx = i - nq_pairs; heads = p.n_kv; }
+    else continue;
+    const int kk = (int)(idx % half);
+    const int64_t token = idx / half / heads;
+    const float pos = (float)(p.pos0 + token % p.S);
+    float s, c;
+    rope_sincos(pos, p.freq[kk], s, c);
+    T* e = base + 2 * idx;
+    const float x0 = Elt<T>::ld(e), x1 = Elt<T>::ld(e + 1);
+    Elt<T>::st(e, x0 * c - x1 * s);
+    Elt<T>::st(e + 1, x0 * s + x1 * c);
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// Generic GEMM D = A B^T (fp32 accumulation), 64x64 tiles, 256 threads, 4x4 per thread.
+// ------------------------------------------------------------------------------------------
+constexpr int SB = 64, SK = 16;
+
+template <typename T>
+__device__ __forceinline__ const T* b_row(const GemmDesc& g, int64_t n) {
+  int64_t off = n;
+  for (int s = 0; s < g.nseg; ++s) {
+    if (off < g.nB[s]) return static_cast<const T*>(g.B[s]) + off * g.K;
+    off -= g.nB[s];
+  }
+  return nullptr;
+}
+
+template <typename T, bool SWIGLU>
+__global__ void __launch_bounds__(256) gemm_simt_kernel(const __grid_constant__ GemmDesc g) {
+  __shared__ float As[SK][SB];
+  __shared__ float Bs[SK][SB];
+  __shared__ float Us[SK][SB];
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const int64_t m0 = (int64_t)blockIdx.y * SB, n0 = (int64_t)blockIdx.x * SB;
+  const int64_t Nout = SWIGLU ? g.nB[0] : g.N;
+  float acc[4][4] = {}, accu[4][4] = {};
+  const T* A = static_cast<const T*>(g.A);
+  for (int64_t k0 = 0; k0 < g.K; k0 += SK) {
+    for (int i = threadIdx.x; i < SB * SK; i += 256) {
+      const int mm = i / SK, kk = i % SK;
+      const int64_t r = m0 + mm, k = k0 + kk;
+      As[kk][mm] = (r < g.M && k < g.K) ? Elt<T>::ld(A + r * g.lda + k) : 0.f;
+      const int64_t n = n0 + mm;
+      float bv = 0.f, uv = 0.f;
+      if (n < Nout && k < g.K) {
+        if (SWIGLU) {
+          bv = Elt<T>::ld(static_cast<const T*>(g.B[0]) + n * g.K + k);
+          uv = Elt<T>::ld(static_cast<const T*>(g.B[1]) + n * g.K + k);
+        } else {
+          bv = Elt<T>::ld(b_row<T>(g, n) + k);
+        }
+      }
+      Bs[kk][mm] = bv;
+      if (SWIGLU) Us[kk][mm] = uv;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < SK; ++kk) {
+      float a[4], b[4], u[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) { a[i] = As[kk][ty * 4 + i]; b[i] = Bs[kk][tx * 4 + i]; if (SWIGLU) u[i] = Us[kk][tx * 4 + i]; }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+          if (SWIGLU) accu[i][j] = fmaf(a[i], u[j], accu[i][j]);
+        }
+    }
+    __syncthreads();
+  }
+  for (int i = 0; i < 4; ++i) {
+    const int64_t r = m0 + ty * 4 + i;
+    if (r >= g.M) continue;
+    for (int j = 0; j < 4; j += 2) {
+      const int64_t c = n0 + tx * 4 + j;
+      if (c + 1 < Nout) {
+        float v[2] = {acc[i][j], acc[i][j + 1]};
+        float u[2] = {accu[i][j], accu[i][j + 1]};
+        epi_run<2>(g.epi, r, c, v, u);
+      } else if (c < Nout) {     // odd tail column (no RoPE pair can straddle: hd is even)
+        float v[1] = {acc[i][j]};
+        float u[1] = {accu[i][j]};
+        epi_run<1>(g.epi, r, c, v, u);
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// Generic causal GQA attention: one warp per (b, s, h) query row, 32 keys per step (one per
+// lane), online softmax (running max and sum), output dims split across lanes.
+// ------------------------------------------------------------------------------------------
+__global__ void widen_bf16_kernel(const uint16_t* __restrict__ src, float* __restrict__ dst, int64_t n) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+    dst[i] = bf2f(src[i]);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(128) attn_simt_kernel(const __grid_constant__ AttnDesc a) {
+  extern __shared__ float qs[];                       // [4 warps][hd]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * 4 + warp;  // (b*S + s)*n_q + h
+  const int64_t rows = a.B * a.S * a.n_q;
+  if (row >= rows) return;
+  const int hd = (int)a.hd;
+  const int64_t h = row % a.n_q, bs = row / a.n_q, s = bs % a.S, b = bs / a.S;
+  const int64_t grp = h / (a.n_q / a.n_kv);
+  const int64_t pos = a.pos0 + s;
+  float* q = qs + warp * hd;
+  const T* qrow = static_cast<const T*>(a.q) + row * hd;
+  for (int i = lane; i < hd; i += 32) q[i] = Elt<T>::ld(qrow + i) * a.scale;
+  __syncwarp();
+  const T* K = static_cast<const T*>(a.k) + (b * a.cap * a.n_kv + grp) * hd;
+  const T* V = static_cast<const T*>(a.v) + (b * a.cap * a.n_kv + grp) * hd;
+  const int64_t kstride = a.n_kv * hd;
+  float m = -INFINITY, l = 0.f;
+  float o[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // dims lane + 32*i
+  for (int64_t j0 = 0; j0 <= pos; j0 += 32) {
+    const int64_t j = j0 + lane;
+    float sc = -INFINITY;
+    if (j <= pos) {
+      const T* kr = K + j * kstride;
+      float acc = 0.f;
+      for (int t = 0; t < hd; ++t) acc = fmaf(q[t], Elt<T>::ld(kr + t), acc);
+      sc = acc;
+    }
+    const float mnew = fmaxf(m, warp_max(sc));
+    const float alpha = __expf(m - mnew);             // m = -inf on the first block -> 0
+    const float p = (j <= pos) ? expf(sc - mnew) : 0.f;
+    l = l * alpha + warp_sum(p);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o[i] *= alpha;
+    const int nk = (pos + 1 - j0) < 32 ? (int)(pos + 1 - j0) : 32;
+    for (int jj = 0; jj < nk; ++jj) {
+      const float pj = __shfl_sync(0xffffffffu, p, jj);
+      const T* vr = V + (j0 + jj) * kstride;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int t = lane + 32 * i;
+        if (t < hd) o[i] = fmaf(pj, Elt<T>::ld(vr + t), o[i]);
+      }
+    }
+    m = mnew;
+  }
+  const float inv = 1.f / l;
+  T* orow = static_cast<T*>(a.o) + row * hd;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int t = lane + 32 * i;
+    if (t < hd) Elt<T>::st(orow + t, o[i] * inv);
+  }
+}
+
+}  // namespace
+
+int launch_rmsnorm(int dtype, int x_f32, int y_f32, const void* x, const void* g, void* y, int64_t rows,
+                   int64_t d, float eps, cudaStream_t st) {
+  if (rows <= 0) return 0;
+  const unsigned grid = (unsigned)((rows + 7) / 8);
+  const bool aligned = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(g) |
+                         reinterpret_cast<uintptr_t>(y)) & 15) == 0;
+  if (dtype == LLAMA_BF16 && !x_f32 && !y_f32) {
+    if (aligned && d % 8 == 0 && d <= 8 * 32 * 16 &&
+        rmsnorm_reg_dispatch<uint16_t>((const uint16_t*)x, (const uint16_t*)g, (uint16_t*)y, rows, d, eps, st) == 0)
+      return 0;
+    rmsnorm_generic_kernel<uint16_t, uint16_t, uint16_t><<<grid, 256, 0, st>>>(
+        (const uint16_t*)x, (const uint16_t*)g, (uint16_t*)y, rows, d, eps);
+  } else if (dtype == LLAMA_F32) {
+    if (aligned && d % 4 == 0 && d <= 4 * 32 * 16 &&
+        rmsnorm_reg_dispatch<float>((const float*)x, (const float*)g, (float*)y, rows, d, eps, st) == 0)
+      return 0;
+    rmsnorm_generic_kernel<float, float, float><<<grid, 256, 0, st>>>((const float*)x, (const float*)g, (float*)y,
+                                                                      rows, d, eps);
+  } else if (x_f32 && !y_f32) {   // bf16 call, fp32 residual stream in, bf16 out
+    rmsnorm_generic_kernel<float, uint16_t, uint16_t><<<grid, 256, 0, st>>>(
+        (const float*)x, (const uint16_t*)g, (uint16_t*)y, rows, d, eps);
+  } else {
+    return -1;
+  }
+  return 0;
+}
+
+int launch_rope(int dtype, void* q, void* k, int64_t B, int64_t S, int64_t n_q, int64_t n_kv, int hd, int64_t pos0,
+                const RopeFreq* freq, cudaStream_t st) {
+  RopeParams p;
+  p.q = q; p.k = k; p.B = B; p.S = S; p.n_q = n_q; p.n_kv = n_kv; p.pos0 = pos0; p.hd = hd;
+  for (int i = 0; i < hd / 2; ++i) p.freq[i] = freq[i];
+  const int64_t total = B * S * (n_q + n_kv) * (hd / 2);
+  if (total <= 0) return 0;
+  const unsigned grid = (unsigned)std::min<int64_t>((total + 255) / 256, 152 * 32);
+  if (dtype == LLAMA_F32) rope_kernel<float><<<grid, 256, 0, st>>>(p);
+  else rope_kernel<uint16_t><<<grid, 256, 0, st>>>(p);
+  return 0;
+}
+
+int launch_gemm_simt(const GemmDesc& g, cudaStream_t st) {
+  const int64_t nout = g.epi.kind == EPI_SWIGLU ? g.nB[0] : g.N;
+  if (g.M <= 0 || nout <= 0) return 0;
+  dim3 grid((unsigned)((nout + SB - 1) / SB), (unsigned)((g.M + SB - 1) / SB));
+  const bool sw = g.epi.kind == EPI_SWIGLU;
+  if (g.dtype == LLAMA_F32) {
+    if (sw) gemm_simt_kernel<float, true><<<grid, 256, 0, st>>>(g);
+    else gemm_simt_kernel<float, false><<<grid, 256, 0, st>>>(g);
+  } else {
+    if (sw) gemm_simt_kernel<uint16_t, true><<<grid, 256, 0, st>>>(g);
+    else gemm_simt_kernel<uint16_t, false><<<grid, 256, 0, st>>>(g);
+  }
+  return 0;
+}
+
+int launch_widen_bf16(const void* src, float* dst, int64_t n, cudaStream_t st) {
+  if (n <= 0) return 0;
+  const unsigned grid = (unsigned)std::min<int64_t>((n + 255) / 256, 152 * 16);
+  widen_bf16_kernel<<<grid, 256, 0, st>>>(static_cast<const uint16_t*>(src), dst, n);
+  return 0;
+}
+
+int launch_attn_simt(const AttnDesc& a, cudaStream_t st) {
+  const int64_t rows = a.B * a.S * a.n_q;
+  if (rows <= 0) return 0;
+  const unsigned grid = (unsigned)((rows + 3) / 4);
+  const size_t smem = 4 * a.hd * sizeof(float);
+  if (a.dtype == LLAMA_F32) attn_simt_kernel<float><<<grid, 128, smem, st>>>(a);
+  else attn_simt_kernel<uint16_t><<<grid, 128, smem, st>>>(a);
+  return 0;
+}
+
+}  // namespace llama

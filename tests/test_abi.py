@@ -1,0 +1,95 @@
+"""The C ABI on the host: the library loads, exports every declared symbol, and rejects bad
+arguments with status codes before touching the GPU.  No compute call is made here."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import llama_decoder_block_fwd_gb300 as L
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(llama_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = L.lib()
+    names = declared_functions()
+    assert "llama_block_forward" in names and "llama_stack_decode_step" in names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings():
+    for code in range(7):
+        assert L.llama_status_string(code) != "unknown status"
+    assert L.llama_status_string(99) == "unknown status"
+
+
+def _dims(**kw):
+    base = dict(B=1, S=4, d_model=16, n_q=8, n_kv=2, head_dim=2, d_ff=48, theta_base=1e4, eps=1e-5)
+    base.update(kw)
+    return L.dims_of(**base)
+
+
+def test_rejects_bad_arguments_without_launching():
+    lib = L.lib()
+    d = _dims()
+    fake = 0x10000  # aligned, never dereferenced: validation fails before any launch
+    # null pointers
+    assert lib.llama_rmsnorm(ctypes.byref(d), L.F32, None, fake, fake, None) == 1
+    # bad dtype
+    assert lib.llama_rmsnorm(ctypes.byref(d), 7, fake, fake, fake, None) == 2
+    # misaligned
+    assert lib.llama_rmsnorm(ctypes.byref(d), L.F32, fake + 4, fake, fake, None) == 3
+    # n_q not a multiple of n_kv
+    bad = _dims(n_kv=3)
+    assert lib.llama_rope(ctypes.byref(bad), L.F32, fake, fake, 0, None) == 1
+    # odd head_dim
+    assert lib.llama_rope(ctypes.byref(_dims(head_dim=3)), L.F32, fake, fake, 0, None) == 1
+    # negative sizes
+    assert lib.llama_rmsnorm(ctypes.byref(_dims(B=-1)), L.F32, fake, fake, fake, None) == 1
+    # attention past the cache capacity
+    assert lib.llama_gqa_attention(ctypes.byref(d), L.F32, fake, fake, fake, 3, 0, fake, None, 0, None) == 1
+    # workspace missing / too small
+    assert lib.llama_swiglu_ffn(ctypes.byref(d), L.F32, fake, fake, fake, fake, fake + 256, None, 0, None) == 4
+    need = L.llama_workspace_bytes(L.OP_SWIGLU_FFN, d, L.F32)
+    assert need >= 4 * 48 * 4
+    assert lib.llama_swiglu_ffn(ctypes.byref(d), L.F32, fake, fake, fake, fake, fake + 256, fake, need - 1, None) == 4
+    # aliasing input and output
+    assert lib.llama_swiglu_ffn(ctypes.byref(d), L.F32, fake, fake, fake, fake, fake, fake, need, None) == 1
+    # decode needs S == 1
+    w = (L.BlockWeights * 1)(L.BlockWeights(*[fake] * 9))
+    assert lib.llama_stack_decode_step(ctypes.byref(d), L.F32, 1, w, fake, fake, 10, fake, fake, fake, 8, 4, fake,
+                                       fake, 1 << 20, None) == 1
+    # block with pos0 > 0 but no cache
+    bw = L.BlockWeights(*[fake] * 9)
+    assert lib.llama_block_forward(ctypes.byref(d), L.F32, ctypes.byref(bw), fake, fake + 256, 2, None, None, 0,
+                                   fake, 1 << 20, None) == 1
+    # one cache only
+    assert lib.llama_block_forward(ctypes.byref(d), L.F32, ctypes.byref(bw), fake, fake + 256, 0, fake, None, 8,
+                                   fake, 1 << 20, None) == 1
+
+
+def test_empty_inputs_are_no_ops():
+    lib = L.lib()
+    d = _dims(B=0)
+    assert lib.llama_rmsnorm(ctypes.byref(d), L.F32, None, None, None, None) == 0
+    assert lib.llama_rope(ctypes.byref(_dims(S=0)), L.BF16, None, None, 0, None) == 0
+
+
+def test_workspace_sizes_grow_with_shape():
+    small = L.llama_workspace_bytes(L.OP_BLOCK_FORWARD, _dims(), L.BF16)
+    big = L.llama_workspace_bytes(L.OP_BLOCK_FORWARD, _dims(S=400), L.BF16)
+    assert 0 < small < big
+    assert L.llama_workspace_bytes(L.OP_STACK_DECODE_STEP, _dims(B=64, S=1), L.BF16) > 0
+    assert L.llama_workspace_bytes(L.OP_RMSNORM, _dims(), L.BF16) == 0

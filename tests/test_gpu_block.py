@@ -1,0 +1,102 @@
+"""GPU vs oracle parity for llama_block_forward (prefill, and chunked prefill on a cache).
+
+The toy and small blocks are checked in full; the Llama-3-8B (B1 S8192) and LLaMA-7B MHA
+(B4 S2048) blocks are checked on 64 rows of every sequence spread over [0, S), including the
+first and last token (the oracle computes K/V for every token and the rest for those rows).
+"""
+import numpy as np
+import pytest
+
+import llama_decoder_block_fwd_gb300 as L
+import oracle as O
+from synth import configs as C
+from synth import workloads as W
+from tests.helpers import assert_parity, assert_sublayer_parity, oracle_dims, sample_rows, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+def _run_block(wl, x, w, pos0=0, kc=None, vc=None, cap=0):
+    import torch
+    y = torch.empty_like(x)
+    dims = wl.dims
+    ws = torch.empty(L.llama_workspace_bytes(L.OP_BLOCK_FORWARD, dims, wl.dtype), dtype=torch.uint8, device="cuda")
+    L.llama_block_forward(dims, wl.dtype, w, x, y, pos0, kc, vc, cap, ws)
+    torch.cuda.synchronize()
+    assert L.llama_get_device_status() == 0
+    return y
+
+
+def _check(wl, y, rows=None):
+    hw = O.BlockWeights(**W.host_layer(wl))
+    d1 = oracle_dims(wl, B=1)
+    for b in range(wl.B):
+        xb = W.host_x(wl, b)[None]
+        ref, _, _ = O.block_forward(xb, hw, d1, rows=rows)
+        got = to_f64(y[b] if rows is None else y[b][rows])
+        assert_parity(got, ref[0], wl.dtype, f"{wl.name} seq {b} y")
+        xs = xb[0] if rows is None else xb[0][rows]
+        assert_sublayer_parity(got, ref[0], xs, wl.dtype, f"{wl.name} seq {b} y-x")
+
+
+@pytest.mark.parametrize("wl", [C.TOY, C.SMALL], ids=lambda w: w.name)
+def test_block_full(wl):
+    x = W.device_x(wl).reshape(wl.B * wl.S, wl.d_model)
+    y = _run_block(wl, x, W.device_layer(wl)).reshape(wl.B, wl.S, wl.d_model)
+    _check(wl, y)
+
+
+@pytest.mark.parametrize("wl", [C.LLAMA3_8B_PREFILL, C.LLAMA_7B_MHA_PREFILL], ids=lambda w: w.name)
+def test_block_full_size_sampled_rows(wl):
+    x = W.device_x(wl).reshape(wl.B * wl.S, wl.d_model)
+    y = _run_block(wl, x, W.device_layer(wl)).reshape(wl.B, wl.S, wl.d_model)
+    if wl.B > 2:   # bound the oracle's time: first and last sequence
+        seqs = [0, wl.B - 1]
+    else:
+        seqs = list(range(wl.B))
+    rows = sample_rows(wl.S)
+    hw = O.BlockWeights(**W.host_layer(wl))
+    d1 = oracle_dims(wl, B=1)
+    for b in seqs:
+        xb = W.host_x(wl, b)[None]
+        ref, _, _ = O.block_forward(xb, hw, d1, rows=rows)
+        got = to_f64(y[b][rows])
+        assert_parity(got, ref[0], wl.dtype, f"{wl.name} seq {b}")
+        assert_sublayer_parity(got, ref[0], xb[0][rows], wl.dtype, f"{wl.name} seq {b} y-x")
+
+
+def test_block_chunked_prefill_against_cache():
+    """A 3-chunk prefill (pos0 = 0, 100, 229) through the cache equals one 300-token prefill."""
+    import torch
+    wl = C.Workload("small-ragged", 5, C.BF16, 2, 300, 512, 8, 2, 64, 1280, 1e4, 1e-5, gain_std=0.1)
+    w = W.device_layer(wl)
+    x = W.device_x(wl)                                    # [B, 300, d]
+    cap = 320
+    kc = torch.zeros((wl.B, cap, wl.n_kv, wl.head_dim), dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    ys = []
+    for p0, p1 in ((0, 100), (100, 229), (229, 300)):
+        wc = C.Workload(wl.name, wl.index, wl.dtype, wl.B, p1 - p0, wl.d_model, wl.n_q, wl.n_kv, wl.head_dim,
+                        wl.d_ff, wl.theta_base, wl.eps, gain_std=wl.gain_std)
+        xc = x[:, p0:p1].contiguous().reshape(-1, wl.d_model)
+        ys.append(_run_block(wc, xc, w, p0, kc, vc, cap).reshape(wl.B, p1 - p0, wl.d_model))
+    y = torch.cat(ys, dim=1)
+    hw = O.BlockWeights(**W.host_layer(wl))
+    for b in range(wl.B):
+        ref, kr, vr = O.block_forward(W.host_x(wl, b)[None], hw, oracle_dims(wl, B=1))
+        assert_parity(to_f64(y[b]), ref[0], wl.dtype, f"chunked seq {b}")
+        assert_parity(to_f64(kc[b, :300]), kr[0], wl.dtype, f"k cache seq {b}")
+        assert_parity(to_f64(vc[b, :300]), vr[0], wl.dtype, f"v cache seq {b}")
+    assert float(kc[:, 300:].abs().max()) == 0.0        # nothing written past the last token
+
+
+def test_block_identity_zero_sublayers():
+    """W_O = 0 and W_down = 0 leave the input unchanged (the residual paths)."""
+    import torch
+    wl = C.SMALL
+    w = W.device_layer(wl)
+    w["wo"].zero_()
+    w["w_down"].zero_()
+    x = W.device_x(wl).reshape(-1, wl.d_model)
+    y = _run_block(wl, x, w)
+    assert torch.equal(y, x)
