@@ -201,6 +201,14 @@ int run_gemm(const GemmDesc& g, const char* role, cudaStream_t st) {
 }
 
 int run_attention(const AttnDesc& a, cudaStream_t st) {
+  if (decode_attn_supported(a) && a.ws && a.ws_bytes >= decode_attn_ws_bytes(a)) {
+    unsigned* status = status_ptr();
+    if (!status) return LLAMA_ERR_CUDA;
+    prof::begin("attn_decode_tc", st);
+    if (launch_decode_attn(a, a.ws, num_sms(), status, st) != 0) return LLAMA_ERR_CUDA;
+    prof::end(st);
+    return launch_status();
+  }
   const bool tc = attn_tc_supported(a);
   prof::begin(tc ? "attn_tc" : "attn_simt", st);
   if (tc) {
@@ -215,9 +223,9 @@ int run_attention(const AttnDesc& a, cudaStream_t st) {
 }
 
 int run_rmsnorm(int dtype, int x_f32, int y_f32, const void* x, const void* g, void* y, int64_t rows, int64_t d,
-                float eps, cudaStream_t st) {
+                float eps, cudaStream_t st, float* rs_out = nullptr) {
   prof::begin("rmsnorm", st);
-  if (launch_rmsnorm(dtype, x_f32, y_f32, x, g, y, rows, d, eps, st) != 0) return LLAMA_ERR_UNSUPPORTED;
+  if (launch_rmsnorm(dtype, x_f32, y_f32, x, g, y, rs_out, rows, d, eps, st) != 0) return LLAMA_ERR_UNSUPPORTED;
   prof::end(st);
   return launch_status();
 }
@@ -255,12 +263,26 @@ struct Carver {
   }
 };
 
+// Scratch the attention call needs when a one-token step runs on the split-K decode kernel,
+// sized for a cache of kv_capacity positions.
+size_t attn_scratch_bytes(const llama_dims* d, int dtype, int64_t kv_capacity) {
+  if (d->S != 1 || kv_capacity < 1) return 0;
+  AttnDesc a;
+  memset(&a, 0, sizeof(a));
+  a.dtype = dtype; a.B = d->B; a.S = 1; a.n_q = d->n_q; a.n_kv = d->n_kv; a.hd = d->head_dim;
+  a.pos0 = kv_capacity - 1;
+  return (dtype == LLAMA_BF16 && d->head_dim == 128) ? decode_attn_ws_bytes(a) : 0;
+}
+
 struct BlockWs {
   void *u, *q, *o, *h, *m, *k, *v;
+  float *rs1, *rs2;   // per-row RMSNorm factors of the attention and FFN norms
+  void* attn;         // split-K attention scratch (one-token steps)
+  size_t attn_bytes;
   size_t bytes;
 };
 
-BlockWs plan_block(const llama_dims* d, int dtype, bool own_kv, void* base) {
+BlockWs plan_block(const llama_dims* d, int dtype, bool own_kv, void* base, int64_t kv_capacity = 0) {
   const size_t es = esize(dtype);
   const size_t T = (size_t)(d->B * d->S);
   Carver c{static_cast<char*>(base)};
@@ -272,16 +294,23 @@ BlockWs plan_block(const llama_dims* d, int dtype, bool own_kv, void* base) {
   w.m = c.take(T * d->d_ff * es);
   w.k = own_kv ? c.take(T * d->n_kv * d->head_dim * es) : nullptr;
   w.v = own_kv ? c.take(T * d->n_kv * d->head_dim * es) : nullptr;
+  w.rs1 = static_cast<float*>(c.take(T * 4));
+  w.rs2 = static_cast<float*>(c.take(T * 4));
+  w.attn_bytes = attn_scratch_bytes(d, dtype, own_kv ? d->S : kv_capacity);
+  w.attn = w.attn_bytes ? c.take(w.attn_bytes) : nullptr;
   w.bytes = c.off;
   return w;
 }
 
 struct DecodeWs {
   void *xres, *u, *q, *o, *m;
+  float *rs1, *rs2;
+  void* attn;
+  size_t attn_bytes;
   size_t bytes;
 };
 
-DecodeWs plan_decode(const llama_dims* d, int dtype, void* base) {
+DecodeWs plan_decode(const llama_dims* d, int dtype, void* base, int64_t kv_capacity) {
   const size_t es = esize(dtype);
   const size_t T = (size_t)d->B;
   Carver c{static_cast<char*>(base)};
@@ -291,13 +320,17 @@ DecodeWs plan_decode(const llama_dims* d, int dtype, void* base) {
   w.q = c.take(T * d->n_q * d->head_dim * es);
   w.o = c.take(T * d->n_q * d->head_dim * es);
   w.m = c.take(T * d->d_ff * es);
+  w.rs1 = static_cast<float*>(c.take(T * 4));
+  w.rs2 = static_cast<float*>(c.take(T * 4));
+  w.attn_bytes = attn_scratch_bytes(d, dtype, kv_capacity);
+  w.attn = w.attn_bytes ? c.take(w.attn_bytes) : nullptr;
   w.bytes = c.off;
   return w;
 }
 
 // The Q/K/V projection with RoPE on Q and K and the K/V write into [B, cap, n_kv*hd] caches.
-int run_qkv(const llama_dims* d, int dtype, const llama_block_weights* w, const void* u, void* q, void* kc,
-            void* vc, int64_t cap, int64_t pos0, cudaStream_t st) {
+int run_qkv(const llama_dims* d, int dtype, const llama_block_weights* w, const void* u, const float* row_scale,
+            void* q, void* kc, void* vc, int64_t cap, int64_t pos0, cudaStream_t st) {
   const int64_t T = d->B * d->S, hq = d->n_q * d->head_dim, hkv = d->n_kv * d->head_dim;
   GemmDesc g = make_gemm(dtype, T, u, d->d_model);
   g.nseg = 3;
@@ -314,6 +347,7 @@ int run_qkv(const llama_dims* d, int dtype, const llama_block_weights* w, const 
   g.epi.cap = cap;
   g.epi.pos0 = pos0;
   g.epi.hd = (int)d->head_dim;
+  g.epi.row_scale = row_scale;
   rope_freqs(d, g.epi.freq);
   return run_gemm(g, nullptr, st);
 }
@@ -333,13 +367,14 @@ int run_linear_resid(int dtype, int64_t M, const void* A, int64_t K, const void*
 }
 
 int run_gate_up(int dtype, int64_t M, const void* A, int64_t K, const void* wg, const void* wu, int64_t dff,
-                void* m, cudaStream_t st) {
+                void* m, cudaStream_t st, const float* row_scale = nullptr) {
   GemmDesc g = make_gemm(dtype, M, A, K);
   g.nseg = 2;
   g.B[0] = wg; g.nB[0] = dff;
   g.B[1] = wu; g.nB[1] = dff;
   g.N = 2 * dff;
   g.epi = make_epi(EPI_SWIGLU, dtype == LLAMA_F32, m, dff);
+  g.epi.row_scale = row_scale;
   return run_gemm(g, nullptr, st);
 }
 
@@ -378,20 +413,24 @@ int block_body(const llama_dims* d, int dtype, const llama_block_weights* w, con
   const int f32 = dtype == LLAMA_F32;
   const float eps = (float)d->eps;
   int rc;
-  // u = RMSNorm(x; g_attn)
-  if ((rc = run_rmsnorm(dtype, x_f32 || f32, f32, x, w->attn_norm_g, ws.u, T, D, eps, st)) != LLAMA_OK) return rc;
+  // RMSNorm(x; g_attn) = rs1 * (x * g_attn): the GEMM takes a = x * g_attn (exact in bf16 when the
+  // gain is one) and multiplies its fp32 accumulator by rs1[row] before RoPE.
+  if ((rc = run_rmsnorm(dtype, x_f32 || f32, f32, x, w->attn_norm_g, ws.u, T, D, eps, st, ws.rs1)) != LLAMA_OK)
+    return rc;
   // q, k, v with RoPE; k, v written into the cache at pos0..pos0+S-1
-  if ((rc = run_qkv(d, dtype, w, ws.u, ws.q, kc, vc, cap, pos0, st)) != LLAMA_OK) return rc;
+  if ((rc = run_qkv(d, dtype, w, ws.u, ws.rs1, ws.q, kc, vc, cap, pos0, st)) != LLAMA_OK) return rc;
   // o = causal GQA attention
   AttnDesc a = make_attn(d, dtype, ws.q, kc, vc, ws.o, cap, pos0);
+  a.ws = ws.attn;
+  a.ws_bytes = ws.attn_bytes;
   if ((rc = run_attention(a, st)) != LLAMA_OK) return rc;
   // h = x + o W_O^T, kept in fp32 (decode: the fp32 stream is updated in place)
   void* h = x_f32 ? y : ws.h;
   if ((rc = run_linear_resid(dtype, T, ws.o, hq, w->wo, D, x, x_f32 || f32, h, 1, st)) != LLAMA_OK) return rc;
-  // w = RMSNorm(h; g_ffn)  (reuses u)
-  if ((rc = run_rmsnorm(dtype, 1, f32, h, w->ffn_norm_g, ws.u, T, D, eps, st)) != LLAMA_OK) return rc;
+  // RMSNorm(h; g_ffn) in the same split form (reuses u), applied inside the gate/up GEMM
+  if ((rc = run_rmsnorm(dtype, 1, f32, h, w->ffn_norm_g, ws.u, T, D, eps, st, ws.rs2)) != LLAMA_OK) return rc;
   // m = SiLU(w W_gate^T) * (w W_up^T)
-  if ((rc = run_gate_up(dtype, T, ws.u, D, w->w_gate, w->w_up, d->d_ff, ws.m, st)) != LLAMA_OK) return rc;
+  if ((rc = run_gate_up(dtype, T, ws.u, D, w->w_gate, w->w_up, d->d_ff, ws.m, st, ws.rs2)) != LLAMA_OK) return rc;
   // y = h + m W_down^T
   return run_linear_resid(dtype, T, ws.m, d->d_ff, w->w_down, D, h, 1, y, x_f32 || f32, st);
 }
@@ -463,13 +502,14 @@ int llama_get_device_status(int* out, void* stream) {
 
 size_t llama_workspace_bytes(int op, const llama_dims* d, int dtype, int n_layers, int64_t vocab,
                              int64_t kv_capacity) {
-  (void)n_layers; (void)vocab; (void)kv_capacity;
+  (void)n_layers; (void)vocab;
   if (!d || check_dtype(dtype) != LLAMA_OK) return 0;
   const size_t es = esize(dtype);
   switch (op) {
     case LLAMA_OP_SWIGLU_FFN: return round256((size_t)(d->B * d->S * d->d_ff) * es);
-    case LLAMA_OP_BLOCK_FORWARD: return plan_block(d, dtype, true, nullptr).bytes;
-    case LLAMA_OP_STACK_DECODE_STEP: return plan_decode(d, dtype, nullptr).bytes;
+    case LLAMA_OP_GQA_ATTENTION: return attn_scratch_bytes(d, dtype, kv_capacity);
+    case LLAMA_OP_BLOCK_FORWARD: return plan_block(d, dtype, kv_capacity <= 0, nullptr, kv_capacity).bytes;
+    case LLAMA_OP_STACK_DECODE_STEP: return plan_decode(d, dtype, nullptr, kv_capacity).bytes;
     default: return 0;
   }
 }
@@ -503,7 +543,6 @@ int llama_rope(const llama_dims* d, int dtype, void* q, void* k, int64_t pos0, v
 
 int llama_gqa_attention(const llama_dims* d, int dtype, const void* q, const void* k, const void* v,
                         int64_t kv_capacity, int64_t pos0, void* o, void* ws, size_t ws_bytes, void* stream) {
-  (void)ws; (void)ws_bytes;
   int rc;
   if ((rc = check_dtype(dtype)) != LLAMA_OK) return rc;
   if ((rc = check_dims(d, NEED_HEADS)) != LLAMA_OK) return rc;
@@ -511,7 +550,11 @@ int llama_gqa_attention(const llama_dims* d, int dtype, const void* q, const voi
   if (d->B * d->S == 0) return LLAMA_OK;
   if (!q || !k || !v || !o) return LLAMA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o)) return LLAMA_ERR_ALIGNMENT;
+  if (ws_bytes > 0 && (!ws || !aligned16(ws))) return ws ? LLAMA_ERR_ALIGNMENT : LLAMA_ERR_WORKSPACE;
+  if (ws_bytes < attn_scratch_bytes(d, dtype, pos0 + d->S)) return LLAMA_ERR_WORKSPACE;
   AttnDesc a = make_attn(d, dtype, q, k, v, o, kv_capacity, pos0);
+  a.ws = ws;
+  a.ws_bytes = ws_bytes;
   return run_attention(a, static_cast<cudaStream_t>(stream));
 }
 
@@ -551,10 +594,10 @@ int llama_block_forward(const llama_dims* d, int dtype, const llama_block_weight
   if (!aligned16(x) || !aligned16(y) || !block_weights_aligned(w) || (k_cache && !aligned16(k_cache)) ||
       (v_cache && !aligned16(v_cache)))
     return LLAMA_ERR_ALIGNMENT;
-  const size_t need = plan_block(d, dtype, own_kv, nullptr).bytes;
+  const size_t need = plan_block(d, dtype, own_kv, nullptr, cache_capacity).bytes;
   if (!ws || ws_bytes < need) return LLAMA_ERR_WORKSPACE;
   if (!aligned16(ws)) return LLAMA_ERR_ALIGNMENT;
-  BlockWs b = plan_block(d, dtype, own_kv, ws);
+  BlockWs b = plan_block(d, dtype, own_kv, ws, cache_capacity);
   void* kc = own_kv ? b.k : k_cache;
   void* vc = own_kv ? b.v : v_cache;
   return block_body(d, dtype, w, x, 0, y, pos0, kc, vc, cache_capacity, b, static_cast<cudaStream_t>(stream));
@@ -579,11 +622,11 @@ int llama_stack_decode_step(const llama_dims* d, int dtype, int n_layers, const 
   if (!aligned16(final_g) || !aligned16(w_lm) || !aligned16(x_emb) || !aligned16(k_cache) || !aligned16(v_cache) ||
       !aligned16(logits))
     return LLAMA_ERR_ALIGNMENT;
-  const size_t need = plan_decode(d, dtype, nullptr).bytes;
+  const size_t need = plan_decode(d, dtype, nullptr, cache_capacity).bytes;
   if (!ws || ws_bytes < need) return LLAMA_ERR_WORKSPACE;
   if (!aligned16(ws)) return LLAMA_ERR_ALIGNMENT;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  DecodeWs dw = plan_decode(d, dtype, ws);
+  DecodeWs dw = plan_decode(d, dtype, ws, cache_capacity);
   const int64_t Bn = d->B, D = d->d_model;
   const size_t es = esize(dtype);
   // fp32 residual stream <- embedding rows
@@ -596,6 +639,8 @@ int llama_stack_decode_step(const llama_dims* d, int dtype, int n_layers, const 
   const size_t layer_cache = (size_t)(Bn * cache_capacity * d->n_kv * d->head_dim) * es;
   BlockWs b;
   b.u = dw.u; b.q = dw.q; b.o = dw.o; b.h = nullptr; b.m = dw.m; b.k = nullptr; b.v = nullptr; b.bytes = 0;
+  b.rs1 = dw.rs1; b.rs2 = dw.rs2;
+  b.attn = dw.attn; b.attn_bytes = dw.attn_bytes;
   for (int l = 0; l < n_layers; ++l) {
     void* kc = static_cast<char*>(k_cache) + l * layer_cache;
     void* vc = static_cast<char*>(v_cache) + l * layer_cache;

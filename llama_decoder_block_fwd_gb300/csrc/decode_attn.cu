@@ -1,0 +1,467 @@
+// Split-K GQA decode attention over a bf16 KV cache: one new query token per sequence attends
+// to every cached key plus its own ("LLaMA-3 8B ...", section 九: the 8193rd token sees the 8192
+// cached keys and itself; "Llama Architecture ...", Mathematical Foundations 4 for GQA).
+//
+//   phase 1 (decode_attn_kernel): persistent CTAs take work items (b, g, chunk of 128-key
+//     tiles).  Per tile, tcgen05 computes S^T = K Q^T (M = 128 keys, N = 16: the r <= 16 query
+//     heads of KV group g, zero-padded; K = hd) and O^T += V^T P^T (M = hd, N = 16, K = 128 keys;
+//     V is read as the MN-major A operand straight from the TMA tile).  One thread per key does
+//     the softmax for the r heads; the running max is shared per head through shared memory and
+//     O^T is rescaled in TMEM only when a head's max grows by more than 2^8.  Each item writes its
+//     unnormalised partial (m, l, O) to the workspace.
+//   phase 2 (decode_combine_kernel): o = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c.
+// The result equals softmax(q K^T / sqrt(hd)) V up to the order of additions.
+#include <algorithm>
+#include <cstring>
+
+#include "kernels.h"
+
+namespace llama {
+namespace {
+
+constexpr int DA_THREADS = 192;          // warp 0 TMA, warp 1 MMA, warps 2-5 softmax
+constexpr int DA_STAGES = 3;
+constexpr int DA_HD = 128;
+constexpr int DA_NPAD = 16;              // MMA N: query heads of the group, zero-padded
+constexpr uint32_t DA_TMEM_COLS = 64;
+constexpr float kDaRescaleLog2 = 8.0f;
+
+struct __align__(64) DecodeAttnParams {
+  CUtensorMap tmK;   // [B, kv_len, n_kv, hd], box (64, 1, 128, 1)
+  CUtensorMap tmV;
+  CUtensorMap tmQ;   // [B, n_q, hd], box (64, r, 1)
+  float* part_o;     // [B, n_chunks, n_q, hd]
+  float* part_ml;    // [B, n_chunks, n_q, 2]  (m in log2 units, l)
+  int B, n_q, n_kv, r, kv_len, kv_tiles, chunk_tiles, n_chunks, n_items;
+  float scale_log2;
+  unsigned* status;
+};
+
+struct DaSmem {
+  static constexpr uint32_t KV = 128 * DA_HD * 2;          // one K or V tile: 32 KB
+  static constexpr uint32_t QB = DA_NPAD * DA_HD * 2;      // one Q operand: 4 KB
+  static constexpr uint32_t PB = DA_NPAD * 128 * 2;        // P^T operand: 4 KB
+  static constexpr uint32_t OFF_K = 0;
+  static constexpr uint32_t OFF_V = OFF_K + DA_STAGES * KV;
+  static constexpr uint32_t OFF_Q = OFF_V + DA_STAGES * KV;   // 2 buffers
+  static constexpr uint32_t OFF_P = OFF_Q + 2 * QB;
+  static constexpr uint32_t OFF_RED = OFF_P + PB;             // [4 warps][16] floats
+  static constexpr uint32_t OFF_BAR = OFF_RED + 4 * 16 * 4;
+  static constexpr uint32_t TOTAL = OFF_BAR + 256 + 1024;
+};
+
+__device__ __forceinline__ void tma_load_4d_da(uint32_t dst, const CUtensorMap* m, uint64_t* bar, int x, int y,
+                                               int z, int w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t (&v)[4]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
+               : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+
+// Named barrier over the 128 softmax threads (warps 2..5).
+__device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ void item_coords(const DecodeAttnParams& p, int item, int& b, int& g, int& t_begin,
+                                            int& t_end, int& chunk) {
+  chunk = item % p.n_chunks;
+  const int bg = item / p.n_chunks;
+  b = bg / p.n_kv;
+  g = bg % p.n_kv;
+  t_begin = chunk * p.chunk_tiles;
+  t_end = min(t_begin + p.chunk_tiles, p.kv_tiles);
+}
+
+__global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_kernel(const __grid_constant__ DecodeAttnParams p) {
+  using L = DaSmem;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
+  uint64_t* k_full = bars + 0;              // [3]
+  uint64_t* v_full = bars + 3;              // [3]
+  uint64_t* kv_empty = bars + 6;            // [3]
+  uint64_t* q_full = bars + 9;              // [2]
+  uint64_t* q_empty = bars + 11;            // [2]
+  uint64_t* s_full = bars + 13;             // [2]
+  uint64_t* s_free = bars + 15;             // [2]  (128 arrivals)
+  uint64_t* p_full = bars + 17;             //      (128 arrivals)
+  uint64_t* o_done = bars + 18;
+  uint64_t* o_free = bars + 19;             //      (128 arrivals)
+  uint64_t* drain = bars + 20;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 21);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* red = reinterpret_cast<float*>(smem + L::OFF_RED);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 21; ++i) {
+      const bool many = (i == 15 || i == 16 || i == 17 || i == 19);
+      mbar_init(&bars[i], many ? 128 : 1);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&p.tmK);
+    tma_prefetch_desc(&p.tmV);
+    tma_prefetch_desc(&p.tmQ);
+  }
+  // Q operand rows r..15 and the padded P^T rows stay zero for the whole kernel.
+  for (int i = threadIdx.x; i < (int)(2 * L::QB + L::PB) / 16; i += DA_THREADS)
+    reinterpret_cast<uint4*>(smem + L::OFF_Q)[i] = make_uint4(0, 0, 0, 0);
+  fence_proxy_async_smem();
+  if (warp == 1) { tmem_alloc(tmem_slot, DA_TMEM_COLS); tmem_relinquish(); }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tS = tmem;          // S^T buffers: columns 0..15 and 16..31
+  const uint32_t tO = tmem + 32;     // O^T: columns 32..47
+  const uint32_t sbase = smem_u32(smem);
+
+  if (warp == 0) {
+    if (lane == 0) {  // ---------------------------------------------------- TMA producer
+      int tile = 0, it = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x, ++it) {
+        int b, g, t0, t1, chunk;
+        item_coords(p, item, b, g, t0, t1, chunk);
+        const int qb = it & 1;
+        if (!mbar_wait(&q_empty[qb], ((it >> 1) & 1) ^ 1, abort_flag, p.status)) break;
+        mbar_arrive_expect_tx(&q_full[qb], 2 * 64 * p.r * 2);
+        for (int hh = 0; hh < 2; ++hh)
+          tma_load_3d(sbase + L::OFF_Q + qb * L::QB + hh * (L::QB / 2), &p.tmQ, &q_full[qb], hh * 64, g * p.r, b);
+        for (int t = t0; t < t1; ++t, ++tile) {
+          const int st = tile % DA_STAGES;
+          const uint32_t ph = (tile / DA_STAGES) & 1;
+          if (!mbar_wait(&kv_empty[st], ph ^ 1, abort_flag, p.status)) { ok = false; break; }
+          mbar_arrive_expect_tx(&k_full[st], L::KV);
+          for (int hh = 0; hh < 2; ++hh)
+            tma_load_4d_da(sbase + L::OFF_K + st * L::KV + hh * 16384, &p.tmK, &k_full[st], hh * 64, g, t * 128, b);
+          mbar_arrive_expect_tx(&v_full[st], L::KV);
+          for (int hh = 0; hh < 2; ++hh)
+            tma_load_4d_da(sbase + L::OFF_V + st * L::KV + hh * 16384, &p.tmV, &v_full[st], hh * 64, g, t * 128, b);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // ---------------------------------------------------- MMA issuer
+      const uint32_t idesc_s = idesc_bf16(128, DA_NPAD);
+      const uint32_t idesc_o = idesc_bf16(128, DA_NPAD, /*b_mn_major=*/false, /*a_mn_major=*/true);
+      int tile = 0, it = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x, ++it) {
+        int b, g, t0, t1, chunk;
+        item_coords(p, item, b, g, t0, t1, chunk);
+        const int qb = it & 1;
+        if (!mbar_wait(&q_full[qb], (it >> 1) & 1, abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t qa = sbase + L::OFF_Q + qb * L::QB;
+        const int n = t1 - t0;
+        auto issue_s = [&](int j) -> bool {    // tile j of this item (global tile index tile + j)
+          const int gt = tile + j;
+          const int st = gt % DA_STAGES;
+          const int sb = gt & 1;
+          if (!mbar_wait(&k_full[st], (gt / DA_STAGES) & 1, abort_flag, p.status)) return false;
+          if (!mbar_wait(&s_free[sb], ((gt >> 1) & 1) ^ 1, abort_flag, p.status)) return false;
+          tc_fence_after();
+          const uint32_t ka = sbase + L::OFF_K + st * L::KV;
+#pragma unroll
+          for (int k = 0; k < DA_HD / 16; ++k) {
+            const uint64_t ad = sdesc_sw128(ka + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(qa + (k >> 2) * (L::QB / 2) + (k & 3) * 32, 16, 1024);
+            tc_mma(tS + sb * 16, ad, bd, idesc_s, k > 0 ? 1u : 0u);
+          }
+          tc_commit(&s_full[sb]);
+          return true;
+        };
+        auto issue_pv = [&](int j) -> bool {
+          const int gt = tile + j;
+          const int st = gt % DA_STAGES;
+          if (!mbar_wait(p_full, gt & 1, abort_flag, p.status)) return false;
+          if (!mbar_wait(&v_full[st], (gt / DA_STAGES) & 1, abort_flag, p.status)) return false;
+          // the first P V of an item overwrites O^T: the previous item's O^T must have been read
+          if (j == 0 && !mbar_wait(o_free, (it & 1) ^ 1, abort_flag, p.status)) return false;
+          tc_fence_after();
+          const uint32_t va = sbase + L::OFF_V + st * L::KV;
+          const uint32_t pa = sbase + L::OFF_P;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {     // 16 keys per step
+            const uint64_t ad = sdesc_sw128(va + k * 2048, 16384, 1024);           // V^T, MN-major
+            const uint64_t bd = sdesc_sw128(pa + (k >> 2) * (L::PB / 2) + (k & 3) * 32, 16, 1024);
+            tc_mma(tO, ad, bd, idesc_o, (j > 0 || k > 0) ? 1u : 0u);
+          }
+          tc_commit(o_done);
+          tc_commit(&kv_empty[st]);
+          return true;
+        };
+        for (int j = 0; j < n; ++j) {
+          if (!issue_s(j)) { ok = false; break; }
+          if (j > 0 && !issue_pv(j - 1)) { ok = false; break; }
+        }
+        if (!ok) break;
+        tc_commit(&q_empty[qb]);
+        if (!issue_pv(n - 1)) break;
+        tile += n;
+      }
+      int no_abort = 0;
+      tc_commit(drain);
+      mbar_wait(drain, 0, &no_abort, p.status);
+    }
+  } else {  // ------------------------------------------------------------ softmax warps 2..5
+    const int qw = warp & 3;
+    const int t = qw * 32 + lane;                 // TMEM lane: key of the tile / hd index of O^T
+    const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
+    const int r = p.r;
+    int tile = 0, it = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x, ++it) {
+      int b, g, t0, t1, chunk;
+      item_coords(p, item, b, g, t0, t1, chunk);
+      float m_ref[DA_NPAD], lsum[DA_NPAD];
+#pragma unroll
+      for (int h = 0; h < DA_NPAD; ++h) { m_ref[h] = -INFINITY; lsum[h] = 0.f; }
+      for (int tt = t0; tt < t1; ++tt, ++tile) {
+        const int sb = tile & 1;
+        if (!mbar_wait(&s_full[sb], (tile >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t sv[16];
+        tmem_ld16(tS + sb * 16 + lane_off, sv);
+        tc_wait_ld();
+        tc_fence_before();
+        mbar_arrive(&s_free[sb]);
+        const bool valid = tt * 128 + t < p.kv_len;
+        float s[DA_NPAD];
+#pragma unroll
+        for (int h = 0; h < DA_NPAD; ++h) s[h] = valid ? __uint_as_float(sv[h]) * p.scale_log2 : -INFINITY;
+        // per-head max over the 128 keys of the tile
+        float mx[DA_NPAD];
+#pragma unroll
+        for (int h = 0; h < DA_NPAD; ++h) {
+          float v = h < r ? s[h] : -INFINITY;
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+          mx[h] = v;
+        }
+        if (lane < DA_NPAD) {
+          float mine = mx[0];
+#pragma unroll
+          for (int h = 1; h < DA_NPAD; ++h) if (lane == h) mine = mx[h];
+          red[qw * 16 + lane] = mine;
+        }
+        softmax_sync();
+        float alpha[DA_NPAD];
+        bool resc = false;
+#pragma unroll
+        for (int h = 0; h < DA_NPAD; ++h) {
+          const float tm = fmaxf(fmaxf(red[h], red[16 + h]), fmaxf(red[32 + h], red[48 + h]));
+          alpha[h] = 1.f;
+          if (h < r) {
+            if (m_ref[h] == -INFINITY) {
+              m_ref[h] = tm;
+            } else if (tm > m_ref[h] + kDaRescaleLog2) {
+              alpha[h] = exp2f(m_ref[h] - tm);
+              m_ref[h] = tm;
+              resc = true;
+            }
+          }
+        }
+        softmax_sync();     // everyone has read `red` before the next tile overwrites it
+        // O^T and the P buffer are free once the previous tile's P V has completed
+        if (tt > t0) {
+          if (!mbar_wait(o_done, (tile - 1) & 1, abort_flag, p.status)) { ok = false; break; }
+          tc_fence_after();
+          if (resc) {     // uniform across the 128 threads: every thread saw the same maxima
+            uint32_t ov[16];
+            tmem_ld16(tO + lane_off, ov);
+            tc_wait_ld();
+#pragma unroll
+            for (int h = 0; h < DA_NPAD; ++h) ov[h] = __float_as_uint(__uint_as_float(ov[h]) * alpha[h]);
+            tmem_st16(tO + lane_off, ov);
+            tc_wait_st();
+#pragma unroll
+            for (int h = 0; h < DA_NPAD; ++h) lsum[h] *= alpha[h];
+          }
+        }
+        // P^T rows = heads, columns = keys (K-major, 128B swizzle, two 64-key atoms)
+        uint8_t* pbase = smem + L::OFF_P + (t >> 6) * (L::PB / 2);
+        const int kin = t & 63;
+#pragma unroll
+        for (int h = 0; h < DA_NPAD; ++h) {
+          if (h < r) {
+            const float pv = exp2f(s[h] - m_ref[h]);
+            const __nv_bfloat16 pb = __float2bfloat16_rn(pv);
+            lsum[h] += __bfloat162float(pb);
+            const int chunk16 = (kin >> 3) ^ (h & 7);
+            *reinterpret_cast<__nv_bfloat16*>(pbase + h * 128 + chunk16 * 16 + (kin & 7) * 2) = pb;
+          }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(p_full);
+      }
+      if (!ok) break;
+      // ---- item done: write the unnormalised partial (m, l, O)
+      if (!mbar_wait(o_done, (tile - 1) & 1, abort_flag, p.status)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t ov[16];
+      tmem_ld16(tO + lane_off, ov);
+      tc_wait_ld();
+      tc_fence_before();
+      mbar_arrive(o_free);
+      const int64_t base = ((int64_t)b * p.n_chunks + chunk) * p.n_q + (int64_t)g * r;
+#pragma unroll
+      for (int h = 0; h < DA_NPAD; ++h)
+        if (h < r) p.part_o[(base + h) * DA_HD + t] = __uint_as_float(ov[h]);
+      // l: sum the per-thread partial sums over the 128 keys of each head
+#pragma unroll
+      for (int h = 0; h < DA_NPAD; ++h) {
+        float v = h < r ? lsum[h] : 0.f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        lsum[h] = v;
+      }
+      if (lane < DA_NPAD) {
+        float mine = lsum[0];
+#pragma unroll
+        for (int h = 1; h < DA_NPAD; ++h) if (lane == h) mine = lsum[h];
+        red[qw * 16 + lane] = mine;
+      }
+      softmax_sync();
+      if (t < r) {
+        const float l = red[t] + red[16 + t] + red[32 + t] + red[48 + t];
+        float mm = -INFINITY;
+#pragma unroll
+        for (int h = 0; h < DA_NPAD; ++h) if (h == t) mm = m_ref[h];
+        p.part_ml[(base + t) * 2 + 0] = mm;
+        p.part_ml[(base + t) * 2 + 1] = l;
+      }
+      softmax_sync();
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, DA_TMEM_COLS);
+  }
+}
+
+// o[b, h, :] = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c; one warp per (b, h).
+__global__ void decode_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml,
+                                      uint16_t* __restrict__ o, int B, int n_q, int n_chunks) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (warp >= B * n_q) return;
+  const int b = warp / n_q, h = warp % n_q;
+  float M = -INFINITY;
+  for (int c = 0; c < n_chunks; ++c) M = fmaxf(M, part_ml[(((int64_t)b * n_chunks + c) * n_q + h) * 2]);
+  float l = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int c = 0; c < n_chunks; ++c) {
+    const int64_t idx = ((int64_t)b * n_chunks + c) * n_q + h;
+    const float w = exp2f(part_ml[idx * 2] - M);
+    l += w * part_ml[idx * 2 + 1];
+    const float4 v = *reinterpret_cast<const float4*>(part_o + idx * DA_HD + lane * 4);
+    acc[0] += w * v.x; acc[1] += w * v.y; acc[2] += w * v.z; acc[3] += w * v.w;
+  }
+  const float inv = 1.f / l;
+  uint2 out;
+  out.x = pack_bf2(acc[0] * inv, acc[1] * inv);
+  out.y = pack_bf2(acc[2] * inv, acc[3] * inv);
+  *reinterpret_cast<uint2*>(o + ((int64_t)b * n_q + h) * DA_HD + lane * 4) = out;
+}
+
+struct DecodePlan {
+  int kv_tiles, chunk_tiles, n_chunks;
+};
+
+DecodePlan plan(int64_t B, int64_t n_kv, int64_t kv_len) {
+  DecodePlan d;
+  d.kv_tiles = (int)((kv_len + 127) / 128);
+  d.chunk_tiles = std::max(1, std::min(d.kv_tiles, 8));
+  d.n_chunks = (d.kv_tiles + d.chunk_tiles - 1) / d.chunk_tiles;
+  (void)B; (void)n_kv;
+  return d;
+}
+
+}  // namespace
+
+bool decode_attn_supported(const AttnDesc& a) {
+  if (a.dtype != LLAMA_BF16 || a.hd != DA_HD || a.S != 1) return false;
+  if (a.n_kv <= 0 || a.n_q % a.n_kv != 0 || a.n_q / a.n_kv > DA_NPAD) return false;
+  if (a.pos0 + 1 > ((int64_t)1 << 30)) return false;
+  const uintptr_t al = reinterpret_cast<uintptr_t>(a.q) | reinterpret_cast<uintptr_t>(a.k) |
+                       reinterpret_cast<uintptr_t>(a.v) | reinterpret_cast<uintptr_t>(a.o);
+  return (al & 15) == 0;
+}
+
+size_t decode_attn_ws_bytes(const AttnDesc& a) {
+  const DecodePlan d = plan(a.B, a.n_kv, a.pos0 + 1);
+  const size_t o = (size_t)a.B * d.n_chunks * a.n_q * DA_HD * 4;
+  const size_t ml = (size_t)a.B * d.n_chunks * a.n_q * 2 * 4;
+  return ((o + 255) & ~size_t(255)) + ((ml + 255) & ~size_t(255));
+}
+
+int launch_decode_attn(const AttnDesc& a, void* ws, int num_sms, unsigned* status, cudaStream_t st) {
+  DecodeAttnParams p;
+  memset(&p, 0, sizeof(p));
+  const int r = (int)(a.n_q / a.n_kv);
+  const int64_t kv_len = a.pos0 + 1;
+  const DecodePlan d = plan(a.B, a.n_kv, kv_len);
+  const uint64_t dims[4] = {(uint64_t)DA_HD, (uint64_t)a.n_kv, (uint64_t)kv_len, (uint64_t)a.B};
+  const uint64_t strides[3] = {(uint64_t)DA_HD * 2, (uint64_t)a.n_kv * DA_HD * 2, (uint64_t)a.cap * a.n_kv * DA_HD * 2};
+  const uint32_t box[4] = {64, 1, 128, 1};
+  if (!encode_tmap_4d_bf16(&p.tmK, a.k, dims, strides, box)) return -1;
+  if (!encode_tmap_4d_bf16(&p.tmV, a.v, dims, strides, box)) return -1;
+  if (!encode_tmap_3d_bf16(&p.tmQ, a.q, DA_HD, (uint64_t)a.n_q, (uint64_t)a.B, DA_HD * 2,
+                           (uint64_t)a.n_q * DA_HD * 2, 64, (uint32_t)r, 1))
+    return -1;
+  const size_t o_bytes = (((size_t)a.B * d.n_chunks * a.n_q * DA_HD * 4) + 255) & ~size_t(255);
+  p.part_o = static_cast<float*>(ws);
+  p.part_ml = reinterpret_cast<float*>(static_cast<char*>(ws) + o_bytes);
+  p.B = (int)a.B; p.n_q = (int)a.n_q; p.n_kv = (int)a.n_kv; p.r = r;
+  p.kv_len = (int)kv_len;
+  p.kv_tiles = d.kv_tiles;
+  p.chunk_tiles = d.chunk_tiles;
+  p.n_chunks = d.n_chunks;
+  p.n_items = (int)(a.B * a.n_kv * d.n_chunks);
+  p.scale_log2 = a.scale * 1.4426950408889634f;
+  p.status = status;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  static bool attr_set[64] = {};
+  if (dev < 0 || dev >= 64) return -1;
+  if (!attr_set[dev]) {
+    if (cudaFuncSetAttribute(decode_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, DaSmem::TOTAL) !=
+        cudaSuccess)
+      return -1;
+    attr_set[dev] = true;
+  }
+  const int grid = std::max(1, std::min(p.n_items, num_sms));
+  decode_attn_kernel<<<grid, DA_THREADS, DaSmem::TOTAL, st>>>(p);
+  const int warps = (int)(a.B * a.n_q);
+  decode_combine_kernel<<<(warps * 32 + 255) / 256, 256, 0, st>>>(p.part_o, p.part_ml, static_cast<uint16_t*>(a.o),
+                                                                   (int)a.B, (int)a.n_q, d.n_chunks);
+  return 0;
+}
+
+}  // namespace llama

@@ -98,7 +98,16 @@ __device__ __forceinline__ void rope_run(const Epi& e, int64_t c_in_seg, float p
 // lies inside one of the Q/K/V column ranges; for EPI_SWIGLU `v` holds gate values and `u` the
 // matching up values and c indexes the d_ff output).
 template <int n>
-__device__ __forceinline__ void epi_run(const Epi& e, int64_t r, int64_t c, float* v, const float* u) {
+__device__ __forceinline__ void epi_run(const Epi& e, int64_t r, int64_t c, float* v, float* u) {
+  if (e.row_scale) {   // RMSNorm's per-row factor, applied to the fp32 accumulator
+    const float rs = __ldg(e.row_scale + r);
+#pragma unroll
+    for (int i = 0; i < n; ++i) v[i] *= rs;
+    if (e.kind == EPI_SWIGLU) {
+#pragma unroll
+      for (int i = 0; i < n; ++i) u[i] *= rs;
+    }
+  }
   switch (e.kind) {
     case EPI_STORE:
       store_run<n>(e.out, e.out_f32, e.ldo, r, c, v);

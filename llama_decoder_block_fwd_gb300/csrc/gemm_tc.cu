@@ -196,7 +196,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tc_kernel(const __grid_co
             float fv[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) fv[i] = __uint_as_float(v[i]);
-            epi_run<32>(p.epi, r, (int64_t)nb * TN + c * 32, fv, nullptr);
+            epi_run<32>(p.epi, r, (int64_t)nb * TN + c * 32, fv, fv);
           }
         }
       }

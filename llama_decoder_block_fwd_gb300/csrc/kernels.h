@@ -23,6 +23,7 @@ enum EpiKind : int {
 struct Epi {
   int kind;
   int out_f32;          // 1: out is float32, 0: bf16
+  const float* row_scale;  // when set, D[r, :] is first multiplied by row_scale[r]
   void* out;            // STORE/RESID/SWIGLU/ATOMIC: [M, ldo]; QKV: q [M, nq_cols]
   int64_t ldo;
   const void* resid;
@@ -59,11 +60,14 @@ struct AttnDesc {
   void* o;              // [B, S, n_q, hd]
   int64_t B, S, n_q, n_kv, hd, cap, pos0;
   float scale;          // 1/sqrt(hd)
+  void* ws;             // scratch for the split-K decode kernel (may be null)
+  size_t ws_bytes;
 };
 
 // rows x d RMSNorm; x_f32/y_f32 give the element types of x and y, g has type `dtype`.
-int launch_rmsnorm(int dtype, int x_f32, int y_f32, const void* x, const void* g, void* y, int64_t rows,
-                   int64_t d, float eps, cudaStream_t st);
+// rs_out == nullptr: y = x * rs * g.  Otherwise y = x * g and rs_out[row] = rs (split form).
+int launch_rmsnorm(int dtype, int x_f32, int y_f32, const void* x, const void* g, void* y, float* rs_out,
+                   int64_t rows, int64_t d, float eps, cudaStream_t st);
 int launch_rope(int dtype, void* q, void* k, int64_t B, int64_t S, int64_t n_q, int64_t n_kv, int hd,
                 int64_t pos0, const RopeFreq* freq, cudaStream_t st);
 int launch_gemm_simt(const GemmDesc& g, cudaStream_t st);
@@ -74,6 +78,9 @@ int launch_widen_bf16(const void* src, float* dst, int64_t n, cudaStream_t st);
 bool gemm_tc_supported(const GemmDesc& g);
 int launch_gemm_tc(const GemmDesc& g, int num_sms, unsigned* status, cudaStream_t st);
 bool attn_tc_supported(const AttnDesc& a);
+bool decode_attn_supported(const AttnDesc& a);
+size_t decode_attn_ws_bytes(const AttnDesc& a);   // for kv_len = pos0 + 1
+int launch_decode_attn(const AttnDesc& a, void* ws, int num_sms, unsigned* status, cudaStream_t st);
 int launch_attn_tc(const AttnDesc& a, int num_sms, unsigned* status, cudaStream_t st);
 
 // tensor-map encoding (driver entry point resolved through the runtime)

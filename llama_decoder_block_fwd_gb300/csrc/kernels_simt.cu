@@ -14,20 +14,20 @@ namespace {
 // it works").  One warp per row, fp32 sum of squares, 128-bit loads; the row stays in
 // registers between the reduction and the scaling pass (CH 16-byte chunks per lane).
 // ------------------------------------------------------------------------------------------
-template <typename T> struct V16;
-template <> struct V16<float> {
-  static constexpr int N = 4;
-  static __device__ __forceinline__ void unpack(const uint4& w, float* f) {
-    f[0] = __uint_as_float(w.x); f[1] = __uint_as_float(w.y);
-    f[2] = __uint_as_float(w.z); f[3] = __uint_as_float(w.w);
+// N consecutive elements <-> floats, one vector access (p aligned to N * sizeof(T)).
+template <typename T, int N> struct VecIO;
+template <> struct VecIO<float, 4> {
+  static __device__ __forceinline__ void ld(const float* p, float* f) {
+    const float4 w = __ldg(reinterpret_cast<const float4*>(p));
+    f[0] = w.x; f[1] = w.y; f[2] = w.z; f[3] = w.w;
   }
-  static __device__ __forceinline__ uint4 pack(const float* f) {
-    return make_uint4(__float_as_uint(f[0]), __float_as_uint(f[1]), __float_as_uint(f[2]), __float_as_uint(f[3]));
+  static __device__ __forceinline__ void st(float* p, const float* f) {
+    __stcs(reinterpret_cast<float4*>(p), make_float4(f[0], f[1], f[2], f[3]));
   }
 };
-template <> struct V16<uint16_t> {
-  static constexpr int N = 8;
-  static __device__ __forceinline__ void unpack(const uint4& w, float* f) {
+template <> struct VecIO<uint16_t, 8> {
+  static __device__ __forceinline__ void ld(const uint16_t* p, float* f) {
+    const uint4 w = __ldg(reinterpret_cast<const uint4*>(p));
     const uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -35,8 +35,19 @@ template <> struct V16<uint16_t> {
       f[2 * j + 1] = __uint_as_float(u[j] & 0xFFFF0000u);
     }
   }
-  static __device__ __forceinline__ uint4 pack(const float* f) {
-    return make_uint4(pack_bf2(f[0], f[1]), pack_bf2(f[2], f[3]), pack_bf2(f[4], f[5]), pack_bf2(f[6], f[7]));
+  static __device__ __forceinline__ void st(uint16_t* p, const float* f) {
+    __stcs(reinterpret_cast<uint4*>(p),
+           make_uint4(pack_bf2(f[0], f[1]), pack_bf2(f[2], f[3]), pack_bf2(f[4], f[5]), pack_bf2(f[6], f[7])));
+  }
+};
+template <> struct VecIO<uint16_t, 4> {
+  static __device__ __forceinline__ void ld(const uint16_t* p, float* f) {
+    const uint2 w = __ldg(reinterpret_cast<const uint2*>(p));
+    f[0] = __uint_as_float(w.x << 16); f[1] = __uint_as_float(w.x & 0xFFFF0000u);
+    f[2] = __uint_as_float(w.y << 16); f[3] = __uint_as_float(w.y & 0xFFFF0000u);
+  }
+  static __device__ __forceinline__ void st(uint16_t* p, const float* f) {
+    __stcs(reinterpret_cast<uint2*>(p), make_uint2(pack_bf2(f[0], f[1]), pack_bf2(f[2], f[3])));
   }
 };
 
@@ -51,10 +62,27 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
-template <typename T, int CH>
-__global__ void __launch_bounds__(256) rmsnorm_reg_kernel(const T* __restrict__ x, const T* __restrict__ g,
-                                                          T* __restrict__ y, int64_t rows, int d, float eps) {
-  constexpr int N = V16<T>::N;
+// The N = 16 / sizeof(T) elements of a 16-byte value (held in registers) as floats.
+__device__ __forceinline__ void unpack16(const uint4& w, float* f, float) {
+  f[0] = __uint_as_float(w.x); f[1] = __uint_as_float(w.y); f[2] = __uint_as_float(w.z); f[3] = __uint_as_float(w.w);
+}
+__device__ __forceinline__ void unpack16(const uint4& w, float* f, uint16_t) {
+  const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    f[2 * j] = __uint_as_float(u[j] << 16);
+    f[2 * j + 1] = __uint_as_float(u[j] & 0xFFFF0000u);
+  }
+}
+
+// One warp per row; the row is held in registers (CH 16-byte chunks per lane) between the
+// sum of squares and the scaling pass.  SPLIT: write a = x * g and rs[row] = rsqrt(mean(x^2)+eps)
+// instead of y = x * rs * g, for a consumer GEMM that applies rs to its fp32 accumulator.
+template <typename TX, typename TG, typename TY, int CH, bool SPLIT>
+__global__ void __launch_bounds__(256) rmsnorm_reg_kernel(const TX* __restrict__ x, const TG* __restrict__ g,
+                                                          TY* __restrict__ y, float* __restrict__ rs_out,
+                                                          int64_t rows, int d, float eps) {
+  constexpr int N = 16 / (int)sizeof(TX);
   const int lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   if (row >= rows) return;
@@ -66,37 +94,37 @@ __global__ void __launch_bounds__(256) rmsnorm_reg_kernel(const T* __restrict__ 
   for (int i = 0; i < CH; ++i) {
     const int c = lane + 32 * i;
     if (c < nch) {
-      buf[i] = __ldcs(xr + c);   // streamed once: do not keep in L1
+      buf[i] = __ldcs(xr + c);   // streamed once: keep it out of L1
       float f[N];
-      V16<T>::unpack(buf[i], f);
+      unpack16(buf[i], f, TX());
 #pragma unroll
       for (int j = 0; j < N; ++j) ss = fmaf(f[j], f[j], ss);
     }
   }
   ss = warp_sum(ss);
   const float rs = rsqrtf(ss / (float)d + eps);
-  const uint4* gr = reinterpret_cast<const uint4*>(g);
-  uint4* yr = reinterpret_cast<uint4*>(y + row * d);
+  if (SPLIT && lane == 0) rs_out[row] = rs;
+  const float mul = SPLIT ? 1.f : rs;
+  TY* yr = y + row * d;
 #pragma unroll
   for (int i = 0; i < CH; ++i) {
     const int c = lane + 32 * i;
     if (c < nch) {
       float f[N], w[N];
-      V16<T>::unpack(buf[i], f);
-      V16<T>::unpack(__ldg(gr + c), w);
+      unpack16(buf[i], f, TX());
+      VecIO<TG, N>::ld(g + c * N, w);
 #pragma unroll
-      for (int j = 0; j < N; ++j) f[j] = f[j] * rs * w[j];
-      __stcs(yr + c, V16<T>::pack(f));
+      for (int j = 0; j < N; ++j) f[j] = f[j] * mul * w[j];
+      VecIO<TY, N>::st(yr + c * N, f);
     }
   }
 }
 
-// Any widths and any mix of x / y element types (the decode path normalises its fp32
-// residual stream into bf16).  Two passes over the row.
-template <typename TX, typename TG, typename TY>
+// Any width, any alignment.  Two passes over the row.
+template <typename TX, typename TG, typename TY, bool SPLIT>
 __global__ void __launch_bounds__(256) rmsnorm_generic_kernel(const TX* __restrict__ x, const TG* __restrict__ g,
-                                                              TY* __restrict__ y, int64_t rows, int64_t d,
-                                                              float eps) {
+                                                              TY* __restrict__ y, float* __restrict__ rs_out,
+                                                              int64_t rows, int64_t d, float eps) {
   const int lane = threadIdx.x & 31;
   const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
   if (row >= rows) return;
@@ -108,22 +136,33 @@ __global__ void __launch_bounds__(256) rmsnorm_generic_kernel(const TX* __restri
   }
   ss = warp_sum(ss);
   const float rs = rsqrtf(ss / (float)d + eps);
+  if (SPLIT && lane == 0) rs_out[row] = rs;
+  const float mul = SPLIT ? 1.f : rs;
   TY* yr = y + row * d;
-  for (int64_t c = lane; c < d; c += 32) Elt<TY>::st(yr + c, Elt<TX>::ld(xr + c) * rs * Elt<TG>::ld(g + c));
+  for (int64_t c = lane; c < d; c += 32) Elt<TY>::st(yr + c, Elt<TX>::ld(xr + c) * mul * Elt<TG>::ld(g + c));
 }
 
-template <typename T>
-int rmsnorm_reg_dispatch(const T* x, const T* g, T* y, int64_t rows, int64_t d, float eps, cudaStream_t st) {
-  constexpr int N = V16<T>::N;
-  const int64_t nch = d / N;
-  const int64_t per_lane = (nch + 31) / 32;
+template <typename TX, typename TG, typename TY, bool SPLIT>
+int rmsnorm_dispatch(const void* xv, const void* gv, void* yv, float* rs, int64_t rows, int64_t d, float eps,
+                     cudaStream_t st) {
+  constexpr int N = 16 / (int)sizeof(TX);
+  const TX* x = static_cast<const TX*>(xv);
+  const TG* g = static_cast<const TG*>(gv);
+  TY* y = static_cast<TY*>(yv);
   const unsigned grid = (unsigned)((rows + 7) / 8);
-  if (per_lane <= 1) rmsnorm_reg_kernel<T, 1><<<grid, 256, 0, st>>>(x, g, y, rows, (int)d, eps);
-  else if (per_lane <= 2) rmsnorm_reg_kernel<T, 2><<<grid, 256, 0, st>>>(x, g, y, rows, (int)d, eps);
-  else if (per_lane <= 4) rmsnorm_reg_kernel<T, 4><<<grid, 256, 0, st>>>(x, g, y, rows, (int)d, eps);
-  else if (per_lane <= 8) rmsnorm_reg_kernel<T, 8><<<grid, 256, 0, st>>>(x, g, y, rows, (int)d, eps);
-  else if (per_lane <= 16) rmsnorm_reg_kernel<T, 16><<<grid, 256, 0, st>>>(x, g, y, rows, (int)d, eps);
-  else return -1;
+  const bool aligned = ((reinterpret_cast<uintptr_t>(xv) | reinterpret_cast<uintptr_t>(gv) |
+                         reinterpret_cast<uintptr_t>(yv)) & 15) == 0;
+  const int64_t per_lane = (d / N + 31) / 32;
+  if (aligned && d % N == 0 && per_lane <= 32) {
+    if (per_lane <= 1) rmsnorm_reg_kernel<TX, TG, TY, 1, SPLIT><<<grid, 256, 0, st>>>(x, g, y, rs, rows, (int)d, eps);
+    else if (per_lane <= 2) rmsnorm_reg_kernel<TX, TG, TY, 2, SPLIT><<<grid, 256, 0, st>>>(x, g, y, rs, rows, (int)d, eps);
+    else if (per_lane <= 4) rmsnorm_reg_kernel<TX, TG, TY, 4, SPLIT><<<grid, 256, 0, st>>>(x, g, y, rs, rows, (int)d, eps);
+    else if (per_lane <= 8) rmsnorm_reg_kernel<TX, TG, TY, 8, SPLIT><<<grid, 256, 0, st>>>(x, g, y, rs, rows, (int)d, eps);
+    else if (per_lane <= 16) rmsnorm_reg_kernel<TX, TG, TY, 16, SPLIT><<<grid, 256, 0, st>>>(x, g, y, rs, rows, (int)d, eps);
+    else rmsnorm_reg_kernel<TX, TG, TY, 32, SPLIT><<<grid, 256, 0, st>>>(x, g, y, rs, rows, (int)d, eps);
+  } else {
+    rmsnorm_generic_kernel<TX, TG, TY, SPLIT><<<grid, 256, 0, st>>>(x, g, y, rs, rows, d, eps);
+  }
   return 0;
 }
 
@@ -306,31 +345,22 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(const __grid_constant__ 
 
 }  // namespace
 
-int launch_rmsnorm(int dtype, int x_f32, int y_f32, const void* x, const void* g, void* y, int64_t rows,
-                   int64_t d, float eps, cudaStream_t st) {
+int launch_rmsnorm(int dtype, int x_f32, int y_f32, const void* x, const void* g, void* y, float* rs_out,
+                   int64_t rows, int64_t d, float eps, cudaStream_t st) {
   if (rows <= 0) return 0;
-  const unsigned grid = (unsigned)((rows + 7) / 8);
-  const bool aligned = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(g) |
-                         reinterpret_cast<uintptr_t>(y)) & 15) == 0;
-  if (dtype == LLAMA_BF16 && !x_f32 && !y_f32) {
-    if (aligned && d % 8 == 0 && d <= 8 * 32 * 16 &&
-        rmsnorm_reg_dispatch<uint16_t>((const uint16_t*)x, (const uint16_t*)g, (uint16_t*)y, rows, d, eps, st) == 0)
-      return 0;
-    rmsnorm_generic_kernel<uint16_t, uint16_t, uint16_t><<<grid, 256, 0, st>>>(
-        (const uint16_t*)x, (const uint16_t*)g, (uint16_t*)y, rows, d, eps);
-  } else if (dtype == LLAMA_F32) {
-    if (aligned && d % 4 == 0 && d <= 4 * 32 * 16 &&
-        rmsnorm_reg_dispatch<float>((const float*)x, (const float*)g, (float*)y, rows, d, eps, st) == 0)
-      return 0;
-    rmsnorm_generic_kernel<float, float, float><<<grid, 256, 0, st>>>((const float*)x, (const float*)g, (float*)y,
-                                                                      rows, d, eps);
-  } else if (x_f32 && !y_f32) {   // bf16 call, fp32 residual stream in, bf16 out
-    rmsnorm_generic_kernel<float, uint16_t, uint16_t><<<grid, 256, 0, st>>>(
-        (const float*)x, (const uint16_t*)g, (uint16_t*)y, rows, d, eps);
-  } else {
-    return -1;
+  using bf = uint16_t;
+  const bool split = rs_out != nullptr;
+  if (dtype == LLAMA_F32) {
+    if (!x_f32 || !y_f32) return -1;
+    return split ? rmsnorm_dispatch<float, float, float, true>(x, g, y, rs_out, rows, d, eps, st)
+                 : rmsnorm_dispatch<float, float, float, false>(x, g, y, rs_out, rows, d, eps, st);
   }
-  return 0;
+  if (y_f32) return -1;
+  if (x_f32)
+    return split ? rmsnorm_dispatch<float, bf, bf, true>(x, g, y, rs_out, rows, d, eps, st)
+                 : rmsnorm_dispatch<float, bf, bf, false>(x, g, y, rs_out, rows, d, eps, st);
+  return split ? rmsnorm_dispatch<bf, bf, bf, true>(x, g, y, rs_out, rows, d, eps, st)
+               : rmsnorm_dispatch<bf, bf, bf, false>(x, g, y, rs_out, rows, d, eps, st);
 }
 
 int launch_rope(int dtype, void* q, void* k, int64_t B, int64_t S, int64_t n_q, int64_t n_kv, int hd, int64_t pos0,

@@ -46,8 +46,12 @@ def _oracle(wl, rows, cap):
                                caches, fg, wlm)
 
 
-def test_decode_small_stack_full():
-    wl = C.Workload("small-stack", 6, C.BF16, 5, 1, 256, 8, 2, 64, 384, 1e4, 1e-5, gain_std=0.1, n_layers=3,
+@pytest.mark.parametrize("hd", [128, 64])
+def test_decode_small_stack_full(hd):
+    # hd 128 runs the tcgen05 split-K decode attention (ragged last tile: 301 keys); hd 64 the
+    # CUDA-core one.  The LM head (1000 rows) exercises the generic GEMM.
+    nq, nkv = (4, 1) if hd == 128 else (8, 2)
+    wl = C.Workload("small-stack", 6, C.BF16, 5, 1, 512, nq, nkv, hd, 384, 1e4, 1e-5, gain_std=0.1, n_layers=3,
                     t_cache=300, vocab=1000)
     cap = 333
     logits, kc, vc = _decode(wl, cap)

@@ -99,7 +99,10 @@ def _attn_case(dtype, B, S, nq, nkv, hd, cap, pos0):
     (synth.BF16, 1, 300, 8, 2, 128, 300, 0),       # ragged tail (300 = 2*128 + 44)
     (synth.BF16, 2, 130, 4, 4, 128, 130, 0),       # MHA, ragged
     (synth.BF16, 2, 77, 8, 2, 64, 300, 200),       # chunk after a 200-token cache
-    (synth.BF16, 3, 1, 32, 8, 128, 1100, 1040),    # decode shape: one query, long cache
+    (synth.BF16, 3, 1, 32, 8, 128, 1100, 1040),    # decode shape: one query, long cache (split-K kernel)
+    (synth.BF16, 2, 1, 8, 1, 128, 4000, 3999),     # decode, r = 8, cache full to capacity
+    (synth.BF16, 2, 1, 4, 4, 128, 130, 128),       # decode, MHA (r = 1), 129 keys: ragged tile
+    (synth.BF16, 1, 1, 16, 1, 128, 1, 0),          # decode, first token: one key
     (synth.F32, 2, 5, 6, 3, 8, 9, 4),
 ])
 def test_gqa_attention(dtype, B, S, nq, nkv, hd, cap, pos0):
