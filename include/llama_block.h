@@ -149,6 +149,27 @@ int llama_stack_decode_step(const llama_dims* dims, int dtype, int n_layers,
                             void* v_cache, int64_t cache_capacity, int64_t t_cache, float* logits,
                             void* ws, size_t ws_bytes, void* stream);
 
+/* Allocation-free one-token GQA attention (the paper has no counterpart: this is a library entry
+ * point for callers that cannot allocate device memory at the call site, e.g. code running under
+ * an allocator that owns all of device memory, or loops where cudaMalloc/cudaFree would
+ * synchronise the device).  Same arguments and result as llama_gqa_attention with dims->S == 1,
+ * minus the workspace: its split-K partials live in a 12 MiB device array inside the library
+ * (created when the library is loaded, resident on every device that loads it until exit).
+ *   - bf16 only, head_dim 128, n_q / n_kv <= 16.  Returns LLAMA_ERR_WORKSPACE, launching nothing,
+ *     when even a single key chunk of partials (about 520 bytes per query head and sequence)
+ *     exceeds the 12 MiB array, i.e. when B * n_q > 24197.  Below that, the keys are cut into
+ *     fewer, longer chunks whenever the usual chunking would not fit (the Llama-3-8B decode
+ *     shape, 64 sequences x 32 heads x 8193 keys, fits the usual chunking).
+ *   - The first call on a device looks up the array's device address (cudaGetSymbolAddress);
+ *     make that first call before any stream capture.
+ *   - Every call uses the same array: calls that overlap on the GPU (other streams, other host
+ *     threads) race on it.  Each call overwrites every partial it reads, so nothing needs
+ *     clearing between calls.
+ *   - Calls no cudaMalloc, cudaFree or other allocating routine.                              */
+int llama_gqa_attention_decode_noalloc(const llama_dims* dims, int dtype, const void* q,
+                                       const void* k, const void* v, int64_t kv_capacity,
+                                       int64_t pos0, void* o, void* stream);
+
 /* Workspace bytes the call `op` needs for these arguments (0 if none).  kv_capacity is the
  * cache capacity for attention/decode and is ignored otherwise.                              */
 size_t llama_workspace_bytes(int op, const llama_dims* dims, int dtype, int n_layers,

@@ -14,7 +14,7 @@ from typing import Sequence
 
 __all__ = [
     "F32", "BF16", "LlamaError", "Dims", "BlockWeights", "lib", "dims_of",
-    "llama_rmsnorm", "llama_rope", "llama_gqa_attention", "llama_swiglu_ffn",
+    "llama_rmsnorm", "llama_rope", "llama_gqa_attention", "llama_gqa_attention_decode_noalloc", "llama_swiglu_ffn",
     "llama_block_forward", "llama_stack_decode_step", "llama_workspace_bytes",
     "llama_get_device_status", "llama_status_string", "llama_profile_enable", "llama_profile_read",
     "OP_RMSNORM", "OP_ROPE", "OP_GQA_ATTENTION", "OP_SWIGLU_FFN", "OP_BLOCK_FORWARD",
@@ -75,6 +75,7 @@ def lib() -> ctypes.CDLL:
                 "llama_stack_decode_step": [pd, i32, i32, ctypes.POINTER(BlockWeights), vp, vp, i64, vp,
                                             vp, vp, i64, i64, vp, vp, sz, vp],
                 "llama_get_device_status": [ctypes.POINTER(ctypes.c_int), vp],
+                "llama_gqa_attention_decode_noalloc": [pd, i32, vp, vp, vp, i64, i64, vp, vp],
             }
             for name, args in sig.items():
                 fn = getattr(L, name)
@@ -150,6 +151,13 @@ def llama_rope(dims, dtype, q, k, pos0=0, stream=None):
 def llama_gqa_attention(dims, dtype, q, k, v, kv_capacity, pos0, o, ws=None, stream=None):
     _check(lib().llama_gqa_attention(ctypes.byref(_d(dims)), dtype, _p(q), _p(k), _p(v), int(kv_capacity),
                                      int(pos0), _p(o), _p(ws), _nbytes(ws), _s(stream)), "llama_gqa_attention")
+
+
+def llama_gqa_attention_decode_noalloc(dims, dtype, q, k, v, kv_capacity, pos0, o, stream=None):
+    """One-token attention with the library's own fixed scratch (no workspace argument)."""
+    _check(lib().llama_gqa_attention_decode_noalloc(ctypes.byref(_d(dims)), dtype, _p(q), _p(k), _p(v),
+                                                    int(kv_capacity), int(pos0), _p(o), _s(stream)),
+           "llama_gqa_attention_decode_noalloc")
 
 
 def llama_swiglu_ffn(dims, dtype, x, w_gate, w_up, w_down, y, ws, stream=None):

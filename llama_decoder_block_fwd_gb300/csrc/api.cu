@@ -17,7 +17,7 @@ namespace llama {
 // ------------------------------------------------------------------ device status word
 __device__ unsigned g_device_status;
 
-static unsigned* status_ptr() {
+unsigned* status_ptr() {
   static unsigned* cached[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
@@ -29,7 +29,7 @@ static unsigned* status_ptr() {
   return cached[dev];
 }
 
-static int num_sms() {
+int num_sms() {
   static int cached[64] = {};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;

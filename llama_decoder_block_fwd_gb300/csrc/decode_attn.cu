@@ -12,6 +12,7 @@
 //   phase 2 (decode_combine_kernel): o = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c.
 // The result equals softmax(q K^T / sqrt(hd)) V up to the order of additions.
 #include <algorithm>
+#include <cmath>
 #include <cstring>
 
 #include "kernels.h"
@@ -464,4 +465,110 @@ int launch_decode_attn(const AttnDesc& a, void* ws, int num_sms, unsigned* statu
   return 0;
 }
 
+// ------------------------------------------------------------------------------------------
+// Allocation-free variant of the decode attention call.  Its split-K partials live in one
+// file-scope device array instead of a caller workspace, so callers that cannot allocate device
+// memory where they call (code running under an allocator that owns all of device memory, such
+// as a fixed-budget arena or a caching allocator, where a stray cudaMalloc would fail or split
+// the pool; latency-bound loops where cudaMalloc/cudaFree would synchronise the device) can run
+// it with only their inputs and output.  The array is created when the library is loaded and
+// stays resident on every device that loads it until the process exits.
+// ------------------------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = (size_t)12 << 20;   // 12 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of g_noalloc_scratch on the current device, looked up on first use per device.
+// (In host code the array's name is only a host-side stand-in, not a device address.)
+void* noalloc_scratch_ptr() {
+  static void* cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!cached[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess) return nullptr;
+    cached[dev] = ptr;
+  }
+  return cached[dev];
+}
+
+size_t round256(size_t b) { return (b + 255) & ~size_t(255); }
+
+// The default chunking, with fewer (longer) chunks when the partials would not fit in `cap`.
+bool plan_within(int64_t B, int64_t n_q, int64_t n_kv, int64_t kv_len, size_t cap, DecodePlan& d) {
+  d = plan(B, n_kv, kv_len);
+  auto bytes = [&](int chunks) {
+    return round256((size_t)B * chunks * n_q * DA_HD * 4) + round256((size_t)B * chunks * n_q * 2 * 4);
+  };
+  if (bytes(1) > cap) return false;
+  while (bytes(d.n_chunks) > cap) {
+    d.chunk_tiles += 1;
+    d.n_chunks = (d.kv_tiles + d.chunk_tiles - 1) / d.chunk_tiles;
+  }
+  return true;
+}
+
+}  // namespace
+
 }  // namespace llama
+
+using namespace llama;
+
+extern "C" int llama_gqa_attention_decode_noalloc(const llama_dims* dims, int dtype, const void* q, const void* k,
+                                                   const void* v, int64_t kv_capacity, int64_t pos0, void* o,
+                                                   void* stream) {
+  if (!dims || dtype != LLAMA_BF16) return dtype == LLAMA_BF16 ? LLAMA_ERR_INVALID_ARG : LLAMA_ERR_UNSUPPORTED;
+  if (dims->B < 0 || dims->S != 1 || dims->n_q <= 0 || dims->n_kv <= 0 || dims->n_q % dims->n_kv != 0)
+    return LLAMA_ERR_INVALID_ARG;
+  if (dims->head_dim != DA_HD || dims->n_q / dims->n_kv > DA_NPAD) return LLAMA_ERR_UNSUPPORTED;
+  if (pos0 < 0 || kv_capacity < pos0 + 1 || pos0 + 1 > ((int64_t)1 << 30)) return LLAMA_ERR_INVALID_ARG;
+  if (dims->B == 0) return LLAMA_OK;
+  if (!q || !k || !v || !o) return LLAMA_ERR_INVALID_ARG;
+  const uintptr_t al = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                       reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o);
+  if (al & 15) return LLAMA_ERR_ALIGNMENT;
+  DecodePlan d;
+  if (!plan_within(dims->B, dims->n_q, dims->n_kv, pos0 + 1, kNoAllocScratchBytes, d))
+    return LLAMA_ERR_WORKSPACE;   // B * n_q too large for the fixed scratch, even as one chunk
+  void* scratch = noalloc_scratch_ptr();
+  unsigned* status = status_ptr();
+  if (!scratch || !status) return LLAMA_ERR_CUDA;
+
+  DecodeAttnParams p;
+  memset(&p, 0, sizeof(p));
+  const int r = (int)(dims->n_q / dims->n_kv);
+  const int64_t kv_len = pos0 + 1;
+  const uint64_t tdims[4] = {(uint64_t)DA_HD, (uint64_t)dims->n_kv, (uint64_t)kv_len, (uint64_t)dims->B};
+  const uint64_t strides[3] = {(uint64_t)DA_HD * 2, (uint64_t)dims->n_kv * DA_HD * 2,
+                               (uint64_t)kv_capacity * dims->n_kv * DA_HD * 2};
+  const uint32_t box[4] = {64, 1, 128, 1};
+  if (!encode_tmap_4d_bf16(&p.tmK, k, tdims, strides, box) || !encode_tmap_4d_bf16(&p.tmV, v, tdims, strides, box) ||
+      !encode_tmap_3d_bf16(&p.tmQ, q, DA_HD, (uint64_t)dims->n_q, (uint64_t)dims->B, DA_HD * 2,
+                           (uint64_t)dims->n_q * DA_HD * 2, 64, (uint32_t)r, 1))
+    return LLAMA_ERR_CUDA;
+  // Every partial a work item owns is overwritten by that item: nothing has to start at zero.
+  p.part_o = static_cast<float*>(scratch);
+  p.part_ml = reinterpret_cast<float*>(static_cast<char*>(scratch) +
+                                       round256((size_t)dims->B * d.n_chunks * dims->n_q * DA_HD * 4));
+  p.B = (int)dims->B; p.n_q = (int)dims->n_q; p.n_kv = (int)dims->n_kv; p.r = r;
+  p.kv_len = (int)kv_len;
+  p.kv_tiles = d.kv_tiles;
+  p.chunk_tiles = d.chunk_tiles;
+  p.n_chunks = d.n_chunks;
+  p.n_items = (int)(dims->B * dims->n_kv * d.n_chunks);
+  p.scale_log2 = (float)(1.0 / std::sqrt((double)DA_HD)) * 1.4426950408889634f;
+  p.status = status;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (cudaFuncSetAttribute(decode_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, DaSmem::TOTAL) !=
+      cudaSuccess)
+    return LLAMA_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int grid = std::max(1, std::min(p.n_items, num_sms()));
+  decode_attn_kernel<<<grid, DA_THREADS, DaSmem::TOTAL, st>>>(p);
+  const int warps = (int)(dims->B * dims->n_q);
+  decode_combine_kernel<<<(warps * 32 + 255) / 256, 256, 0, st>>>(p.part_o, p.part_ml, static_cast<uint16_t*>(o),
+                                                                   (int)dims->B, (int)dims->n_q, d.n_chunks);
+  return cudaGetLastError() == cudaSuccess ? LLAMA_OK : LLAMA_ERR_CUDA;
+}

@@ -83,6 +83,10 @@ size_t decode_attn_ws_bytes(const AttnDesc& a);   // for kv_len = pos0 + 1
 int launch_decode_attn(const AttnDesc& a, void* ws, int num_sms, unsigned* status, cudaStream_t st);
 int launch_attn_tc(const AttnDesc& a, int num_sms, unsigned* status, cudaStream_t st);
 
+// The current device's status word (device address) and SM count.
+unsigned* status_ptr();
+int num_sms();
+
 // tensor-map encoding (driver entry point resolved through the runtime)
 bool encode_tmap_2d_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
                          uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer);
