@@ -27,6 +27,27 @@ METRIC = "block-forward tokens/s (prefill & decode) at 1 GB300; % of TC/HBM roof
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+def kernel_traffic(role: str):
+    """Measured DRAM bytes per launch of a kernel role from profiles/traffic.json, or None when the
+    kernel sources have changed since that capture."""
+    import glob
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            t = json.load(f)
+    except Exception:
+        return None
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "llama_decoder_block_fwd_gb300", "csrc", "*"))):
+        h.update(os.path.basename(p).encode())
+        with open(p, "rb") as f:
+            h.update(f.read())
+    if h.hexdigest()[:16] != t.get("source_sha"):
+        return None
+    k = t.get("kernels", {}).get(role)
+    return None if k is None else k["bytes_per_launch"]
+
+
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -161,6 +182,9 @@ def bench_prefill(args, world, rank):
     from synth import workloads as W
 
     wl = C.LLAMA3_8B_PREFILL
+    if args.prefill_seq != wl.S:   # smaller sequence for sizing profiler captures
+        import dataclasses
+        wl = dataclasses.replace(wl, S=args.prefill_seq, name=f"{wl.name}-S{args.prefill_seq}")
     T = wl.B * wl.S
     w = W.device_layer(wl)
     x = W.device_x(wl).reshape(T, wl.d_model)
@@ -242,7 +266,7 @@ def bench_prefill(args, world, rank):
                 "d2h_bytes_per_step": y.numel() * y.element_size()},
         "gpu_launches": launches,
         "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
-                     "frac": achieved / peak_tf, "traffic": None,
+                     "frac": achieved / peak_tf, "traffic": kernel_traffic(dom) if wl.S == 8192 else None,
                      "peak_source": f"{pk_src} bf16 {'sustained' if timed_s > 1.0 else 'burst'}"},
         "block_tc_frac": step_flops / (ms_step / 1e3) / 1e12 / peak_tf,
         "block_tflops": step_flops / (ms_step / 1e3) / 1e12,
@@ -266,6 +290,9 @@ def bench_decode(args, world, rank):
     from synth import workloads as W
 
     wl = C.LLAMA3_8B_DECODE
+    if args.decode_layers != wl.n_layers:   # fewer layers for sizing profiler captures
+        import dataclasses
+        wl = dataclasses.replace(wl, n_layers=args.decode_layers, name=f"{wl.name}-L{args.decode_layers}")
     cap = wl.t_cache + 1
     tensors = []
     layers = []
@@ -336,7 +363,8 @@ def bench_decode(args, world, rank):
         per_launch_bytes = nb["kv_read"] / wl.n_layers
         achieved = per_launch_bytes / (t / n / 1e3) / 1e9
         out["roofline"] = {"bound": "hbm", "kernel": a, "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                           "frac": achieved / pk["hbm_gbs"], "traffic": None, "peak_source": f"{pk_src} hbm"}
+                           "frac": achieved / pk["hbm_gbs"], "traffic": kernel_traffic(a), "peak_source": f"{pk_src} hbm",
+                           "algorithmic_bytes_per_launch": per_launch_bytes}
     del tensors, layers, kc, vc, final_g, w_lm, x, logits, ws, g
     torch.cuda.empty_cache()
     return out
@@ -396,6 +424,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prefill-seq", type=int, default=8192, help="tokens of the prefill workload (default 8192)")
+    ap.add_argument("--decode-layers", type=int, default=32, help="layers of the decode stack (default 32)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
