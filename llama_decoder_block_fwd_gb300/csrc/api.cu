@@ -186,9 +186,8 @@ int run_gemm(const GemmDesc& g, const char* role, cudaStream_t st) {
                                          "gemm_tc_atomic"};
   static const char* const simt_names[] = {"gemm_simt_store", "gemm_simt_resid", "gemm_simt_swiglu",
                                            "gemm_simt_qkv", "gemm_simt_atomic"};
-  (void)role;
   const bool tc = gemm_tc_supported(g);
-  prof::begin(tc ? tc_names[g.epi.kind] : simt_names[g.epi.kind], st);
+  prof::begin(role ? role : (tc ? tc_names[g.epi.kind] : simt_names[g.epi.kind]), st);
   if (tc) {
     unsigned* status = status_ptr();
     if (!status) return LLAMA_ERR_CUDA;
@@ -435,6 +434,168 @@ int block_body(const llama_dims* d, int dtype, const llama_block_weights* w, con
   return run_linear_resid(dtype, T, ws.m, d->d_ff, w->w_down, D, h, 1, y, x_f32 || f32, st);
 }
 
+// ------------------------------------------------------------------------------------------
+// Decode stack on the tensor cores.  Every projection is a weight-streaming GEMM over B <= 128
+// token rows: 128-column tiles split along K into ~kDecodeUnits work units write fp32 partials,
+// and a finisher reduces them and applies what follows (row scale, RoPE and the KV write,
+// SiLU*mul, the residual add and the next RMSNorm).  GEMM inputs are passed as bf16 hi + lo
+// parts (two MMAs per k-step into one accumulator): the weights are still read once, and the
+// activations keep ~16 mantissa bits, which holds the 32-layer drift of a bf16-only data flow.
+// ------------------------------------------------------------------------------------------
+constexpr int kDecodeUnits = 320;
+
+int decode_splits(int64_t n_cols, int64_t K) {
+  const int64_t tiles = (n_cols + 127) / 128;
+  const int want = (int)std::max<int64_t>(1, (kDecodeUnits + tiles - 1) / tiles);
+  return gemm_tc_effective_splits(K, want);
+}
+
+bool decode_tc_path(const llama_dims* d, int dtype) {
+  if (dtype != LLAMA_BF16 || d->B > 128 || d->head_dim != 128 || d->d_model > 8192) return false;
+  const int64_t hq = d->n_q * d->head_dim, hkv = d->n_kv * d->head_dim;
+  if (d->d_model % 128 || hq % 128 || hkv % 128 || d->d_ff % 128) return false;
+  if (d->n_q / d->n_kv > 16) return false;
+  return true;
+}
+
+struct DecodeTcWs {
+  float* xres;
+  void *act_hi, *act_lo, *q;
+  float *rs1, *rs2, *part;
+  void* attn;
+  size_t attn_bytes, bytes;
+  int s_qkv, s_o, s_gu, s_down;
+};
+
+DecodeTcWs plan_decode_tc(const llama_dims* d, void* base, int64_t kv_capacity) {
+  const size_t Bn = (size_t)d->B;
+  const int64_t hq = d->n_q * d->head_dim, hkv = d->n_kv * d->head_dim;
+  DecodeTcWs w;
+  w.s_qkv = decode_splits(hq + 2 * hkv, d->d_model);
+  w.s_o = decode_splits(d->d_model, hq);
+  w.s_gu = decode_splits(2 * d->d_ff, d->d_model);
+  w.s_down = decode_splits(d->d_model, d->d_ff);
+  const size_t act = (size_t)std::max(std::max(d->d_model, hq), d->d_ff);
+  const size_t part = std::max(std::max((size_t)w.s_qkv * (hq + 2 * hkv), (size_t)w.s_o * d->d_model),
+                               std::max((size_t)w.s_gu * 2 * d->d_ff, (size_t)w.s_down * d->d_model));
+  Carver c{static_cast<char*>(base)};
+  w.xres = static_cast<float*>(c.take(Bn * d->d_model * 4));
+  w.act_hi = c.take(Bn * act * 2);
+  w.act_lo = c.take(Bn * act * 2);
+  w.q = c.take(Bn * hq * 2);
+  w.rs1 = static_cast<float*>(c.take(Bn * 4));
+  w.rs2 = static_cast<float*>(c.take(Bn * 4));
+  w.part = static_cast<float*>(c.take(Bn * part * 4));
+  w.attn_bytes = attn_scratch_bytes(d, LLAMA_BF16, kv_capacity);
+  w.attn = c.take(w.attn_bytes);
+  w.bytes = c.off;
+  return w;
+}
+
+// out = (A_hi + A_lo) W^T as split-K fp32 partials [splits, M, N] (or, with splits == 1 and a
+// row scale, directly the scaled fp32 result).
+int run_dual_gemm(const char* role, int64_t M, const void* a_hi, const void* a_lo, int64_t K, const void* const* W,
+                  const int64_t* n_rows, int nseg, int splits, float* out, const float* row_scale, cudaStream_t st) {
+  GemmDesc g = make_gemm(LLAMA_BF16, M, a_hi, K);
+  g.A_lo = a_lo;
+  g.nseg = nseg;
+  g.N = 0;
+  for (int s = 0; s < nseg; ++s) { g.B[s] = W[s]; g.nB[s] = n_rows[s]; g.N += n_rows[s]; }
+  g.k_splits = splits;
+  g.narrow = 1;
+  g.epi = make_epi(EPI_STORE, 1, out, g.N);
+  g.epi.row_scale = row_scale;
+  if (!gemm_tc_supported(g)) return LLAMA_ERR_UNSUPPORTED;
+  return run_gemm(g, role, st);
+}
+
+int run_fin(const char* role, int launch_rc, cudaStream_t st) {
+  (void)role;
+  if (launch_rc != 0) return LLAMA_ERR_CUDA;
+  return launch_status();
+}
+
+int decode_stack_tc(const llama_dims* d, int n_layers, const llama_block_weights* layers, const void* final_g,
+                    const void* w_lm, int64_t vocab, const void* x_emb, void* k_cache, void* v_cache, int64_t cap,
+                    int64_t t_cache, float* logits, const DecodeTcWs& w, cudaStream_t st) {
+  const int B = (int)d->B, D = (int)d->d_model;
+  const int64_t hq = d->n_q * d->head_dim, hkv = d->n_kv * d->head_dim;
+  const float eps = (float)d->eps;
+  const size_t layer_cache = (size_t)(d->B * cap * hkv) * 2;
+  RopeFreq freq[kMaxRopePairs];
+  rope_freqs(d, freq);
+  int rc;
+  for (int l = 0; l < n_layers; ++l) {
+    const llama_block_weights& lw = layers[l];
+    void* kc = static_cast<char*>(k_cache) + l * layer_cache;
+    void* vc = static_cast<char*>(v_cache) + l * layer_cache;
+    // x (+)= down-projection partials of the previous layer; a = x * g_attn (hi, lo); rs1
+    prof::begin("fin_norm", st);
+    rc = launch_fin_norm(w.xres, l == 0 ? x_emb : nullptr, w.part, l == 0 ? 0 : w.s_down, lw.attn_norm_g, w.act_hi,
+                         w.act_lo, w.rs1, B, D, eps, st);
+    prof::end(st);
+    if ((rc = run_fin("fin_norm", rc, st)) != LLAMA_OK) return rc;
+    // Q/K/V partials
+    const void* wqkv[3] = {lw.wq, lw.wk, lw.wv};
+    const int64_t nqkv[3] = {hq, hkv, hkv};
+    if ((rc = run_dual_gemm("gemm_tc_dec_qkv", B, w.act_hi, w.act_lo, D, wqkv, nqkv, 3, w.s_qkv, w.part, nullptr, st)) !=
+        LLAMA_OK)
+      return rc;
+    prof::begin("fin_qkv", st);
+    rc = launch_fin_qkv(w.part, w.s_qkv, w.rs1, w.q, kc, vc, B, (int)hq, (int)hkv, (int)d->head_dim, cap, t_cache, freq,
+                        st);
+    prof::end(st);
+    if ((rc = run_fin("fin_qkv", rc, st)) != LLAMA_OK) return rc;
+    // attention over t_cache + 1 keys; o as hi + lo into the activation buffers
+    AttnDesc a = make_attn(d, LLAMA_BF16, w.q, kc, vc, w.act_hi, cap, t_cache);
+    a.o_lo = w.act_lo;
+    a.ws = w.attn;
+    a.ws_bytes = w.attn_bytes;
+    if ((rc = run_attention(a, st)) != LLAMA_OK) return rc;
+    // O projection partials; h = x + sum; a2 = h * g_ffn (hi, lo); rs2
+    const void* wo[1] = {lw.wo};
+    const int64_t no[1] = {D};
+    if ((rc = run_dual_gemm("gemm_tc_dec_o", B, w.act_hi, w.act_lo, hq, wo, no, 1, w.s_o, w.part, nullptr, st)) !=
+        LLAMA_OK)
+      return rc;
+    prof::begin("fin_norm", st);
+    rc = launch_fin_norm(w.xres, nullptr, w.part, w.s_o, lw.ffn_norm_g, w.act_hi, w.act_lo, w.rs2, B, D, eps, st);
+    prof::end(st);
+    if ((rc = run_fin("fin_norm", rc, st)) != LLAMA_OK) return rc;
+    // gate | up partials; m = SiLU(rs2 gate) * (rs2 up) (hi, lo)
+    const void* wgu[2] = {lw.w_gate, lw.w_up};
+    const int64_t ngu[2] = {d->d_ff, d->d_ff};
+    if ((rc = run_dual_gemm("gemm_tc_dec_gateup", B, w.act_hi, w.act_lo, D, wgu, ngu, 2, w.s_gu, w.part, nullptr,
+                            st)) != LLAMA_OK)
+      return rc;
+    prof::begin("fin_swiglu", st);
+    rc = launch_fin_swiglu(w.part, w.s_gu, w.rs2, w.act_hi, w.act_lo, B, (int)d->d_ff, st);
+    prof::end(st);
+    if ((rc = run_fin("fin_swiglu", rc, st)) != LLAMA_OK) return rc;
+    // down partials (added to x by the next fin_norm)
+    const void* wd[1] = {lw.w_down};
+    const int64_t nd[1] = {D};
+    if ((rc = run_dual_gemm("gemm_tc_dec_down", B, w.act_hi, w.act_lo, d->d_ff, wd, nd, 1, w.s_down, w.part, nullptr,
+                            st)) != LLAMA_OK)
+      return rc;
+  }
+  // final RMSNorm in split form, then the LM head with the row scale in its epilogue
+  prof::begin("fin_norm", st);
+  rc = launch_fin_norm(w.xres, nullptr, w.part, w.s_down, final_g, w.act_hi, w.act_lo, w.rs1, B, D, eps, st);
+  prof::end(st);
+  if ((rc = run_fin("fin_norm", rc, st)) != LLAMA_OK) return rc;
+  const void* wl[1] = {w_lm};
+  const int64_t nl[1] = {vocab};
+  if (vocab % 128 == 0)
+    return run_dual_gemm("gemm_tc_lm_head", B, w.act_hi, w.act_lo, D, wl, nl, 1, 1, logits, w.rs1, st);
+  // a vocabulary that is not a multiple of 128 rows: generic GEMM on the hi part with the row scale
+  GemmDesc g = make_gemm(LLAMA_BF16, B, w.act_hi, D);
+  g.nseg = 1; g.B[0] = w_lm; g.nB[0] = vocab; g.N = vocab;
+  g.epi = make_epi(EPI_STORE, 1, logits, vocab);
+  g.epi.row_scale = w.rs1;
+  return run_gemm(g, "gemm_lm_head", st);
+}
+
 }  // namespace
 }  // namespace llama
 
@@ -509,7 +670,9 @@ size_t llama_workspace_bytes(int op, const llama_dims* d, int dtype, int n_layer
     case LLAMA_OP_SWIGLU_FFN: return round256((size_t)(d->B * d->S * d->d_ff) * es);
     case LLAMA_OP_GQA_ATTENTION: return attn_scratch_bytes(d, dtype, kv_capacity);
     case LLAMA_OP_BLOCK_FORWARD: return plan_block(d, dtype, kv_capacity <= 0, nullptr, kv_capacity).bytes;
-    case LLAMA_OP_STACK_DECODE_STEP: return plan_decode(d, dtype, nullptr, kv_capacity).bytes;
+    case LLAMA_OP_STACK_DECODE_STEP:
+      return decode_tc_path(d, dtype) ? plan_decode_tc(d, nullptr, kv_capacity).bytes
+                                      : plan_decode(d, dtype, nullptr, kv_capacity).bytes;
     default: return 0;
   }
 }
@@ -622,10 +785,17 @@ int llama_stack_decode_step(const llama_dims* d, int dtype, int n_layers, const 
   if (!aligned16(final_g) || !aligned16(w_lm) || !aligned16(x_emb) || !aligned16(k_cache) || !aligned16(v_cache) ||
       !aligned16(logits))
     return LLAMA_ERR_ALIGNMENT;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (decode_tc_path(d, dtype)) {
+    const size_t need_tc = plan_decode_tc(d, nullptr, cache_capacity).bytes;
+    if (!ws || ws_bytes < need_tc) return LLAMA_ERR_WORKSPACE;
+    if (!aligned16(ws)) return LLAMA_ERR_ALIGNMENT;
+    return decode_stack_tc(d, n_layers, layers, final_g, w_lm, vocab, x_emb, k_cache, v_cache, cache_capacity, t_cache,
+                           logits, plan_decode_tc(d, ws, cache_capacity), st);
+  }
   const size_t need = plan_decode(d, dtype, nullptr, cache_capacity).bytes;
   if (!ws || ws_bytes < need) return LLAMA_ERR_WORKSPACE;
   if (!aligned16(ws)) return LLAMA_ERR_ALIGNMENT;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
   DecodeWs dw = plan_decode(d, dtype, ws, cache_capacity);
   const int64_t Bn = d->B, D = d->d_model;
   const size_t es = esize(dtype);

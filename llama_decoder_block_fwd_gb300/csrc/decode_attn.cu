@@ -369,8 +369,11 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_kernel(const __grid
 }
 
 // o[b, h, :] = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c; one warp per (b, h).
+// With o_lo set, o receives the bf16 rounding of the result and o_lo the bf16 rounding of what it
+// missed (hi + lo carries ~16 mantissa bits into the next GEMM).
 __global__ void decode_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml,
-                                      uint16_t* __restrict__ o, int B, int n_q, int n_chunks) {
+                                      uint16_t* __restrict__ o, uint16_t* __restrict__ o_lo, int B, int n_q,
+                                      int n_chunks) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (warp >= B * n_q) return;
   const int b = warp / n_q, h = warp % n_q;
@@ -385,10 +388,20 @@ __global__ void decode_combine_kernel(const float* __restrict__ part_o, const fl
     acc[0] += w * v.x; acc[1] += w * v.y; acc[2] += w * v.z; acc[3] += w * v.w;
   }
   const float inv = 1.f / l;
+  float r[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) r[i] = acc[i] * inv;
   uint2 out;
-  out.x = pack_bf2(acc[0] * inv, acc[1] * inv);
-  out.y = pack_bf2(acc[2] * inv, acc[3] * inv);
-  *reinterpret_cast<uint2*>(o + ((int64_t)b * n_q + h) * DA_HD + lane * 4) = out;
+  out.x = pack_bf2(r[0], r[1]);
+  out.y = pack_bf2(r[2], r[3]);
+  const int64_t off = ((int64_t)b * n_q + h) * DA_HD + lane * 4;
+  *reinterpret_cast<uint2*>(o + off) = out;
+  if (o_lo) {
+    uint2 lo;
+    lo.x = pack_bf2(r[0] - __uint_as_float(out.x << 16), r[1] - __uint_as_float(out.x & 0xFFFF0000u));
+    lo.y = pack_bf2(r[2] - __uint_as_float(out.y << 16), r[3] - __uint_as_float(out.y & 0xFFFF0000u));
+    *reinterpret_cast<uint2*>(o_lo + off) = lo;
+  }
 }
 
 struct DecodePlan {
@@ -461,7 +474,8 @@ int launch_decode_attn(const AttnDesc& a, void* ws, int num_sms, unsigned* statu
   decode_attn_kernel<<<grid, DA_THREADS, DaSmem::TOTAL, st>>>(p);
   const int warps = (int)(a.B * a.n_q);
   decode_combine_kernel<<<(warps * 32 + 255) / 256, 256, 0, st>>>(p.part_o, p.part_ml, static_cast<uint16_t*>(a.o),
-                                                                   (int)a.B, (int)a.n_q, d.n_chunks);
+                                                                   static_cast<uint16_t*>(a.o_lo), (int)a.B,
+                                                                   (int)a.n_q, d.n_chunks);
   return 0;
 }
 
@@ -569,6 +583,6 @@ extern "C" int llama_gqa_attention_decode_noalloc(const llama_dims* dims, int dt
   decode_attn_kernel<<<grid, DA_THREADS, DaSmem::TOTAL, st>>>(p);
   const int warps = (int)(dims->B * dims->n_q);
   decode_combine_kernel<<<(warps * 32 + 255) / 256, 256, 0, st>>>(p.part_o, p.part_ml, static_cast<uint16_t*>(o),
-                                                                   (int)dims->B, (int)dims->n_q, d.n_chunks);
+                                                                   nullptr, (int)dims->B, (int)dims->n_q, d.n_chunks);
   return cudaGetLastError() == cudaSuccess ? LLAMA_OK : LLAMA_ERR_CUDA;
 }

@@ -33,8 +33,12 @@ constexpr uint32_t TMEM_COLS = 512;
 
 struct __align__(64) TcParams {
   CUtensorMap tmA;
+  CUtensorMap tmA_lo;    // dual: low bf16 part of A (A = hi + lo)
   CUtensorMap tmB[3];
   int M, K;
+  int dual;              // two MMAs per k-step (A hi and A lo) into one accumulator; N tiles of 128
+  int max_halves;        // 128-column halves per tile: 2, or 1 (dual / skinny)
+  int k_splits, kb_per_split, num_units;
   int n_halves;          // 128-column halves of the virtual N
   int seg_half_end[3];   // cumulative halves per B segment
   int nseg;
@@ -54,13 +58,23 @@ __device__ __forceinline__ void tile_coords(const TcParams& p, int t, int& mb, i
 }
 
 __device__ __forceinline__ int tile_halves(const TcParams& p, int nb) {
-  return p.swiglu ? 2 : min(2, p.n_halves - 2 * nb);
+  return p.swiglu ? 2 : min(p.max_halves, p.n_halves - p.max_halves * nb);
+}
+
+// Work unit u -> output tile and K range [kb0, kb1) in 64-wide k-blocks.
+__device__ __forceinline__ void unit_coords(const TcParams& p, int u, int nkb, int& mb, int& nb, int& split, int& kb0,
+                                            int& kb1) {
+  const int t = u / p.k_splits;
+  split = u - t * p.k_splits;
+  tile_coords(p, t, mb, nb);
+  kb0 = split * p.kb_per_split;
+  kb1 = min(nkb, kb0 + p.kb_per_split);
 }
 
 // Which B segment, and which row of it, supplies half hh of column tile nb.
 __device__ __forceinline__ void half_source(const TcParams& p, int nb, int hh, int& seg, int& row) {
   if (p.swiglu) { seg = hh; row = nb * 128; return; }
-  const int gh = 2 * nb + hh;
+  const int gh = p.max_halves * nb + hh;
   seg = 0;
   int start = 0;
   while (seg < p.nseg - 1 && gh >= p.seg_half_end[seg]) { start = p.seg_half_end[seg]; ++seg; }
@@ -100,21 +114,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tc_kernel(const __grid_co
     if (lane == 0) {  // ---------------- TMA producer
       int stage = 0;
       uint32_t phase = 0;
-      for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
-        int mb, nb;
-        tile_coords(p, t, mb, nb);
+      for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
+        int mb, nb, split, kb0, kb1;
+        unit_coords(p, u, nkb, mb, nb, split, kb0, kb1);
         const int nvh = tile_halves(p, nb);
         int seg[2], row[2];
         for (int hh = 0; hh < nvh; ++hh) half_source(p, nb, hh, seg[hh], row[hh]);
-        const uint32_t bytes = A_BYTES + nvh * BH_BYTES;
+        // stage layout: [A | B half 0 | B half 1], or with dual A: [A hi | A lo | B half 0]
+        const uint32_t bytes = A_BYTES * (p.dual ? 2 : 1) + nvh * BH_BYTES;
+        const uint32_t boff = p.dual ? 2 * A_BYTES : A_BYTES;
         bool ok = true;
-        for (int kb = 0; kb < nkb; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) { ok = false; break; }
           mbar_arrive_expect_tx(&full[stage], bytes);
           const uint32_t sa = smem_base + stage * STAGE_BYTES;
           tma_load_2d(sa, &p.tmA, &full[stage], kb * TK, mb * TM);
+          if (p.dual) tma_load_2d(sa + A_BYTES, &p.tmA_lo, &full[stage], kb * TK, mb * TM);
           for (int hh = 0; hh < nvh; ++hh)
-            tma_load_2d(sa + A_BYTES + hh * BH_BYTES, &p.tmB[seg[hh]], &full[stage], kb * TK, row[hh]);
+            tma_load_2d(sa + boff + hh * BH_BYTES, &p.tmB[seg[hh]], &full[stage], kb * TK, row[hh]);
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
         }
         if (!ok) break;
@@ -125,9 +142,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tc_kernel(const __grid_co
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
-      for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++it) {
-        int mb, nb;
-        tile_coords(p, t, mb, nb);
+      for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++it) {
+        int mb, nb, split, kb0, kb1;
+        unit_coords(p, u, nkb, mb, nb, split, kb0, kb1);
         const int nvh = tile_halves(p, nb);
         const uint32_t idesc = idesc_bf16(TM, nvh * 128);
         const int buf = it & 1;
@@ -136,15 +153,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tc_kernel(const __grid_co
         tc_fence_after();
         const uint32_t d = tmem + buf * 256;
         bool ok = true;
-        for (int kb = 0; kb < nkb; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sa = smem_base + stage * STAGE_BYTES;
-          const uint32_t sb = sa + A_BYTES;
+          const uint32_t sb = sa + (p.dual ? 2 * A_BYTES : A_BYTES);
 #pragma unroll
           for (int k = 0; k < TK / 16; ++k) {
-            tc_mma(d, sdesc_sw128(sa + k * 32, 16, 1024), sdesc_sw128(sb + k * 32, 16, 1024), idesc,
-                   (kb | k) != 0);
+            const uint64_t bd = sdesc_sw128(sb + k * 32, 16, 1024);
+            tc_mma(d, sdesc_sw128(sa + k * 32, 16, 1024), bd, idesc, (kb != kb0 || k != 0) ? 1u : 0u);
+            if (p.dual) tc_mma(d, sdesc_sw128(sa + A_BYTES + k * 32, 16, 1024), bd, idesc, 1u);
           }
           tc_commit(&empty[stage]);
           if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -161,9 +179,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tc_kernel(const __grid_co
     const int q = warp & 3;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     int it = 0;
-    for (int t = blockIdx.x; t < p.num_tiles; t += gridDim.x, ++it) {
-      int mb, nb;
-      tile_coords(p, t, mb, nb);
+    for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++it) {
+      int mb, nb, split, kb0, kb1;
+      unit_coords(p, u, nkb, mb, nb, split, kb0, kb1);
       const int nvh = tile_halves(p, nb);
       const int buf = it & 1;
       const uint32_t aphase = (it >> 1) & 1;
@@ -171,6 +189,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tc_kernel(const __grid_co
       tc_fence_after();
       const int64_t r = (int64_t)mb * TM + q * 32 + lane;
       const bool live = r < p.M;
+      const int64_t r_out = r + (int64_t)split * p.M;    // split-K partials: [k_splits, M, N]
       const uint32_t tb = tmem + buf * 256 + lane_base;
       if (p.swiglu) {
 #pragma unroll 1
@@ -196,7 +215,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tc_kernel(const __grid_co
             float fv[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) fv[i] = __uint_as_float(v[i]);
-            epi_run<32>(p.epi, r, (int64_t)nb * TN + c * 32, fv, fv);
+            epi_run<32>(p.epi, r_out, (int64_t)nb * 128 * p.max_halves + c * 32, fv, fv);
           }
         }
       }
@@ -215,8 +234,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tc_kernel(const __grid_co
 
 }  // namespace
 
+int gemm_tc_effective_splits(int64_t K, int requested) {
+  const int nkb = (int)((K + TK - 1) / TK);
+  const int ks = std::max(1, std::min(requested, nkb));
+  const int kbps = (nkb + ks - 1) / ks;
+  return (nkb + kbps - 1) / kbps;
+}
+
 bool gemm_tc_supported(const GemmDesc& g) {
   if (g.dtype != LLAMA_BF16 || g.M <= 0 || g.K <= 0 || g.K % 8 != 0 || g.lda != g.K) return false;
+  if (g.A_lo && ((reinterpret_cast<uintptr_t>(g.A_lo) & 15) || g.epi.kind == EPI_SWIGLU)) return false;
+  if (g.k_splits > 1 && (g.epi.kind != EPI_STORE || !g.epi.out_f32 || g.epi.row_scale)) return false;
   if (g.K > (int64_t)1 << 30 || g.M > (int64_t)1 << 30) return false;
   if (reinterpret_cast<uintptr_t>(g.A) & 15) return false;
   const int ns = g.epi.kind == EPI_SWIGLU ? 2 : g.nseg;
@@ -241,6 +269,10 @@ int launch_gemm_tc(const GemmDesc& g, int num_sms, unsigned* status, cudaStream_
   memset(&p, 0, sizeof(p));
   const int ns = g.epi.kind == EPI_SWIGLU ? 2 : g.nseg;
   if (!encode_tmap_2d_bf16(&p.tmA, g.A, (uint64_t)g.K, (uint64_t)g.M, (uint64_t)g.lda * 2, TK, TM)) return -1;
+  p.dual = g.A_lo != nullptr;
+  if (p.dual && !encode_tmap_2d_bf16(&p.tmA_lo, g.A_lo, (uint64_t)g.K, (uint64_t)g.M, (uint64_t)g.lda * 2, TK, TM))
+    return -1;
+  p.max_halves = (p.dual || g.narrow) ? 1 : 2;
   int64_t halves = 0;
   for (int s = 0; s < ns; ++s) {
     if (!encode_tmap_2d_bf16(&p.tmB[s], g.B[s], (uint64_t)g.K, (uint64_t)g.nB[s], (uint64_t)g.K * 2, TK, 128))
@@ -254,8 +286,13 @@ int launch_gemm_tc(const GemmDesc& g, int num_sms, unsigned* status, cudaStream_
   p.swiglu = g.epi.kind == EPI_SWIGLU;
   p.n_halves = (int)halves;
   p.m_tiles = (int)((g.M + TM - 1) / TM);
-  p.n_tiles = p.swiglu ? (int)(g.nB[0] / 128) : (int)((halves + 1) / 2);
+  p.n_tiles = p.swiglu ? (int)(g.nB[0] / 128) : (int)((halves + p.max_halves - 1) / p.max_halves);
   p.num_tiles = p.m_tiles * p.n_tiles;
+  const int nkb = (int)((g.K + TK - 1) / TK);
+  const int ks = std::max(1, std::min(g.k_splits, nkb));
+  p.kb_per_split = (nkb + ks - 1) / ks;
+  p.k_splits = (nkb + p.kb_per_split - 1) / p.kb_per_split;
+  p.num_units = p.num_tiles * p.k_splits;
   p.status = status;
   p.epi = g.epi;
   int dev = 0;
@@ -267,7 +304,7 @@ int launch_gemm_tc(const GemmDesc& g, int num_sms, unsigned* status, cudaStream_
       return -1;
     attr_set[dev] = true;
   }
-  const int grid = std::max(1, std::min(p.num_tiles, num_sms));
+  const int grid = std::max(1, std::min(p.num_units, num_sms));
   gemm_tc_kernel<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(p);
   return 0;
 }

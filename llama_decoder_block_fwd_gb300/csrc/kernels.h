@@ -40,12 +40,16 @@ struct Epi {
 };
 
 // D[M, N] = A[M, K] * B[N, K]^T with B the row-concatenation of nseg segments
+// (the returned split count can be lower than asked: see launch_gemm_tc)
 // (for EPI_SWIGLU: B[0] = W_gate, B[1] = W_up, N = 2 * d_ff, output width d_ff).
 struct GemmDesc {
   int64_t M, N, K;
   int dtype;            // LLAMA_F32 or LLAMA_BF16, for A and B
   const void* A;
+  const void* A_lo;     // optional low bf16 part of A (A = A + A_lo), same layout; tcgen05 path only
   int64_t lda;          // elements
+  int k_splits;         // > 1: fp32 partial sums of K ranges to out[split * M + r, c] (EPI_STORE only)
+  int narrow;           // 1: 128-column tiles (more tiles for skinny M)
   const void* B[3];
   int64_t nB[3];        // rows of each segment
   int nseg;
@@ -58,6 +62,7 @@ struct AttnDesc {
   const void* k;        // [B, cap, n_kv, hd]
   const void* v;
   void* o;              // [B, S, n_q, hd]
+  void* o_lo;           // decode kernel only, optional: low bf16 part of o
   int64_t B, S, n_q, n_kv, hd, cap, pos0;
   float scale;          // 1/sqrt(hd)
   void* ws;             // scratch for the split-K decode kernel (may be null)
@@ -77,11 +82,21 @@ int launch_widen_bf16(const void* src, float* dst, int64_t n, cudaStream_t st);
 // tensor-core paths (bf16 only)
 bool gemm_tc_supported(const GemmDesc& g);
 int launch_gemm_tc(const GemmDesc& g, int num_sms, unsigned* status, cudaStream_t st);
+// The number of K splits launch_gemm_tc uses for a requested count.
+int gemm_tc_effective_splits(int64_t K, int requested);
 bool attn_tc_supported(const AttnDesc& a);
 bool decode_attn_supported(const AttnDesc& a);
 size_t decode_attn_ws_bytes(const AttnDesc& a);   // for kv_len = pos0 + 1
 int launch_decode_attn(const AttnDesc& a, void* ws, int num_sms, unsigned* status, cudaStream_t st);
 int launch_attn_tc(const AttnDesc& a, int num_sms, unsigned* status, cudaStream_t st);
+
+// Decode-step finishers (decode_fin.cu): split-K reductions fused with what follows each GEMM.
+int launch_fin_norm(float* x, const void* init_bf16, const float* part, int n_split, const void* g, void* a_hi,
+                    void* a_lo, float* rs, int B, int d, float eps, cudaStream_t st);
+int launch_fin_qkv(const float* part, int n_split, const float* rs, void* q, void* kc, void* vc, int B, int nq_cols,
+                   int nkv_cols, int hd, int64_t cap, int64_t t, const RopeFreq* freq, cudaStream_t st);
+int launch_fin_swiglu(const float* part, int n_split, const float* rs, void* m_hi, void* m_lo, int B, int dff,
+                      cudaStream_t st);
 
 // The current device's status word (device address) and SM count.
 unsigned* status_ptr();

@@ -46,13 +46,14 @@ def _oracle(wl, rows, cap):
                                caches, fg, wlm)
 
 
-@pytest.mark.parametrize("hd", [128, 64])
-def test_decode_small_stack_full(hd):
-    # hd 128 runs the tcgen05 split-K decode attention (ragged last tile: 301 keys); hd 64 the
-    # CUDA-core one.  The LM head (1000 rows) exercises the generic GEMM.
+@pytest.mark.parametrize("hd,vocab", [(128, 1000), (128, 1024), (64, 1000)])
+def test_decode_small_stack_full(hd, vocab):
+    # hd 128: the tensor-core decode path (split-K hi/lo GEMMs, finishers, split-K attention with a
+    # ragged last tile of 301 keys); a 1024-row LM head runs on the hi/lo GEMM, a 1000-row one on
+    # the generic GEMM.  hd 64: the per-block path with CUDA-core attention.
     nq, nkv = (4, 1) if hd == 128 else (8, 2)
     wl = C.Workload("small-stack", 6, C.BF16, 5, 1, 512, nq, nkv, hd, 384, 1e4, 1e-5, gain_std=0.1, n_layers=3,
-                    t_cache=300, vocab=1000)
+                    t_cache=300, vocab=vocab)
     cap = 333
     logits, kc, vc = _decode(wl, cap)
     ref = _oracle(wl, list(range(wl.B)), cap)
