@@ -476,8 +476,7 @@ DecodeTcWs plan_decode_tc(const llama_dims* d, void* base, int64_t kv_capacity) 
   w.s_gu = decode_splits(2 * d->d_ff, d->d_model);
   w.s_down = decode_splits(d->d_model, d->d_ff);
   const size_t act = (size_t)std::max(std::max(d->d_model, hq), d->d_ff);
-  const size_t part = std::max(std::max((size_t)w.s_qkv * (hq + 2 * hkv), (size_t)w.s_o * d->d_model),
-                               std::max((size_t)w.s_gu * 2 * d->d_ff, (size_t)w.s_down * d->d_model));
+  const size_t part = std::max((size_t)w.s_qkv * (hq + 2 * hkv), (size_t)w.s_gu * 2 * d->d_ff);
   Carver c{static_cast<char*>(base)};
   w.xres = static_cast<float*>(c.take(Bn * d->d_model * 4));
   w.act_hi = c.take(Bn * act * 2);
@@ -495,7 +494,8 @@ DecodeTcWs plan_decode_tc(const llama_dims* d, void* base, int64_t kv_capacity) 
 // out = (A_hi + A_lo) W^T as split-K fp32 partials [splits, M, N] (or, with splits == 1 and a
 // row scale, directly the scaled fp32 result).
 int run_dual_gemm(const char* role, int64_t M, const void* a_hi, const void* a_lo, int64_t K, const void* const* W,
-                  const int64_t* n_rows, int nseg, int splits, float* out, const float* row_scale, cudaStream_t st) {
+                  const int64_t* n_rows, int nseg, int splits, float* out, const float* row_scale, cudaStream_t st,
+                  int kind = EPI_STORE) {
   GemmDesc g = make_gemm(LLAMA_BF16, M, a_hi, K);
   g.A_lo = a_lo;
   g.nseg = nseg;
@@ -503,7 +503,7 @@ int run_dual_gemm(const char* role, int64_t M, const void* a_hi, const void* a_l
   for (int s = 0; s < nseg; ++s) { g.B[s] = W[s]; g.nB[s] = n_rows[s]; g.N += n_rows[s]; }
   g.k_splits = splits;
   g.narrow = 1;
-  g.epi = make_epi(EPI_STORE, 1, out, g.N);
+  g.epi = make_epi(kind, 1, out, g.N);
   g.epi.row_scale = row_scale;
   if (!gemm_tc_supported(g)) return LLAMA_ERR_UNSUPPORTED;
   return run_gemm(g, role, st);
@@ -529,10 +529,10 @@ int decode_stack_tc(const llama_dims* d, int n_layers, const llama_block_weights
     const llama_block_weights& lw = layers[l];
     void* kc = static_cast<char*>(k_cache) + l * layer_cache;
     void* vc = static_cast<char*>(v_cache) + l * layer_cache;
-    // x (+)= down-projection partials of the previous layer; a = x * g_attn (hi, lo); rs1
+    // (layer 0: x = embedding rows) a = x * g_attn (hi, lo); rs1
     prof::begin("fin_norm", st);
-    rc = launch_fin_norm(w.xres, l == 0 ? x_emb : nullptr, w.part, l == 0 ? 0 : w.s_down, lw.attn_norm_g, w.act_hi,
-                         w.act_lo, w.rs1, B, D, eps, st);
+    rc = launch_fin_norm(w.xres, l == 0 ? x_emb : nullptr, nullptr, 0, lw.attn_norm_g, w.act_hi, w.act_lo, w.rs1, B, D,
+                         eps, st);
     prof::end(st);
     if ((rc = run_fin("fin_norm", rc, st)) != LLAMA_OK) return rc;
     // Q/K/V partials
@@ -552,14 +552,15 @@ int decode_stack_tc(const llama_dims* d, int n_layers, const llama_block_weights
     a.ws = w.attn;
     a.ws_bytes = w.attn_bytes;
     if ((rc = run_attention(a, st)) != LLAMA_OK) return rc;
-    // O projection partials; h = x + sum; a2 = h * g_ffn (hi, lo); rs2
+    // h = x + o W_O^T: the split-K partials are added straight into the fp32 residual stream
     const void* wo[1] = {lw.wo};
     const int64_t no[1] = {D};
-    if ((rc = run_dual_gemm("gemm_tc_dec_o", B, w.act_hi, w.act_lo, hq, wo, no, 1, w.s_o, w.part, nullptr, st)) !=
-        LLAMA_OK)
+    if ((rc = run_dual_gemm("gemm_tc_dec_o", B, w.act_hi, w.act_lo, hq, wo, no, 1, w.s_o, w.xres, nullptr, st,
+                            EPI_ATOMIC)) != LLAMA_OK)
       return rc;
+    // a2 = h * g_ffn (hi, lo); rs2
     prof::begin("fin_norm", st);
-    rc = launch_fin_norm(w.xres, nullptr, w.part, w.s_o, lw.ffn_norm_g, w.act_hi, w.act_lo, w.rs2, B, D, eps, st);
+    rc = launch_fin_norm(w.xres, nullptr, nullptr, 0, lw.ffn_norm_g, w.act_hi, w.act_lo, w.rs2, B, D, eps, st);
     prof::end(st);
     if ((rc = run_fin("fin_norm", rc, st)) != LLAMA_OK) return rc;
     // gate | up partials; m = SiLU(rs2 gate) * (rs2 up) (hi, lo)
@@ -572,16 +573,16 @@ int decode_stack_tc(const llama_dims* d, int n_layers, const llama_block_weights
     rc = launch_fin_swiglu(w.part, w.s_gu, w.rs2, w.act_hi, w.act_lo, B, (int)d->d_ff, st);
     prof::end(st);
     if ((rc = run_fin("fin_swiglu", rc, st)) != LLAMA_OK) return rc;
-    // down partials (added to x by the next fin_norm)
+    // y = h + m W_down^T, added into the residual stream the same way
     const void* wd[1] = {lw.w_down};
     const int64_t nd[1] = {D};
-    if ((rc = run_dual_gemm("gemm_tc_dec_down", B, w.act_hi, w.act_lo, d->d_ff, wd, nd, 1, w.s_down, w.part, nullptr,
-                            st)) != LLAMA_OK)
+    if ((rc = run_dual_gemm("gemm_tc_dec_down", B, w.act_hi, w.act_lo, d->d_ff, wd, nd, 1, w.s_down, w.xres, nullptr,
+                            st, EPI_ATOMIC)) != LLAMA_OK)
       return rc;
   }
   // final RMSNorm in split form, then the LM head with the row scale in its epilogue
   prof::begin("fin_norm", st);
-  rc = launch_fin_norm(w.xres, nullptr, w.part, w.s_down, final_g, w.act_hi, w.act_lo, w.rs1, B, D, eps, st);
+  rc = launch_fin_norm(w.xres, nullptr, nullptr, 0, final_g, w.act_hi, w.act_lo, w.rs1, B, D, eps, st);
   prof::end(st);
   if ((rc = run_fin("fin_norm", rc, st)) != LLAMA_OK) return rc;
   const void* wl[1] = {w_lm};

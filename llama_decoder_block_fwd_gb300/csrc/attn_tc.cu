@@ -52,8 +52,8 @@ struct Smem {
   static constexpr uint32_t OFF_Q = 0;
   static constexpr uint32_t OFF_K = OFF_Q + Q;               // 2 stages
   static constexpr uint32_t OFF_V = OFF_K + 2 * KV;          // 2 stages
-  static constexpr uint32_t OFF_P = OFF_V + 2 * KV;
-  static constexpr uint32_t OFF_BAR = OFF_P + P;
+  static constexpr uint32_t OFF_P = OFF_V + 2 * KV;          // 2 buffers
+  static constexpr uint32_t OFF_BAR = OFF_P + 2 * P;
   static constexpr uint32_t TOTAL = OFF_BAR + 256 + 1024;
 };
 
@@ -84,10 +84,10 @@ __global__ void __launch_bounds__(AT_THREADS, 1) attn_tc_kernel(const __grid_con
   uint64_t* kv_empty = bars + 5;   // [2]
   uint64_t* s_full = bars + 7;     // [2]
   uint64_t* s_free = bars + 9;     // [2]
-  uint64_t* p_full = bars + 11;
-  uint64_t* o_done = bars + 12;
-  uint64_t* drain = bars + 13;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
+  uint64_t* p_full = bars + 11;    // [2] one per P buffer
+  uint64_t* o_done = bars + 13;    // [2] one per P buffer
+  uint64_t* drain = bars + 15;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   // ---- which tile: longest (latest tokens) first for load balance
@@ -102,7 +102,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1) attn_tc_kernel(const __grid_con
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 14; ++i) mbar_init(&bars[i], (i == 9 || i == 10 || i == 11) ? 128 : 1);
+    for (int i = 0; i < 16; ++i) mbar_init(&bars[i], (i == 9 || i == 10 || i == 11 || i == 12) ? 128 : 1);
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&p.tmQ);
@@ -143,10 +143,11 @@ __global__ void __launch_bounds__(AT_THREADS, 1) attn_tc_kernel(const __grid_con
       tc_fence_after();
       auto issue_pv = [&](int i) -> bool {
         const int st = i & 1;
-        if (!mbar_wait(p_full, i & 1, abort_flag, p.status)) return false;
+        const int pb = i & 1;
+        if (!mbar_wait(&p_full[pb], (i >> 1) & 1, abort_flag, p.status)) return false;
         if (!mbar_wait(&v_full[st], (i >> 1) & 1, abort_flag, p.status)) return false;
         tc_fence_after();
-        const uint32_t pa = sbase + L::OFF_P;
+        const uint32_t pa = sbase + L::OFF_P + pb * L::P;
         const uint32_t va = sbase + L::OFF_V + st * L::KV;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {   // 16 keys per step
@@ -154,7 +155,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1) attn_tc_kernel(const __grid_con
           const uint64_t bd = sdesc_sw128(va + k * 2048, 16384, 1024);
           tc_mma(tO, ad, bd, idesc_o, (i > 0 || k > 0) ? 1u : 0u);
         }
-        tc_commit(o_done);
+        tc_commit(&o_done[pb]);
         tc_commit(&kv_empty[st]);
         return true;
       };
@@ -189,7 +190,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1) attn_tc_kernel(const __grid_con
     const int full_tiles = (p.pos0 + t0 + 1) / 128;     // tiles entirely visible to every row
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
-    uint8_t* prow = smem + L::OFF_P + row * 128;
+    uint8_t* prow0 = smem + L::OFF_P + row * 128;
     const int sw = row & 7;
     for (int j = 0; j < n_tiles; ++j) {
       const int st = j & 1;
@@ -219,10 +220,10 @@ __global__ void __launch_bounds__(AT_THREADS, 1) attn_tc_kernel(const __grid_con
 #pragma unroll
       for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
       const float mt = mx * p.scale_log2;
-      // P_{j-1} V_{j-1} must be finished before O or the P buffer is touched.
-      if (j > 0) {
-        if (!mbar_wait(o_done, (j - 1) & 1, abort_flag, p.status)) { ok = false; break; }
-        tc_fence_after();
+      const int pb = j & 1;
+      // P buffer pb is free once P_{j-2} V_{j-2} (the same buffer) has completed
+      if (j >= 2) {
+        if (!mbar_wait(&o_done[pb], ((j - 2) >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
       }
       float alpha = 1.f;
       bool resc = false;
@@ -234,6 +235,9 @@ __global__ void __launch_bounds__(AT_THREADS, 1) attn_tc_kernel(const __grid_con
         resc = true;
       }
       if (j > 0 && __any_sync(0xffffffffu, resc)) {
+        // rescaling O needs every P V issued so far (up to tile j-1) to have completed
+        if (!mbar_wait(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
+        tc_fence_after();
         l *= alpha;
 #pragma unroll 1
         for (int c = 0; c < HD / 32; ++c) {
@@ -259,14 +263,14 @@ __global__ void __launch_bounds__(AT_THREADS, 1) attn_tc_kernel(const __grid_con
           lsum += __uint_as_float(w[e] << 16) + __uint_as_float(w[e] & 0xFFFF0000u);
         }
         const int atom = c >> 3, chunk = (c & 7) ^ sw;
-        *reinterpret_cast<uint4*>(prow + atom * 16384 + chunk * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(prow0 + pb * L::P + atom * 16384 + chunk * 16) = make_uint4(w[0], w[1], w[2], w[3]);
       }
       l += lsum;
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(p_full);
+      mbar_arrive(&p_full[pb]);
     }
-    if (ok && mbar_wait(o_done, (n_tiles - 1) & 1, abort_flag, p.status)) {
+    if (ok && mbar_wait(&o_done[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1, abort_flag, p.status)) {
       tc_fence_after();
       const float inv = 1.f / l;
       const bool live = tok < p.S;

@@ -45,9 +45,9 @@ struct DaSmem {
   static constexpr uint32_t OFF_K = 0;
   static constexpr uint32_t OFF_V = OFF_K + DA_STAGES * KV;
   static constexpr uint32_t OFF_Q = OFF_V + DA_STAGES * KV;   // 2 buffers
-  static constexpr uint32_t OFF_P = OFF_Q + 2 * QB;
-  static constexpr uint32_t OFF_RED = OFF_P + PB;             // [4 warps][16] floats
-  static constexpr uint32_t OFF_BAR = OFF_RED + 4 * 16 * 4;
+  static constexpr uint32_t OFF_P = OFF_Q + 2 * QB;           // 2 buffers
+  static constexpr uint32_t OFF_RED = OFF_P + 2 * PB;         // [3][4 warps][16] floats
+  static constexpr uint32_t OFF_BAR = OFF_RED + 3 * 4 * 16 * 4;
   static constexpr uint32_t TOTAL = OFF_BAR + 256 + 1024;
 };
 
@@ -106,18 +106,18 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_kernel(const __grid
   uint64_t* q_empty = bars + 11;            // [2]
   uint64_t* s_full = bars + 13;             // [2]
   uint64_t* s_free = bars + 15;             // [2]  (128 arrivals)
-  uint64_t* p_full = bars + 17;             //      (128 arrivals)
-  uint64_t* o_done = bars + 18;
-  uint64_t* o_free = bars + 19;             //      (128 arrivals)
-  uint64_t* drain = bars + 20;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 21);
+  uint64_t* p_full = bars + 17;             // [2]  (128 arrivals), one per P buffer
+  uint64_t* o_done = bars + 19;             // [2]  one per P buffer
+  uint64_t* o_free = bars + 21;             //      (128 arrivals)
+  uint64_t* drain = bars + 22;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 23);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* red = reinterpret_cast<float*>(smem + L::OFF_RED);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 21; ++i) {
-      const bool many = (i == 15 || i == 16 || i == 17 || i == 19);
+    for (int i = 0; i < 23; ++i) {
+      const bool many = (i == 15 || i == 16 || i == 17 || i == 18 || i == 21);
       mbar_init(&bars[i], many ? 128 : 1);
     }
     *abort_flag = 0;
@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_kernel(const __grid
     tma_prefetch_desc(&p.tmQ);
   }
   // Q operand rows r..15 and the padded P^T rows stay zero for the whole kernel.
-  for (int i = threadIdx.x; i < (int)(2 * L::QB + L::PB) / 16; i += DA_THREADS)
+  for (int i = threadIdx.x; i < (int)(2 * L::QB + 2 * L::PB) / 16; i += DA_THREADS)
     reinterpret_cast<uint4*>(smem + L::OFF_Q)[i] = make_uint4(0, 0, 0, 0);
   fence_proxy_async_smem();
   if (warp == 1) { tmem_alloc(tmem_slot, DA_TMEM_COLS); tmem_relinquish(); }
@@ -198,20 +198,21 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_kernel(const __grid
         auto issue_pv = [&](int j) -> bool {
           const int gt = tile + j;
           const int st = gt % DA_STAGES;
-          if (!mbar_wait(p_full, gt & 1, abort_flag, p.status)) return false;
+          const int pb = gt & 1;
+          if (!mbar_wait(&p_full[pb], (gt >> 1) & 1, abort_flag, p.status)) return false;
           if (!mbar_wait(&v_full[st], (gt / DA_STAGES) & 1, abort_flag, p.status)) return false;
           // the first P V of an item overwrites O^T: the previous item's O^T must have been read
           if (j == 0 && !mbar_wait(o_free, (it & 1) ^ 1, abort_flag, p.status)) return false;
           tc_fence_after();
           const uint32_t va = sbase + L::OFF_V + st * L::KV;
-          const uint32_t pa = sbase + L::OFF_P;
+          const uint32_t pa = sbase + L::OFF_P + pb * L::PB;
 #pragma unroll
           for (int k = 0; k < 8; ++k) {     // 16 keys per step
             const uint64_t ad = sdesc_sw128(va + k * 2048, 16384, 1024);           // V^T, MN-major
             const uint64_t bd = sdesc_sw128(pa + (k >> 2) * (L::PB / 2) + (k & 3) * 32, 16, 1024);
             tc_mma(tO, ad, bd, idesc_o, (j > 0 || k > 0) ? 1u : 0u);
           }
-          tc_commit(o_done);
+          tc_commit(&o_done[pb]);
           tc_commit(&kv_empty[st]);
           return true;
         };
@@ -263,18 +264,19 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_kernel(const __grid
           for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
           mx[h] = v;
         }
+        float* rbuf = red + (tile & 1) * 64;    // alternate halves: one barrier per tile suffices
         if (lane < DA_NPAD) {
           float mine = mx[0];
 #pragma unroll
           for (int h = 1; h < DA_NPAD; ++h) if (lane == h) mine = mx[h];
-          red[qw * 16 + lane] = mine;
+          rbuf[qw * 16 + lane] = mine;
         }
         softmax_sync();
         float alpha[DA_NPAD];
         bool resc = false;
 #pragma unroll
         for (int h = 0; h < DA_NPAD; ++h) {
-          const float tm = fmaxf(fmaxf(red[h], red[16 + h]), fmaxf(red[32 + h], red[48 + h]));
+          const float tm = fmaxf(fmaxf(rbuf[h], rbuf[16 + h]), fmaxf(rbuf[32 + h], rbuf[48 + h]));
           alpha[h] = 1.f;
           if (h < r) {
             if (m_ref[h] == -INFINITY) {
@@ -286,12 +288,17 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_kernel(const __grid
             }
           }
         }
-        softmax_sync();     // everyone has read `red` before the next tile overwrites it
-        // O^T and the P buffer are free once the previous tile's P V has completed
-        if (tt > t0) {
-          if (!mbar_wait(o_done, (tile - 1) & 1, abort_flag, p.status)) { ok = false; break; }
+        const int pb = tile & 1;
+        // P buffer pb is free once the P V of tile - 2 (the same buffer) has completed
+        if (tile >= 2) {
+          if (!mbar_wait(&o_done[pb], ((tile - 2) >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
+        }
+        // a rescale of O^T (rare; uniform across the 128 threads, which saw the same maxima) needs
+        // every P V issued so far to have completed
+        if (resc) {
+          if (!mbar_wait(&o_done[(tile - 1) & 1], ((tile - 1) >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
           tc_fence_after();
-          if (resc) {     // uniform across the 128 threads: every thread saw the same maxima
+          {
             uint32_t ov[16];
             tmem_ld16(tO + lane_off, ov);
             tc_wait_ld();
@@ -304,25 +311,25 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_kernel(const __grid
           }
         }
         // P^T rows = heads, columns = keys (K-major, 128B swizzle, two 64-key atoms)
-        uint8_t* pbase = smem + L::OFF_P + (t >> 6) * (L::PB / 2);
+        uint8_t* pbase = smem + L::OFF_P + pb * L::PB + (t >> 6) * (L::PB / 2);
         const int kin = t & 63;
 #pragma unroll
         for (int h = 0; h < DA_NPAD; ++h) {
           if (h < r) {
             const float pv = exp2f(s[h] - m_ref[h]);
-            const __nv_bfloat16 pb = __float2bfloat16_rn(pv);
-            lsum[h] += __bfloat162float(pb);
+            const __nv_bfloat16 pq = __float2bfloat16_rn(pv);
+            lsum[h] += __bfloat162float(pq);
             const int chunk16 = (kin >> 3) ^ (h & 7);
-            *reinterpret_cast<__nv_bfloat16*>(pbase + h * 128 + chunk16 * 16 + (kin & 7) * 2) = pb;
+            *reinterpret_cast<__nv_bfloat16*>(pbase + h * 128 + chunk16 * 16 + (kin & 7) * 2) = pq;
           }
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(p_full);
+        mbar_arrive(&p_full[pb]);
       }
       if (!ok) break;
       // ---- item done: write the unnormalised partial (m, l, O)
-      if (!mbar_wait(o_done, (tile - 1) & 1, abort_flag, p.status)) { ok = false; break; }
+      if (!mbar_wait(&o_done[(tile - 1) & 1], ((tile - 1) >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
       tc_fence_after();
       uint32_t ov[16];
       tmem_ld16(tO + lane_off, ov);
@@ -341,22 +348,24 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_kernel(const __grid
         for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
         lsum[h] = v;
       }
+      float* lbuf = red + 128;
       if (lane < DA_NPAD) {
         float mine = lsum[0];
 #pragma unroll
         for (int h = 1; h < DA_NPAD; ++h) if (lane == h) mine = lsum[h];
-        red[qw * 16 + lane] = mine;
+        lbuf[qw * 16 + lane] = mine;
       }
       softmax_sync();
       if (t < r) {
-        const float l = red[t] + red[16 + t] + red[32 + t] + red[48 + t];
+        const float l = lbuf[t] + lbuf[16 + t] + lbuf[32 + t] + lbuf[48 + t];
         float mm = -INFINITY;
 #pragma unroll
         for (int h = 0; h < DA_NPAD; ++h) if (h == t) mm = m_ref[h];
         p.part_ml[(base + t) * 2 + 0] = mm;
         p.part_ml[(base + t) * 2 + 1] = l;
       }
-      softmax_sync();
+      // lbuf is written again only after the next item's first tile barrier, which every thread
+      // passes after reading it here
     }
   }
   __syncwarp();

@@ -126,10 +126,15 @@ __device__ __forceinline__ void epi_run(const Epi& e, int64_t r, int64_t c, floa
       store_run<n>(e.out, e.out_f32, e.ldo, r, c, v);
       break;
     }
-    case EPI_ATOMIC: {
+    case EPI_ATOMIC: {   // partial sums of a split K range, added into an fp32 buffer
       float* p = static_cast<float*>(e.out) + r * e.ldo + c;
+      if constexpr (n % 4 == 0) {
 #pragma unroll
-      for (int i = 0; i < n; ++i) atomicAdd(p + i, v[i]);
+        for (int i = 0; i < n; i += 4) atomicAdd(reinterpret_cast<float4*>(p + i), make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]));
+      } else {
+#pragma unroll
+        for (int i = 0; i < n; ++i) atomicAdd(p + i, v[i]);
+      }
       break;
     }
     case EPI_QKV: {

@@ -39,6 +39,7 @@ struct __align__(64) TcParams {
   int dual;              // two MMAs per k-step (A hi and A lo) into one accumulator; N tiles of 128
   int max_halves;        // 128-column halves per tile: 2, or 1 (dual / skinny)
   int k_splits, kb_per_split, num_units;
+  int split_rows;        // 1: split s writes rows s*M + r (fp32 partials); 0: all splits write row r
   int n_halves;          // 128-column halves of the virtual N
   int seg_half_end[3];   // cumulative halves per B segment
   int nseg;
@@ -189,7 +190,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tc_kernel(const __grid_co
       tc_fence_after();
       const int64_t r = (int64_t)mb * TM + q * 32 + lane;
       const bool live = r < p.M;
-      const int64_t r_out = r + (int64_t)split * p.M;    // split-K partials: [k_splits, M, N]
+      const int64_t r_out = p.split_rows ? r + (int64_t)split * p.M : r;   // partials: [k_splits, M, N]
       const uint32_t tb = tmem + buf * 256 + lane_base;
       if (p.swiglu) {
 #pragma unroll 1
@@ -244,7 +245,8 @@ int gemm_tc_effective_splits(int64_t K, int requested) {
 bool gemm_tc_supported(const GemmDesc& g) {
   if (g.dtype != LLAMA_BF16 || g.M <= 0 || g.K <= 0 || g.K % 8 != 0 || g.lda != g.K) return false;
   if (g.A_lo && ((reinterpret_cast<uintptr_t>(g.A_lo) & 15) || g.epi.kind == EPI_SWIGLU)) return false;
-  if (g.k_splits > 1 && (g.epi.kind != EPI_STORE || !g.epi.out_f32 || g.epi.row_scale)) return false;
+  if (g.k_splits > 1 && ((g.epi.kind != EPI_STORE && g.epi.kind != EPI_ATOMIC) || !g.epi.out_f32 || g.epi.row_scale))
+    return false;
   if (g.K > (int64_t)1 << 30 || g.M > (int64_t)1 << 30) return false;
   if (reinterpret_cast<uintptr_t>(g.A) & 15) return false;
   const int ns = g.epi.kind == EPI_SWIGLU ? 2 : g.nseg;
@@ -293,6 +295,7 @@ int launch_gemm_tc(const GemmDesc& g, int num_sms, unsigned* status, cudaStream_
   p.kb_per_split = (nkb + ks - 1) / ks;
   p.k_splits = (nkb + p.kb_per_split - 1) / p.kb_per_split;
   p.num_units = p.num_tiles * p.k_splits;
+  p.split_rows = (p.k_splits > 1 && g.epi.kind == EPI_STORE) ? 1 : 0;
   p.status = status;
   p.epi = g.epi;
   int dev = 0;
