@@ -191,7 +191,8 @@ int run_gemm(const GemmDesc& g, const char* role, cudaStream_t st) {
   if (tc) {
     unsigned* status = status_ptr();
     if (!status) return LLAMA_ERR_CUDA;
-    if (launch_gemm_tc(g, num_sms(), status, st) != 0) return LLAMA_ERR_CUDA;
+    const int rc = gemm_tc2_supported(g) ? launch_gemm_tc2(g, status, st) : launch_gemm_tc(g, num_sms(), status, st);
+    if (rc != 0) return LLAMA_ERR_CUDA;
   } else {
     if (launch_gemm_simt(g, st) != 0) return LLAMA_ERR_CUDA;
   }

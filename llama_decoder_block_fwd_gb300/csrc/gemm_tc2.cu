@@ -1,0 +1,336 @@
+// tcgen05 GEMM on SM pairs (cta_group::2) for the prefill projections:
+// D[M, N] = A[M, K] * B[N, K]^T, bf16 operands, fp32 accumulation, same epilogues as gemm_tc.cu.
+//
+// A cluster of two CTAs owns a 256 x 256 output tile.  CTA r (r = 0, 1) stages rows
+// 128r..128r+127 of the A tile and the r-th 128-row half of the B tile; the leader (r = 0) issues
+// tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16), which reads both CTAs' shared memory and
+// leaves rows 128r.. of the accumulator in CTA r's tensor memory.  Per SM and k-step this moves
+// half the B bytes of the one-SM 128 x 256 tile through shared memory, which is what lets the
+// tensor pipe run near its rate.
+//   * TMA loads of both CTAs complete on the leader's stage barrier (.cta_group::2 form);
+//   * the leader's commits are multicast to the stage and accumulator barriers of both CTAs;
+//   * both CTAs' epilogue threads release an accumulator on the leader's barrier.
+// Tiles are walked in bands of 8 column tiles as in gemm_tc.cu; the grid holds as many clusters
+// as can be resident at once (persistent).
+#include <algorithm>
+#include <cstring>
+
+#include "epilogue.cuh"
+#include "kernels.h"
+
+namespace llama {
+namespace {
+
+constexpr int T2M = 256, T2N = 256, T2K = 64, S2 = 6, BAND2 = 8;
+constexpr uint32_t A2_BYTES = 128 * T2K * 2;    // this CTA's 128 rows of A: 16 KB
+constexpr uint32_t B2_BYTES = 128 * T2K * 2;    // this CTA's 128-row half of B: 16 KB
+constexpr uint32_t STAGE2 = A2_BYTES + B2_BYTES;
+constexpr uint32_t SMEM2 = S2 * STAGE2 + 1024 + 256;
+constexpr int THREADS2 = 192;
+constexpr uint32_t TMEM2_COLS = 512;
+
+struct __align__(64) Tc2Params {
+  CUtensorMap tmA;
+  CUtensorMap tmB[3];
+  int M, K;
+  int n_halves;
+  int seg_half_end[3];
+  int nseg;
+  int swiglu;
+  int m_tiles, n_tiles, num_tiles;
+  unsigned* status;
+  Epi epi;
+};
+
+__device__ __forceinline__ void tile2_coords(const Tc2Params& p, int t, int& mb, int& nb) {
+  const int band_tiles = p.m_tiles * BAND2;
+  const int band = t / band_tiles;
+  const int rem = t - band * band_tiles;
+  const int gw = min(BAND2, p.n_tiles - band * BAND2);
+  nb = band * BAND2 + rem % gw;
+  mb = rem / gw;
+}
+
+__device__ __forceinline__ void half2_source(const Tc2Params& p, int nb, int hh, int& seg, int& row) {
+  if (p.swiglu) { seg = hh; row = nb * 128; return; }
+  const int gh = 2 * nb + hh;
+  seg = 0;
+  int start = 0;
+  while (seg < p.nseg - 1 && gh >= p.seg_half_end[seg]) { start = p.seg_half_end[seg]; ++seg; }
+  row = (gh - start) * 128;
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait with cluster-scope acquire (for barriers that receive the peer CTA's arrivals).
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                                  unsigned* status) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_try_wait_cluster(a, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait_cluster(a, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*abort) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        atomicOr(status, STATUS_TIMEOUT);
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* m, uint32_t leader_bar, int x,
+                                                 int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(leader_bar)
+      : "memory");
+}
+__device__ __forceinline__ void tc2_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive on the barrier at this shared-memory offset in every CTA of `mask` once all tcgen05
+// operations issued so far by this thread have completed.
+__device__ __forceinline__ void tc2_commit_mc(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(mask)
+      : "memory");
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS2, 1)
+    gemm_tc2_kernel(const __grid_constant__ Tc2Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S2 * STAGE2);   // used in the leader
+  uint64_t* empty = full + S2;                                         // both CTAs
+  uint64_t* acc_full = empty + S2;                                     // both CTAs
+  uint64_t* acc_empty = acc_full + 2;                                  // used in the leader
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;
+  const int cluster_id = (int)(blockIdx.x >> 1), n_clusters = (int)(gridDim.x >> 1);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S2; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
+    for (int b = 0; b < 2; ++b) { mbar_init(&acc_full[b], 1); mbar_init(&acc_empty[b], 2 * 128); }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&p.tmA);
+    for (int s = 0; s < p.nseg; ++s) tma_prefetch_desc(&p.tmB[s]);
+  }
+  if (warp == 1) {   // one warp in each CTA of the pair allocates, jointly
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                 "r"(TMEM2_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  cluster_sync_all();     // barriers of both CTAs initialised before any remote use
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int nkb = (p.K + T2K - 1) / T2K;
+  const uint32_t smem_base = smem_u32(smem);
+
+  if (warp == 0) {
+    if (lane == 0) {  // ---------------- TMA producer (both CTAs)
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int t = cluster_id; t < p.num_tiles; t += n_clusters) {
+        int mb, nb, seg, row;
+        tile2_coords(p, t, mb, nb);
+        half2_source(p, nb, (int)rank, seg, row);
+        bool ok = true;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) { ok = false; break; }
+          const uint32_t lbar = map_to_rank(smem_u32(&full[stage]), 0);
+          if (leader) mbar_arrive_expect_tx(&full[stage], 2 * STAGE2);   // both CTAs' bytes
+          const uint32_t sa = smem_base + stage * STAGE2;
+          tma_load_2d_pair(sa, &p.tmA, lbar, kb * T2K, mb * T2M + (int)rank * 128);
+          tma_load_2d_pair(sa + A2_BYTES, &p.tmB[seg], lbar, kb * T2K, row);
+          if (++stage == S2) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && leader) {  // ---------------- MMA issuer (leader CTA only)
+      const uint32_t idesc = idesc_bf16(T2M, T2N);
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      for (int t = cluster_id; t < p.num_tiles; t += n_clusters, ++it) {
+        const int buf = it & 1;
+        const uint32_t aphase = (it >> 1) & 1;
+        if (!mbar_wait_cluster(&acc_empty[buf], aphase ^ 1, abort_flag, p.status)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + buf * 256;
+        bool ok = true;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait_cluster(&full[stage], phase, abort_flag, p.status)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = smem_base + stage * STAGE2;
+          const uint32_t sb = sa + A2_BYTES;
+#pragma unroll
+          for (int k = 0; k < T2K / 16; ++k)
+            tc2_mma(d, sdesc_sw128(sa + k * 32, 16, 1024), sdesc_sw128(sb + k * 32, 16, 1024), idesc,
+                    (kb | k) != 0);
+          tc2_commit_mc(&empty[stage], 0x3);
+          if (++stage == S2) { stage = 0; phase ^= 1; }
+        }
+        if (!ok) break;
+        tc2_commit_mc(&acc_full[buf], 0x3);
+      }
+      int no_abort = 0;
+      tc2_commit_mc(drain, 0x1);
+      mbar_wait(drain, 0, &no_abort, p.status);
+    }
+  } else {  // ---------------- epilogue warps 2..5 (both CTAs)
+    const int q = warp & 3;
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    int it = 0;
+    for (int t = cluster_id; t < p.num_tiles; t += n_clusters, ++it) {
+      int mb, nb;
+      tile2_coords(p, t, mb, nb);
+      const int buf = it & 1;
+      const uint32_t aphase = (it >> 1) & 1;
+      if (!mbar_wait(&acc_full[buf], aphase, abort_flag, p.status)) break;
+      tc_fence_after();
+      const int64_t r = (int64_t)mb * T2M + rank * 128 + q * 32 + lane;
+      const bool live = r < p.M;
+      const uint32_t tb = tmem + buf * 256 + lane_base;
+      if (p.swiglu) {
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t g[32], u[32];
+          tmem_ld32(tb + c * 32, g);
+          tmem_ld32(tb + 128 + c * 32, u);
+          tc_wait_ld();
+          if (live) {
+            float gv[32], uv[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) { gv[i] = __uint_as_float(g[i]); uv[i] = __uint_as_float(u[i]); }
+            epi_run<32>(p.epi, r, (int64_t)nb * 128 + c * 32, gv, uv);
+          }
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < 8; ++c) {
+          uint32_t v[32];
+          tmem_ld32(tb + c * 32, v);
+          tc_wait_ld();
+          if (live) {
+            float fv[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) fv[i] = __uint_as_float(v[i]);
+            epi_run<32>(p.epi, r, (int64_t)nb * T2N + c * 32, fv, fv);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive_cluster(map_to_rank(smem_u32(&acc_empty[buf]), 0));
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  cluster_sync_all();    // the pair is done with tensor memory and with each other's barriers
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM2_COLS) : "memory");
+  }
+}
+
+}  // namespace
+
+bool gemm_tc2_supported(const GemmDesc& g) {
+  if (!gemm_tc_supported(g) || g.A_lo || g.k_splits > 1 || g.narrow) return false;
+  if (g.M < 256) return false;
+  const int ns = g.epi.kind == EPI_SWIGLU ? 2 : g.nseg;
+  int64_t halves = 0;
+  for (int s = 0; s < ns; ++s) halves += g.nB[s] / 128;
+  return g.epi.kind == EPI_SWIGLU || halves % 2 == 0;   // every tile has both 128-row halves
+}
+
+int launch_gemm_tc2(const GemmDesc& g, unsigned* status, cudaStream_t st) {
+  Tc2Params p;
+  memset(&p, 0, sizeof(p));
+  const int ns = g.epi.kind == EPI_SWIGLU ? 2 : g.nseg;
+  if (!encode_tmap_2d_bf16(&p.tmA, g.A, (uint64_t)g.K, (uint64_t)g.M, (uint64_t)g.lda * 2, T2K, 128)) return -1;
+  int64_t halves = 0;
+  for (int s = 0; s < ns; ++s) {
+    if (!encode_tmap_2d_bf16(&p.tmB[s], g.B[s], (uint64_t)g.K, (uint64_t)g.nB[s], (uint64_t)g.K * 2, T2K, 128))
+      return -1;
+    halves += g.nB[s] / 128;
+    p.seg_half_end[s] = (int)halves;
+  }
+  p.M = (int)g.M;
+  p.K = (int)g.K;
+  p.nseg = ns;
+  p.swiglu = g.epi.kind == EPI_SWIGLU;
+  p.n_halves = (int)halves;
+  p.m_tiles = (int)((g.M + T2M - 1) / T2M);
+  p.n_tiles = p.swiglu ? (int)(g.nB[0] / 128) : (int)(halves / 2);
+  p.num_tiles = p.m_tiles * p.n_tiles;
+  p.status = status;
+  p.epi = g.epi;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  static int max_clusters[64] = {};
+  if (dev < 0 || dev >= 64) return -1;
+  if (!max_clusters[dev]) {
+    if (cudaFuncSetAttribute(gemm_tc2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM2) != cudaSuccess)
+      return -1;
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(2 * 128, 1, 1);
+    cfg.blockDim = dim3(THREADS2, 1, 1);
+    cfg.dynamicSmemBytes = SMEM2;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_tc2_kernel, &cfg) != cudaSuccess || n <= 0) return -1;
+    max_clusters[dev] = n;
+  }
+  const int clusters = std::max(1, std::min(p.num_tiles, max_clusters[dev]));
+  gemm_tc2_kernel<<<2 * clusters, THREADS2, SMEM2, st>>>(p);
+  return 0;
+}
+
+}  // namespace llama

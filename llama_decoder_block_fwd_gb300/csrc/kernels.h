@@ -82,6 +82,9 @@ int launch_widen_bf16(const void* src, float* dst, int64_t n, cudaStream_t st);
 // tensor-core paths (bf16 only)
 bool gemm_tc_supported(const GemmDesc& g);
 int launch_gemm_tc(const GemmDesc& g, int num_sms, unsigned* status, cudaStream_t st);
+// The SM-pair (cta_group::2) version for large M: 256 x 256 tiles, no dual A / split K.
+bool gemm_tc2_supported(const GemmDesc& g);
+int launch_gemm_tc2(const GemmDesc& g, unsigned* status, cudaStream_t st);
 // The number of K splits launch_gemm_tc uses for a requested count.
 int gemm_tc_effective_splits(int64_t K, int requested);
 bool attn_tc_supported(const AttnDesc& a);
