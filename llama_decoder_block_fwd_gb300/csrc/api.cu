@@ -277,6 +277,7 @@ size_t attn_scratch_bytes(const llama_dims* d, int dtype, int64_t kv_capacity) {
 struct BlockWs {
   void *u, *q, *o, *h, *m, *k, *v;
   float *rs1, *rs2;   // per-row RMSNorm factors of the attention and FFN norms
+  float2* rope_tab;   // [S, hd/2] (cos, sin) of the call's positions
   void* attn;         // split-K attention scratch (one-token steps)
   size_t attn_bytes;
   size_t bytes;
@@ -296,6 +297,7 @@ BlockWs plan_block(const llama_dims* d, int dtype, bool own_kv, void* base, int6
   w.v = own_kv ? c.take(T * d->n_kv * d->head_dim * es) : nullptr;
   w.rs1 = static_cast<float*>(c.take(T * 4));
   w.rs2 = static_cast<float*>(c.take(T * 4));
+  w.rope_tab = static_cast<float2*>(c.take((size_t)d->S * (d->head_dim / 2) * sizeof(float2)));
   w.attn_bytes = attn_scratch_bytes(d, dtype, own_kv ? d->S : kv_capacity);
   w.attn = w.attn_bytes ? c.take(w.attn_bytes) : nullptr;
   w.bytes = c.off;
@@ -330,7 +332,7 @@ DecodeWs plan_decode(const llama_dims* d, int dtype, void* base, int64_t kv_capa
 
 // The Q/K/V projection with RoPE on Q and K and the K/V write into [B, cap, n_kv*hd] caches.
 int run_qkv(const llama_dims* d, int dtype, const llama_block_weights* w, const void* u, const float* row_scale,
-            void* q, void* kc, void* vc, int64_t cap, int64_t pos0, cudaStream_t st) {
+            void* q, void* kc, void* vc, int64_t cap, int64_t pos0, cudaStream_t st, float2* rope_tab = nullptr) {
   const int64_t T = d->B * d->S, hq = d->n_q * d->head_dim, hkv = d->n_kv * d->head_dim;
   GemmDesc g = make_gemm(dtype, T, u, d->d_model);
   g.nseg = 3;
@@ -349,6 +351,12 @@ int run_qkv(const llama_dims* d, int dtype, const llama_block_weights* w, const 
   g.epi.hd = (int)d->head_dim;
   g.epi.row_scale = row_scale;
   rope_freqs(d, g.epi.freq);
+  if (rope_tab) {   // one (cos, sin) per position and frequency, shared by every head of the token
+    prof::begin("rope_table", st);
+    if (launch_rope_table(rope_tab, d->S, (int)d->head_dim, pos0, g.epi.freq, st) != 0) return LLAMA_ERR_CUDA;
+    prof::end(st);
+    g.epi.rope_tab = rope_tab;
+  }
   return run_gemm(g, nullptr, st);
 }
 
@@ -418,7 +426,7 @@ int block_body(const llama_dims* d, int dtype, const llama_block_weights* w, con
   if ((rc = run_rmsnorm(dtype, x_f32 || f32, f32, x, w->attn_norm_g, ws.u, T, D, eps, st, ws.rs1)) != LLAMA_OK)
     return rc;
   // q, k, v with RoPE; k, v written into the cache at pos0..pos0+S-1
-  if ((rc = run_qkv(d, dtype, w, ws.u, ws.rs1, ws.q, kc, vc, cap, pos0, st)) != LLAMA_OK) return rc;
+  if ((rc = run_qkv(d, dtype, w, ws.u, ws.rs1, ws.q, kc, vc, cap, pos0, st, ws.rope_tab)) != LLAMA_OK) return rc;
   // o = causal GQA attention
   AttnDesc a = make_attn(d, dtype, ws.q, kc, vc, ws.o, cap, pos0);
   a.ws = ws.attn;
@@ -812,6 +820,7 @@ int llama_stack_decode_step(const llama_dims* d, int dtype, int n_layers, const 
   BlockWs b;
   b.u = dw.u; b.q = dw.q; b.o = dw.o; b.h = nullptr; b.m = dw.m; b.k = nullptr; b.v = nullptr; b.bytes = 0;
   b.rs1 = dw.rs1; b.rs2 = dw.rs2;
+  b.rope_tab = nullptr;   // one position per step: computed in the epilogue
   b.attn = dw.attn; b.attn_bytes = dw.attn_bytes;
   for (int l = 0; l < n_layers; ++l) {
     void* kc = static_cast<char*>(k_cache) + l * layer_cache;

@@ -1,4 +1,4 @@
-// tcgen05 causal GQA flash attention (prefill and chunked prefill against a cache).
+// tcgen05 causal GQA flash attention (prefill, and chunked prefill against a cache).
 //
 // What it computes ("Llama Architecture ...", Mathematical Foundations 4; "LLaMA-3 8B ...",
 // section 四.4): for query head h at absolute position m and its KV head g = h / r,
@@ -8,19 +8,20 @@
 // the same up to the order of floating-point additions.
 //
 // Layout of the work (sm_103a):
-//   * A CTA owns one Q tile of 128 rows = (128/r) consecutive tokens x the r query heads of one
-//     KV group, so every K/V tile staged in shared memory serves all r heads of the group.
-//     The tile is one 3-D TMA box of Q [B*S, n_q, hd]: rows are (token, head) pairs.
-//   * warp 0 (one thread): TMA loads of Q once and of K/V tiles (128 keys x hd) into a
-//     2-stage ring.  K/V use a 4-D tensor map whose position extent is the number of valid keys,
-//     so positions past the cached ones read as zeros.
-//   * warp 1 (one thread): tcgen05.mma S = Q K^T (M=128, N=128, K=hd) into one of two TMEM
-//     score buffers, then O += P V (M=128, N=hd, K=128; V is the MN-major operand).  S_{j+1}
-//     is issued before P_j V_j so scores are ready when the softmax warps need them.
-//   * warps 2-5 (one thread per row = TMEM lane): read S, mask, keep the running max m and sum
-//     l, write P = exp2(S*scale*log2e - m) as bf16 into shared memory (128B swizzle), and
-//     rescale O in TMEM only when the row max grew by more than 2^8 (the bound keeps P <= 256).
-//     At the end they divide O by l and store bf16 rows.
+//   * A Q tile is 128 rows = (128/r) consecutive tokens x the r query heads of one KV group (one
+//     3-D TMA box of Q [B*S, n_q, hd]).  A CTA owns TWO Q tiles of the same group (adjacent token
+//     blocks), so each K/V tile staged in shared memory serves 2 x r query heads, and two softmax
+//     warp groups take turns with the tensor core.
+//   * warp 0 (one thread): TMA loads of both Q tiles once, then K/V tiles (128 keys x hd) into a
+//     2-stage ring.  K/V use a 4-D tensor map whose position extent is the number of valid keys.
+//   * warp 1 (one thread): per Q tile X and key tile j it issues S_X = Q_X K_j^T (M=128, N=128,
+//     K=hd) into TMEM, then, once the softmax has written P_X, O_X += P_X V_j with P_X read from
+//     TMEM (it overwrites S_X's columns) and V the MN-major operand, then S_X for tile j+1.
+//   * warps 2-5 / 6-9 (one thread per row = TMEM lane, one group per Q tile): read S in two
+//     passes (row max, then P = exp2(S*scale*log2e - m)), write P back to TMEM as bf16, keep the
+//     running sum, and rescale O in TMEM only when the row max grew by more than 2^8.  At the end
+//     they divide O by the sum and store bf16 rows.
+// TMEM: S_0 [0,128), S_1 [128,256), O_0 [256,384), O_1 [384,512).
 #include <algorithm>
 #include <cstring>
 
@@ -29,7 +30,7 @@
 namespace llama {
 namespace {
 
-constexpr int AT_THREADS = 192;
+constexpr int AT_THREADS = 320;
 constexpr uint32_t TMEM_COLS_ATTN = 512;
 constexpr float kRescaleLog2 = 8.0f;
 
@@ -38,7 +39,7 @@ struct __align__(64) AttnParams {
   CUtensorMap tmK;   // [B, kv_len, n_kv, hd], box (64, 1, 128, 1)
   CUtensorMap tmV;
   uint16_t* o;       // [B, S, n_q, hd]
-  int B, S, n_q, n_kv, hd, r, tokens_per_tile, t_blocks;
+  int B, S, n_q, n_kv, hd, r, tokens_per_tile, t_blocks, pairs;
   int pos0;
   float scale_log2;  // log2(e) / sqrt(hd)
   unsigned* status;
@@ -46,14 +47,12 @@ struct __align__(64) AttnParams {
 
 template <int HD>
 struct Smem {
-  static constexpr uint32_t Q = 128 * HD * 2;       // Q tile
+  static constexpr uint32_t QT = 128 * HD * 2;      // one Q tile
   static constexpr uint32_t KV = 128 * HD * 2;      // one K or V tile
-  static constexpr uint32_t P = 128 * 128 * 2;      // P tile (bf16)
-  static constexpr uint32_t OFF_Q = 0;
-  static constexpr uint32_t OFF_K = OFF_Q + Q;               // 2 stages
-  static constexpr uint32_t OFF_V = OFF_K + 2 * KV;          // 2 stages
-  static constexpr uint32_t OFF_P = OFF_V + 2 * KV;          // 2 buffers
-  static constexpr uint32_t OFF_BAR = OFF_P + 2 * P;
+  static constexpr uint32_t OFF_Q = 0;              // 2 Q tiles
+  static constexpr uint32_t OFF_K = OFF_Q + 2 * QT; // 2 stages
+  static constexpr uint32_t OFF_V = OFF_K + 2 * KV; // 2 stages
+  static constexpr uint32_t OFF_BAR = OFF_V + 2 * KV;
   static constexpr uint32_t TOTAL = OFF_BAR + 256 + 1024;
 };
 
@@ -64,6 +63,20 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* m, 
       " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
       : "memory");
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// 2^x with one MUFU instruction (PTX ex2.approx.ftz: relative error about 2^-22, subnormal
+// results flushed to zero -- exact enough for P, which is rounded to bf16).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -79,30 +92,38 @@ __global__ void __launch_bounds__(AT_THREADS, 1) attn_tc_kernel(const __grid_con
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
   uint64_t* q_full = bars + 0;
-  uint64_t* k_full = bars + 1;     // [2]
+  uint64_t* k_full = bars + 1;     // [2] per stage
   uint64_t* v_full = bars + 3;     // [2]
   uint64_t* kv_empty = bars + 5;   // [2]
-  uint64_t* s_full = bars + 7;     // [2]
-  uint64_t* s_free = bars + 9;     // [2]
-  uint64_t* p_full = bars + 11;    // [2] one per P buffer
-  uint64_t* o_done = bars + 13;    // [2] one per P buffer
-  uint64_t* drain = bars + 15;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  uint64_t* s_full = bars + 7;     // [2] per Q tile
+  uint64_t* p_full = bars + 9;     // [2] per Q tile (128 arrivals)
+  uint64_t* o_done = bars + 11;    // [2] per Q tile
+  uint64_t* drain = bars + 13;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
-  // ---- which tile: longest (latest tokens) first for load balance
+  // ---- the two Q tiles: token blocks 2*pair+1 (X=0, the later one, with at least as many key
+  //      tiles) and 2*pair (X=1); pairs with the most work run first
   const int groups = p.B * p.n_kv;
-  const int tb = p.t_blocks - 1 - (int)(blockIdx.x / groups);
+  const int pair = p.pairs - 1 - (int)(blockIdx.x / groups);
   const int bg = (int)(blockIdx.x % groups);
   const int b = bg / p.n_kv, g = bg % p.n_kv;
-  const int t0 = tb * p.tokens_per_tile;
-  const int t_end = min(t0 + p.tokens_per_tile, p.S);
-  const int last_key = p.pos0 + t_end - 1;               // largest position any valid row sees
-  const int n_tiles = last_key / 128 + 1;
+  int t0[2], ntile[2], full_tiles[2];
+#pragma unroll
+  for (int x = 0; x < 2; ++x) {
+    const int tb = 2 * pair + 1 - x;
+    t0[x] = tb * p.tokens_per_tile;
+    if (tb >= p.t_blocks) { ntile[x] = 0; full_tiles[x] = 0; continue; }
+    const int t_end = min(t0[x] + p.tokens_per_tile, p.S);
+    ntile[x] = (p.pos0 + t_end - 1) / 128 + 1;          // key tiles any valid row of the tile sees
+    full_tiles[x] = (p.pos0 + t0[x] + 1) / 128;          // tiles entirely visible to every row
+  }
+  const int nmax = max(ntile[0], ntile[1]);
+  const int nq_tiles = (ntile[0] > 0) + (ntile[1] > 0);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 16; ++i) mbar_init(&bars[i], (i == 9 || i == 10 || i == 11 || i == 12) ? 128 : 1);
+    for (int i = 0; i < 14; ++i) mbar_init(&bars[i], (i == 9 || i == 10) ? 128 : 1);
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&p.tmQ);
@@ -115,15 +136,16 @@ __global__ void __launch_bounds__(AT_THREADS, 1) attn_tc_kernel(const __grid_con
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t tS = tmem;              // S buffers at columns 0 and 128
-  const uint32_t tO = tmem + 256;        // O at columns 256 .. 256+HD-1
 
   if (warp == 0) {
     if (lane == 0) {  // ------------------------------------------------ TMA producer
-      mbar_arrive_expect_tx(q_full, L::Q);
-      for (int hh = 0; hh < HALVES; ++hh)
-        tma_load_3d(sbase + L::OFF_Q + hh * 16384, &p.tmQ, q_full, hh * 64, g * p.r, b * p.S + t0);
-      for (int j = 0; j < n_tiles; ++j) {
+      mbar_arrive_expect_tx(q_full, nq_tiles * L::QT);
+      for (int x = 0; x < 2; ++x) {
+        if (ntile[x] == 0) continue;
+        for (int hh = 0; hh < HALVES; ++hh)
+          tma_load_3d(sbase + L::OFF_Q + x * L::QT + hh * 16384, &p.tmQ, q_full, hh * 64, g * p.r, b * p.S + t0[x]);
+      }
+      for (int j = 0; j < nmax; ++j) {
         const int st = j & 1;
         const uint32_t ph = (j >> 1) & 1;
         if (!mbar_wait(&kv_empty[st], ph ^ 1, abort_flag, p.status)) break;
@@ -141,136 +163,149 @@ __global__ void __launch_bounds__(AT_THREADS, 1) attn_tc_kernel(const __grid_con
       const uint32_t idesc_o = idesc_bf16(128, HD, /*b_mn_major=*/true);
       bool ok = mbar_wait(q_full, 0, abort_flag, p.status);
       tc_fence_after();
-      auto issue_pv = [&](int i) -> bool {
-        const int st = i & 1;
-        const int pb = i & 1;
-        if (!mbar_wait(&p_full[pb], (i >> 1) & 1, abort_flag, p.status)) return false;
-        if (!mbar_wait(&v_full[st], (i >> 1) & 1, abort_flag, p.status)) return false;
-        tc_fence_after();
-        const uint32_t pa = sbase + L::OFF_P + pb * L::P;
-        const uint32_t va = sbase + L::OFF_V + st * L::KV;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {   // 16 keys per step
-          const uint64_t ad = sdesc_sw128(pa + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(va + k * 2048, 16384, 1024);
-          tc_mma(tO, ad, bd, idesc_o, (i > 0 || k > 0) ? 1u : 0u);
-        }
-        tc_commit(&o_done[pb]);
-        tc_commit(&kv_empty[st]);
-        return true;
-      };
-      for (int j = 0; ok && j < n_tiles; ++j) {
+      auto issue_s = [&](int x, int j) -> bool {
         const int st = j & 1;
-        const uint32_t ph = (j >> 1) & 1;
-        if (!mbar_wait(&k_full[st], ph, abort_flag, p.status)) { ok = false; break; }
-        if (!mbar_wait(&s_free[st], ph ^ 1, abort_flag, p.status)) { ok = false; break; }
+        if (!mbar_wait(&k_full[st], (j >> 1) & 1, abort_flag, p.status)) return false;
         tc_fence_after();
         const uint32_t ka = sbase + L::OFF_K + st * L::KV;
-        const uint32_t qa = sbase + L::OFF_Q;
+        const uint32_t qa = sbase + L::OFF_Q + x * L::QT;
 #pragma unroll
         for (int k = 0; k < HD / 16; ++k) {
           const uint64_t ad = sdesc_sw128(qa + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
           const uint64_t bd = sdesc_sw128(ka + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
-          tc_mma(tS + st * 128, ad, bd, idesc_s, k > 0 ? 1u : 0u);
+          tc_mma(tmem + x * 128, ad, bd, idesc_s, k > 0 ? 1u : 0u);
         }
-        tc_commit(&s_full[st]);
-        if (j > 0 && !issue_pv(j - 1)) { ok = false; break; }
+        tc_commit(&s_full[x]);
+        return true;
+      };
+      auto issue_pv = [&](int x, int j) -> bool {
+        const int st = j & 1;
+        if (!mbar_wait(&p_full[x], j & 1, abort_flag, p.status)) return false;
+        if (!mbar_wait(&v_full[st], (j >> 1) & 1, abort_flag, p.status)) return false;
+        tc_fence_after();
+        const uint32_t va = sbase + L::OFF_V + st * L::KV;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {   // 16 keys per step; P_X k-step k is TMEM columns 8k..8k+7
+          const uint64_t bd = sdesc_sw128(va + k * 2048, 16384, 1024);
+          tc_mma_ts(tmem + 256 + x * 128, tmem + x * 128 + k * 8, bd, idesc_o, (j > 0 || k > 0) ? 1u : 0u);
+        }
+        tc_commit(&o_done[x]);
+        return true;
+      };
+      for (int x = 0; ok && x < 2; ++x)
+        if (ntile[x] > 0) ok = issue_s(x, 0);
+      for (int j = 0; ok && j < nmax; ++j) {
+        for (int x = 0; ok && x < 2; ++x) {
+          if (j >= ntile[x]) continue;
+          if (!issue_pv(x, j)) { ok = false; break; }
+          // the last user of key tile j releases its stage
+          const bool last_user = (x == 1) || (j >= ntile[1]);
+          if (last_user) tc_commit(&kv_empty[j & 1]);
+          if (j + 1 < ntile[x] && !issue_s(x, j + 1)) { ok = false; break; }
+        }
       }
-      if (ok) issue_pv(n_tiles - 1);
       int no_abort = 0;
       tc_commit(drain);
       mbar_wait(drain, 0, &no_abort, p.status);
     }
-  } else {  // ------------------------------------------------------------ softmax warps 2..5
+  } else {  // ------------------------------------------------------------ softmax groups
+    const int x = (warp - 2) >> 2;                      // warps 2-5: Q tile 0, warps 6-9: Q tile 1
     const int qw = warp & 3;
     const int row = qw * 32 + lane;                     // TMEM lane = Q tile row
     const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
-    const int tok = t0 + row / p.r;                     // token within the sequence
+    const uint32_t tS = tmem + x * 128 + lane_off;
+    const uint32_t tO = tmem + 256 + x * 128 + lane_off;
+    const int n = ntile[x];
+    const int tok = t0[x] + row / p.r;                  // token within the sequence
     const int qpos = p.pos0 + tok;                      // absolute position of this row
-    const int full_tiles = (p.pos0 + t0 + 1) / 128;     // tiles entirely visible to every row
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
-    uint8_t* prow0 = smem + L::OFF_P + row * 128;
-    const int sw = row & 7;
-    for (int j = 0; j < n_tiles; ++j) {
-      const int st = j & 1;
-      const uint32_t ph = (j >> 1) & 1;
-      if (!mbar_wait(&s_full[st], ph, abort_flag, p.status)) { ok = false; break; }
+    for (int j = 0; j < n; ++j) {
+      if (!mbar_wait(&s_full[x], j & 1, abort_flag, p.status)) { ok = false; break; }
       tc_fence_after();
-      float s[128];
-      {
+      const bool mask = j >= full_tiles[x];
+      const int kbase = j * 128;
+      // pass 1: row maximum (key positions past the query's only on the diagonal tiles)
+      float mx = -INFINITY;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
         uint32_t v[32];
+        tmem_ld32(tS + c * 32, v);
+        tc_wait_ld();
+        if (mask) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          tmem_ld32(tS + st * 128 + lane_off + c * 32, v);
-          tc_wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(v[i]);
+          for (int i = 0; i < 32; ++i)
+            if (kbase + c * 32 + i > qpos) v[i] = __float_as_uint(-INFINITY);
         }
-      }
-      tc_fence_before();
-      mbar_arrive(&s_free[st]);
-      if (j >= full_tiles) {
-        const int kbase = j * 128;
+        float m0 = mx, m1 = -INFINITY;
 #pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (kbase + c > qpos) s[c] = -INFINITY;
+        for (int i = 0; i < 32; i += 4) {
+          m0 = max3(m0, __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
+          m1 = max3(m1, __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+        }
+        mx = fmaxf(m0, m1);
       }
-      float mx = s[0];
-#pragma unroll
-      for (int c = 1; c < 128; ++c) mx = fmaxf(mx, s[c]);
       const float mt = mx * p.scale_log2;
-      const int pb = j & 1;
-      // P buffer pb is free once P_{j-2} V_{j-2} (the same buffer) has completed
-      if (j >= 2) {
-        if (!mbar_wait(&o_done[pb], ((j - 2) >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
-      }
       float alpha = 1.f;
       bool resc = false;
       if (j == 0) {
         m_ref = mt;
       } else if (mt > m_ref + kRescaleLog2) {
-        alpha = exp2f(m_ref - mt);
+        alpha = ex2(m_ref - mt);
         m_ref = mt;
         resc = true;
       }
       if (j > 0 && __any_sync(0xffffffffu, resc)) {
-        // rescaling O needs every P V issued so far (up to tile j-1) to have completed
-        if (!mbar_wait(&o_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
+        // O holds the P V of tiles < j only once P_{j-1} V_{j-1} has completed
+        if (!mbar_wait(&o_done[x], (j - 1) & 1, abort_flag, p.status)) { ok = false; break; }
         tc_fence_after();
         l *= alpha;
 #pragma unroll 1
         for (int c = 0; c < HD / 32; ++c) {
           uint32_t v[32];
-          tmem_ld32(tO + lane_off + c * 32, v);
+          tmem_ld32(tO + c * 32, v);
           tc_wait_ld();
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-          tmem_st32(tO + lane_off + c * 32, v);
+          tmem_st32(tO + c * 32, v);
         }
         tc_wait_st();
       }
+      // pass 2: P = exp2(S * scale_log2 - m) as bf16 pairs into TMEM columns [16c, 16c+16) of S_X
+      // (written only over S columns this pass has already read).  The row sum is taken over the
+      // fp32 values.
       const float mb = m_ref;
-      float lsum = 0.f;
+      float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tS + c * 32, v);
+        tc_wait_ld();
+        if (mask) {
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {      // 16 chunks of 8 keys
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float p0 = exp2f(fmaf(s[c * 8 + 2 * e], p.scale_log2, -mb));
-          const float p1 = exp2f(fmaf(s[c * 8 + 2 * e + 1], p.scale_log2, -mb));
-          w[e] = pack_bf16x2(p0, p1);
-          lsum += __uint_as_float(w[e] << 16) + __uint_as_float(w[e] & 0xFFFF0000u);
+          for (int i = 0; i < 32; ++i)
+            if (kbase + c * 32 + i > qpos) v[i] = __float_as_uint(-INFINITY);
         }
-        const int atom = c >> 3, chunk = (c & 7) ^ sw;
-        *reinterpret_cast<uint4*>(prow0 + pb * L::P + atom * 16384 + chunk * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const float x0 = fmaf(__uint_as_float(v[2 * e]), p.scale_log2, -mb);
+          const float x1 = fmaf(__uint_as_float(v[2 * e + 1]), p.scale_log2, -mb);
+          const float p0 = ex2(x0);
+          const float p1 = ex2(x1);
+          ls0 += p0;
+          ls1 += p1;
+          w[e] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(tS + c * 16, w);
       }
+      const float lsum = ls0 + ls1;
+      tc_wait_st();
       l += lsum;
-      fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(&p_full[pb]);
+      mbar_arrive(&p_full[x]);
     }
-    if (ok && mbar_wait(&o_done[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1, abort_flag, p.status)) {
+    if (ok && n > 0 && mbar_wait(&o_done[x], (n - 1) & 1, abort_flag, p.status)) {
       tc_fence_after();
       const float inv = 1.f / l;
       const bool live = tok < p.S;
@@ -279,7 +314,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1) attn_tc_kernel(const __grid_con
 #pragma unroll 1
       for (int c = 0; c < HD / 32; ++c) {
         uint32_t v[32];
-        tmem_ld32(tO + lane_off + c * 32, v);
+        tmem_ld32(tO + c * 32, v);
         tc_wait_ld();
         if (live) {
 #pragma unroll
@@ -315,17 +350,16 @@ int launch_hd(const AttnDesc& a, unsigned* status, cudaStream_t st) {
                            (uint64_t)a.n_q * HD * 2, 64, (uint32_t)r, (uint32_t)tpt))
     return -1;
   // K/V: dims (hd, n_kv, kv_len, B), strides in bytes for dims 1..3
-  auto enc4 = [&](CUtensorMap* m, const void* base) -> bool {
-    const uint64_t dims[4] = {(uint64_t)HD, (uint64_t)a.n_kv, (uint64_t)kv_len, (uint64_t)a.B};
-    const uint64_t strides[3] = {(uint64_t)HD * 2, (uint64_t)a.n_kv * HD * 2, (uint64_t)a.cap * a.n_kv * HD * 2};
-    const uint32_t box[4] = {64, 1, 128, 1};
-    return encode_tmap_4d_bf16(m, base, dims, strides, box);
-  };
-  if (!enc4(&p.tmK, a.k) || !enc4(&p.tmV, a.v)) return -1;
+  const uint64_t dims[4] = {(uint64_t)HD, (uint64_t)a.n_kv, (uint64_t)kv_len, (uint64_t)a.B};
+  const uint64_t strides[3] = {(uint64_t)HD * 2, (uint64_t)a.n_kv * HD * 2, (uint64_t)a.cap * a.n_kv * HD * 2};
+  const uint32_t box[4] = {64, 1, 128, 1};
+  if (!encode_tmap_4d_bf16(&p.tmK, a.k, dims, strides, box) || !encode_tmap_4d_bf16(&p.tmV, a.v, dims, strides, box))
+    return -1;
   p.o = static_cast<uint16_t*>(a.o);
   p.B = (int)a.B; p.S = (int)a.S; p.n_q = (int)a.n_q; p.n_kv = (int)a.n_kv; p.hd = HD; p.r = r;
   p.tokens_per_tile = tpt;
   p.t_blocks = (int)((a.S + tpt - 1) / tpt);
+  p.pairs = (p.t_blocks + 1) / 2;
   p.pos0 = (int)a.pos0;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.status = status;
@@ -339,7 +373,7 @@ int launch_hd(const AttnDesc& a, unsigned* status, cudaStream_t st) {
       return -1;
     attr_set[dev] = true;
   }
-  const int64_t grid = (int64_t)p.t_blocks * a.B * a.n_kv;
+  const int64_t grid = (int64_t)p.pairs * a.B * a.n_kv;
   attn_tc_kernel<HD><<<(unsigned)grid, AT_THREADS, Smem<HD>::TOTAL, st>>>(p);
   return 0;
 }

@@ -78,19 +78,43 @@ __device__ __forceinline__ void load_run(const void* base, int is_f32, int64_t l
   }
 }
 
-// Rotate n/2 consecutive pairs starting at column c (c even) of a head-major row at position pos.
+// Rotate n/2 consecutive pairs starting at column c (c even) of a head-major row at position pos
+// (token s of the call).  With a table, (cos, sin) are read from it; otherwise computed.
 template <int n>
-__device__ __forceinline__ void rope_run(const Epi& e, int64_t c_in_seg, float pos, float* v) {
+__device__ __forceinline__ void rope_run(const Epi& e, int64_t c_in_seg, float pos, int64_t s, float* v) {
   static_assert(n % 2 == 0 || n == 1, "runs of pairs");
   if constexpr (n == 1) return;   // a lone column never carries RoPE (head_dim is even)
+  if (n <= e.hd && e.hd % n == 0) {   // the run lies inside one head
+    const int k0 = (int)(c_in_seg % e.hd) >> 1;
+    if (e.rope_tab) {
+      const float2* t = e.rope_tab + s * (e.hd >> 1) + k0;
+#pragma unroll
+      for (int i = 0; i + 1 < n; i += 2) {
+        const float2 cs = __ldg(t + (i >> 1));
+        const float x0 = v[i], x1 = v[i + 1];
+        v[i] = x0 * cs.x - x1 * cs.y;
+        v[i + 1] = x0 * cs.y + x1 * cs.x;
+      }
+      return;
+    }
+#pragma unroll
+    for (int i = 0; i + 1 < n; i += 2) {
+      float sn, co;
+      rope_sincos(pos, e.freq[k0 + (i >> 1)], sn, co);
+      const float x0 = v[i], x1 = v[i + 1];
+      v[i] = x0 * co - x1 * sn;
+      v[i + 1] = x0 * sn + x1 * co;
+    }
+    return;
+  }
 #pragma unroll
   for (int i = 0; i + 1 < n; i += 2) {
     const int k = (int)((c_in_seg + i) % e.hd) >> 1;
-    float s, co;
-    rope_sincos(pos, e.freq[k], s, co);
+    float sn, co;
+    rope_sincos(pos, e.freq[k], sn, co);
     const float x0 = v[i], x1 = v[i + 1];
-    v[i] = x0 * co - x1 * s;
-    v[i + 1] = x0 * s + x1 * co;
+    v[i] = x0 * co - x1 * sn;
+    v[i + 1] = x0 * sn + x1 * co;
   }
 }
 
@@ -141,13 +165,13 @@ __device__ __forceinline__ void epi_run(const Epi& e, int64_t r, int64_t c, floa
       const int64_t s = r % e.S;
       const float pos = (float)(e.pos0 + s);
       if (c < e.nq_cols) {
-        rope_run<n>(e, c, pos, v);
+        rope_run<n>(e, c, pos, s, v);
         store_run<n>(e.out, e.out_f32, e.nq_cols, r, c, v);
       } else {
         const int64_t krow = (r / e.S) * e.cap + e.pos0 + s;
         if (c < e.nq_cols + e.nkv_cols) {
           const int64_t cc = c - e.nq_cols;
-          rope_run<n>(e, cc, pos, v);
+          rope_run<n>(e, cc, pos, s, v);
           store_run<n>(e.k_out, e.out_f32, e.nkv_cols, krow, cc, v);
         } else {
           store_run<n>(e.v_out, e.out_f32, e.nkv_cols, krow, c - e.nq_cols - e.nkv_cols, v);

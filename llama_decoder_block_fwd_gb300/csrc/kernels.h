@@ -36,6 +36,7 @@ struct Epi {
   int64_t nq_cols, nkv_cols;
   int64_t S, cap, pos0;
   int hd;
+  const float2* rope_tab;   // optional [S, hd/2] (cos, sin) for positions pos0 .. pos0+S-1
   RopeFreq freq[kMaxRopePairs];
 };
 
@@ -78,6 +79,8 @@ int launch_rope(int dtype, void* q, void* k, int64_t B, int64_t S, int64_t n_q, 
 int launch_gemm_simt(const GemmDesc& g, cudaStream_t st);
 int launch_attn_simt(const AttnDesc& a, cudaStream_t st);
 int launch_widen_bf16(const void* src, float* dst, int64_t n, cudaStream_t st);
+// tab[s, k] = (cos, sin)((pos0 + s) * theta_k) for s < S, k < hd/2.
+int launch_rope_table(float2* tab, int64_t S, int hd, int64_t pos0, const RopeFreq* freq, cudaStream_t st);
 
 // tensor-core paths (bf16 only)
 bool gemm_tc_supported(const GemmDesc& g);

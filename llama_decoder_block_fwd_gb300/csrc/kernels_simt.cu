@@ -1,6 +1,7 @@
 // CUDA-core kernels: RMSNorm (the one used on every path), RoPE, and the generic GEMM and
 // attention used for float32 and for bf16 shapes the tcgen05 kernels do not take.
 #include <algorithm>
+#include <cstring>
 
 #include "epilogue.cuh"
 #include "kernels.h"
@@ -282,6 +283,16 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const __grid_constant__ 
 // Generic causal GQA attention: one warp per (b, s, h) query row, 32 keys per step (one per
 // lane), online softmax (running max and sum), output dims split across lanes.
 // ------------------------------------------------------------------------------------------
+__global__ void rope_table_kernel(float2* __restrict__ tab, int64_t S, int half, int64_t pos0,
+                                  const __grid_constant__ RopeParams p) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= S * half) return;
+  const int k = (int)(i % half);
+  float s, c;
+  rope_sincos((float)(pos0 + i / half), p.freq[k], s, c);
+  tab[i] = make_float2(c, s);
+}
+
 __global__ void widen_bf16_kernel(const uint16_t* __restrict__ src, float* __restrict__ dst, int64_t n) {
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
     dst[i] = bf2f(src[i]);
@@ -388,6 +399,17 @@ int launch_gemm_simt(const GemmDesc& g, cudaStream_t st) {
     if (sw) gemm_simt_kernel<uint16_t, true><<<grid, 256, 0, st>>>(g);
     else gemm_simt_kernel<uint16_t, false><<<grid, 256, 0, st>>>(g);
   }
+  return 0;
+}
+
+int launch_rope_table(float2* tab, int64_t S, int hd, int64_t pos0, const RopeFreq* freq, cudaStream_t st) {
+  RopeParams p;
+  memset(&p, 0, sizeof(p));
+  p.hd = hd;
+  for (int i = 0; i < hd / 2; ++i) p.freq[i] = freq[i];
+  const int64_t n = S * (hd / 2);
+  if (n <= 0) return 0;
+  rope_table_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(tab, S, hd / 2, pos0, p);
   return 0;
 }
 
