@@ -155,7 +155,7 @@ int llama_stack_decode_step(const llama_dims* dims, int dtype, int n_layers,
  * synchronise the device).  Same arguments and result as llama_gqa_attention with dims->S == 1,
  * minus the workspace: its split-K partials live in a 12 MiB device array inside the library
  * (created when the library is loaded, resident on every device that loads it until exit).
- *   - bf16 only, head_dim 128, n_q / n_kv <= 16.  Returns LLAMA_ERR_WORKSPACE, launching nothing,
+ *   - bf16 only, head_dim 128, n_q / n_kv in {1, 2, 4, 8, 16}.  Returns LLAMA_ERR_WORKSPACE, launching nothing,
  *     when even a single key chunk of partials (about 520 bytes per query head and sequence)
  *     exceeds the 12 MiB array, i.e. when B * n_q > 24197.  Below that, the keys are cut into
  *     fewer, longer chunks whenever the usual chunking would not fit (the Llama-3-8B decode

@@ -463,8 +463,8 @@ bool decode_tc_path(const llama_dims* d, int dtype) {
   if (dtype != LLAMA_BF16 || d->B > 128 || d->head_dim != 128 || d->d_model > 8192) return false;
   const int64_t hq = d->n_q * d->head_dim, hkv = d->n_kv * d->head_dim;
   if (d->d_model % 128 || hq % 128 || hkv % 128 || d->d_ff % 128) return false;
-  if (d->n_q / d->n_kv > 16) return false;
-  return true;
+  const int64_t r = d->n_q / d->n_kv;
+  return r == 1 || r == 2 || r == 4 || r == 8 || r == 16;
 }
 
 struct DecodeTcWs {

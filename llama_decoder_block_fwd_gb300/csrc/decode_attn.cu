@@ -85,6 +85,16 @@ __device__ __forceinline__ void item_coords(const DecodeAttnParams& p, int item,
   t_end = min(t_begin + p.chunk_tiles, p.kv_tiles);
 }
 
+// Warp-wide maximum of a float (one instruction).
+__device__ __forceinline__ float warp_max_f32(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
+
+// R = n_q / n_kv query heads per KV group (1, 2, 4, 8 or 16), a compile-time constant so that the
+// softmax touches only the R real columns of the padded N = 16 operands.
+template <int R>
 __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_kernel(const __grid_constant__ DecodeAttnParams p) {
   using L = DaSmem;
   extern __shared__ uint8_t smem_raw[];
@@ -224,15 +234,15 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_kernel(const __grid
     const int qw = warp & 3;
     const int t = qw * 32 + lane;                 // TMEM lane: key of the tile / hd index of O^T
     const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
-    const int r = p.r;
+    constexpr int r = R;
     int tile = 0, it = 0;
     bool ok = true;
     for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x, ++it) {
       int b, g, t0, t1, chunk;
       item_coords(p, item, b, g, t0, t1, chunk);
-      float m_ref[DA_NPAD], lsum[DA_NPAD];
+      float m_ref[R], lsum[R];
 #pragma unroll
-      for (int h = 0; h < DA_NPAD; ++h) { m_ref[h] = -INFINITY; lsum[h] = 0.f; }
+      for (int h = 0; h < R; ++h) { m_ref[h] = -INFINITY; lsum[h] = 0.f; }
       for (int tt = t0; tt < t1; ++tt, ++tile) {
         const int sb = tile & 1;
         if (!mbar_wait(&s_full[sb], (tile >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
@@ -243,40 +253,29 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_kernel(const __grid
         tc_fence_before();
         mbar_arrive(&s_free[sb]);
         const bool valid = tt * 128 + t < p.kv_len;
-        float s[DA_NPAD];
+        float s[R];
 #pragma unroll
-        for (int h = 0; h < DA_NPAD; ++h) s[h] = valid ? __uint_as_float(sv[h]) * p.scale_log2 : -INFINITY;
-        // per-head max over the 128 keys of the tile
-        float mx[DA_NPAD];
-#pragma unroll
-        for (int h = 0; h < DA_NPAD; ++h) {
-          float v = h < r ? s[h] : -INFINITY;
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-          mx[h] = v;
-        }
+        for (int h = 0; h < R; ++h) s[h] = valid ? __uint_as_float(sv[h]) * p.scale_log2 : -INFINITY;
+        // per-head max over the 128 keys of the tile: warp maxima, then across the four warps
         float* rbuf = red + (tile & 1) * 64;    // alternate halves: one barrier per tile suffices
-        if (lane < DA_NPAD) {
-          float mine = mx[0];
 #pragma unroll
-          for (int h = 1; h < DA_NPAD; ++h) if (lane == h) mine = mx[h];
-          rbuf[qw * 16 + lane] = mine;
+        for (int h = 0; h < R; ++h) {
+          const float v = warp_max_f32(s[h]);
+          if (lane == h) rbuf[qw * 16 + h] = v;
         }
         softmax_sync();
-        float alpha[DA_NPAD];
+        float alpha[R];
         bool resc = false;
 #pragma unroll
-        for (int h = 0; h < DA_NPAD; ++h) {
+        for (int h = 0; h < R; ++h) {
           const float tm = fmaxf(fmaxf(rbuf[h], rbuf[16 + h]), fmaxf(rbuf[32 + h], rbuf[48 + h]));
           alpha[h] = 1.f;
-          if (h < r) {
-            if (m_ref[h] == -INFINITY) {
-              m_ref[h] = tm;
-            } else if (tm > m_ref[h] + kDaRescaleLog2) {
-              alpha[h] = exp2f(m_ref[h] - tm);
-              m_ref[h] = tm;
-              resc = true;
-            }
+          if (m_ref[h] == -INFINITY) {
+            m_ref[h] = tm;
+          } else if (tm > m_ref[h] + kDaRescaleLog2) {
+            alpha[h] = exp2f(m_ref[h] - tm);
+            m_ref[h] = tm;
+            resc = true;
           }
         }
         const int pb = tile & 1;
@@ -294,25 +293,23 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_kernel(const __grid
             tmem_ld16(tO + lane_off, ov);
             tc_wait_ld();
 #pragma unroll
-            for (int h = 0; h < DA_NPAD; ++h) ov[h] = __float_as_uint(__uint_as_float(ov[h]) * alpha[h]);
+            for (int h = 0; h < R; ++h) ov[h] = __float_as_uint(__uint_as_float(ov[h]) * alpha[h]);
             tmem_st16(tO + lane_off, ov);
             tc_wait_st();
 #pragma unroll
-            for (int h = 0; h < DA_NPAD; ++h) lsum[h] *= alpha[h];
+            for (int h = 0; h < R; ++h) lsum[h] *= alpha[h];
           }
         }
         // P^T rows = heads, columns = keys (K-major, 128B swizzle, two 64-key atoms)
         uint8_t* pbase = smem + L::OFF_P + pb * L::PB + (t >> 6) * (L::PB / 2);
         const int kin = t & 63;
 #pragma unroll
-        for (int h = 0; h < DA_NPAD; ++h) {
-          if (h < r) {
-            const float pv = exp2f(s[h] - m_ref[h]);
-            const __nv_bfloat16 pq = __float2bfloat16_rn(pv);
-            lsum[h] += __bfloat162float(pq);
-            const int chunk16 = (kin >> 3) ^ (h & 7);
-            *reinterpret_cast<__nv_bfloat16*>(pbase + h * 128 + chunk16 * 16 + (kin & 7) * 2) = pq;
-          }
+        for (int h = 0; h < R; ++h) {
+          const float pv = exp2f(s[h] - m_ref[h]);
+          const __nv_bfloat16 pq = __float2bfloat16_rn(pv);
+          lsum[h] += pv;
+          const int chunk16 = (kin >> 3) ^ (h & 7);
+          *reinterpret_cast<__nv_bfloat16*>(pbase + h * 128 + chunk16 * 16 + (kin & 7) * 2) = pq;
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -329,29 +326,22 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_kernel(const __grid
       mbar_arrive(o_free);
       const int64_t base = ((int64_t)b * p.n_chunks + chunk) * p.n_q + (int64_t)g * r;
 #pragma unroll
-      for (int h = 0; h < DA_NPAD; ++h)
-        if (h < r) p.part_o[(base + h) * DA_HD + t] = __uint_as_float(ov[h]);
+      for (int h = 0; h < R; ++h) p.part_o[(base + h) * DA_HD + t] = __uint_as_float(ov[h]);
       // l: sum the per-thread partial sums over the 128 keys of each head
+      float* lbuf = red + 128;
 #pragma unroll
-      for (int h = 0; h < DA_NPAD; ++h) {
-        float v = h < r ? lsum[h] : 0.f;
+      for (int h = 0; h < R; ++h) {
+        float v = lsum[h];
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-        lsum[h] = v;
-      }
-      float* lbuf = red + 128;
-      if (lane < DA_NPAD) {
-        float mine = lsum[0];
-#pragma unroll
-        for (int h = 1; h < DA_NPAD; ++h) if (lane == h) mine = lsum[h];
-        lbuf[qw * 16 + lane] = mine;
+        if (lane == h) lbuf[qw * 16 + h] = v;
       }
       softmax_sync();
       if (t < r) {
         const float l = lbuf[t] + lbuf[16 + t] + lbuf[32 + t] + lbuf[48 + t];
         float mm = -INFINITY;
 #pragma unroll
-        for (int h = 0; h < DA_NPAD; ++h) if (h == t) mm = m_ref[h];
+        for (int h = 0; h < R; ++h) if (h == t) mm = m_ref[h];
         p.part_ml[(base + t) * 2 + 0] = mm;
         p.part_ml[(base + t) * 2 + 1] = l;
       }
@@ -404,6 +394,31 @@ __global__ void decode_combine_kernel(const float* __restrict__ part_o, const fl
   }
 }
 
+// Launch phase 1 for the params' head ratio (attributes set once per device).
+int launch_decode_kernel(const DecodeAttnParams& p, int grid, cudaStream_t st) {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  static bool attr_set[64] = {};
+  if (dev < 0 || dev >= 64) return -1;
+  if (!attr_set[dev]) {
+    const void* fns[5] = {(const void*)decode_attn_kernel<1>, (const void*)decode_attn_kernel<2>,
+                          (const void*)decode_attn_kernel<4>, (const void*)decode_attn_kernel<8>,
+                          (const void*)decode_attn_kernel<16>};
+    for (const void* f : fns)
+      if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, DaSmem::TOTAL) != cudaSuccess) return -1;
+    attr_set[dev] = true;
+  }
+  switch (p.r) {
+    case 1: decode_attn_kernel<1><<<grid, DA_THREADS, DaSmem::TOTAL, st>>>(p); break;
+    case 2: decode_attn_kernel<2><<<grid, DA_THREADS, DaSmem::TOTAL, st>>>(p); break;
+    case 4: decode_attn_kernel<4><<<grid, DA_THREADS, DaSmem::TOTAL, st>>>(p); break;
+    case 8: decode_attn_kernel<8><<<grid, DA_THREADS, DaSmem::TOTAL, st>>>(p); break;
+    case 16: decode_attn_kernel<16><<<grid, DA_THREADS, DaSmem::TOTAL, st>>>(p); break;
+    default: return -1;
+  }
+  return 0;
+}
+
 struct DecodePlan {
   int kv_tiles, chunk_tiles, n_chunks;
 };
@@ -421,7 +436,9 @@ DecodePlan plan(int64_t B, int64_t n_kv, int64_t kv_len) {
 
 bool decode_attn_supported(const AttnDesc& a) {
   if (a.dtype != LLAMA_BF16 || a.hd != DA_HD || a.S != 1) return false;
-  if (a.n_kv <= 0 || a.n_q % a.n_kv != 0 || a.n_q / a.n_kv > DA_NPAD) return false;
+  if (a.n_kv <= 0 || a.n_q % a.n_kv != 0) return false;
+  const int64_t r = a.n_q / a.n_kv;
+  if (r != 1 && r != 2 && r != 4 && r != 8 && r != 16) return false;
   if (a.pos0 + 1 > ((int64_t)1 << 30)) return false;
   const uintptr_t al = reinterpret_cast<uintptr_t>(a.q) | reinterpret_cast<uintptr_t>(a.k) |
                        reinterpret_cast<uintptr_t>(a.v) | reinterpret_cast<uintptr_t>(a.o);
@@ -460,18 +477,8 @@ int launch_decode_attn(const AttnDesc& a, void* ws, int num_sms, unsigned* statu
   p.n_items = (int)(a.B * a.n_kv * d.n_chunks);
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.status = status;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  static bool attr_set[64] = {};
-  if (dev < 0 || dev >= 64) return -1;
-  if (!attr_set[dev]) {
-    if (cudaFuncSetAttribute(decode_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, DaSmem::TOTAL) !=
-        cudaSuccess)
-      return -1;
-    attr_set[dev] = true;
-  }
   const int grid = std::max(1, std::min(p.n_items, num_sms));
-  decode_attn_kernel<<<grid, DA_THREADS, DaSmem::TOTAL, st>>>(p);
+  if (launch_decode_kernel(p, grid, st) != 0) return -1;
   const int warps = (int)(a.B * a.n_q);
   decode_combine_kernel<<<(warps * 32 + 255) / 256, 256, 0, st>>>(p.part_o, p.part_ml, static_cast<uint16_t*>(a.o),
                                                                    static_cast<uint16_t*>(a.o_lo), (int)a.B,
@@ -535,7 +542,10 @@ extern "C" int llama_gqa_attention_decode_noalloc(const llama_dims* dims, int dt
   if (!dims || dtype != LLAMA_BF16) return dtype == LLAMA_BF16 ? LLAMA_ERR_INVALID_ARG : LLAMA_ERR_UNSUPPORTED;
   if (dims->B < 0 || dims->S != 1 || dims->n_q <= 0 || dims->n_kv <= 0 || dims->n_q % dims->n_kv != 0)
     return LLAMA_ERR_INVALID_ARG;
-  if (dims->head_dim != DA_HD || dims->n_q / dims->n_kv > DA_NPAD) return LLAMA_ERR_UNSUPPORTED;
+  {
+    const int64_t rr = dims->n_q / dims->n_kv;
+    if (dims->head_dim != DA_HD || (rr != 1 && rr != 2 && rr != 4 && rr != 8 && rr != 16)) return LLAMA_ERR_UNSUPPORTED;
+  }
   if (pos0 < 0 || kv_capacity < pos0 + 1 || pos0 + 1 > ((int64_t)1 << 30)) return LLAMA_ERR_INVALID_ARG;
   if (dims->B == 0) return LLAMA_OK;
   if (!q || !k || !v || !o) return LLAMA_ERR_INVALID_ARG;
@@ -573,14 +583,9 @@ extern "C" int llama_gqa_attention_decode_noalloc(const llama_dims* dims, int dt
   p.n_items = (int)(dims->B * dims->n_kv * d.n_chunks);
   p.scale_log2 = (float)(1.0 / std::sqrt((double)DA_HD)) * 1.4426950408889634f;
   p.status = status;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (cudaFuncSetAttribute(decode_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, DaSmem::TOTAL) !=
-      cudaSuccess)
-    return LLAMA_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int grid = std::max(1, std::min(p.n_items, num_sms()));
-  decode_attn_kernel<<<grid, DA_THREADS, DaSmem::TOTAL, st>>>(p);
+  if (launch_decode_kernel(p, grid, st) != 0) return LLAMA_ERR_CUDA;
   const int warps = (int)(dims->B * dims->n_q);
   decode_combine_kernel<<<(warps * 32 + 255) / 256, 256, 0, st>>>(p.part_o, p.part_ml, static_cast<uint16_t*>(o),
                                                                    nullptr, (int)dims->B, (int)dims->n_q, d.n_chunks);
