@@ -456,7 +456,7 @@ constexpr int kDecodeUnits = 320;
 int decode_splits(int64_t n_cols, int64_t K) {
   const int64_t tiles = (n_cols + 127) / 128;
   const int want = (int)std::max<int64_t>(1, (kDecodeUnits + tiles - 1) / tiles);
-  return gemm_tc_effective_splits(K, want);
+  return gemm_skinny_splits(K, want);
 }
 
 bool decode_tc_path(const llama_dims* d, int dtype) {
@@ -469,7 +469,9 @@ bool decode_tc_path(const llama_dims* d, int dtype) {
 
 struct DecodeTcWs {
   float* xres;
-  void *act_hi, *act_lo, *q;
+  void* act;          // stacked GEMM input [2 Mp, width]: hi rows 0..B-1, lo rows Mp..Mp+B-1
+  int64_t mp;
+  void* q;
   float *rs1, *rs2, *part;
   void* attn;
   size_t attn_bytes, bytes;
@@ -485,11 +487,11 @@ DecodeTcWs plan_decode_tc(const llama_dims* d, void* base, int64_t kv_capacity) 
   w.s_gu = decode_splits(2 * d->d_ff, d->d_model);
   w.s_down = decode_splits(d->d_model, d->d_ff);
   const size_t act = (size_t)std::max(std::max(d->d_model, hq), d->d_ff);
+  w.mp = skinny_mp(d->B);
   const size_t part = std::max((size_t)w.s_qkv * (hq + 2 * hkv), (size_t)w.s_gu * 2 * d->d_ff);
   Carver c{static_cast<char*>(base)};
   w.xres = static_cast<float*>(c.take(Bn * d->d_model * 4));
-  w.act_hi = c.take(Bn * act * 2);
-  w.act_lo = c.take(Bn * act * 2);
+  w.act = c.take((size_t)(2 * w.mp) * act * 2);
   w.q = c.take(Bn * hq * 2);
   w.rs1 = static_cast<float*>(c.take(Bn * 4));
   w.rs2 = static_cast<float*>(c.take(Bn * 4));
@@ -500,22 +502,28 @@ DecodeTcWs plan_decode_tc(const llama_dims* d, void* base, int64_t kv_capacity) 
   return w;
 }
 
-// out = (A_hi + A_lo) W^T as split-K fp32 partials [splits, M, N] (or, with splits == 1 and a
-// row scale, directly the scaled fp32 result).
-int run_dual_gemm(const char* role, int64_t M, const void* a_hi, const void* a_lo, int64_t K, const void* const* W,
-                  const int64_t* n_rows, int nseg, int splits, float* out, const float* row_scale, cudaStream_t st,
-                  int kind = EPI_STORE) {
-  GemmDesc g = make_gemm(LLAMA_BF16, M, a_hi, K);
-  g.A_lo = a_lo;
+// out = (X_hi + X_lo) W^T on the weight-streaming GEMM: fp32 split-K partials (mode 0), added
+// into out (mode 1), or stored with the row scale (mode 2).
+int run_skinny(const char* role, int64_t M, const void* x2, int64_t K, const void* const* W, const int64_t* n_rows,
+               int nseg, int splits, int mode, float* out, int64_t ldo, const float* row_scale, cudaStream_t st) {
+  SkinnyDesc g;
+  memset(&g, 0, sizeof(g));
+  g.M = M;
+  g.K = K;
+  g.X2 = x2;
   g.nseg = nseg;
-  g.N = 0;
-  for (int s = 0; s < nseg; ++s) { g.B[s] = W[s]; g.nB[s] = n_rows[s]; g.N += n_rows[s]; }
+  for (int s = 0; s < nseg; ++s) { g.W[s] = W[s]; g.nW[s] = n_rows[s]; }
   g.k_splits = splits;
-  g.narrow = 1;
-  g.epi = make_epi(kind, 1, out, g.N);
-  g.epi.row_scale = row_scale;
-  if (!gemm_tc_supported(g)) return LLAMA_ERR_UNSUPPORTED;
-  return run_gemm(g, role, st);
+  g.mode = mode;
+  g.out = out;
+  g.ldo = ldo;
+  g.row_scale = row_scale;
+  unsigned* status = status_ptr();
+  if (!status) return LLAMA_ERR_CUDA;
+  prof::begin(role, st);
+  if (launch_gemm_skinny(g, num_sms(), status, st) != 0) return LLAMA_ERR_UNSUPPORTED;
+  prof::end(st);
+  return launch_status();
 }
 
 int run_fin(const char* role, int launch_rc, cudaStream_t st) {
@@ -540,15 +548,15 @@ int decode_stack_tc(const llama_dims* d, int n_layers, const llama_block_weights
     void* vc = static_cast<char*>(v_cache) + l * layer_cache;
     // (layer 0: x = embedding rows) a = x * g_attn (hi, lo); rs1
     prof::begin("fin_norm", st);
-    rc = launch_fin_norm(w.xres, l == 0 ? x_emb : nullptr, nullptr, 0, lw.attn_norm_g, w.act_hi, w.act_lo, w.rs1, B, D,
-                         eps, st);
+    rc = launch_fin_norm(w.xres, l == 0 ? x_emb : nullptr, nullptr, 0, lw.attn_norm_g, w.act,
+                         static_cast<char*>(w.act) + w.mp * D * 2, w.rs1, B, D, eps, st);
     prof::end(st);
     if ((rc = run_fin("fin_norm", rc, st)) != LLAMA_OK) return rc;
     // Q/K/V partials
     const void* wqkv[3] = {lw.wq, lw.wk, lw.wv};
     const int64_t nqkv[3] = {hq, hkv, hkv};
-    if ((rc = run_dual_gemm("gemm_tc_dec_qkv", B, w.act_hi, w.act_lo, D, wqkv, nqkv, 3, w.s_qkv, w.part, nullptr, st)) !=
-        LLAMA_OK)
+    if ((rc = run_skinny("gemm_tc_dec_qkv", B, w.act, D, wqkv, nqkv, 3, w.s_qkv, 0, w.part, hq + 2 * hkv, nullptr,
+                         st)) != LLAMA_OK)
       return rc;
     prof::begin("fin_qkv", st);
     rc = launch_fin_qkv(w.part, w.s_qkv, w.rs1, w.q, kc, vc, B, (int)hq, (int)hkv, (int)d->head_dim, cap, t_cache, freq,
@@ -556,50 +564,52 @@ int decode_stack_tc(const llama_dims* d, int n_layers, const llama_block_weights
     prof::end(st);
     if ((rc = run_fin("fin_qkv", rc, st)) != LLAMA_OK) return rc;
     // attention over t_cache + 1 keys; o as hi + lo into the activation buffers
-    AttnDesc a = make_attn(d, LLAMA_BF16, w.q, kc, vc, w.act_hi, cap, t_cache);
-    a.o_lo = w.act_lo;
+    AttnDesc a = make_attn(d, LLAMA_BF16, w.q, kc, vc, w.act, cap, t_cache);
+    a.o_lo = static_cast<char*>(w.act) + w.mp * hq * 2;
     a.ws = w.attn;
     a.ws_bytes = w.attn_bytes;
     if ((rc = run_attention(a, st)) != LLAMA_OK) return rc;
     // h = x + o W_O^T: the split-K partials are added straight into the fp32 residual stream
     const void* wo[1] = {lw.wo};
     const int64_t no[1] = {D};
-    if ((rc = run_dual_gemm("gemm_tc_dec_o", B, w.act_hi, w.act_lo, hq, wo, no, 1, w.s_o, w.xres, nullptr, st,
-                            EPI_ATOMIC)) != LLAMA_OK)
+    if ((rc = run_skinny("gemm_tc_dec_o", B, w.act, hq, wo, no, 1, w.s_o, 1, w.xres, D, nullptr, st)) != LLAMA_OK)
       return rc;
     // a2 = h * g_ffn (hi, lo); rs2
     prof::begin("fin_norm", st);
-    rc = launch_fin_norm(w.xres, nullptr, nullptr, 0, lw.ffn_norm_g, w.act_hi, w.act_lo, w.rs2, B, D, eps, st);
+    rc = launch_fin_norm(w.xres, nullptr, nullptr, 0, lw.ffn_norm_g, w.act, static_cast<char*>(w.act) + w.mp * D * 2,
+                         w.rs2, B, D, eps, st);
     prof::end(st);
     if ((rc = run_fin("fin_norm", rc, st)) != LLAMA_OK) return rc;
     // gate | up partials; m = SiLU(rs2 gate) * (rs2 up) (hi, lo)
     const void* wgu[2] = {lw.w_gate, lw.w_up};
     const int64_t ngu[2] = {d->d_ff, d->d_ff};
-    if ((rc = run_dual_gemm("gemm_tc_dec_gateup", B, w.act_hi, w.act_lo, D, wgu, ngu, 2, w.s_gu, w.part, nullptr,
-                            st)) != LLAMA_OK)
+    if ((rc = run_skinny("gemm_tc_dec_gateup", B, w.act, D, wgu, ngu, 2, w.s_gu, 0, w.part, 2 * d->d_ff, nullptr,
+                         st)) != LLAMA_OK)
       return rc;
     prof::begin("fin_swiglu", st);
-    rc = launch_fin_swiglu(w.part, w.s_gu, w.rs2, w.act_hi, w.act_lo, B, (int)d->d_ff, st);
+    rc = launch_fin_swiglu(w.part, w.s_gu, w.rs2, w.act, static_cast<char*>(w.act) + w.mp * d->d_ff * 2, B,
+                           (int)d->d_ff, st);
     prof::end(st);
     if ((rc = run_fin("fin_swiglu", rc, st)) != LLAMA_OK) return rc;
     // y = h + m W_down^T, added into the residual stream the same way
     const void* wd[1] = {lw.w_down};
     const int64_t nd[1] = {D};
-    if ((rc = run_dual_gemm("gemm_tc_dec_down", B, w.act_hi, w.act_lo, d->d_ff, wd, nd, 1, w.s_down, w.xres, nullptr,
-                            st, EPI_ATOMIC)) != LLAMA_OK)
+    if ((rc = run_skinny("gemm_tc_dec_down", B, w.act, d->d_ff, wd, nd, 1, w.s_down, 1, w.xres, D, nullptr, st)) !=
+        LLAMA_OK)
       return rc;
   }
   // final RMSNorm in split form, then the LM head with the row scale in its epilogue
   prof::begin("fin_norm", st);
-  rc = launch_fin_norm(w.xres, nullptr, nullptr, 0, final_g, w.act_hi, w.act_lo, w.rs1, B, D, eps, st);
+  rc = launch_fin_norm(w.xres, nullptr, nullptr, 0, final_g, w.act, static_cast<char*>(w.act) + w.mp * D * 2, w.rs1,
+                       B, D, eps, st);
   prof::end(st);
   if ((rc = run_fin("fin_norm", rc, st)) != LLAMA_OK) return rc;
   const void* wl[1] = {w_lm};
   const int64_t nl[1] = {vocab};
   if (vocab % 128 == 0)
-    return run_dual_gemm("gemm_tc_lm_head", B, w.act_hi, w.act_lo, D, wl, nl, 1, 1, logits, w.rs1, st);
+    return run_skinny("gemm_tc_lm_head", B, w.act, D, wl, nl, 1, 1, 2, logits, vocab, w.rs1, st);
   // a vocabulary that is not a multiple of 128 rows: generic GEMM on the hi part with the row scale
-  GemmDesc g = make_gemm(LLAMA_BF16, B, w.act_hi, D);
+  GemmDesc g = make_gemm(LLAMA_BF16, B, w.act, D);
   g.nseg = 1; g.B[0] = w_lm; g.nB[0] = vocab; g.N = vocab;
   g.epi = make_epi(EPI_STORE, 1, logits, vocab);
   g.epi.row_scale = w.rs1;

@@ -85,6 +85,24 @@ int launch_rope_table(float2* tab, int64_t S, int hd, int64_t pos0, const RopeFr
 // tensor-core paths (bf16 only)
 bool gemm_tc_supported(const GemmDesc& g);
 int launch_gemm_tc(const GemmDesc& g, int num_sms, unsigned* status, cudaStream_t st);
+// Weight-streaming GEMM for M <= 128 token rows (decode): out = (X_hi + X_lo) W^T with the token
+// rows stacked in X2 = [hi rows 0..M-1 | lo rows Mp..Mp+M-1], Mp = skinny_mp(M).
+struct SkinnyDesc {
+  int64_t M, K;
+  const void* X2;
+  const void* W[3];
+  int64_t nW[3];          // rows of each weight segment (multiples of 128)
+  int nseg;
+  int k_splits;
+  int mode;               // 0: fp32 partials out[split*M + c, n]; 1: atomic add out[c, n]; 2: store (x row_scale)
+  float* out;
+  int64_t ldo;
+  const float* row_scale;
+};
+inline int64_t skinny_mp(int64_t M) { return M <= 64 ? 64 : 128; }
+int launch_gemm_skinny(const SkinnyDesc& g, int num_sms, unsigned* status, cudaStream_t st);
+int gemm_skinny_splits(int64_t K, int requested);
+
 // The SM-pair (cta_group::2) version for large M: 256 x 256 tiles, no dual A / split K.
 bool gemm_tc2_supported(const GemmDesc& g);
 int launch_gemm_tc2(const GemmDesc& g, unsigned* status, cudaStream_t st);
