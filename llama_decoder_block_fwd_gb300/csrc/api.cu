@@ -79,6 +79,11 @@ static void end(cudaStream_t st) {
 }
 }  // namespace prof
 
+// ------------------------------------------------------------------ programmatic dependent launch
+static thread_local bool t_pdl = false;
+void set_pdl(bool on) { t_pdl = on; }
+bool pdl_enabled() { return t_pdl; }
+
 // ------------------------------------------------------------------ tensor maps
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -810,8 +815,12 @@ int llama_stack_decode_step(const llama_dims* d, int dtype, int n_layers, const 
     const size_t need_tc = plan_decode_tc(d, nullptr, cache_capacity).bytes;
     if (!ws || ws_bytes < need_tc) return LLAMA_ERR_WORKSPACE;
     if (!aligned16(ws)) return LLAMA_ERR_ALIGNMENT;
-    return decode_stack_tc(d, n_layers, layers, final_g, w_lm, vocab, x_emb, k_cache, v_cache, cache_capacity, t_cache,
-                           logits, plan_decode_tc(d, ws, cache_capacity), st);
+    // the decode chain's kernels may overlap their predecessors' tails (each waits for its inputs)
+    set_pdl(true);
+    const int rc_tc = decode_stack_tc(d, n_layers, layers, final_g, w_lm, vocab, x_emb, k_cache, v_cache, cache_capacity,
+                                      t_cache, logits, plan_decode_tc(d, ws, cache_capacity), st);
+    set_pdl(false);
+    return rc_tc;
   }
   const size_t need = plan_decode(d, dtype, nullptr, cache_capacity).bytes;
   if (!ws || ws_bytes < need) return LLAMA_ERR_WORKSPACE;

@@ -234,6 +234,12 @@ __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint
       : "memory");
 }
 
+// Programmatic dependent launch: let the next kernel of the stream begin launching, and wait until
+// every earlier kernel has completed and its writes are visible (no-ops without the launch
+// attribute).  A kernel reads nothing an earlier kernel wrote, and writes nothing, before pdl_wait.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

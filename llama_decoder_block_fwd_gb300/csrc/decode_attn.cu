@@ -116,6 +116,7 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_kernel(const __grid
   float* red = reinterpret_cast<float*>(smem + L::OFF_RED);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_trigger();
   if (threadIdx.x == 0) {
     for (int i = 0; i < 23; ++i) {
       const bool many = (i == 15 || i == 16 || i == 17 || i == 18 || i == 21);
@@ -140,6 +141,7 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_kernel(const __grid
   const uint32_t tO = tmem + 32;     // O^T: columns 32..47
   const uint32_t sbase = smem_u32(smem);
 
+  pdl_wait();   // q and the newest K/V come from the previous kernel; the partials may still be read
   if (warp == 0) {
     if (lane == 0) {  // ---------------------------------------------------- TMA producer
       int tile = 0, it = 0;
@@ -364,6 +366,8 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_kernel(const __grid
 __global__ void decode_combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml,
                                       uint16_t* __restrict__ o, uint16_t* __restrict__ o_lo, int B, int n_q,
                                       int n_chunks) {
+  pdl_trigger();
+  pdl_wait();
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (warp >= B * n_q) return;
   const int b = warp / n_q, h = warp % n_q;
@@ -408,15 +412,16 @@ int launch_decode_kernel(const DecodeAttnParams& p, int grid, cudaStream_t st) {
       if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, DaSmem::TOTAL) != cudaSuccess) return -1;
     attr_set[dev] = true;
   }
+  cudaError_t e;
   switch (p.r) {
-    case 1: decode_attn_kernel<1><<<grid, DA_THREADS, DaSmem::TOTAL, st>>>(p); break;
-    case 2: decode_attn_kernel<2><<<grid, DA_THREADS, DaSmem::TOTAL, st>>>(p); break;
-    case 4: decode_attn_kernel<4><<<grid, DA_THREADS, DaSmem::TOTAL, st>>>(p); break;
-    case 8: decode_attn_kernel<8><<<grid, DA_THREADS, DaSmem::TOTAL, st>>>(p); break;
-    case 16: decode_attn_kernel<16><<<grid, DA_THREADS, DaSmem::TOTAL, st>>>(p); break;
+    case 1: e = launch_k(decode_attn_kernel<1>, dim3(grid), dim3(DA_THREADS), DaSmem::TOTAL, st, p); break;
+    case 2: e = launch_k(decode_attn_kernel<2>, dim3(grid), dim3(DA_THREADS), DaSmem::TOTAL, st, p); break;
+    case 4: e = launch_k(decode_attn_kernel<4>, dim3(grid), dim3(DA_THREADS), DaSmem::TOTAL, st, p); break;
+    case 8: e = launch_k(decode_attn_kernel<8>, dim3(grid), dim3(DA_THREADS), DaSmem::TOTAL, st, p); break;
+    case 16: e = launch_k(decode_attn_kernel<16>, dim3(grid), dim3(DA_THREADS), DaSmem::TOTAL, st, p); break;
     default: return -1;
   }
-  return 0;
+  return e == cudaSuccess ? 0 : -1;
 }
 
 struct DecodePlan {
@@ -480,9 +485,10 @@ int launch_decode_attn(const AttnDesc& a, void* ws, int num_sms, unsigned* statu
   const int grid = std::max(1, std::min(p.n_items, num_sms));
   if (launch_decode_kernel(p, grid, st) != 0) return -1;
   const int warps = (int)(a.B * a.n_q);
-  decode_combine_kernel<<<(warps * 32 + 255) / 256, 256, 0, st>>>(p.part_o, p.part_ml, static_cast<uint16_t*>(a.o),
-                                                                   static_cast<uint16_t*>(a.o_lo), (int)a.B,
-                                                                   (int)a.n_q, d.n_chunks);
+  if (launch_k(decode_combine_kernel, dim3((warps * 32 + 255) / 256), dim3(256), 0, st, (const float*)p.part_o,
+               (const float*)p.part_ml, static_cast<uint16_t*>(a.o), static_cast<uint16_t*>(a.o_lo), (int)a.B,
+               (int)a.n_q, d.n_chunks) != cudaSuccess)
+    return -1;
   return 0;
 }
 

@@ -29,6 +29,8 @@ __global__ void __launch_bounds__(FN_THREADS) fin_norm_kernel(float* __restrict_
                                                               uint16_t* __restrict__ a_lo, float* __restrict__ rs_out,
                                                               int B, int d, float eps) {
   __shared__ float red[FN_THREADS / 32];
+  pdl_trigger();
+  pdl_wait();
   const int r = blockIdx.x;
   float v[FN_MAX_PER_THREAD];
   float ss = 0.f;
@@ -78,6 +80,8 @@ struct FinQkvParams {
 
 // One thread per (row, column pair).
 __global__ void fin_qkv_kernel(const __grid_constant__ FinQkvParams p) {
+  pdl_trigger();
+  pdl_wait();
   const int n_cols = p.nq_cols + 2 * p.nkv_cols;
   const int pairs = n_cols / 2;
   const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -113,6 +117,8 @@ __global__ void fin_qkv_kernel(const __grid_constant__ FinQkvParams p) {
 // One thread per (row, hidden unit): gate in columns [0, d_ff), up in [d_ff, 2 d_ff).
 __global__ void fin_swiglu_kernel(const float* __restrict__ part, const float* __restrict__ rs, uint16_t* __restrict__ m_hi,
                                   uint16_t* __restrict__ m_lo, int n_split, int B, int dff) {
+  pdl_trigger();
+  pdl_wait();
   const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= (int64_t)B * dff) return;
   const int r = (int)(idx / dff), j = (int)(idx % dff);
@@ -135,10 +141,9 @@ __global__ void fin_swiglu_kernel(const float* __restrict__ part, const float* _
 int launch_fin_norm(float* x, const void* init_bf16, const float* part, int n_split, const void* g, void* a_hi,
                     void* a_lo, float* rs, int B, int d, float eps, cudaStream_t st) {
   if (d > FN_THREADS * FN_MAX_PER_THREAD) return -1;
-  fin_norm_kernel<<<B, FN_THREADS, 0, st>>>(x, static_cast<const uint16_t*>(init_bf16), part, n_split,
-                                            static_cast<const uint16_t*>(g), static_cast<uint16_t*>(a_hi),
-                                            static_cast<uint16_t*>(a_lo), rs, B, d, eps);
-  return 0;
+  return launch_k(fin_norm_kernel, dim3(B), dim3(FN_THREADS), 0, st, x, static_cast<const uint16_t*>(init_bf16), part,
+                  n_split, static_cast<const uint16_t*>(g), static_cast<uint16_t*>(a_hi), static_cast<uint16_t*>(a_lo),
+                  rs, B, d, eps) == cudaSuccess ? 0 : -1;
 }
 
 int launch_fin_qkv(const float* part, int n_split, const float* rs, void* q, void* kc, void* vc, int B, int nq_cols,
@@ -149,16 +154,14 @@ int launch_fin_qkv(const float* part, int n_split, const float* rs, void* q, voi
   p.n_split = n_split; p.B = B; p.nq_cols = nq_cols; p.nkv_cols = nkv_cols; p.hd = hd; p.cap = cap; p.t = t;
   for (int i = 0; i < hd / 2; ++i) p.freq[i] = freq[i];
   const int64_t n = (int64_t)B * (nq_cols + 2 * nkv_cols) / 2;
-  fin_qkv_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(p);
-  return 0;
+  return launch_k(fin_qkv_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st, p) == cudaSuccess ? 0 : -1;
 }
 
 int launch_fin_swiglu(const float* part, int n_split, const float* rs, void* m_hi, void* m_lo, int B, int dff,
                       cudaStream_t st) {
   const int64_t n = (int64_t)B * dff;
-  fin_swiglu_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(part, rs, static_cast<uint16_t*>(m_hi),
-                                                                  static_cast<uint16_t*>(m_lo), n_split, B, dff);
-  return 0;
+  return launch_k(fin_swiglu_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st, part, rs,
+                  static_cast<uint16_t*>(m_hi), static_cast<uint16_t*>(m_lo), n_split, B, dff) == cudaSuccess ? 0 : -1;
 }
 
 }  // namespace llama

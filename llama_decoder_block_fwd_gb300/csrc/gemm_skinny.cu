@@ -63,6 +63,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1) gemm_skinny_kernel(const __grid
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_trigger();
   if (threadIdx.x == 0) {
     for (int s = 0; s < p.stages; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
     for (int b = 0; b < 2; ++b) { mbar_init(&acc_full[b], 1); mbar_init(&acc_empty[b], 128); }
@@ -83,21 +84,41 @@ __global__ void __launch_bounds__(SK_THREADS, 1) gemm_skinny_kernel(const __grid
 
   if (warp == 0) {
     if (lane == 0) {  // ---------------- TMA producer
+      // The weights are never written by an earlier kernel: the first unit's first stages are
+      // loaded before waiting for the kernel that produced the activations.
+      int pre = 0;
+      if ((int)blockIdx.x < p.num_units) {
+        int nt, split, kb0, kb1, seg, row;
+        sk_unit(p, blockIdx.x, nkb, nt, split, kb0, kb1);
+        sk_seg(p, nt, seg, row);
+        pre = min(p.stages, kb1 - kb0);
+        for (int i = 0; i < pre; ++i) {
+          mbar_arrive_expect_tx(&full[i], stage_bytes);
+          tma_load_2d(smem_base + i * stage_bytes, &p.tmW[seg], &full[i], (kb0 + i) * SK_TK, row);
+        }
+      }
+      pdl_wait();
       int stage = 0;
       uint32_t phase = 0;
+      bool first_unit = true;
       for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
         int nt, split, kb0, kb1, seg, row;
         sk_unit(p, u, nkb, nt, split, kb0, kb1);
         sk_seg(p, nt, seg, row);
         bool ok = true;
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) { ok = false; break; }
-          mbar_arrive_expect_tx(&full[stage], stage_bytes);
           const uint32_t sa = smem_base + stage * stage_bytes;
-          tma_load_2d(sa, &p.tmW[seg], &full[stage], kb * SK_TK, row);
-          tma_load_2d(sa + SK_A_BYTES, &p.tmX, &full[stage], kb * SK_TK, 0);
+          if (first_unit && kb - kb0 < pre) {   // weights already on their way
+            tma_load_2d(sa + SK_A_BYTES, &p.tmX, &full[stage], kb * SK_TK, 0);
+          } else {
+            if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) { ok = false; break; }
+            mbar_arrive_expect_tx(&full[stage], stage_bytes);
+            tma_load_2d(sa, &p.tmW[seg], &full[stage], kb * SK_TK, row);
+            tma_load_2d(sa + SK_A_BYTES, &p.tmX, &full[stage], kb * SK_TK, 0);
+          }
           if (++stage == p.stages) { stage = 0; phase ^= 1; }
         }
+        first_unit = false;
         if (!ok) break;
       }
     }
@@ -135,6 +156,7 @@ __global__ void __launch_bounds__(SK_THREADS, 1) gemm_skinny_kernel(const __grid
       mbar_wait(drain, 0, &no_abort, p.status);
     }
   } else {  // ---------------- epilogue warps 2..5: one weight row per thread
+    pdl_wait();   // outputs may still be read by an earlier kernel
     const int q = warp & 3;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     int it = 0;
@@ -238,8 +260,7 @@ int launch_gemm_skinny(const SkinnyDesc& g, int num_sms, unsigned* status, cudaS
     attr_set[dev] = true;
   }
   const int grid = std::max(1, std::min(p.num_units, num_sms));
-  gemm_skinny_kernel<<<grid, SK_THREADS, smem, st>>>(p);
-  return 0;
+  return launch_k(gemm_skinny_kernel, dim3(grid), dim3(SK_THREADS), smem, st, p) == cudaSuccess ? 0 : -1;
 }
 
 }  // namespace llama

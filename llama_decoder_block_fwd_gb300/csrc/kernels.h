@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstring>
+#include <utility>
 
 #include "common.cuh"
 
@@ -121,6 +123,29 @@ int launch_fin_qkv(const float* part, int n_split, const float* rs, void* q, voi
                    int nkv_cols, int hd, int64_t cap, int64_t t, const RopeFreq* freq, cudaStream_t st);
 int launch_fin_swiglu(const float* part, int n_split, const float* rs, void* m_hi, void* m_lo, int B, int dff,
                       cudaStream_t st);
+
+// Kernels of the decode chain are launched with programmatic stream serialization (they may
+// begin while their predecessor drains; see pdl_trigger / pdl_wait) while this is on.
+void set_pdl(bool on);
+bool pdl_enabled();
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  if (pdl_enabled()) {
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // The current device's status word (device address) and SM count.
 unsigned* status_ptr();
