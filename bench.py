@@ -27,25 +27,28 @@ METRIC = "block-forward tokens/s (prefill & decode) at 1 GB300; % of TC/HBM roof
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
-def kernel_traffic(role: str):
-    """Measured DRAM bytes per launch of a kernel role from profiles/traffic.json, or None when the
-    kernel sources have changed since that capture."""
-    import glob
+def sources_sha(files) -> str:
+    """Hash of the named kernel sources (file names under the package's csrc/)."""
     import hashlib
+    h = hashlib.sha256()
+    for name in sorted(files):
+        h.update(name.encode())
+        with open(os.path.join(ROOT, "llama_decoder_block_fwd_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def kernel_traffic(role: str):
+    """Measured DRAM bytes per launch of a kernel role from profiles/traffic.json, or None when that
+    kernel's sources have changed since the capture."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
-            t = json.load(f)
+            k = json.load(f).get("kernels", {}).get(role)
+        if k is None or sources_sha(k["sources"]) != k["sha"]:
+            return None
     except Exception:
         return None
-    h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "llama_decoder_block_fwd_gb300", "csrc", "*"))):
-        h.update(os.path.basename(p).encode())
-        with open(p, "rb") as f:
-            h.update(f.read())
-    if h.hexdigest()[:16] != t.get("source_sha"):
-        return None
-    k = t.get("kernels", {}).get(role)
-    return None if k is None else k["bytes_per_launch"]
+    return k["bytes_per_launch"]
 
 
 def peaks():
