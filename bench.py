@@ -191,6 +191,47 @@ def decode_bytes(wl, cap_unused=None):
 
 
 # ----------------------------------------------------------------------------- our arm
+def bench_mha_prefill(args, world):
+    """The LLaMA-7B (MHA, n_kv = n_q) block prefill, B4 S2048: device-timed steps only."""
+    import torch
+
+    import llama_decoder_block_fwd_gb300 as L
+    from synth import configs as C
+    from synth import workloads as W
+
+    wl = C.LLAMA_7B_MHA_PREFILL
+    T = wl.B * wl.S
+    w = W.device_layer(wl)
+    x = W.device_x(wl).reshape(T, wl.d_model)
+    y = torch.empty_like(x)
+    ws = torch.empty(L.llama_workspace_bytes(L.OP_BLOCK_FORWARD, wl.dims, wl.dtype), dtype=torch.uint8,
+                     device="cuda")
+    bw = L.block_weights(w)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        L.llama_block_forward(wl.dims, wl.dtype, bw, x, y, 0, None, None, 0, ws, stream)
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        L.llama_block_forward(wl.dims, wl.dtype, bw, x, y, 0, None, None, 0, ws, stream)
+    e1.record(stream)
+    barrier(world)
+    if L.llama_get_device_status() != 0:
+        raise RuntimeError("device status word set during the MHA prefill")
+    ms = max_over_ranks(world, e0.elapsed_time(e1)) / args.steps
+    pk, pk_src = peaks()
+    hq = wl.n_q * wl.head_dim
+    flops = 2.0 * T * (wl.d_model * (hq + 2 * wl.n_kv * wl.head_dim) + hq * wl.d_model + 3 * wl.d_model * wl.d_ff) \
+        + 4.0 * wl.n_q * wl.head_dim * wl.B * wl.S * (wl.S + 1) / 2
+    out = {"workload": wl.name, "value": aggregate_rate(world, T, ms), "unit": "tokens/s", "ms_per_step": ms,
+           "flops_per_step": flops, "block_tflops": flops / (ms / 1e3) / 1e12,
+           "block_tc_frac": flops / (ms / 1e3) / 1e12 / pk["bf16_tflops"], "peak_source": f"{pk_src} bf16 burst"}
+    del w, x, y, ws
+    torch.cuda.empty_cache()
+    return out
+
+
 def bench_prefill(args, world, rank):
     import torch
 
@@ -441,6 +482,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-mha", action="store_true", help="skip the LLaMA-7B MHA block prefill")
     ap.add_argument("--prefill-seq", type=int, default=8192, help="tokens of the prefill workload (default 8192)")
     ap.add_argument("--decode-layers", type=int, default=32, help="layers of the decode stack (default 32)")
     args = ap.parse_args()
@@ -454,6 +496,7 @@ def main():
 
     world, rank, local = dist_setup()
     pre = bench_prefill(args, world, rank)
+    mha = None if args.no_mha else bench_mha_prefill(args, world)
     dec = None if args.no_decode else bench_decode(args, world, rank)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -471,7 +514,7 @@ def main():
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,0.02) weights, N(0,1) inputs)",
             "config": pre["config"], "roofline": pre["roofline"], "cpu_baseline": cpu, "e2e": pre["e2e"],
             "gpu_launches": pre["gpu_launches"], "clocks": pre["clocks"], "block_tc_frac": pre["block_tc_frac"],
-            "block_tflops": pre["block_tflops"], "kernels": pre["kernels"], "decode": dec,
+            "block_tflops": pre["block_tflops"], "kernels": pre["kernels"], "decode": dec, "mha_prefill": mha,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
