@@ -175,8 +175,39 @@ int llama_gqa_attention_decode_noalloc(const llama_dims* dims, int dtype, const 
 size_t llama_workspace_bytes(int op, const llama_dims* dims, int dtype, int n_layers,
                              int64_t vocab, int64_t kv_capacity);
 
+/* Next-token choice from the LM head's logits ("LLaMA-3 8B 现代 LLM 架构、计算规模与能耗", section 十:
+ * softmax over the vocabulary, then argmax, or a draw shaped by temperature, top-k and top-p).
+ *   logits  [B, ld] fp32 (device), row b's first `vocab` entries used; finite values or -inf,
+ *           at least one finite per row
+ *   temperature  T > 0 draws from softmax(z / T); T <= 0 returns the argmax
+ *   top_k   keep the k most probable tokens (k <= 0 or k >= vocab: all; k = 1: argmax)
+ *   top_p   then keep the shortest run of most probable tokens whose share of the top-k mass
+ *           reaches p (p >= 1: all; p <= 0: the argmax)
+ *   u       [B] fp32 (device): one uniform draw in [0, 1) per row, supplied by the caller (values
+ *           outside are clamped into it)
+ *   tokens  [B] int32 (device): the chosen token ids
+ * Ranking is by logit, larger first, ties by the lower id.  The draw walks the kept tokens in
+ * increasing id and returns the first whose cumulative probability exceeds u.  Probabilities are
+ * exp((z - z_max) / T) in fp32 summed exactly in 2^-40 fixed point, so the result does not depend
+ * on thread timing.  Errors: LLAMA_ERR_INVALID_ARG for B < 0, vocab < 1 or > 2^30, ld < vocab,
+ * NaN temperature or top_p, or a NULL pointer with B > 0; LLAMA_ERR_ALIGNMENT for pointers not
+ * 4-byte aligned.  B = 0 launches nothing.                                                      */
+int llama_sample(const float* logits, int64_t B, int64_t vocab, int64_t ld, float temperature,
+                 int64_t top_k, float top_p, const float* u, int32_t* tokens, void* stream);
+
+/* Embedding lookup ("LLaMA-3 8B ...", section 三): x[i] = table[tokens[i]] for i < n.
+ *   table  [vocab, d_model] of `dtype` (device), row-major
+ *   tokens [n] int32 (device)
+ *   x      [n, d_model] of `dtype` (device)
+ * A token id outside [0, vocab) gives a zero row and latches LLAMA_ERR_INVALID_ARG in the device
+ * status word (read with llama_get_device_status).  Errors returned synchronously:
+ * LLAMA_ERR_INVALID_ARG for vocab < 1, d_model < 1, n < 0 or NULL pointers with n > 0.        */
+int llama_embed(int dtype, const void* table, int64_t vocab, int64_t d_model, const int32_t* tokens,
+                int64_t n, void* x, void* stream);
+
 /* Synchronises `stream`, then reads and clears the device status word of the current device.
- * *out receives LLAMA_OK or LLAMA_ERR_TIMEOUT (a kernel's bounded wait ran out and it exited).
+ * *out receives LLAMA_OK, LLAMA_ERR_TIMEOUT (a kernel's bounded wait ran out and it exited) or
+ * LLAMA_ERR_INVALID_ARG (llama_embed met a token id outside the table).
  * Returns LLAMA_OK, or LLAMA_ERR_CUDA if the synchronisation or the copy failed.             */
 int llama_get_device_status(int* out, void* stream);
 

@@ -16,6 +16,7 @@ __all__ = [
     "F32", "BF16", "LlamaError", "Dims", "BlockWeights", "lib", "dims_of",
     "llama_rmsnorm", "llama_rope", "llama_gqa_attention", "llama_gqa_attention_decode_noalloc", "llama_swiglu_ffn",
     "llama_block_forward", "llama_stack_decode_step", "llama_workspace_bytes",
+    "llama_sample", "llama_embed",
     "llama_get_device_status", "llama_status_string", "llama_profile_enable", "llama_profile_read",
     "OP_RMSNORM", "OP_ROPE", "OP_GQA_ATTENTION", "OP_SWIGLU_FFN", "OP_BLOCK_FORWARD",
     "OP_STACK_DECODE_STEP",
@@ -76,6 +77,8 @@ def lib() -> ctypes.CDLL:
                                             vp, vp, i64, i64, vp, vp, sz, vp],
                 "llama_get_device_status": [ctypes.POINTER(ctypes.c_int), vp],
                 "llama_gqa_attention_decode_noalloc": [pd, i32, vp, vp, vp, i64, i64, vp, vp],
+                "llama_sample": [vp, i64, i64, i64, ctypes.c_float, i64, ctypes.c_float, vp, vp, vp],
+                "llama_embed": [i32, vp, i64, i64, vp, i64, vp, vp],
             }
             for name, args in sig.items():
                 fn = getattr(L, name)
@@ -180,6 +183,21 @@ def llama_stack_decode_step(dims, dtype, layers, final_g, w_lm, vocab, x_emb, k_
     _check(lib().llama_stack_decode_step(ctypes.byref(_d(dims)), dtype, n, arr, _p(final_g), _p(w_lm), int(vocab),
                                          _p(x_emb), _p(k_cache), _p(v_cache), int(cache_capacity), int(t_cache),
                                          _p(logits), _p(ws), _nbytes(ws), _s(stream)), "llama_stack_decode_step")
+
+
+def llama_sample(logits, temperature, top_k, top_p, u, tokens, vocab=None, stream=None):
+    """tokens[b] <- the token chosen from logits[b, :vocab] (fp32 [B, ld]) with the uniform u[b]."""
+    B = 0 if logits is None else int(logits.shape[0])
+    ld = 0 if logits is None else int(logits.stride(0))
+    V = int(logits.shape[1]) if vocab is None else int(vocab)
+    _check(lib().llama_sample(_p(logits), B, V, ld, float(temperature), int(top_k), float(top_p), _p(u), _p(tokens),
+                              _s(stream)), "llama_sample")
+
+
+def llama_embed(dtype, table, tokens, x, stream=None):
+    """x[i] <- table[tokens[i]] (table [vocab, d_model], tokens int32 [n], x [n, d_model])."""
+    _check(lib().llama_embed(dtype, _p(table), int(table.shape[0]), int(table.shape[1]), _p(tokens),
+                             int(tokens.numel()), _p(x), _s(stream)), "llama_embed")
 
 
 def llama_workspace_bytes(op, dims, dtype, n_layers=0, vocab=0, kv_capacity=0) -> int:

@@ -5,6 +5,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <climits>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -682,8 +683,38 @@ int llama_get_device_status(int* out, void* stream) {
     const unsigned zero = 0;
     if (cudaMemcpy(p, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return LLAMA_ERR_CUDA;
   }
-  *out = (v & STATUS_TIMEOUT) ? LLAMA_ERR_TIMEOUT : LLAMA_OK;
+  *out = (v & STATUS_TIMEOUT) ? LLAMA_ERR_TIMEOUT : (v & STATUS_BAD_TOKEN) ? LLAMA_ERR_INVALID_ARG : LLAMA_OK;
   return LLAMA_OK;
+}
+
+int llama_sample(const float* logits, int64_t B, int64_t vocab, int64_t ld, float temperature, int64_t top_k,
+                 float top_p, const float* u, int32_t* tokens, void* stream) {
+  if (B < 0 || vocab < 1 || vocab > (int64_t(1) << 30) || ld < vocab || B > INT32_MAX) return LLAMA_ERR_INVALID_ARG;
+  if (std::isnan(temperature) || std::isnan(top_p)) return LLAMA_ERR_INVALID_ARG;
+  if (B == 0) return LLAMA_OK;
+  if (!logits || !u || !tokens) return LLAMA_ERR_INVALID_ARG;
+  if ((uintptr_t)logits % 4 || (uintptr_t)u % 4 || (uintptr_t)tokens % 4) return LLAMA_ERR_ALIGNMENT;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  prof::begin("sample", st);
+  const int rc = launch_sample(logits, B, vocab, ld, temperature, top_k, top_p, u, tokens, st);
+  prof::end(st);
+  return rc ? LLAMA_ERR_CUDA : launch_status();
+}
+
+int llama_embed(int dtype, const void* table, int64_t vocab, int64_t d_model, const int32_t* tokens, int64_t n,
+                void* x, void* stream) {
+  int rc;
+  if ((rc = check_dtype(dtype)) != LLAMA_OK) return rc;
+  if (vocab < 1 || d_model < 1 || n < 0 || n > INT32_MAX || vocab > INT32_MAX) return LLAMA_ERR_INVALID_ARG;
+  if (n == 0) return LLAMA_OK;
+  if (!table || !tokens || !x) return LLAMA_ERR_INVALID_ARG;
+  unsigned* status = status_ptr();
+  if (!status) return LLAMA_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  prof::begin("embed", st);
+  rc = launch_embed(dtype, table, vocab, d_model, tokens, n, x, status, st);
+  prof::end(st);
+  return rc ? LLAMA_ERR_CUDA : launch_status();
 }
 
 size_t llama_workspace_bytes(int op, const llama_dims* d, int dtype, int n_layers, int64_t vocab,

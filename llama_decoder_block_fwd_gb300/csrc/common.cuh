@@ -14,7 +14,7 @@ namespace llama {
 
 // ---------------------------------------------------------------- status word
 // Bit flags latched by kernels; read and cleared by llama_get_device_status().
-enum : unsigned { STATUS_TIMEOUT = 1u };
+enum : unsigned { STATUS_TIMEOUT = 1u, STATUS_BAD_TOKEN = 2u };
 
 // A bounded wait gives up after this many nanoseconds of %globaltimer.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;

@@ -147,6 +147,12 @@ cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// sample.cu: next-token choice (one CTA per row) and the embedding lookup
+int launch_sample(const float* logits, int64_t B, int64_t V, int64_t ld, float temperature, int64_t top_k,
+                  float top_p, const float* u, int* tokens, cudaStream_t st);
+int launch_embed(int dtype, const void* table, int64_t V, int64_t d, const int* tokens, int64_t n, void* x,
+                 unsigned* status, cudaStream_t st);
+
 // The current device's status word (device address) and SM count.
 unsigned* status_ptr();
 int num_sms();

@@ -41,6 +41,8 @@ TID_KCACHE = 11
 TID_VCACHE = 12
 TID_FINAL_G = 13
 TID_WLM = 14
+TID_EMBED = 15     # token embedding table [vocab, d_model]
+TID_LOGITS = 16    # stand-alone logits for the next-token choice
 LAYER_STRIDE = 32
 
 

@@ -84,3 +84,15 @@ def device_x_emb(wl: C.Workload):
 def host_x_emb(wl: C.Workload, rows) -> np.ndarray:
     d = wl.d_model
     return np.stack([host_f64(wl.dtype, (d,), wl.seed, TID_X, 0.0, 1.0, offset=int(b) * d) for b in rows])
+
+
+def device_embed(wl: C.Workload):
+    """The [vocab, d_model] token embedding table, rows N(0, 1)."""
+    from . import TID_EMBED
+    return device_tensor(wl.dtype, (wl.vocab, wl.d_model), wl.seed, TID_EMBED, 0.0, 1.0)
+
+
+def host_embed_rows(wl: C.Workload, tokens) -> np.ndarray:
+    from . import TID_EMBED
+    d = wl.d_model
+    return np.stack([host_f64(wl.dtype, (d,), wl.seed, TID_EMBED, 0.0, 1.0, offset=int(t) * d) for t in tokens])

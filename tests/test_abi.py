@@ -93,3 +93,23 @@ def test_workspace_sizes_grow_with_shape():
     assert 0 < small < big
     assert L.llama_workspace_bytes(L.OP_STACK_DECODE_STEP, _dims(B=64, S=1), L.BF16) > 0
     assert L.llama_workspace_bytes(L.OP_RMSNORM, _dims(), L.BF16) == 0
+
+
+def test_sample_and_embed_reject_bad_arguments():
+    lib = L.lib()
+    fake = 0x10000
+    nan = float("nan")
+    # B < 0, vocab < 1, ld < vocab, NaN temperature / top_p, NULL pointers
+    assert lib.llama_sample(fake, -1, 10, 10, 1.0, 0, 1.0, fake, fake, None) == 1
+    assert lib.llama_sample(fake, 2, 0, 10, 1.0, 0, 1.0, fake, fake, None) == 1
+    assert lib.llama_sample(fake, 2, 10, 5, 1.0, 0, 1.0, fake, fake, None) == 1
+    assert lib.llama_sample(fake, 2, 10, 10, nan, 0, 1.0, fake, fake, None) == 1
+    assert lib.llama_sample(fake, 2, 10, 10, 1.0, 0, nan, fake, fake, None) == 1
+    assert lib.llama_sample(None, 2, 10, 10, 1.0, 0, 1.0, fake, fake, None) == 1
+    assert lib.llama_sample(fake + 2, 2, 10, 10, 1.0, 0, 1.0, fake, fake, None) == 3
+    assert lib.llama_sample(None, 0, 10, 10, 1.0, 0, 1.0, None, None, None) == 0   # nothing to do
+    assert lib.llama_embed(7, fake, 10, 16, fake, 4, fake, None) == 2
+    assert lib.llama_embed(L.BF16, fake, 0, 16, fake, 4, fake, None) == 1
+    assert lib.llama_embed(L.BF16, fake, 10, 0, fake, 4, fake, None) == 1
+    assert lib.llama_embed(L.BF16, None, 10, 16, fake, 4, fake, None) == 1
+    assert lib.llama_embed(L.BF16, None, 10, 16, None, 0, None, None) == 0
