@@ -232,6 +232,43 @@ def bench_mha_prefill(args, world):
     return out
 
 
+def bench_sample(args, world):
+    """Next-token choice for the decode batch: 64 rows of 128256 fp32 logits, temperature 0.8,
+    top-k 50, top-p 0.95.  L2 is flushed (a 256 MB write) before every timed call."""
+    import numpy as np
+    import torch
+
+    import llama_decoder_block_fwd_gb300 as L
+    from synth import F32, TID_LOGITS
+    from synth import configs as C
+    from synth import workloads as W
+
+    wl = C.LLAMA3_8B_DECODE
+    z = W.device_tensor(F32, (wl.B, wl.vocab), wl.seed, TID_LOGITS, 0.0, 2.5)
+    u = torch.from_numpy(np.random.default_rng(wl.seed).random(wl.B).astype(np.float32)).cuda()
+    tok = torch.empty(wl.B, dtype=torch.int32, device="cuda")
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        L.llama_sample(z, 0.8, 50, 0.95, u, tok)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier(world)
+    for a, b in ev:
+        flush.fill_(1)
+        a.record(stream)
+        L.llama_sample(z, 0.8, 50, 0.95, u, tok)
+        b.record(stream)
+    barrier(world)
+    ms = max_over_ranks(world, sum(a.elapsed_time(b) for a, b in ev) / args.steps)
+    nbytes = z.numel() * 4
+    out = {"workload": f"{wl.B} x {wl.vocab} fp32 logits, T 0.8, top-k 50, top-p 0.95", "us_per_call": ms * 1e3,
+           "rows_per_s": aggregate_rate(world, wl.B, ms), "logits_gbs": nbytes / (ms / 1e3) / 1e9,
+           "l2": "flushed before every call"}
+    del z, u, tok, flush
+    torch.cuda.empty_cache()
+    return out
+
+
 def bench_prefill(args, world, rank):
     import torch
 
@@ -498,6 +535,7 @@ def main():
     pre = bench_prefill(args, world, rank)
     mha = None if args.no_mha else bench_mha_prefill(args, world)
     dec = None if args.no_decode else bench_decode(args, world, rank)
+    smp = None if args.no_decode else bench_sample(args, world)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         S_sample, n_seq, total = 1024, 0, 0.0
@@ -515,6 +553,7 @@ def main():
             "config": pre["config"], "roofline": pre["roofline"], "cpu_baseline": cpu, "e2e": pre["e2e"],
             "gpu_launches": pre["gpu_launches"], "clocks": pre["clocks"], "block_tc_frac": pre["block_tc_frac"],
             "block_tflops": pre["block_tflops"], "kernels": pre["kernels"], "decode": dec, "mha_prefill": mha,
+            "sample": smp,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

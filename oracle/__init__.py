@@ -2,3 +2,4 @@
 from .llama_oracle import *  # noqa: F401,F403
 from .llama_oracle import Dims, BlockWeights  # noqa: F401
 from . import sampling  # noqa: F401
+from . import fp8  # noqa: F401

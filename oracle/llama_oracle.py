@@ -201,16 +201,20 @@ def project_kv(x: np.ndarray, w: BlockWeights, dims: Dims, pos0: int = 0):
 
 def block_forward(x: np.ndarray, w: BlockWeights, dims: Dims, pos0: int = 0,
                   k_past: np.ndarray | None = None, v_past: np.ndarray | None = None,
-                  rows: np.ndarray | None = None):
+                  rows: np.ndarray | None = None, kv_store=None):
     """h = x + Attn(RMSNorm(x)); y = h + FFN(RMSNorm(h)).
 
     x: [B, S, d] for positions pos0 .. pos0+S-1.  k_past/v_past: [B, pos0, n_kv, hd] keys and
     values already cached for positions 0..pos0-1 (None when pos0 == 0).  When rows is given,
     K and V are still computed for every token, but the query side (and the output) only for
-    those token rows.  Returns (y [B, len(rows) or S, d], k_new, v_new [B, S, n_kv, hd]).
+    those token rows.  kv_store, if given, maps (k_new, v_new) to the values the cache holds
+    (an 8-bit cache encodes them); attention then reads those.  Returns (y [B, len(rows) or S, d],
+    k_new, v_new [B, S, n_kv, hd]).
     """
     B, S, d = x.shape
     k_new, v_new = project_kv(x, w, dims, pos0)
+    if kv_store is not None:
+        k_new, v_new = kv_store(k_new, v_new)
     if pos0 > 0:
         k_all = np.concatenate([k_past[:, :pos0], k_new], axis=1)
         v_all = np.concatenate([v_past[:, :pos0], v_new], axis=1)
@@ -230,19 +234,21 @@ def block_forward(x: np.ndarray, w: BlockWeights, dims: Dims, pos0: int = 0,
 # Stack decode step  [P3 section 二 data flow, section 九 decode, section 十 head]
 # ----------------------------------------------------------------------------------------
 def stack_decode_step(x_emb: np.ndarray, layer_weights, n_layers: int, dims: Dims, t_cache: int,
-                      kv_cache, final_g: np.ndarray, w_lm: np.ndarray) -> np.ndarray:
+                      kv_cache, final_g: np.ndarray, w_lm: np.ndarray, kv_store=None) -> np.ndarray:
     """One new token per sequence through n_layers blocks, then RMSNorm and the untied LM head.
 
     x_emb: [B, d] embedding rows of the new tokens (position t_cache).  layer_weights(l) returns
     the BlockWeights of layer l; kv_cache(l) returns (k, v) [B, >=t_cache, n_kv, hd] holding
-    positions 0..t_cache-1.  The residual stream stays in fp64 across layers.
+    positions 0..t_cache-1.  kv_store(l), if given, returns layer l's map from the new token's
+    K/V to the values the cache holds.  The residual stream stays in fp64 across layers.
     Returns logits [B, vocab].
     """
     x = x_emb[:, None, :].astype(np.float64)
     for l in range(n_layers):
         k_past, v_past = kv_cache(l)
         x, _, _ = block_forward(x, layer_weights(l), dims, pos0=t_cache,
-                                k_past=k_past, v_past=v_past)
+                                k_past=k_past, v_past=v_past,
+                                kv_store=None if kv_store is None else kv_store(l))
     z = rmsnorm(x[:, 0, :], final_g, dims.eps)
     return z @ w_lm.T
 
