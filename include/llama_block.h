@@ -175,6 +175,43 @@ int llama_gqa_attention_decode_noalloc(const llama_dims* dims, int dtype, const 
 size_t llama_workspace_bytes(int op, const llama_dims* dims, int dtype, int n_layers,
                              int64_t vocab, int64_t kv_capacity);
 
+/* 8-bit KV cache.  The pages size the cache in bf16 and give no 8-bit format; this library's
+ * format is OCP E4M3 ("e4m3fn") codes, one byte per element, with one fp32 scale per
+ * (layer, K or V, KV head): the stored value is code * scale.  Encoding divides in fp32, rounds to
+ * the nearest E4M3 value (ties to even) and saturates at +-448.  The cache layout is the bf16
+ * one with 1-byte elements: [n_layers, B, capacity, n_kv, head_dim].                          */
+
+/* codes[t, g, i] = E4M3(x[t, g, i] / scale[g]) for n_tokens rows of n_kv heads x head_dim bf16
+ * values (x [n_tokens, n_kv, head_dim] bf16 and codes of the same shape, device; scale [n_kv]
+ * fp32, device).  Errors: LLAMA_ERR_INVALID_ARG for n_tokens < 0, n_kv < 1, head_dim not a
+ * positive multiple of 8, or NULL pointers with n_tokens > 0; LLAMA_ERR_ALIGNMENT unless x is
+ * 16-byte, codes 8-byte and scale 4-byte aligned.                                              */
+int llama_kv_quantize(const void* x, int64_t n_tokens, int64_t n_kv, int64_t head_dim,
+                      const float* scale, void* codes, void* stream);
+
+/* llama_gqa_attention for one new token per sequence (S = 1) over an 8-bit cache: k and v are
+ * codes [B, kv_capacity, n_kv, head_dim] holding positions 0..pos0 (the new token's K/V already
+ * written), k_scale / v_scale [n_kv] fp32 (device); q and o bf16 [B, n_q, head_dim].
+ * Needs head_dim 128, n_q / n_kv in {1, 2, 4, 8, 16} (else LLAMA_ERR_UNSUPPORTED) and the
+ * workspace llama_workspace_bytes(LLAMA_OP_GQA_ATTENTION, ...) gives for this shape.          */
+int llama_gqa_attention_decode_kv8(const llama_dims* dims, const void* q, const void* k,
+                                   const void* v, const float* k_scale, const float* v_scale,
+                                   int64_t kv_capacity, int64_t pos0, void* o, void* ws,
+                                   size_t ws_bytes, void* stream);
+
+/* llama_stack_decode_step with bf16 weights and an 8-bit cache: k_cache / v_cache hold codes
+ * [n_layers, B, cache_capacity, n_kv, head_dim]; kv_scales [n_layers][2][n_kv] fp32 (device),
+ * index 0 for K and 1 for V.  The new token's K/V are encoded into the cache at t_cache and
+ * attention reads the stored values.  Same workspace as the bf16 call; supported for the shapes
+ * of its tensor-core path (bf16, B <= 128, head_dim 128, d_model, n_q*head_dim, n_kv*head_dim
+ * and d_ff multiples of 128, n_q / n_kv in {1, 2, 4, 8, 16}), else LLAMA_ERR_UNSUPPORTED.     */
+int llama_stack_decode_step_kv8(const llama_dims* dims, int n_layers,
+                                const llama_block_weights* layers, const void* final_g,
+                                const void* w_lm, int64_t vocab, const void* x_emb,
+                                void* k_cache, void* v_cache, const float* kv_scales,
+                                int64_t cache_capacity, int64_t t_cache, float* logits, void* ws,
+                                size_t ws_bytes, void* stream);
+
 /* Next-token choice from the LM head's logits ("LLaMA-3 8B 现代 LLM 架构、计算规模与能耗", section 十:
  * softmax over the vocabulary, then argmax, or a draw shaped by temperature, top-k and top-p).
  *   logits  [B, ld] fp32 (device), row b's first `vocab` entries used; finite values or -inf,

@@ -16,7 +16,8 @@ __all__ = [
     "F32", "BF16", "LlamaError", "Dims", "BlockWeights", "lib", "dims_of",
     "llama_rmsnorm", "llama_rope", "llama_gqa_attention", "llama_gqa_attention_decode_noalloc", "llama_swiglu_ffn",
     "llama_block_forward", "llama_stack_decode_step", "llama_workspace_bytes",
-    "llama_sample", "llama_embed",
+    "llama_sample", "llama_embed", "llama_kv_quantize", "llama_gqa_attention_decode_kv8",
+    "llama_stack_decode_step_kv8",
     "llama_get_device_status", "llama_status_string", "llama_profile_enable", "llama_profile_read",
     "OP_RMSNORM", "OP_ROPE", "OP_GQA_ATTENTION", "OP_SWIGLU_FFN", "OP_BLOCK_FORWARD",
     "OP_STACK_DECODE_STEP",
@@ -79,6 +80,10 @@ def lib() -> ctypes.CDLL:
                 "llama_gqa_attention_decode_noalloc": [pd, i32, vp, vp, vp, i64, i64, vp, vp],
                 "llama_sample": [vp, i64, i64, i64, ctypes.c_float, i64, ctypes.c_float, vp, vp, vp],
                 "llama_embed": [i32, vp, i64, i64, vp, i64, vp, vp],
+                "llama_kv_quantize": [vp, i64, i64, i64, vp, vp, vp],
+                "llama_gqa_attention_decode_kv8": [pd, vp, vp, vp, vp, vp, i64, i64, vp, vp, sz, vp],
+                "llama_stack_decode_step_kv8": [pd, i32, ctypes.POINTER(BlockWeights), vp, vp, i64, vp, vp, vp, vp,
+                                                i64, i64, vp, vp, sz, vp],
             }
             for name, args in sig.items():
                 fn = getattr(L, name)
@@ -198,6 +203,29 @@ def llama_embed(dtype, table, tokens, x, stream=None):
     """x[i] <- table[tokens[i]] (table [vocab, d_model], tokens int32 [n], x [n, d_model])."""
     _check(lib().llama_embed(dtype, _p(table), int(table.shape[0]), int(table.shape[1]), _p(tokens),
                              int(tokens.numel()), _p(x), _s(stream)), "llama_embed")
+
+
+def llama_kv_quantize(x, scale, codes, stream=None):
+    """codes <- E4M3(x / scale[head]) for x bf16 [..., n_kv, head_dim], scale fp32 [n_kv]."""
+    n_kv, hd = int(x.shape[-2]), int(x.shape[-1])
+    _check(lib().llama_kv_quantize(_p(x), int(x.numel() // (n_kv * hd)), n_kv, hd, _p(scale), _p(codes), _s(stream)),
+           "llama_kv_quantize")
+
+
+def llama_gqa_attention_decode_kv8(dims, q, k, v, k_scale, v_scale, kv_capacity, pos0, o, ws, stream=None):
+    _check(lib().llama_gqa_attention_decode_kv8(ctypes.byref(_d(dims)), _p(q), _p(k), _p(v), _p(k_scale),
+                                                _p(v_scale), int(kv_capacity), int(pos0), _p(o), _p(ws), _nbytes(ws),
+                                                _s(stream)), "llama_gqa_attention_decode_kv8")
+
+
+def llama_stack_decode_step_kv8(dims, layers, final_g, w_lm, vocab, x_emb, k_cache, v_cache, kv_scales,
+                                cache_capacity, t_cache, logits, ws, stream=None):
+    n = len(layers)
+    arr = (BlockWeights * n)(*[lw if isinstance(lw, BlockWeights) else block_weights(lw) for lw in layers])
+    _check(lib().llama_stack_decode_step_kv8(ctypes.byref(_d(dims)), n, arr, _p(final_g), _p(w_lm), int(vocab),
+                                             _p(x_emb), _p(k_cache), _p(v_cache), _p(kv_scales), int(cache_capacity),
+                                             int(t_cache), _p(logits), _p(ws), _nbytes(ws), _s(stream)),
+           "llama_stack_decode_step_kv8")
 
 
 def llama_workspace_bytes(op, dims, dtype, n_layers=0, vocab=0, kv_capacity=0) -> int:

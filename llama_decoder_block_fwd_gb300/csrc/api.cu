@@ -126,6 +126,19 @@ bool encode_tmap_3d_bf16(CUtensorMap* m, const void* base, uint64_t d0, uint64_t
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_tmap_4d_u8(CUtensorMap* m, const void* base, const uint64_t* dims, const uint64_t* strides_bytes,
+                       const uint32_t* box) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t d[4] = {dims[0], dims[1], dims[2], dims[3]};
+  cuuint64_t s[3] = {strides_bytes[0], strides_bytes[1], strides_bytes[2]};
+  cuuint32_t b[4] = {box[0], box[1], box[2], box[3]};
+  cuuint32_t e[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), d, s, b, e, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
 bool encode_tmap_4d_bf16(CUtensorMap* m, const void* base, const uint64_t* dims, const uint64_t* strides_bytes,
                          const uint32_t* box) {
   auto fn = encode_fn();
@@ -207,6 +220,16 @@ int run_gemm(const GemmDesc& g, const char* role, cudaStream_t st) {
 }
 
 int run_attention(const AttnDesc& a, cudaStream_t st) {
+  if (a.k_scale) {   // 8-bit cache: the tensor-core decode kernel is the only path
+    if (!decode_attn8_supported(a)) return LLAMA_ERR_UNSUPPORTED;
+    if (!a.ws || a.ws_bytes < decode_attn_ws_bytes(a)) return LLAMA_ERR_WORKSPACE;
+    unsigned* status = status_ptr();
+    if (!status) return LLAMA_ERR_CUDA;
+    prof::begin("attn_decode_kv8", st);
+    if (launch_decode_attn8(a, a.ws, num_sms(), status, st) != 0) return LLAMA_ERR_CUDA;
+    prof::end(st);
+    return launch_status();
+  }
   if (decode_attn_supported(a) && a.ws && a.ws_bytes >= decode_attn_ws_bytes(a)) {
     unsigned* status = status_ptr();
     if (!status) return LLAMA_ERR_CUDA;
@@ -538,13 +561,14 @@ int run_fin(const char* role, int launch_rc, cudaStream_t st) {
   return launch_status();
 }
 
+// kv_scales: null for a bf16 cache; for an 8-bit cache, [n_layers][2 (K, V)][n_kv] fp32 scales.
 int decode_stack_tc(const llama_dims* d, int n_layers, const llama_block_weights* layers, const void* final_g,
                     const void* w_lm, int64_t vocab, const void* x_emb, void* k_cache, void* v_cache, int64_t cap,
-                    int64_t t_cache, float* logits, const DecodeTcWs& w, cudaStream_t st) {
+                    int64_t t_cache, float* logits, const DecodeTcWs& w, const float* kv_scales, cudaStream_t st) {
   const int B = (int)d->B, D = (int)d->d_model;
   const int64_t hq = d->n_q * d->head_dim, hkv = d->n_kv * d->head_dim;
   const float eps = (float)d->eps;
-  const size_t layer_cache = (size_t)(d->B * cap * hkv) * 2;
+  const size_t layer_cache = (size_t)(d->B * cap * hkv) * (kv_scales ? 1 : 2);
   RopeFreq freq[kMaxRopePairs];
   rope_freqs(d, freq);
   int rc;
@@ -552,6 +576,8 @@ int decode_stack_tc(const llama_dims* d, int n_layers, const llama_block_weights
     const llama_block_weights& lw = layers[l];
     void* kc = static_cast<char*>(k_cache) + l * layer_cache;
     void* vc = static_cast<char*>(v_cache) + l * layer_cache;
+    const float* ks = kv_scales ? kv_scales + (size_t)l * 2 * d->n_kv : nullptr;
+    const float* vs = kv_scales ? ks + d->n_kv : nullptr;
     // (layer 0: x = embedding rows) a = x * g_attn (hi, lo); rs1
     prof::begin("fin_norm", st);
     rc = launch_fin_norm(w.xres, l == 0 ? x_emb : nullptr, nullptr, 0, lw.attn_norm_g, w.act,
@@ -566,7 +592,7 @@ int decode_stack_tc(const llama_dims* d, int n_layers, const llama_block_weights
       return rc;
     prof::begin("fin_qkv", st);
     rc = launch_fin_qkv(w.part, w.s_qkv, w.rs1, w.q, kc, vc, B, (int)hq, (int)hkv, (int)d->head_dim, cap, t_cache, freq,
-                        st);
+                        ks, vs, st);
     prof::end(st);
     if ((rc = run_fin("fin_qkv", rc, st)) != LLAMA_OK) return rc;
     // attention over t_cache + 1 keys; o as hi + lo into the activation buffers
@@ -574,6 +600,8 @@ int decode_stack_tc(const llama_dims* d, int n_layers, const llama_block_weights
     a.o_lo = static_cast<char*>(w.act) + w.mp * hq * 2;
     a.ws = w.attn;
     a.ws_bytes = w.attn_bytes;
+    a.k_scale = ks;
+    a.v_scale = vs;
     if ((rc = run_attention(a, st)) != LLAMA_OK) return rc;
     // h = x + o W_O^T: the split-K partials are added straight into the fp32 residual stream
     const void* wo[1] = {lw.wo};
@@ -849,7 +877,7 @@ int llama_stack_decode_step(const llama_dims* d, int dtype, int n_layers, const 
     // the decode chain's kernels may overlap their predecessors' tails (each waits for its inputs)
     set_pdl(true);
     const int rc_tc = decode_stack_tc(d, n_layers, layers, final_g, w_lm, vocab, x_emb, k_cache, v_cache, cache_capacity,
-                                      t_cache, logits, plan_decode_tc(d, ws, cache_capacity), st);
+                                      t_cache, logits, plan_decode_tc(d, ws, cache_capacity), nullptr, st);
     set_pdl(false);
     return rc_tc;
   }
@@ -883,6 +911,72 @@ int llama_stack_decode_step(const llama_dims* d, int dtype, int n_layers, const 
   if ((rc = run_rmsnorm(dtype, 1, dtype == LLAMA_F32, dw.xres, final_g, dw.u, Bn, D, (float)d->eps, st)) != LLAMA_OK)
     return rc;
   return run_linear_resid(dtype, Bn, dw.u, D, w_lm, vocab, nullptr, 0, logits, 1, st);
+}
+
+int llama_stack_decode_step_kv8(const llama_dims* d, int n_layers, const llama_block_weights* layers,
+                                const void* final_g, const void* w_lm, int64_t vocab, const void* x_emb,
+                                void* k_cache, void* v_cache, const float* kv_scales, int64_t cache_capacity,
+                                int64_t t_cache, float* logits, void* ws, size_t ws_bytes, void* stream) {
+  int rc;
+  if ((rc = check_dims(d, NEED_D | NEED_HEADS | NEED_FF)) != LLAMA_OK) return rc;
+  if (d->S != 1 || n_layers <= 0 || vocab <= 0 || !layers || !final_g || !w_lm || !x_emb || !k_cache || !v_cache ||
+      !kv_scales || !logits)
+    return LLAMA_ERR_INVALID_ARG;
+  if (t_cache < 0 || t_cache + 1 > cache_capacity || t_cache + 1 > kMaxPos) return LLAMA_ERR_INVALID_ARG;
+  for (int l = 0; l < n_layers; ++l)
+    if (!block_weights_ok(&layers[l])) return LLAMA_ERR_INVALID_ARG;
+  if (!decode_tc_path(d, LLAMA_BF16)) return LLAMA_ERR_UNSUPPORTED;
+  if (d->B == 0) return LLAMA_OK;
+  for (int l = 0; l < n_layers; ++l)
+    if (!block_weights_aligned(&layers[l])) return LLAMA_ERR_ALIGNMENT;
+  if (!aligned16(final_g) || !aligned16(w_lm) || !aligned16(x_emb) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      !aligned16(logits) || ((uintptr_t)kv_scales & 3))
+    return LLAMA_ERR_ALIGNMENT;
+  const size_t need = plan_decode_tc(d, nullptr, cache_capacity).bytes;
+  if (!ws || ws_bytes < need) return LLAMA_ERR_WORKSPACE;
+  if (!aligned16(ws)) return LLAMA_ERR_ALIGNMENT;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  set_pdl(true);
+  rc = decode_stack_tc(d, n_layers, layers, final_g, w_lm, vocab, x_emb, k_cache, v_cache, cache_capacity, t_cache,
+                       logits, plan_decode_tc(d, ws, cache_capacity), kv_scales, st);
+  set_pdl(false);
+  return rc;
+}
+
+int llama_gqa_attention_decode_kv8(const llama_dims* d, const void* q, const void* k, const void* v,
+                                   const float* k_scale, const float* v_scale, int64_t kv_capacity, int64_t pos0,
+                                   void* o, void* ws, size_t ws_bytes, void* stream) {
+  int rc;
+  if ((rc = check_dims(d, NEED_HEADS)) != LLAMA_OK) return rc;
+  if (d->S != 1 || pos0 < 0 || kv_capacity < 0 || pos0 + 1 > kv_capacity || pos0 + 1 > kMaxPos)
+    return LLAMA_ERR_INVALID_ARG;
+  if (d->B == 0) return LLAMA_OK;
+  if (!q || !k || !v || !o || !k_scale || !v_scale) return LLAMA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || ((uintptr_t)k_scale & 3) ||
+      ((uintptr_t)v_scale & 3))
+    return LLAMA_ERR_ALIGNMENT;
+  AttnDesc a = make_attn(d, LLAMA_BF16, q, k, v, o, kv_capacity, pos0);
+  a.k_scale = k_scale;
+  a.v_scale = v_scale;
+  if (!decode_attn8_supported(a)) return LLAMA_ERR_UNSUPPORTED;
+  if (!ws || ws_bytes < decode_attn_ws_bytes(a)) return LLAMA_ERR_WORKSPACE;
+  if (!aligned16(ws)) return LLAMA_ERR_ALIGNMENT;
+  a.ws = ws;
+  a.ws_bytes = ws_bytes;
+  return run_attention(a, static_cast<cudaStream_t>(stream));
+}
+
+int llama_kv_quantize(const void* x, int64_t n_tokens, int64_t n_kv, int64_t head_dim, const float* scale,
+                      void* codes, void* stream) {
+  if (n_tokens < 0 || n_kv < 1 || head_dim < 8 || head_dim % 8) return LLAMA_ERR_INVALID_ARG;
+  if (n_tokens == 0) return LLAMA_OK;
+  if (!x || !scale || !codes) return LLAMA_ERR_INVALID_ARG;
+  if (!aligned16(x) || ((uintptr_t)codes & 7) || ((uintptr_t)scale & 3)) return LLAMA_ERR_ALIGNMENT;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  prof::begin("kv_quantize", st);
+  const int rc = launch_kv_quantize(x, scale, codes, n_tokens * n_kv * head_dim, (int)n_kv, (int)head_dim, st);
+  prof::end(st);
+  return rc ? LLAMA_ERR_CUDA : launch_status();
 }
 
 }  // extern "C"

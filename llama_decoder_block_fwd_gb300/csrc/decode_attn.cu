@@ -484,12 +484,23 @@ int launch_decode_attn(const AttnDesc& a, void* ws, int num_sms, unsigned* statu
   p.status = status;
   const int grid = std::max(1, std::min(p.n_items, num_sms));
   if (launch_decode_kernel(p, grid, st) != 0) return -1;
-  const int warps = (int)(a.B * a.n_q);
-  if (launch_k(decode_combine_kernel, dim3((warps * 32 + 255) / 256), dim3(256), 0, st, (const float*)p.part_o,
-               (const float*)p.part_ml, static_cast<uint16_t*>(a.o), static_cast<uint16_t*>(a.o_lo), (int)a.B,
-               (int)a.n_q, d.n_chunks) != cudaSuccess)
-    return -1;
-  return 0;
+  return launch_decode_combine(p.part_o, p.part_ml, a.o, a.o_lo, a.B, a.n_q, d.n_chunks, st);
+}
+
+void decode_attn_plan(int64_t kv_len, int& kv_tiles, int& chunk_tiles, int& n_chunks) {
+  const DecodePlan d = plan(0, 0, kv_len);
+  kv_tiles = d.kv_tiles;
+  chunk_tiles = d.chunk_tiles;
+  n_chunks = d.n_chunks;
+}
+
+int launch_decode_combine(const float* part_o, const float* part_ml, void* o, void* o_lo, int64_t B, int64_t n_q,
+                          int n_chunks, cudaStream_t st) {
+  const int warps = (int)(B * n_q);
+  return launch_k(decode_combine_kernel, dim3((warps * 32 + 255) / 256), dim3(256), 0, st, part_o, part_ml,
+                  static_cast<uint16_t*>(o), static_cast<uint16_t*>(o_lo), (int)B, (int)n_q, n_chunks) == cudaSuccess
+             ? 0
+             : -1;
 }
 
 // ------------------------------------------------------------------------------------------

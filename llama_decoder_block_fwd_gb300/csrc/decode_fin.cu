@@ -5,7 +5,7 @@
 //   fin_norm   : x (+)= sum_s partial_s (O or down projection) in the fp32 residual stream, then
 //                RMSNorm in split form: rs = rsqrt(mean(x^2) + eps), a = x * g as hi + lo.
 //   fin_qkv    : (q, k, v) = rs * sum_s partial_s; RoPE on q and k at position t; q to its buffer,
-//                k and v into the caches at position t.
+//                k and v into the caches at position t (bf16, or E4M3 codes of x / scale).
 //   fin_swiglu : m = SiLU(rs * gate) * (rs * up) as hi + lo.
 // ("Llama Architecture ...", Mathematical Foundations 1-3; "LLaMA-3 8B ...", section 九.)
 #include "epilogue.cuh"
@@ -71,8 +71,10 @@ struct FinQkvParams {
   const float* part;     // [n_split, B, n_cols]
   const float* rs;       // [B]
   uint16_t* q;           // [B, nq_cols]
-  uint16_t* kc;          // layer cache [B, cap, nkv_cols]
-  uint16_t* vc;
+  void* kc;              // layer cache [B, cap, nkv_cols]: bf16, or E4M3 codes with k_scale set
+  void* vc;
+  const float* k_scale;  // [n_kv] or null
+  const float* v_scale;
   int n_split, B, nq_cols, nkv_cols, hd;
   int64_t cap, t;
   RopeFreq freq[kMaxRopePairs];
@@ -106,12 +108,21 @@ __global__ void fin_qkv_kernel(const __grid_constant__ FinQkvParams p) {
     v0 = x0 * cs - x1 * sn;
     v1 = x0 * sn + x1 * cs;
   }
-  const uint32_t packed = pack_bf2(v0, v1);
-  uint16_t* dst;
-  if (c < p.nq_cols) dst = p.q + (int64_t)r * p.nq_cols + c;
-  else if (c < p.nq_cols + p.nkv_cols) dst = p.kc + ((int64_t)r * p.cap + p.t) * p.nkv_cols + (c - p.nq_cols);
-  else dst = p.vc + ((int64_t)r * p.cap + p.t) * p.nkv_cols + (c - p.nq_cols - p.nkv_cols);
-  *reinterpret_cast<uint32_t*>(dst) = packed;
+  if (c < p.nq_cols) {
+    *reinterpret_cast<uint32_t*>(p.q + (int64_t)r * p.nq_cols + c) = pack_bf2(v0, v1);
+    return;
+  }
+  const bool is_k = c < p.nq_cols + p.nkv_cols;
+  const int cc = is_k ? c - p.nq_cols : c - p.nq_cols - p.nkv_cols;
+  const int64_t off = ((int64_t)r * p.cap + p.t) * p.nkv_cols + cc;
+  if (p.k_scale) {   // 8-bit cache: code = E4M3(fl32(x) / scale), rounded to nearest even, saturating
+    const float s = (is_k ? p.k_scale : p.v_scale)[cc / p.hd];
+    uint16_t code;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(code) : "f"(v1 / s), "f"(v0 / s));
+    *reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(is_k ? p.kc : p.vc) + off) = code;
+  } else {
+    *reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(is_k ? p.kc : p.vc) + off) = pack_bf2(v0, v1);
+  }
 }
 
 // One thread per (row, hidden unit): gate in columns [0, d_ff), up in [d_ff, 2 d_ff).
@@ -147,10 +158,12 @@ int launch_fin_norm(float* x, const void* init_bf16, const float* part, int n_sp
 }
 
 int launch_fin_qkv(const float* part, int n_split, const float* rs, void* q, void* kc, void* vc, int B, int nq_cols,
-                   int nkv_cols, int hd, int64_t cap, int64_t t, const RopeFreq* freq, cudaStream_t st) {
+                   int nkv_cols, int hd, int64_t cap, int64_t t, const RopeFreq* freq, const float* k_scale,
+                   const float* v_scale, cudaStream_t st) {
   FinQkvParams p;
   p.part = part; p.rs = rs;
-  p.q = static_cast<uint16_t*>(q); p.kc = static_cast<uint16_t*>(kc); p.vc = static_cast<uint16_t*>(vc);
+  p.q = static_cast<uint16_t*>(q); p.kc = kc; p.vc = vc;
+  p.k_scale = k_scale; p.v_scale = v_scale;
   p.n_split = n_split; p.B = B; p.nq_cols = nq_cols; p.nkv_cols = nkv_cols; p.hd = hd; p.cap = cap; p.t = t;
   for (int i = 0; i < hd / 2; ++i) p.freq[i] = freq[i];
   const int64_t n = (int64_t)B * (nq_cols + 2 * nkv_cols) / 2;

@@ -70,6 +70,8 @@ struct AttnDesc {
   float scale;          // 1/sqrt(hd)
   void* ws;             // scratch for the split-K decode kernel (may be null)
   size_t ws_bytes;
+  const float* k_scale; // 8-bit cache: k and v hold E4M3 codes, x = code * scale[kv head]
+  const float* v_scale;
 };
 
 // rows x d RMSNorm; x_f32/y_f32 give the element types of x and y, g has type `dtype`.
@@ -114,13 +116,22 @@ bool attn_tc_supported(const AttnDesc& a);
 bool decode_attn_supported(const AttnDesc& a);
 size_t decode_attn_ws_bytes(const AttnDesc& a);   // for kv_len = pos0 + 1
 int launch_decode_attn(const AttnDesc& a, void* ws, int num_sms, unsigned* status, cudaStream_t st);
+void decode_attn_plan(int64_t kv_len, int& kv_tiles, int& chunk_tiles, int& n_chunks);
+int launch_decode_combine(const float* part_o, const float* part_ml, void* o, void* o_lo, int64_t B, int64_t n_q,
+                          int n_chunks, cudaStream_t st);
+// decode_attn8.cu: the same over an 8-bit (E4M3) cache with per-head scales; same workspace size
+bool decode_attn8_supported(const AttnDesc& a);
+int launch_decode_attn8(const AttnDesc& a, void* ws, int num_sms, unsigned* status, cudaStream_t st);
+// codes[i] = E4M3(fl32(x[i]) / scale[head of i]) for n bf16 elements laid out [.., n_kv, hd]
+int launch_kv_quantize(const void* x, const float* scale, void* codes, int64_t n, int n_kv, int hd, cudaStream_t st);
 int launch_attn_tc(const AttnDesc& a, int num_sms, unsigned* status, cudaStream_t st);
 
 // Decode-step finishers (decode_fin.cu): split-K reductions fused with what follows each GEMM.
 int launch_fin_norm(float* x, const void* init_bf16, const float* part, int n_split, const void* g, void* a_hi,
                     void* a_lo, float* rs, int B, int d, float eps, cudaStream_t st);
 int launch_fin_qkv(const float* part, int n_split, const float* rs, void* q, void* kc, void* vc, int B, int nq_cols,
-                   int nkv_cols, int hd, int64_t cap, int64_t t, const RopeFreq* freq, cudaStream_t st);
+                   int nkv_cols, int hd, int64_t cap, int64_t t, const RopeFreq* freq, const float* k_scale,
+                   const float* v_scale, cudaStream_t st);
 int launch_fin_swiglu(const float* part, int n_split, const float* rs, void* m_hi, void* m_lo, int B, int dff,
                       cudaStream_t st);
 
@@ -160,6 +171,8 @@ int num_sms();
 // tensor-map encoding (driver entry point resolved through the runtime)
 bool encode_tmap_2d_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
                          uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer);
+bool encode_tmap_4d_u8(CUtensorMap* m, const void* base, const uint64_t* dims, const uint64_t* strides_bytes,
+                       const uint32_t* box);
 bool encode_tmap_4d_bf16(CUtensorMap* m, const void* base, const uint64_t* dims, const uint64_t* strides_bytes,
                          const uint32_t* box);
 bool encode_tmap_3d_bf16(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,

@@ -113,3 +113,27 @@ def test_sample_and_embed_reject_bad_arguments():
     assert lib.llama_embed(L.BF16, fake, 10, 0, fake, 4, fake, None) == 1
     assert lib.llama_embed(L.BF16, None, 10, 16, fake, 4, fake, None) == 1
     assert lib.llama_embed(L.BF16, None, 10, 16, None, 0, None, None) == 0
+
+
+def test_kv8_calls_reject_bad_arguments():
+    lib = L.lib()
+    fake = 0x10000
+    d1 = _dims(S=1, n_q=32, n_kv=8, head_dim=128, d_model=4096)
+    # llama_kv_quantize: head_dim not a multiple of 8, NULL scale, misaligned codes
+    assert lib.llama_kv_quantize(fake, 4, 8, 12, fake, fake, None) == 1
+    assert lib.llama_kv_quantize(fake, 4, 8, 128, None, fake, None) == 1
+    assert lib.llama_kv_quantize(fake, 4, 8, 128, fake, fake + 4, None) == 3
+    assert lib.llama_kv_quantize(None, 0, 8, 128, None, None, None) == 0
+    # attention over codes: S != 1, pos0 beyond capacity, NULL scales, missing workspace
+    d2 = _dims(S=2, n_q=32, n_kv=8, head_dim=128, d_model=4096)
+    assert lib.llama_gqa_attention_decode_kv8(ctypes.byref(d2), fake, fake, fake, fake, fake, 100, 10, fake, fake, 1 << 20, None) == 1
+    assert lib.llama_gqa_attention_decode_kv8(ctypes.byref(d1), fake, fake, fake, fake, fake, 100, 100, fake, fake, 1 << 20, None) == 1
+    assert lib.llama_gqa_attention_decode_kv8(ctypes.byref(d1), fake, fake, fake, None, fake, 100, 10, fake, fake, 1 << 20, None) == 1
+    # head_dim 64 is not supported on this path
+    d3 = _dims(S=1, n_q=8, n_kv=2, head_dim=64, d_model=512)
+    assert lib.llama_gqa_attention_decode_kv8(ctypes.byref(d3), fake, fake, fake, fake, fake, 100, 10, fake, fake, 1 << 20, None) == 2
+    # the stack call needs kv_scales
+    w = (L.BlockWeights * 1)(L.BlockWeights(*([fake] * 9)))
+    dd = _dims(B=4, S=1, n_q=32, n_kv=8, head_dim=128, d_model=4096, d_ff=14336)
+    assert lib.llama_stack_decode_step_kv8(ctypes.byref(dd), 1, w, fake, fake, 128, fake, fake, fake, None, 100, 10,
+                                           fake, fake, 1 << 30, None) == 1
