@@ -172,19 +172,19 @@ def prefill_flops(wl):
     }
 
 
-def decode_bytes(wl, cap_unused=None):
-    """Algorithmic HBM bytes of one decode step (bf16): every cached K/V read once, every weight
-    read once, the new K/V written, inputs read and logits written."""
+def decode_bytes(wl, kv_elem_bytes=2):
+    """Algorithmic HBM bytes of one decode step: every cached K/V read once (kv_elem_bytes per
+    element), every bf16 weight read once, the new K/V written, inputs read and logits written."""
     L, B, t = wl.n_layers, wl.B, wl.t_cache
     row = wl.n_kv * wl.head_dim
-    kv_read = L * B * (t + 1) * row * 2 * 2
+    kv_read = L * B * (t + 1) * row * 2 * kv_elem_bytes
     hq = wl.n_q * wl.head_dim
     layer_w = (wl.d_model * (hq + 2 * row) + hq * wl.d_model + 3 * wl.d_model * wl.d_ff + 2 * wl.d_model) * 2
     return {
         "kv_read": kv_read,
         "weights": L * layer_w,
         "lm_head": wl.vocab * wl.d_model * 2 + wl.d_model * 2,
-        "kv_append": L * B * row * 2 * 2,
+        "kv_append": L * B * row * 2 * kv_elem_bytes,
         "logits": B * wl.vocab * 4,
         "input": B * wl.d_model * 2,
     }
@@ -377,7 +377,11 @@ def bench_prefill(args, world, rank):
     return out
 
 
-def bench_decode(args, world, rank):
+def bench_decode(args, world, rank, kv8=False):
+    """One 32-layer decode step for 64 sequences holding 8192 cached positions.  kv8: the cache
+    holds E4M3 codes with per-head scales (made from the same synthetic values by
+    llama_kv_quantize) instead of bf16."""
+    import numpy as np
     import torch
 
     import llama_decoder_block_fwd_gb300 as L
@@ -395,7 +399,21 @@ def bench_decode(args, world, rank):
         t = W.device_layer(wl, l)
         tensors.append(t)
         layers.append(L.block_weights(t))
-    kc, vc = W.device_caches(wl, cap)
+    scales = None
+    if kv8:
+        scales = torch.full((wl.n_layers, 2, wl.n_kv), 0.03125, dtype=torch.float32, device="cuda")
+        kc = torch.empty((wl.n_layers, wl.B, cap, wl.n_kv, wl.head_dim), dtype=torch.uint8, device="cuda")
+        vc = torch.empty_like(kc)
+        for l in range(wl.n_layers):
+            for which, dst in (("k", kc), ("v", vc)):
+                x = W.device_tensor(wl.dtype, (wl.B, cap, wl.n_kv, wl.head_dim), wl.seed, W.cache_tid(which, l),
+                                    0.0, 1.0)
+                L.llama_kv_quantize(x, scales[l, 0 if which == "k" else 1], dst[l])
+                del x
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    else:
+        kc, vc = W.device_caches(wl, cap)
     final_g, w_lm = W.device_final(wl)
     x = W.device_x_emb(wl)
     logits = torch.empty((wl.B, wl.vocab), dtype=torch.float32, device="cuda")
@@ -403,8 +421,12 @@ def bench_decode(args, world, rank):
                      dtype=torch.uint8, device="cuda")
 
     def step(stream=None):
-        L.llama_stack_decode_step(wl.dims, wl.dtype, layers, final_g, w_lm, wl.vocab, x, kc, vc, cap, wl.t_cache,
-                                  logits, ws, stream)
+        if kv8:
+            L.llama_stack_decode_step_kv8(wl.dims, layers, final_g, w_lm, wl.vocab, x, kc, vc, scales, cap,
+                                          wl.t_cache, logits, ws, stream)
+        else:
+            L.llama_stack_decode_step(wl.dims, wl.dtype, layers, final_g, w_lm, wl.vocab, x, kc, vc, cap, wl.t_cache,
+                                      logits, ws, stream)
 
     # eager pass with per-launch events (per-kernel durations), then graph replay for the step time
     step()
@@ -438,20 +460,22 @@ def bench_decode(args, world, rank):
         raise RuntimeError("device status word set during decode")
     ms = max_over_ranks(world, e0.elapsed_time(e1)) / args.steps
     pk, pk_src = peaks()
-    nb = decode_bytes(wl)
+    nb = decode_bytes(wl, kv_elem_bytes=1 if kv8 else 2)
     step_bytes = sum(nb.values())
     kernels = {k: {"launches": n // nprof, "ms_per_step": t / nprof} for k, (n, t) in prof.items()}
     attn = [k for k in prof if k.startswith("attn")]
     dom = max(prof.items(), key=lambda kv: kv[1][1])[0]
     out = {
-        "workload": wl.name, "value": aggregate_rate(world, wl.B, ms), "unit": "tokens/s", "ms_per_step": ms,
-        "bytes_per_step": step_bytes,
+        "workload": wl.name + ("-kv8" if kv8 else ""), "value": aggregate_rate(world, wl.B, ms), "unit": "tokens/s",
+        "ms_per_step": ms, "bytes_per_step": step_bytes,
         "hbm_frac_step": step_bytes / (ms / 1e3) / 1e9 / pk["hbm_gbs"],
         "gpu_launches_per_step": sum(n for n, _ in prof.values()) // nprof,
         "kernels": kernels, "dominant_kernel": dom,
-        "graph": "CUDA graph replay of one llama_stack_decode_step",
-        "l2": "inputs larger than L2 (69 GB KV cache + 15 GB weights)",
+        "graph": "CUDA graph replay of one decode step",
+        "l2": f"inputs larger than L2 ({step_bytes / 1e9:.0f} GB per step)",
     }
+    if kv8:
+        out["kv_cache"] = "E4M3 codes, per-(layer, K/V, head) fp32 scale 2^-5"
     if attn:
         a = attn[0]
         n, t = prof[a]
@@ -460,7 +484,7 @@ def bench_decode(args, world, rank):
         out["roofline"] = {"bound": "hbm", "kernel": a, "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                            "frac": achieved / pk["hbm_gbs"], "traffic": kernel_traffic(a), "peak_source": f"{pk_src} hbm",
                            "algorithmic_bytes_per_launch": per_launch_bytes}
-    del tensors, layers, kc, vc, final_g, w_lm, x, logits, ws, g
+    del tensors, layers, kc, vc, final_g, w_lm, x, logits, ws, g, scales
     torch.cuda.empty_cache()
     return out
 
@@ -520,6 +544,7 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-mha", action="store_true", help="skip the LLaMA-7B MHA block prefill")
+    ap.add_argument("--no-kv8", action="store_true", help="skip the decode step over an 8-bit KV cache")
     ap.add_argument("--prefill-seq", type=int, default=8192, help="tokens of the prefill workload (default 8192)")
     ap.add_argument("--decode-layers", type=int, default=32, help="layers of the decode stack (default 32)")
     args = ap.parse_args()
@@ -535,6 +560,7 @@ def main():
     pre = bench_prefill(args, world, rank)
     mha = None if args.no_mha else bench_mha_prefill(args, world)
     dec = None if args.no_decode else bench_decode(args, world, rank)
+    dec8 = None if (args.no_decode or args.no_kv8) else bench_decode(args, world, rank, kv8=True)
     smp = None if args.no_decode else bench_sample(args, world)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -553,7 +579,7 @@ def main():
             "config": pre["config"], "roofline": pre["roofline"], "cpu_baseline": cpu, "e2e": pre["e2e"],
             "gpu_launches": pre["gpu_launches"], "clocks": pre["clocks"], "block_tc_frac": pre["block_tc_frac"],
             "block_tflops": pre["block_tflops"], "kernels": pre["kernels"], "decode": dec, "mha_prefill": mha,
-            "sample": smp,
+            "decode_kv8": dec8, "sample": smp,
         }
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -7,8 +7,10 @@
 // heads of the group padded to N = 16, and each item leaves an unnormalised partial (m, l, O) for
 // the combine pass.  What differs:
 //   * TMA brings 128 keys x 128 codes (16 KB) per K or V tile into a 4-stage ring;
-//   * two converter warps per operand expand the codes to f16 (exact: every E4M3 value is an
-//     f16 value) in the 128-byte-swizzled layout the MMA reads, one K and one V tile buffer;
+//   * the codes are expanded to f16 (exact: every E4M3 value is an f16 value): K by four warps,
+//     one key row per thread, straight into tensor memory, where S^T = K Q^T reads its A operand;
+//     V by two warps into the 128-byte-swizzled shared-memory layout the P V MMA reads.  Both
+//     are double-buffered, so the expansion of tile j + 1 overlaps the MMAs of tile j;
 //   * the MMAs run in f16 (kind::f16 with f16 A and B): q is converted from bf16 in place when
 //     it lands, P is written as f16;
 //   * the K scale multiplies the scores, the V scale the partial O.
@@ -23,11 +25,11 @@
 namespace llama {
 namespace {
 
-constexpr int D8_THREADS = 320;   // warp 0 TMA, 1 MMA, 2-5 softmax, 6-7 convert K (+ q), 8-9 convert V
+constexpr int D8_THREADS = 384;   // warp 0 TMA, 1 MMA, 2-5 softmax, 6-9 expand K, 10-11 expand V (+ q)
 constexpr int D8_STAGES = 4;
 constexpr int D8_HD = 128;
 constexpr int D8_NPAD = 16;
-constexpr uint32_t D8_TMEM_COLS = 64;
+constexpr uint32_t D8_TMEM_COLS = 256;   // S^T 2 x 16, O^T 16, K (f16, A operand) 2 x 64
 constexpr float kD8RescaleLog2 = 8.0f;
 
 struct __align__(64) DecodeAttn8Params {
@@ -50,9 +52,8 @@ struct D8Smem {
   static constexpr uint32_t PB = D8_NPAD * 128 * 2;        // 4 KB
   static constexpr uint32_t OFF_K8 = 0;
   static constexpr uint32_t OFF_V8 = OFF_K8 + D8_STAGES * F8;
-  static constexpr uint32_t OFF_K16 = OFF_V8 + D8_STAGES * F8;
-  static constexpr uint32_t OFF_V16 = OFF_K16 + H16;
-  static constexpr uint32_t OFF_Q = OFF_V16 + H16;          // 2 buffers
+  static constexpr uint32_t OFF_V16 = OFF_V8 + D8_STAGES * F8;    // 2 buffers
+  static constexpr uint32_t OFF_Q = OFF_V16 + 2 * H16;            // 2 buffers
   static constexpr uint32_t OFF_P = OFF_Q + 2 * QB;         // 2 buffers
   static constexpr uint32_t OFF_RED = OFF_P + 2 * PB;       // [3][4][16] floats
   static constexpr uint32_t OFF_BAR = OFF_RED + 3 * 4 * 16 * 4;
@@ -62,9 +63,9 @@ static_assert(D8Smem::TOTAL <= 232448, "shared memory");
 
 // barrier slots
 enum : int {
-  B_K8F = 0, B_V8F = 4, B_K8E = 8, B_V8E = 12, B_K16F = 16, B_K16E = 17, B_V16F = 18, B_V16E = 19,
-  B_QF = 20, B_QR = 22, B_QE = 24, B_SF = 26, B_SFREE = 28, B_PF = 30, B_OD = 32, B_OFREE = 34, B_DRAIN = 35,
-  B_COUNT = 36
+  B_K8F = 0, B_V8F = 4, B_K8E = 8, B_V8E = 12, B_K16F = 16, B_K16E = 18, B_V16F = 20, B_V16E = 22,
+  B_QF = 24, B_QR = 26, B_QE = 28, B_SF = 30, B_SFREE = 32, B_PF = 34, B_OD = 36, B_OFREE = 38, B_DRAIN = 39,
+  B_COUNT = 40
 };
 
 __device__ __forceinline__ void tma_load_4d_d8(uint32_t dst, const CUtensorMap* m, uint64_t* bar, int x, int y,
@@ -104,7 +105,7 @@ __device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32
 
 // Expand one 128 x 128 code tile (TMA 128-byte swizzle: the 16-byte chunk c of key row k sits at
 // chunk c ^ (k & 7)) into the f16 operand layout (two 64-column halves, same swizzle), with the
-// 64 threads of one converter pair.
+// 64 threads of the two V warps.
 __device__ __forceinline__ void expand_tile(const uint8_t* src, uint8_t* dst, int t64) {
 #pragma unroll 4
   for (int u = t64; u < 1024; u += 64) {
@@ -147,8 +148,11 @@ __global__ void __launch_bounds__(D8_THREADS, 1) decode_attn8_kernel(const __gri
   if (threadIdx.x == 0) {
     for (int i = 0; i < B_COUNT; ++i) {
       int cnt = 1;
-      if ((i >= B_K8E && i < B_K8E + 8) || i == B_K16F || i == B_V16F || i == B_QR || i == B_QR + 1) cnt = 64;
-      if (i == B_SFREE || i == B_SFREE + 1 || i == B_PF || i == B_PF + 1 || i == B_OFREE) cnt = 128;
+      if ((i >= B_V8E && i < B_V8E + D8_STAGES) || i == B_V16F || i == B_V16F + 1 || i == B_QR || i == B_QR + 1)
+        cnt = 64;
+      if ((i >= B_K8E && i < B_K8E + D8_STAGES) || i == B_K16F || i == B_K16F + 1 || i == B_SFREE ||
+          i == B_SFREE + 1 || i == B_PF || i == B_PF + 1 || i == B_OFREE)
+        cnt = 128;
       mbar_init(&bars[i], cnt);
     }
     *abort_flag = 0;
@@ -168,6 +172,7 @@ __global__ void __launch_bounds__(D8_THREADS, 1) decode_attn8_kernel(const __gri
   const uint32_t tmem = *tmem_slot;
   const uint32_t tS = tmem;          // S^T buffers: columns 0..15 and 16..31
   const uint32_t tO = tmem + 32;     // O^T: columns 32..47
+  const uint32_t tK = tmem + 64;     // K tiles (f16 pairs): columns 64..127 and 128..191
   const uint32_t sbase = smem_u32(smem);
 
   pdl_wait();
@@ -199,7 +204,7 @@ __global__ void __launch_bounds__(D8_THREADS, 1) decode_attn8_kernel(const __gri
     if (lane == 0) {  // ---------------------------------------------------- MMA issuer
       const uint32_t idesc_s = idesc_f16(128, D8_NPAD);
       const uint32_t idesc_o = idesc_f16(128, D8_NPAD, /*b_mn_major=*/false, /*a_mn_major=*/true);
-      const uint32_t ka = sbase + L::OFF_K16, va = sbase + L::OFF_V16;
+      const uint32_t va0 = sbase + L::OFF_V16;
       int tile = 0, it = 0;
       bool ok = true;
       for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x, ++it) {
@@ -213,24 +218,24 @@ __global__ void __launch_bounds__(D8_THREADS, 1) decode_attn8_kernel(const __gri
         auto issue_s = [&](int j) -> bool {
           const int gt = tile + j;
           const int sb = gt & 1;
-          if (!mbar_wait(&bars[B_K16F], gt & 1, abort_flag, p.status)) return false;
+          if (!mbar_wait(&bars[B_K16F + sb], (gt >> 1) & 1, abort_flag, p.status)) return false;
           if (!mbar_wait(&bars[B_SFREE + sb], ((gt >> 1) & 1) ^ 1, abort_flag, p.status)) return false;
           tc_fence_after();
 #pragma unroll
-          for (int k = 0; k < D8_HD / 16; ++k) {
-            const uint64_t ad = sdesc_sw128(ka + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
+          for (int k = 0; k < D8_HD / 16; ++k) {   // A = K from tensor memory, 16 hd per step
             const uint64_t bd = sdesc_sw128(qa + (k >> 2) * (L::QB / 2) + (k & 3) * 32, 16, 1024);
-            tc_mma(tS + sb * 16, ad, bd, idesc_s, k > 0 ? 1u : 0u);
+            tc_mma_ts(tS + sb * 16, tK + sb * 64 + k * 8, bd, idesc_s, k > 0 ? 1u : 0u);
           }
           tc_commit(&bars[B_SF + sb]);
-          tc_commit(&bars[B_K16E]);
+          tc_commit(&bars[B_K16E + sb]);
           return true;
         };
         auto issue_pv = [&](int j) -> bool {
           const int gt = tile + j;
           const int pb = gt & 1;
           if (!mbar_wait(&bars[B_PF + pb], (gt >> 1) & 1, abort_flag, p.status)) return false;
-          if (!mbar_wait(&bars[B_V16F], gt & 1, abort_flag, p.status)) return false;
+          if (!mbar_wait(&bars[B_V16F + pb], (gt >> 1) & 1, abort_flag, p.status)) return false;
+          const uint32_t va = va0 + pb * L::H16;
           if (j == 0 && !mbar_wait(&bars[B_OFREE], (it & 1) ^ 1, abort_flag, p.status)) return false;
           tc_fence_after();
           const uint32_t pa = sbase + L::OFF_P + pb * L::PB;
@@ -241,7 +246,7 @@ __global__ void __launch_bounds__(D8_THREADS, 1) decode_attn8_kernel(const __gri
             tc_mma(tO, ad, bd, idesc_o, (j > 0 || k > 0) ? 1u : 0u);
           }
           tc_commit(&bars[B_OD + pb]);
-          tc_commit(&bars[B_V16E]);
+          tc_commit(&bars[B_V16E + pb]);
           return true;
         };
         for (int j = 0; j < n; ++j) {
@@ -257,15 +262,50 @@ __global__ void __launch_bounds__(D8_THREADS, 1) decode_attn8_kernel(const __gri
       tc_commit(&bars[B_DRAIN]);
       mbar_wait(&bars[B_DRAIN], 0, &no_abort, p.status);
     }
-  } else if (warp >= 6) {  // ------------------------------------------------ converters
-    const bool conv_k = warp < 8;
+  } else if (warp >= 6 && warp < 10) {  // -------------------------------- K codes -> f16 in TMEM
+    const int key = (warp & 3) * 32 + lane;          // this thread's TMEM lane = key row of the tile
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    int tile = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
+      int b, g, t0, t1, chunk;
+      item_coords8(p, item, b, g, t0, t1, chunk);
+      for (int tt = t0; tt < t1; ++tt, ++tile) {
+        const int st = tile % D8_STAGES;
+        const int hb = tile & 1;
+        if (!mbar_wait(&bars[B_K8F + st], (tile / D8_STAGES) & 1, abort_flag, p.status)) { ok = false; break; }
+        if (!mbar_wait(&bars[B_K16E + hb], ((tile >> 1) & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
+        tc_fence_after();
+        const uint8_t* row = smem + L::OFF_K8 + st * L::F8 + key * 128;
+        const int sw = key & 7;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t w[32];
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            const int c = half * 4 + cc;
+            const uint4 v = *reinterpret_cast<const uint4*>(row + ((c ^ sw) << 4));
+            e4m3x4_to_f16x4(v.x, w[cc * 8 + 0], w[cc * 8 + 1]);
+            e4m3x4_to_f16x4(v.y, w[cc * 8 + 2], w[cc * 8 + 3]);
+            e4m3x4_to_f16x4(v.z, w[cc * 8 + 4], w[cc * 8 + 5]);
+            e4m3x4_to_f16x4(v.w, w[cc * 8 + 6], w[cc * 8 + 7]);
+          }
+          tmem_st32(tK + hb * 64 + half * 32 + lane_off, w);
+        }
+        tc_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bars[B_K16F + hb]);
+        mbar_arrive(&bars[B_K8E + st]);
+      }
+    }
+  } else if (warp >= 10) {  // ------------------------------------ V codes -> f16 in shared memory; q
     const int t64 = (warp & 1) * 32 + lane;
     int tile = 0, it = 0;
     bool ok = true;
     for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x, ++it) {
       int b, g, t0, t1, chunk;
       item_coords8(p, item, b, g, t0, t1, chunk);
-      if (conv_k) {   // q: bf16 -> f16 in place (same 2-byte layout)
+      {   // q: bf16 -> f16 in place (same 2-byte layout)
         const int qb = it & 1;
         if (!mbar_wait(&bars[B_QF + qb], (it >> 1) & 1, abort_flag, p.status)) break;
         uint4* q = reinterpret_cast<uint4*>(smem + L::OFF_Q + qb * L::QB);
@@ -285,16 +325,13 @@ __global__ void __launch_bounds__(D8_THREADS, 1) decode_attn8_kernel(const __gri
       }
       for (int tt = t0; tt < t1; ++tt, ++tile) {
         const int st = tile % D8_STAGES;
-        const uint32_t ph = (tile / D8_STAGES) & 1;
-        const int full = conv_k ? B_K8F : B_V8F, empty = conv_k ? B_K8E : B_V8E;
-        const int hfull = conv_k ? B_K16F : B_V16F, hempty = conv_k ? B_K16E : B_V16E;
-        if (!mbar_wait(&bars[full + st], ph, abort_flag, p.status)) { ok = false; break; }
-        if (!mbar_wait(&bars[hempty], (tile & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
-        expand_tile(smem + (conv_k ? L::OFF_K8 : L::OFF_V8) + st * L::F8, smem + (conv_k ? L::OFF_K16 : L::OFF_V16),
-                    t64);
+        const int hb = tile & 1;
+        if (!mbar_wait(&bars[B_V8F + st], (tile / D8_STAGES) & 1, abort_flag, p.status)) { ok = false; break; }
+        if (!mbar_wait(&bars[B_V16E + hb], ((tile >> 1) & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
+        expand_tile(smem + L::OFF_V8 + st * L::F8, smem + L::OFF_V16 + hb * L::H16, t64);
         fence_proxy_async_smem();
-        mbar_arrive(&bars[hfull]);
-        mbar_arrive(&bars[empty + st]);
+        mbar_arrive(&bars[B_V16F + hb]);
+        mbar_arrive(&bars[B_V8E + st]);
       }
     }
   } else {  // ------------------------------------------------------------ softmax warps 2..5

@@ -6,9 +6,12 @@
 // so N = 2 Mp), so one MMA per k-step yields W X_hi^T and W X_lo^T side by side in TMEM and the
 // epilogue adds column c and column Mp + c.  Per stage the shared memory holds 16 KB of weights
 // and 16 KB (Mp = 64) of activations; six stages keep ~96 KB of weights in flight per SM.
-// Work units are (128 weight rows, K range); split-K partials are written as fp32
-// out[split * M + c, n] or added into out[c, n] (the residual stream); with one split and a row
-// scale the result is stored scaled (the LM head after the final RMSNorm).
+// Work units are (128 weight rows, K range).  Split-K partials are either written as fp32
+// out[split * M + c, n] (fixed splits, units dealt round robin), or added atomically into
+// out[c, n] -- the residual stream, or a zeroed buffer the next kernel reads -- in which case the
+// (weight tile, k-block) items are cut into equal contiguous ranges, one per CTA, so every SM
+// streams the same number of weight bytes.  With one split and a row scale the result is stored
+// scaled (the LM head after the final RMSNorm).
 #include <algorithm>
 #include <cstring>
 
@@ -29,6 +32,8 @@ struct __align__(64) SkParams {
   int nseg;
   int n_tiles, k_splits, kb_per_split, num_units, stages;
   int mode;             // 0: partials [split*M + c, n]; 1: atomic add into out[c, n]; 2: store (x row scale)
+  int streamk;          // mode 1: equal item ranges per CTA instead of fixed units
+  int64_t total_items;  // n_tiles * k-blocks
   float* out;
   int64_t ldo;
   const float* row_scale;
@@ -47,6 +52,35 @@ __device__ __forceinline__ void sk_seg(const SkParams& p, int nt, int& seg, int&
   int start = 0;
   while (seg < p.nseg - 1 && nt >= p.seg_tile_end[seg]) { start = p.seg_tile_end[seg]; ++seg; }
   row = (nt - start) * 128;
+}
+
+// The units of this CTA, in order.
+struct UnitIter {
+  int64_t pos, end;   // stream-K: the CTA's range of (tile, k-block) items, tile-major
+  int u;              // fixed units: the next unit index
+};
+__device__ __forceinline__ UnitIter unit_begin(const SkParams& p) {
+  UnitIter it;
+  it.pos = (int64_t)blockIdx.x * p.total_items / gridDim.x;
+  it.end = (int64_t)(blockIdx.x + 1) * p.total_items / gridDim.x;
+  it.u = blockIdx.x;
+  return it;
+}
+__device__ __forceinline__ bool unit_next(const SkParams& p, UnitIter& it, int nkb, int& nt, int& split, int& kb0,
+                                          int& kb1) {
+  if (p.streamk) {
+    if (it.pos >= it.end) return false;
+    nt = (int)(it.pos / nkb);
+    kb0 = (int)(it.pos - (int64_t)nt * nkb);
+    kb1 = (int)min((int64_t)nkb, (int64_t)kb0 + (it.end - it.pos));
+    split = 0;
+    it.pos += kb1 - kb0;
+    return true;
+  }
+  if (it.u >= p.num_units) return false;
+  sk_unit(p, it.u, nkb, nt, split, kb0, kb1);
+  it.u += gridDim.x;
+  return true;
 }
 
 __global__ void __launch_bounds__(SK_THREADS, 1) gemm_skinny_kernel(const __grid_constant__ SkParams p) {
@@ -87,9 +121,9 @@ __global__ void __launch_bounds__(SK_THREADS, 1) gemm_skinny_kernel(const __grid
       // The weights are never written by an earlier kernel: the first unit's first stages are
       // loaded before waiting for the kernel that produced the activations.
       int pre = 0;
-      if ((int)blockIdx.x < p.num_units) {
-        int nt, split, kb0, kb1, seg, row;
-        sk_unit(p, blockIdx.x, nkb, nt, split, kb0, kb1);
+      UnitIter first = unit_begin(p);
+      int nt, split, kb0, kb1, seg, row;
+      if (unit_next(p, first, nkb, nt, split, kb0, kb1)) {
         sk_seg(p, nt, seg, row);
         pre = min(p.stages, kb1 - kb0);
         for (int i = 0; i < pre; ++i) {
@@ -101,9 +135,8 @@ __global__ void __launch_bounds__(SK_THREADS, 1) gemm_skinny_kernel(const __grid
       int stage = 0;
       uint32_t phase = 0;
       bool first_unit = true;
-      for (int u = blockIdx.x; u < p.num_units; u += gridDim.x) {
-        int nt, split, kb0, kb1, seg, row;
-        sk_unit(p, u, nkb, nt, split, kb0, kb1);
+      UnitIter ui = unit_begin(p);
+      while (unit_next(p, ui, nkb, nt, split, kb0, kb1)) {
         sk_seg(p, nt, seg, row);
         bool ok = true;
         for (int kb = kb0; kb < kb1; ++kb) {
@@ -128,9 +161,9 @@ __global__ void __launch_bounds__(SK_THREADS, 1) gemm_skinny_kernel(const __grid
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
-      for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++it) {
-        int nt, split, kb0, kb1;
-        sk_unit(p, u, nkb, nt, split, kb0, kb1);
+      int nt, split, kb0, kb1;
+      UnitIter ui = unit_begin(p);
+      for (; unit_next(p, ui, nkb, nt, split, kb0, kb1); ++it) {
         const int buf = it & 1;
         if (!mbar_wait(&acc_empty[buf], ((it >> 1) & 1) ^ 1, abort_flag, p.status)) break;
         tc_fence_after();
@@ -160,9 +193,9 @@ __global__ void __launch_bounds__(SK_THREADS, 1) gemm_skinny_kernel(const __grid
     const int q = warp & 3;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     int it = 0;
-    for (int u = blockIdx.x; u < p.num_units; u += gridDim.x, ++it) {
-      int nt, split, kb0, kb1;
-      sk_unit(p, u, nkb, nt, split, kb0, kb1);
+    int nt, split, kb0, kb1;
+    UnitIter ui = unit_begin(p);
+    for (; unit_next(p, ui, nkb, nt, split, kb0, kb1); ++it) {
       const int buf = it & 1;
       if (!mbar_wait(&acc_full[buf], (it >> 1) & 1, abort_flag, p.status)) break;
       tc_fence_after();
@@ -241,6 +274,8 @@ int launch_gemm_skinny(const SkinnyDesc& g, int num_sms, unsigned* status, cudaS
   p.k_splits = (nkb + p.kb_per_split - 1) / p.kb_per_split;
   p.num_units = p.n_tiles * p.k_splits;
   p.mode = g.mode;
+  p.streamk = g.mode == 1;
+  p.total_items = (int64_t)p.n_tiles * nkb;
   p.out = g.out;
   p.ldo = g.ldo;
   p.row_scale = g.row_scale;
@@ -259,7 +294,8 @@ int launch_gemm_skinny(const SkinnyDesc& g, int num_sms, unsigned* status, cudaS
       return -1;
     attr_set[dev] = true;
   }
-  const int grid = std::max(1, std::min(p.num_units, num_sms));
+  const int grid = p.streamk ? (int)std::max<int64_t>(1, std::min<int64_t>(p.total_items, num_sms))
+                             : std::max(1, std::min(p.num_units, num_sms));
   return launch_k(gemm_skinny_kernel, dim3(grid), dim3(SK_THREADS), smem, st, p) == cudaSuccess ? 0 : -1;
 }
 
