@@ -212,6 +212,39 @@ int llama_stack_decode_step_kv8(const llama_dims* dims, int n_layers,
                                 int64_t cache_capacity, int64_t t_cache, float* logits, void* ws,
                                 size_t ws_bytes, void* stream);
 
+/* Paged KV cache with per-sequence lengths (long contexts: the pages size the 8B cache at 4 GB for
+ * 32K positions and 15.6 GB for 128K, "LLaMA-3 8B ...", section 七; "Llama Architecture ...",
+ * Mathematical Foundations 4).  K and V of layer l live in a pool of 128-position pages,
+ * [n_layers, n_pages, 128, n_kv, head_dim] bf16; sequence b's positions 128j .. 128j+127 are in
+ * page block_table[b * max_pages + j].  seq_pos[b] is the position of b's new token, i.e. the
+ * number of positions already cached (b attends to positions 0 .. seq_pos[b]); max_pos is an
+ * upper bound of seq_pos over the batch (host value: it sizes the work split and the workspace,
+ * llama_workspace_bytes(..., kv_capacity = max_pos + 1)).  block_table and seq_pos are int32
+ * device arrays; every page that a sequence uses up to its new position must be listed.  Rows of
+ * a sequence's last page past its new position are never used (their contents do not matter).  */
+
+/* llama_stack_decode_step over a paged cache: writes each sequence's new K/V into its page at
+ * seq_pos[b] and runs RoPE at that position.  Same shapes as the tensor-core dense call (else
+ * LLAMA_ERR_UNSUPPORTED).  LLAMA_ERR_INVALID_ARG for n_pages or max_pages < 1, max_pos < 0 or
+ * max_pos + 1 > 128 * max_pages, or NULL pointers.                                              */
+int llama_stack_decode_step_paged(const llama_dims* dims, int n_layers,
+                                  const llama_block_weights* layers, const void* final_g,
+                                  const void* w_lm, int64_t vocab, const void* x_emb,
+                                  void* k_pool, void* v_pool, int64_t n_pages,
+                                  const int32_t* block_table, int64_t max_pages,
+                                  const int32_t* seq_pos, int64_t max_pos, float* logits, void* ws,
+                                  size_t ws_bytes, void* stream);
+
+/* One-token attention over a paged cache (S = 1, head_dim 128, n_q / n_kv in {1, 2, 4, 8, 16}):
+ * q and o bf16 [B, n_q, head_dim]; k_pool / v_pool one layer's pools [n_pages, 128, n_kv,
+ * head_dim] holding every sequence's positions 0 .. seq_pos[b].  Workspace:
+ * llama_workspace_bytes(LLAMA_OP_GQA_ATTENTION, dims with S = 1, ..., kv_capacity = max_pos + 1). */
+int llama_gqa_attention_decode_paged(const llama_dims* dims, const void* q, const void* k_pool,
+                                     const void* v_pool, int64_t n_pages,
+                                     const int32_t* block_table, int64_t max_pages,
+                                     const int32_t* seq_pos, int64_t max_pos, void* o, void* ws,
+                                     size_t ws_bytes, void* stream);
+
 /* Next-token choice from the LM head's logits ("LLaMA-3 8B 现代 LLM 架构、计算规模与能耗", section 十:
  * softmax over the vocabulary, then argmax, or a draw shaped by temperature, top-k and top-p).
  *   logits  [B, ld] fp32 (device), row b's first `vocab` entries used; finite values or -inf,

@@ -17,7 +17,7 @@ __all__ = [
     "llama_rmsnorm", "llama_rope", "llama_gqa_attention", "llama_gqa_attention_decode_noalloc", "llama_swiglu_ffn",
     "llama_block_forward", "llama_stack_decode_step", "llama_workspace_bytes",
     "llama_sample", "llama_embed", "llama_kv_quantize", "llama_gqa_attention_decode_kv8",
-    "llama_stack_decode_step_kv8",
+    "llama_stack_decode_step_kv8", "llama_stack_decode_step_paged", "llama_gqa_attention_decode_paged",
     "llama_get_device_status", "llama_status_string", "llama_profile_enable", "llama_profile_read",
     "OP_RMSNORM", "OP_ROPE", "OP_GQA_ATTENTION", "OP_SWIGLU_FFN", "OP_BLOCK_FORWARD",
     "OP_STACK_DECODE_STEP",
@@ -84,6 +84,9 @@ def lib() -> ctypes.CDLL:
                 "llama_gqa_attention_decode_kv8": [pd, vp, vp, vp, vp, vp, i64, i64, vp, vp, sz, vp],
                 "llama_stack_decode_step_kv8": [pd, i32, ctypes.POINTER(BlockWeights), vp, vp, i64, vp, vp, vp, vp,
                                                 i64, i64, vp, vp, sz, vp],
+                "llama_stack_decode_step_paged": [pd, i32, ctypes.POINTER(BlockWeights), vp, vp, i64, vp, vp, vp,
+                                                  i64, vp, i64, vp, i64, vp, vp, sz, vp],
+                "llama_gqa_attention_decode_paged": [pd, vp, vp, vp, i64, vp, i64, vp, i64, vp, vp, sz, vp],
             }
             for name, args in sig.items():
                 fn = getattr(L, name)
@@ -226,6 +229,26 @@ def llama_stack_decode_step_kv8(dims, layers, final_g, w_lm, vocab, x_emb, k_cac
                                              _p(x_emb), _p(k_cache), _p(v_cache), _p(kv_scales), int(cache_capacity),
                                              int(t_cache), _p(logits), _p(ws), _nbytes(ws), _s(stream)),
            "llama_stack_decode_step_kv8")
+
+
+def llama_stack_decode_step_paged(dims, layers, final_g, w_lm, vocab, x_emb, k_pool, v_pool, block_table, seq_pos,
+                                  max_pos, logits, ws, stream=None):
+    """k_pool / v_pool [n_layers, n_pages, 128, n_kv, hd] bf16; block_table int32 [B, max_pages]."""
+    n = len(layers)
+    arr = (BlockWeights * n)(*[lw if isinstance(lw, BlockWeights) else block_weights(lw) for lw in layers])
+    _check(lib().llama_stack_decode_step_paged(ctypes.byref(_d(dims)), n, arr, _p(final_g), _p(w_lm), int(vocab),
+                                               _p(x_emb), _p(k_pool), _p(v_pool), int(k_pool.shape[1]),
+                                               _p(block_table), int(block_table.shape[1]), _p(seq_pos), int(max_pos),
+                                               _p(logits), _p(ws), _nbytes(ws), _s(stream)),
+           "llama_stack_decode_step_paged")
+
+
+def llama_gqa_attention_decode_paged(dims, q, k_pool, v_pool, block_table, seq_pos, max_pos, o, ws, stream=None):
+    """k_pool / v_pool [n_pages, 128, n_kv, hd] bf16 (one layer); block_table int32 [B, max_pages]."""
+    _check(lib().llama_gqa_attention_decode_paged(ctypes.byref(_d(dims)), _p(q), _p(k_pool), _p(v_pool),
+                                                  int(k_pool.shape[0]), _p(block_table), int(block_table.shape[1]),
+                                                  _p(seq_pos), int(max_pos), _p(o), _p(ws), _nbytes(ws), _s(stream)),
+           "llama_gqa_attention_decode_paged")
 
 
 def llama_workspace_bytes(op, dims, dtype, n_layers=0, vocab=0, kv_capacity=0) -> int:

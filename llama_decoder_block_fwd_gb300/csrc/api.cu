@@ -230,6 +230,8 @@ int run_attention(const AttnDesc& a, cudaStream_t st) {
     prof::end(st);
     return launch_status();
   }
+  if (a.block_table && !(decode_attn_supported(a) && a.ws && a.ws_bytes >= decode_attn_ws_bytes(a)))
+    return LLAMA_ERR_UNSUPPORTED;   // a paged cache is read by the split-K decode kernel only
   if (decode_attn_supported(a) && a.ws && a.ws_bytes >= decode_attn_ws_bytes(a)) {
     unsigned* status = status_ptr();
     if (!status) return LLAMA_ERR_CUDA;
@@ -562,13 +564,24 @@ int run_fin(const char* role, int launch_rc, cudaStream_t st) {
 }
 
 // kv_scales: null for a bf16 cache; for an 8-bit cache, [n_layers][2 (K, V)][n_kv] fp32 scales.
+// Where the decode step's K/V live: a dense cache [L, B, cap, n_kv, hd] with every sequence at
+// position t, or (block_table set) a paged pool [L, n_pages, 128, n_kv, hd] with per-sequence
+// positions seq_pos (t is then their upper bound).
+struct PagedCache {
+  const int* block_table = nullptr;
+  const int* seq_pos = nullptr;
+  int64_t max_pages = 0, n_pages = 0;
+};
+
 int decode_stack_tc(const llama_dims* d, int n_layers, const llama_block_weights* layers, const void* final_g,
                     const void* w_lm, int64_t vocab, const void* x_emb, void* k_cache, void* v_cache, int64_t cap,
-                    int64_t t_cache, float* logits, const DecodeTcWs& w, const float* kv_scales, cudaStream_t st) {
+                    int64_t t_cache, float* logits, const DecodeTcWs& w, const float* kv_scales, cudaStream_t st,
+                    const PagedCache& pc = PagedCache()) {
   const int B = (int)d->B, D = (int)d->d_model;
   const int64_t hq = d->n_q * d->head_dim, hkv = d->n_kv * d->head_dim;
   const float eps = (float)d->eps;
-  const size_t layer_cache = (size_t)(d->B * cap * hkv) * (kv_scales ? 1 : 2);
+  const bool paged = pc.block_table != nullptr;
+  const size_t layer_cache = (size_t)((paged ? pc.n_pages * 128 : d->B * cap) * hkv) * (kv_scales ? 1 : 2);
   RopeFreq freq[kMaxRopePairs];
   rope_freqs(d, freq);
   int rc;
@@ -592,7 +605,7 @@ int decode_stack_tc(const llama_dims* d, int n_layers, const llama_block_weights
       return rc;
     prof::begin("fin_qkv", st);
     rc = launch_fin_qkv(w.part, w.s_qkv, w.rs1, w.q, kc, vc, B, (int)hq, (int)hkv, (int)d->head_dim, cap, t_cache, freq,
-                        ks, vs, st);
+                        ks, vs, pc.block_table, (int)pc.max_pages, pc.seq_pos, st);
     prof::end(st);
     if ((rc = run_fin("fin_qkv", rc, st)) != LLAMA_OK) return rc;
     // attention over t_cache + 1 keys; o as hi + lo into the activation buffers
@@ -602,6 +615,10 @@ int decode_stack_tc(const llama_dims* d, int n_layers, const llama_block_weights
     a.ws_bytes = w.attn_bytes;
     a.k_scale = ks;
     a.v_scale = vs;
+    a.block_table = pc.block_table;
+    a.seq_pos = pc.seq_pos;
+    a.max_pages = pc.max_pages;
+    a.n_pages = pc.n_pages;
     if ((rc = run_attention(a, st)) != LLAMA_OK) return rc;
     // h = x + o W_O^T: the split-K partials are added straight into the fp32 residual stream
     const void* wo[1] = {lw.wo};
@@ -941,6 +958,71 @@ int llama_stack_decode_step_kv8(const llama_dims* d, int n_layers, const llama_b
                        logits, plan_decode_tc(d, ws, cache_capacity), kv_scales, st);
   set_pdl(false);
   return rc;
+}
+
+int llama_stack_decode_step_paged(const llama_dims* d, int n_layers, const llama_block_weights* layers,
+                                  const void* final_g, const void* w_lm, int64_t vocab, const void* x_emb,
+                                  void* k_pool, void* v_pool, int64_t n_pages, const int32_t* block_table,
+                                  int64_t max_pages, const int32_t* seq_pos, int64_t max_pos, float* logits, void* ws,
+                                  size_t ws_bytes, void* stream) {
+  int rc;
+  if ((rc = check_dims(d, NEED_D | NEED_HEADS | NEED_FF)) != LLAMA_OK) return rc;
+  if (d->S != 1 || n_layers <= 0 || vocab <= 0 || !layers || !final_g || !w_lm || !x_emb || !k_pool || !v_pool ||
+      !block_table || !seq_pos || !logits)
+    return LLAMA_ERR_INVALID_ARG;
+  if (n_pages < 1 || max_pages < 1 || max_pos < 0 || max_pos + 1 > max_pages * 128 || max_pos + 1 > kMaxPos ||
+      n_pages > INT32_MAX || max_pages > INT32_MAX)
+    return LLAMA_ERR_INVALID_ARG;
+  for (int l = 0; l < n_layers; ++l)
+    if (!block_weights_ok(&layers[l])) return LLAMA_ERR_INVALID_ARG;
+  if (!decode_tc_path(d, LLAMA_BF16)) return LLAMA_ERR_UNSUPPORTED;
+  if (d->B == 0) return LLAMA_OK;
+  for (int l = 0; l < n_layers; ++l)
+    if (!block_weights_aligned(&layers[l])) return LLAMA_ERR_ALIGNMENT;
+  if (!aligned16(final_g) || !aligned16(w_lm) || !aligned16(x_emb) || !aligned16(k_pool) || !aligned16(v_pool) ||
+      !aligned16(logits) || ((uintptr_t)block_table & 3) || ((uintptr_t)seq_pos & 3))
+    return LLAMA_ERR_ALIGNMENT;
+  const size_t need = plan_decode_tc(d, nullptr, max_pos + 1).bytes;
+  if (!ws || ws_bytes < need) return LLAMA_ERR_WORKSPACE;
+  if (!aligned16(ws)) return LLAMA_ERR_ALIGNMENT;
+  PagedCache pc;
+  pc.block_table = block_table;
+  pc.seq_pos = seq_pos;
+  pc.max_pages = max_pages;
+  pc.n_pages = n_pages;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  set_pdl(true);
+  rc = decode_stack_tc(d, n_layers, layers, final_g, w_lm, vocab, x_emb, k_pool, v_pool, max_pos + 1, max_pos, logits,
+                       plan_decode_tc(d, ws, max_pos + 1), nullptr, st, pc);
+  set_pdl(false);
+  return rc;
+}
+
+int llama_gqa_attention_decode_paged(const llama_dims* d, const void* q, const void* k_pool, const void* v_pool,
+                                     int64_t n_pages, const int32_t* block_table, int64_t max_pages,
+                                     const int32_t* seq_pos, int64_t max_pos, void* o, void* ws, size_t ws_bytes,
+                                     void* stream) {
+  int rc;
+  if ((rc = check_dims(d, NEED_HEADS)) != LLAMA_OK) return rc;
+  if (d->S != 1 || n_pages < 1 || max_pages < 1 || max_pos < 0 || max_pos + 1 > max_pages * 128 ||
+      max_pos + 1 > kMaxPos || n_pages > INT32_MAX || max_pages > INT32_MAX)
+    return LLAMA_ERR_INVALID_ARG;
+  if (d->B == 0) return LLAMA_OK;
+  if (!q || !k_pool || !v_pool || !block_table || !seq_pos || !o) return LLAMA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(o) || ((uintptr_t)block_table & 3) ||
+      ((uintptr_t)seq_pos & 3))
+    return LLAMA_ERR_ALIGNMENT;
+  AttnDesc a = make_attn(d, LLAMA_BF16, q, k_pool, v_pool, o, max_pos + 1, max_pos);
+  a.block_table = block_table;
+  a.seq_pos = seq_pos;
+  a.max_pages = max_pages;
+  a.n_pages = n_pages;
+  if (!decode_attn_supported(a)) return LLAMA_ERR_UNSUPPORTED;
+  if (!ws || ws_bytes < decode_attn_ws_bytes(a)) return LLAMA_ERR_WORKSPACE;
+  if (!aligned16(ws)) return LLAMA_ERR_ALIGNMENT;
+  a.ws = ws;
+  a.ws_bytes = ws_bytes;
+  return run_attention(a, static_cast<cudaStream_t>(stream));
 }
 
 int llama_gqa_attention_decode_kv8(const llama_dims* d, const void* q, const void* k, const void* v,

@@ -11,6 +11,12 @@
 //     unnormalised partial (m, l, O) to the workspace.
 //   phase 2 (decode_combine_kernel): o = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c.
 // The result equals softmax(q K^T / sqrt(hd)) V up to the order of additions.
+//
+// Paged cache (block_table set): K and V live in a pool of 128-position pages [n_pages, 128, n_kv,
+// hd]; sequence b's tile t is page block_table[b * max_pages + t], and b holds seq_pos[b] + 1
+// keys, so sequences may have different lengths (items past a sequence's end are empty and
+// leave m = -inf, l = 0).  Positions past a sequence's last key in its last page are not read:
+// their V rows are zeroed in shared memory before the P V MMA (P is 0 there).
 #include <algorithm>
 #include <cmath>
 #include <cstring>
@@ -36,6 +42,9 @@ struct __align__(64) DecodeAttnParams {
   int B, n_q, n_kv, r, kv_len, kv_tiles, chunk_tiles, n_chunks, n_items;
   float scale_log2;
   unsigned* status;
+  const int* block_table;   // paged cache: [B, max_pages] page ids; null: dense [B, cap, n_kv, hd]
+  const int* seq_pos;       // paged cache: [B] position of the new token (keys 0..seq_pos[b])
+  int max_pages;
 };
 
 struct DaSmem {
@@ -76,13 +85,15 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
 __device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 __device__ __forceinline__ void item_coords(const DecodeAttnParams& p, int item, int& b, int& g, int& t_begin,
-                                            int& t_end, int& chunk) {
+                                            int& t_end, int& chunk, int& kv_len) {
   chunk = item % p.n_chunks;
   const int bg = item / p.n_chunks;
   b = bg / p.n_kv;
   g = bg % p.n_kv;
+  kv_len = p.seq_pos ? __ldg(p.seq_pos + b) + 1 : p.kv_len;
+  const int tiles = p.seq_pos ? (kv_len + 127) / 128 : p.kv_tiles;
   t_begin = chunk * p.chunk_tiles;
-  t_end = min(t_begin + p.chunk_tiles, p.kv_tiles);
+  t_end = min(t_begin + p.chunk_tiles, tiles);
 }
 
 // Warp-wide maximum of a float (one instruction).
@@ -146,11 +157,13 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_kernel(const __grid
     if (lane == 0) {  // ---------------------------------------------------- TMA producer
       int tile = 0, it = 0;
       bool ok = true;
-      for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x, ++it) {
-        int b, g, t0, t1, chunk;
-        item_coords(p, item, b, g, t0, t1, chunk);
+      for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
+        int b, g, t0, t1, chunk, kv_len;
+        item_coords(p, item, b, g, t0, t1, chunk, kv_len);
+        if (t1 <= t0) continue;   // past this sequence's end
         const int qb = it & 1;
-        if (!mbar_wait(&q_empty[qb], ((it >> 1) & 1) ^ 1, abort_flag, p.status)) break;
+        ++it;
+        if (!mbar_wait(&q_empty[qb], (((it - 1) >> 1) & 1) ^ 1, abort_flag, p.status)) break;
         mbar_arrive_expect_tx(&q_full[qb], 2 * 64 * p.r * 2);
         for (int hh = 0; hh < 2; ++hh)
           tma_load_3d(sbase + L::OFF_Q + qb * L::QB + hh * (L::QB / 2), &p.tmQ, &q_full[qb], hh * 64, g * p.r, b);
@@ -158,12 +171,14 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_kernel(const __grid
           const int st = tile % DA_STAGES;
           const uint32_t ph = (tile / DA_STAGES) & 1;
           if (!mbar_wait(&kv_empty[st], ph ^ 1, abort_flag, p.status)) { ok = false; break; }
+          const int zc = p.block_table ? 0 : t * 128;
+          const int wc = p.block_table ? __ldg(p.block_table + (int64_t)b * p.max_pages + t) : b;
           mbar_arrive_expect_tx(&k_full[st], L::KV);
           for (int hh = 0; hh < 2; ++hh)
-            tma_load_4d_da(sbase + L::OFF_K + st * L::KV + hh * 16384, &p.tmK, &k_full[st], hh * 64, g, t * 128, b);
+            tma_load_4d_da(sbase + L::OFF_K + st * L::KV + hh * 16384, &p.tmK, &k_full[st], hh * 64, g, zc, wc);
           mbar_arrive_expect_tx(&v_full[st], L::KV);
           for (int hh = 0; hh < 2; ++hh)
-            tma_load_4d_da(sbase + L::OFF_V + st * L::KV + hh * 16384, &p.tmV, &v_full[st], hh * 64, g, t * 128, b);
+            tma_load_4d_da(sbase + L::OFF_V + st * L::KV + hh * 16384, &p.tmV, &v_full[st], hh * 64, g, zc, wc);
         }
       }
     }
@@ -174,8 +189,9 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_kernel(const __grid
       int tile = 0, it = 0;
       bool ok = true;
       for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x, ++it) {
-        int b, g, t0, t1, chunk;
-        item_coords(p, item, b, g, t0, t1, chunk);
+        int b, g, t0, t1, chunk, kv_len;
+        item_coords(p, item, b, g, t0, t1, chunk, kv_len);
+        if (t1 <= t0) { --it; continue; }   // past this sequence's end
         const int qb = it & 1;
         if (!mbar_wait(&q_full[qb], (it >> 1) & 1, abort_flag, p.status)) break;
         tc_fence_after();
@@ -240,8 +256,19 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_kernel(const __grid
     int tile = 0, it = 0;
     bool ok = true;
     for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x, ++it) {
-      int b, g, t0, t1, chunk;
-      item_coords(p, item, b, g, t0, t1, chunk);
+      int b, g, t0, t1, chunk, kv_len;
+      item_coords(p, item, b, g, t0, t1, chunk, kv_len);
+      if (t1 <= t0) {   // past this sequence's end: an empty partial
+        const int64_t base = ((int64_t)b * p.n_chunks + chunk) * p.n_q + (int64_t)g * r;
+#pragma unroll
+        for (int h = 0; h < R; ++h) p.part_o[(base + h) * DA_HD + t] = 0.f;
+        if (t < r) {
+          p.part_ml[(base + t) * 2 + 0] = -INFINITY;
+          p.part_ml[(base + t) * 2 + 1] = 0.f;
+        }
+        --it;
+        continue;
+      }
       float m_ref[R], lsum[R];
 #pragma unroll
       for (int h = 0; h < R; ++h) { m_ref[h] = -INFINITY; lsum[h] = 0.f; }
@@ -254,7 +281,7 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_kernel(const __grid
         tc_wait_ld();
         tc_fence_before();
         mbar_arrive(&s_free[sb]);
-        const bool valid = tt * 128 + t < p.kv_len;
+        const bool valid = tt * 128 + t < kv_len;
         float s[R];
 #pragma unroll
         for (int h = 0; h < R; ++h) s[h] = valid ? __uint_as_float(sv[h]) * p.scale_log2 : -INFINITY;
@@ -300,6 +327,19 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_kernel(const __grid
             tc_wait_st();
 #pragma unroll
             for (int h = 0; h < R; ++h) lsum[h] *= alpha[h];
+          }
+        }
+        // paged cache, a sequence's last page: the rows past its last key hold whatever the pool
+        // held there; zero them so that P = 0 times them stays 0
+        if (p.block_table && (tt + 1) * 128 > kv_len) {
+          const int st = tile % DA_STAGES;
+          if (!mbar_wait(&v_full[st], (tile / DA_STAGES) & 1, abort_flag, p.status)) { ok = false; break; }
+          if (!valid) {
+            uint8_t* vrow = smem + L::OFF_V + st * L::KV + t * 128;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+              for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(vrow + hh * 16384 + c * 16) = make_uint4(0, 0, 0, 0);
           }
         }
         // P^T rows = heads, columns = keys (K-major, 128B swizzle, two 64-key atoms)
@@ -463,11 +503,17 @@ int launch_decode_attn(const AttnDesc& a, void* ws, int num_sms, unsigned* statu
   const int r = (int)(a.n_q / a.n_kv);
   const int64_t kv_len = a.pos0 + 1;
   const DecodePlan d = plan(a.B, a.n_kv, kv_len);
-  const uint64_t dims[4] = {(uint64_t)DA_HD, (uint64_t)a.n_kv, (uint64_t)kv_len, (uint64_t)a.B};
-  const uint64_t strides[3] = {(uint64_t)DA_HD * 2, (uint64_t)a.n_kv * DA_HD * 2, (uint64_t)a.cap * a.n_kv * DA_HD * 2};
+  const bool paged = a.block_table != nullptr;
+  const uint64_t dims[4] = {(uint64_t)DA_HD, (uint64_t)a.n_kv, paged ? 128u : (uint64_t)kv_len,
+                            paged ? (uint64_t)a.n_pages : (uint64_t)a.B};
+  const uint64_t strides[3] = {(uint64_t)DA_HD * 2, (uint64_t)a.n_kv * DA_HD * 2,
+                               (paged ? (uint64_t)128 : (uint64_t)a.cap) * a.n_kv * DA_HD * 2};
   const uint32_t box[4] = {64, 1, 128, 1};
   if (!encode_tmap_4d_bf16(&p.tmK, a.k, dims, strides, box)) return -1;
   if (!encode_tmap_4d_bf16(&p.tmV, a.v, dims, strides, box)) return -1;
+  p.block_table = a.block_table;
+  p.seq_pos = a.seq_pos;
+  p.max_pages = (int)a.max_pages;
   if (!encode_tmap_3d_bf16(&p.tmQ, a.q, DA_HD, (uint64_t)a.n_q, (uint64_t)a.B, DA_HD * 2,
                            (uint64_t)a.n_q * DA_HD * 2, 64, (uint32_t)r, 1))
     return -1;

@@ -8,6 +8,8 @@
 //                k and v into the caches at position t (bf16, or E4M3 codes of x / scale).
 //   fin_swiglu : m = SiLU(rs * gate) * (rs * up) as hi + lo.
 // ("Llama Architecture ...", Mathematical Foundations 1-3; "LLaMA-3 8B ...", section 九.)
+#include <algorithm>
+
 #include "epilogue.cuh"
 #include "kernels.h"
 
@@ -20,9 +22,11 @@ __device__ __forceinline__ void split_bf16(float v, uint16_t& hi, uint16_t& lo) 
 }
 
 constexpr int FN_THREADS = 256;
-constexpr int FN_MAX_PER_THREAD = 32;   // d_model <= 8192
+constexpr int FN_MAX_VEC = 8;   // float4 chunks per thread: d_model <= 8192
 
-// One CTA per row.
+// One CTA per row; every load of the row is issued before the first use (the loads come from L2
+// right after the producing GEMM, so their latency dominates).  x is written back only when it
+// changes (embedding rows on the first layer, or split-K partials added).
 __global__ void __launch_bounds__(FN_THREADS) fin_norm_kernel(float* __restrict__ x, const uint16_t* __restrict__ init,
                                                               const float* __restrict__ part, int n_split,
                                                               const uint16_t* __restrict__ g, uint16_t* __restrict__ a_hi,
@@ -32,18 +36,37 @@ __global__ void __launch_bounds__(FN_THREADS) fin_norm_kernel(float* __restrict_
   pdl_trigger();
   pdl_wait();
   const int r = blockIdx.x;
-  float v[FN_MAX_PER_THREAD];
+  const int nv = d / 4;
+  float4 v[FN_MAX_VEC];
+#pragma unroll
+  for (int j = 0; j < FN_MAX_VEC; ++j) {
+    const int i = threadIdx.x + j * FN_THREADS;
+    v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (i < nv) {
+      if (init) {
+        const uint2 w = *reinterpret_cast<const uint2*>(init + (int64_t)r * d + 4 * i);
+        v[j] = make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u),
+                           __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u));
+      } else {
+        v[j] = *reinterpret_cast<const float4*>(x + (int64_t)r * d + 4 * i);
+      }
+    }
+  }
+  const bool write_x = init != nullptr || n_split > 0;
   float ss = 0.f;
 #pragma unroll
-  for (int j = 0; j < FN_MAX_PER_THREAD; ++j) {
+  for (int j = 0; j < FN_MAX_VEC; ++j) {
     const int i = threadIdx.x + j * FN_THREADS;
-    v[j] = 0.f;
-    if (i < d) {
-      float t = init ? bf2f(init[(int64_t)r * d + i]) : x[(int64_t)r * d + i];
-      for (int s = 0; s < n_split; ++s) t += part[((int64_t)s * B + r) * d + i];
-      x[(int64_t)r * d + i] = t;
-      v[j] = t;
-      ss = fmaf(t, t, ss);
+    if (i < nv) {
+      for (int s = 0; s < n_split; ++s) {
+        const float4 w = *reinterpret_cast<const float4*>(part + ((int64_t)s * B + r) * d + 4 * i);
+        v[j].x += w.x; v[j].y += w.y; v[j].z += w.z; v[j].w += w.w;
+      }
+      if (write_x) *reinterpret_cast<float4*>(x + (int64_t)r * d + 4 * i) = v[j];
+      ss = fmaf(v[j].x, v[j].x, ss);
+      ss = fmaf(v[j].y, v[j].y, ss);
+      ss = fmaf(v[j].z, v[j].z, ss);
+      ss = fmaf(v[j].w, v[j].w, ss);
     }
   }
 #pragma unroll
@@ -56,13 +79,19 @@ __global__ void __launch_bounds__(FN_THREADS) fin_norm_kernel(float* __restrict_
   const float rs = rsqrtf(tot / (float)d + eps);
   if (threadIdx.x == 0) rs_out[r] = rs;
 #pragma unroll
-  for (int j = 0; j < FN_MAX_PER_THREAD; ++j) {
+  for (int j = 0; j < FN_MAX_VEC; ++j) {
     const int i = threadIdx.x + j * FN_THREADS;
-    if (i < d) {
-      uint16_t hi, lo;
-      split_bf16(v[j] * bf2f(g[i]), hi, lo);
-      a_hi[(int64_t)r * d + i] = hi;
-      a_lo[(int64_t)r * d + i] = lo;
+    if (i < nv) {
+      const uint2 gw = *reinterpret_cast<const uint2*>(g + 4 * i);
+      const float y[4] = {v[j].x * __uint_as_float(gw.x << 16), v[j].y * __uint_as_float(gw.x & 0xFFFF0000u),
+                          v[j].z * __uint_as_float(gw.y << 16), v[j].w * __uint_as_float(gw.y & 0xFFFF0000u)};
+      uint16_t hi[4], lo[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) split_bf16(y[k], hi[k], lo[k]);
+      *reinterpret_cast<uint2*>(a_hi + (int64_t)r * d + 4 * i) =
+          make_uint2((uint32_t)hi[0] | ((uint32_t)hi[1] << 16), (uint32_t)hi[2] | ((uint32_t)hi[3] << 16));
+      *reinterpret_cast<uint2*>(a_lo + (int64_t)r * d + 4 * i) =
+          make_uint2((uint32_t)lo[0] | ((uint32_t)lo[1] << 16), (uint32_t)lo[2] | ((uint32_t)lo[3] << 16));
     }
   }
 }
@@ -75,6 +104,9 @@ struct FinQkvParams {
   void* vc;
   const float* k_scale;  // [n_kv] or null
   const float* v_scale;
+  const int* block_table;  // paged cache: [B, max_pages]; position t goes to page t / 128, row t % 128
+  const int* seq_pos;      // paged cache: per-row position of the new token (else all rows at t)
+  int max_pages;
   int n_split, B, nq_cols, nkv_cols, hd;
   int64_t cap, t;
   RopeFreq freq[kMaxRopePairs];
@@ -86,8 +118,9 @@ __global__ void fin_qkv_kernel(const __grid_constant__ FinQkvParams p) {
   pdl_wait();
   const int n_cols = p.nq_cols + 2 * p.nkv_cols;
   const int pairs = n_cols / 2;
-  const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= (int64_t)p.B * pairs) return;
+  const int64_t total = (int64_t)p.B * pairs;
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
   const int r = (int)(idx / pairs);
   const int c = (int)(idx % pairs) * 2;
   float v0 = 0.f, v1 = 0.f;
@@ -99,7 +132,8 @@ __global__ void fin_qkv_kernel(const __grid_constant__ FinQkvParams p) {
   const float rs = p.rs[r];
   v0 *= rs;
   v1 *= rs;
-  const float pos = (float)p.t;
+  const int64_t tpos = p.seq_pos ? (int64_t)__ldg(p.seq_pos + r) : p.t;
+  const float pos = (float)tpos;
   if (c < p.nq_cols + p.nkv_cols) {       // RoPE on q and k
     const int cc = c < p.nq_cols ? c : c - p.nq_cols;
     float sn, cs;
@@ -110,11 +144,13 @@ __global__ void fin_qkv_kernel(const __grid_constant__ FinQkvParams p) {
   }
   if (c < p.nq_cols) {
     *reinterpret_cast<uint32_t*>(p.q + (int64_t)r * p.nq_cols + c) = pack_bf2(v0, v1);
-    return;
+    continue;
   }
   const bool is_k = c < p.nq_cols + p.nkv_cols;
   const int cc = is_k ? c - p.nq_cols : c - p.nq_cols - p.nkv_cols;
-  const int64_t off = ((int64_t)r * p.cap + p.t) * p.nkv_cols + cc;
+  const int64_t slot = p.block_table ? (int64_t)__ldg(p.block_table + (int64_t)r * p.max_pages + tpos / 128) * 128 + tpos % 128
+                                     : (int64_t)r * p.cap + tpos;
+  const int64_t off = slot * p.nkv_cols + cc;
   if (p.k_scale) {   // 8-bit cache: code = E4M3(fl32(x) / scale), rounded to nearest even, saturating
     const float s = (is_k ? p.k_scale : p.v_scale)[cc / p.hd];
     uint16_t code;
@@ -123,35 +159,44 @@ __global__ void fin_qkv_kernel(const __grid_constant__ FinQkvParams p) {
   } else {
     *reinterpret_cast<uint32_t*>(static_cast<uint16_t*>(is_k ? p.kc : p.vc) + off) = pack_bf2(v0, v1);
   }
+  }
 }
 
-// One thread per (row, hidden unit): gate in columns [0, d_ff), up in [d_ff, 2 d_ff).
+// Four hidden units per thread (grid-stride): gate in columns [0, d_ff), up in [d_ff, 2 d_ff).
 __global__ void fin_swiglu_kernel(const float* __restrict__ part, const float* __restrict__ rs, uint16_t* __restrict__ m_hi,
                                   uint16_t* __restrict__ m_lo, int n_split, int B, int dff) {
   pdl_trigger();
   pdl_wait();
-  const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= (int64_t)B * dff) return;
-  const int r = (int)(idx / dff), j = (int)(idx % dff);
-  float gsum = 0.f, usum = 0.f;
-  for (int s = 0; s < n_split; ++s) {
-    const float* row = part + ((int64_t)s * B + r) * 2 * dff;
-    gsum += row[j];
-    usum += row[dff + j];
+  const int q4 = dff / 4;
+  const int64_t total = (int64_t)B * q4;
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int r = (int)(idx / q4), j = (int)(idx % q4) * 4;
+    float4 gs = make_float4(0.f, 0.f, 0.f, 0.f), us = gs;
+    for (int s = 0; s < n_split; ++s) {
+      const float* row = part + ((int64_t)s * B + r) * 2 * dff;
+      const float4 gv = *reinterpret_cast<const float4*>(row + j);
+      const float4 uv = *reinterpret_cast<const float4*>(row + dff + j);
+      gs.x += gv.x; gs.y += gv.y; gs.z += gv.z; gs.w += gv.w;
+      us.x += uv.x; us.y += uv.y; us.z += uv.z; us.w += uv.w;
+    }
+    const float sc = rs[r];
+    uint16_t h0, h1, h2, h3, l0, l1, l2, l3;
+    split_bf16(silu_f(gs.x * sc) * (us.x * sc), h0, l0);
+    split_bf16(silu_f(gs.y * sc) * (us.y * sc), h1, l1);
+    split_bf16(silu_f(gs.z * sc) * (us.z * sc), h2, l2);
+    split_bf16(silu_f(gs.w * sc) * (us.w * sc), h3, l3);
+    const int64_t o = (int64_t)r * dff + j;
+    *reinterpret_cast<uint2*>(m_hi + o) = make_uint2((uint32_t)h0 | ((uint32_t)h1 << 16), (uint32_t)h2 | ((uint32_t)h3 << 16));
+    *reinterpret_cast<uint2*>(m_lo + o) = make_uint2((uint32_t)l0 | ((uint32_t)l1 << 16), (uint32_t)l2 | ((uint32_t)l3 << 16));
   }
-  const float sc = rs[r];
-  const float m = silu_f(gsum * sc) * (usum * sc);
-  uint16_t hi, lo;
-  split_bf16(m, hi, lo);
-  m_hi[idx] = hi;
-  m_lo[idx] = lo;
 }
 
 }  // namespace
 
 int launch_fin_norm(float* x, const void* init_bf16, const float* part, int n_split, const void* g, void* a_hi,
                     void* a_lo, float* rs, int B, int d, float eps, cudaStream_t st) {
-  if (d > FN_THREADS * FN_MAX_PER_THREAD) return -1;
+  if (d % 4 || d > FN_THREADS * FN_MAX_VEC * 4) return -1;
   return launch_k(fin_norm_kernel, dim3(B), dim3(FN_THREADS), 0, st, x, static_cast<const uint16_t*>(init_bf16), part,
                   n_split, static_cast<const uint16_t*>(g), static_cast<uint16_t*>(a_hi), static_cast<uint16_t*>(a_lo),
                   rs, B, d, eps) == cudaSuccess ? 0 : -1;
@@ -159,21 +204,27 @@ int launch_fin_norm(float* x, const void* init_bf16, const float* part, int n_sp
 
 int launch_fin_qkv(const float* part, int n_split, const float* rs, void* q, void* kc, void* vc, int B, int nq_cols,
                    int nkv_cols, int hd, int64_t cap, int64_t t, const RopeFreq* freq, const float* k_scale,
-                   const float* v_scale, cudaStream_t st) {
+                   const float* v_scale, const int* block_table, int max_pages, const int* seq_pos,
+                   cudaStream_t st) {
   FinQkvParams p;
   p.part = part; p.rs = rs;
   p.q = static_cast<uint16_t*>(q); p.kc = kc; p.vc = vc;
   p.k_scale = k_scale; p.v_scale = v_scale;
+  p.block_table = block_table; p.max_pages = max_pages; p.seq_pos = seq_pos;
   p.n_split = n_split; p.B = B; p.nq_cols = nq_cols; p.nkv_cols = nkv_cols; p.hd = hd; p.cap = cap; p.t = t;
   for (int i = 0; i < hd / 2; ++i) p.freq[i] = freq[i];
   const int64_t n = (int64_t)B * (nq_cols + 2 * nkv_cols) / 2;
+  // one thread per pair: B * 3 * 1024 threads at most for the shapes of the decode path, which
+  // are resident at once (the next kernel of the stream can launch early)
   return launch_k(fin_qkv_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st, p) == cudaSuccess ? 0 : -1;
 }
 
 int launch_fin_swiglu(const float* part, int n_split, const float* rs, void* m_hi, void* m_lo, int B, int dff,
                       cudaStream_t st) {
-  const int64_t n = (int64_t)B * dff;
-  return launch_k(fin_swiglu_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st, part, rs,
+  if (dff % 4) return -1;
+  const int64_t n = (int64_t)B * dff / 4;
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>((n + 255) / 256, 2 * num_sms()));
+  return launch_k(fin_swiglu_kernel, dim3(grid), dim3(256), 0, st, part, rs,
                   static_cast<uint16_t*>(m_hi), static_cast<uint16_t*>(m_lo), n_split, B, dff) == cudaSuccess ? 0 : -1;
 }
 

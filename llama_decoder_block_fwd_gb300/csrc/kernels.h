@@ -72,6 +72,9 @@ struct AttnDesc {
   size_t ws_bytes;
   const float* k_scale; // 8-bit cache: k and v hold E4M3 codes, x = code * scale[kv head]
   const float* v_scale;
+  const int* block_table;   // decode kernel, paged cache: k/v are pools [n_pages, 128, n_kv, hd]
+  const int* seq_pos;       //   per-sequence new-token positions (pos0 = their upper bound)
+  int64_t max_pages, n_pages;
 };
 
 // rows x d RMSNorm; x_f32/y_f32 give the element types of x and y, g has type `dtype`.
@@ -131,7 +134,8 @@ int launch_fin_norm(float* x, const void* init_bf16, const float* part, int n_sp
                     void* a_lo, float* rs, int B, int d, float eps, cudaStream_t st);
 int launch_fin_qkv(const float* part, int n_split, const float* rs, void* q, void* kc, void* vc, int B, int nq_cols,
                    int nkv_cols, int hd, int64_t cap, int64_t t, const RopeFreq* freq, const float* k_scale,
-                   const float* v_scale, cudaStream_t st);
+                   const float* v_scale, const int* block_table, int max_pages, const int* seq_pos,
+                   cudaStream_t st);
 int launch_fin_swiglu(const float* part, int n_split, const float* rs, void* m_hi, void* m_lo, int B, int dff,
                       cudaStream_t st);
 
