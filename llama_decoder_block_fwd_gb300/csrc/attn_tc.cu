@@ -84,6 +84,30 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+__device__ __forceinline__ void tmem_ld16_at(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+        "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr));
+}
+
+// 32 scores of a row -> 16 bf16 pairs of P = 2^(s * scale - m) stored at TMEM column `col`; the
+// fp32 values are added to the row sums.
+__device__ __forceinline__ void exp_chunk(const uint32_t (&v)[32], uint32_t col, float scale, float m, float& ls0,
+                                          float& ls1) {
+  uint32_t w[16];
+#pragma unroll
+  for (int e = 0; e < 16; ++e) {
+    const float p0 = ex2(fmaf(__uint_as_float(v[2 * e]), scale, -m));
+    const float p1 = ex2(fmaf(__uint_as_float(v[2 * e + 1]), scale, -m));
+    ls0 += p0;
+    ls1 += p1;
+    w[e] = pack_bf16x2(p0, p1);
+  }
+  tmem_st16(col, w);
+}
+
 template <int HD>
 __global__ void __launch_bounds__(AT_THREADS, 1) attn_tc_kernel(const __grid_constant__ AttnParams p) {
   using L = Smem<HD>;
@@ -167,13 +191,14 @@ __global__ void __launch_bounds__(AT_THREADS, 1) attn_tc_kernel(const __grid_con
         const int st = j & 1;
         if (!mbar_wait(&k_full[st], (j >> 1) & 1, abort_flag, p.status)) return false;
         tc_fence_after();
-        const uint32_t ka = sbase + L::OFF_K + st * L::KV;
-        const uint32_t qa = sbase + L::OFF_Q + x * L::QT;
+        // descriptors of k-step 0; k-step k starts (k >> 2) * 16384 + (k & 3) * 32 bytes further,
+        // which is added to the address field (bits 0-13, in 16-byte units) directly
+        const uint64_t ad0 = sdesc_sw128(sbase + L::OFF_Q + x * L::QT, 16, 1024);
+        const uint64_t bd0 = sdesc_sw128(sbase + L::OFF_K + st * L::KV, 16, 1024);
 #pragma unroll
         for (int k = 0; k < HD / 16; ++k) {
-          const uint64_t ad = sdesc_sw128(qa + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(ka + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
-          tc_mma(tmem + x * 128, ad, bd, idesc_s, k > 0 ? 1u : 0u);
+          const uint64_t off = (uint64_t)(((k >> 2) * 16384 + (k & 3) * 32) >> 4);
+          tc_mma(tmem + x * 128, ad0 + off, bd0 + off, idesc_s, k > 0 ? 1u : 0u);
         }
         tc_commit(&s_full[x]);
         return true;
@@ -183,12 +208,11 @@ __global__ void __launch_bounds__(AT_THREADS, 1) attn_tc_kernel(const __grid_con
         if (!mbar_wait(&p_full[x], j & 1, abort_flag, p.status)) return false;
         if (!mbar_wait(&v_full[st], (j >> 1) & 1, abort_flag, p.status)) return false;
         tc_fence_after();
-        const uint32_t va = sbase + L::OFF_V + st * L::KV;
+        const uint64_t bd0 = sdesc_sw128(sbase + L::OFF_V + st * L::KV, 16384, 1024);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {   // 16 keys per step; P_X k-step k is TMEM columns 8k..8k+7
-          const uint64_t bd = sdesc_sw128(va + k * 2048, 16384, 1024);
-          tc_mma_ts(tmem + 256 + x * 128, tmem + x * 128 + k * 8, bd, idesc_o, (j > 0 || k > 0) ? 1u : 0u);
-        }
+        for (int k = 0; k < 8; ++k)   // 16 keys per step; P_X k-step k is TMEM columns 8k..8k+7
+          tc_mma_ts(tmem + 256 + x * 128, tmem + x * 128 + k * 8, bd0 + (uint64_t)(k * 2048 >> 4), idesc_o,
+                    (j > 0 || k > 0) ? 1u : 0u);
         tc_commit(&o_done[x]);
         return true;
       };
@@ -225,27 +249,31 @@ __global__ void __launch_bounds__(AT_THREADS, 1) attn_tc_kernel(const __grid_con
       tc_fence_after();
       const bool mask = j >= full_tiles[x];
       const int kbase = j * 128;
-      // pass 1: row maximum (key positions past the query's only on the diagonal tiles)
-      float mx = -INFINITY;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tS + c * 32, v);
-        tc_wait_ld();
-        if (mask) {
+      // the row of S (128 scores) is read from TMEM once, into registers
+      uint32_t v0[32], v1[32], v2[32], v3[32];
+      tmem_ld32(tS + 0, v0);
+      tmem_ld32(tS + 32, v1);
+      tmem_ld32(tS + 64, v2);
+      tmem_ld32(tS + 96, v3);
+      tc_wait_ld();
+      if (mask) {   // key positions past the query's, only on the diagonal tiles
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (kbase + c * 32 + i > qpos) v[i] = __float_as_uint(-INFINITY);
+        for (int i = 0; i < 32; ++i) {
+          if (kbase + i > qpos) v0[i] = __float_as_uint(-INFINITY);
+          if (kbase + 32 + i > qpos) v1[i] = __float_as_uint(-INFINITY);
+          if (kbase + 64 + i > qpos) v2[i] = __float_as_uint(-INFINITY);
+          if (kbase + 96 + i > qpos) v3[i] = __float_as_uint(-INFINITY);
         }
-        float m0 = mx, m1 = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          m0 = max3(m0, __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
-          m1 = max3(m1, __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
-        }
-        mx = fmaxf(m0, m1);
       }
-      const float mt = mx * p.scale_log2;
+      float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 32; i += 2) {
+        m0 = max3(m0, __uint_as_float(v0[i]), __uint_as_float(v0[i + 1]));
+        m1 = max3(m1, __uint_as_float(v1[i]), __uint_as_float(v1[i + 1]));
+        m2 = max3(m2, __uint_as_float(v2[i]), __uint_as_float(v2[i + 1]));
+        m3 = max3(m3, __uint_as_float(v3[i]), __uint_as_float(v3[i + 1]));
+      }
+      const float mt = fmaxf(fmaxf(m0, m1), fmaxf(m2, m3)) * p.scale_log2;
       float alpha = 1.f;
       bool resc = false;
       if (j == 0) {
@@ -261,44 +289,24 @@ __global__ void __launch_bounds__(AT_THREADS, 1) attn_tc_kernel(const __grid_con
         tc_fence_after();
         l *= alpha;
 #pragma unroll 1
-        for (int c = 0; c < HD / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(tO + c * 32, v);
+        for (int c = 0; c < HD / 16; ++c) {
+          uint32_t ov[16];
+          tmem_ld16_at(tO + c * 16, ov);
           tc_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-          tmem_st32(tO + c * 32, v);
+          for (int i = 0; i < 16; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+          tmem_st16(tO + c * 16, ov);
         }
         tc_wait_st();
       }
-      // pass 2: P = exp2(S * scale_log2 - m) as bf16 pairs into TMEM columns [16c, 16c+16) of S_X
-      // (written only over S columns this pass has already read).  The row sum is taken over the
-      // fp32 values.
+      // P = exp2(S * scale_log2 - m) as bf16 pairs into TMEM columns [0, 64) of S_X.  The row sum
+      // is taken over the fp32 values.
       const float mb = m_ref;
       float ls0 = 0.f, ls1 = 0.f;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        tmem_ld32(tS + c * 32, v);
-        tc_wait_ld();
-        if (mask) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (kbase + c * 32 + i > qpos) v[i] = __float_as_uint(-INFINITY);
-        }
-        uint32_t w[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const float x0 = fmaf(__uint_as_float(v[2 * e]), p.scale_log2, -mb);
-          const float x1 = fmaf(__uint_as_float(v[2 * e + 1]), p.scale_log2, -mb);
-          const float p0 = ex2(x0);
-          const float p1 = ex2(x1);
-          ls0 += p0;
-          ls1 += p1;
-          w[e] = pack_bf16x2(p0, p1);
-        }
-        tmem_st16(tS + c * 16, w);
-      }
+      exp_chunk(v0, tS + 0, p.scale_log2, mb, ls0, ls1);
+      exp_chunk(v1, tS + 16, p.scale_log2, mb, ls0, ls1);
+      exp_chunk(v2, tS + 32, p.scale_log2, mb, ls0, ls1);
+      exp_chunk(v3, tS + 48, p.scale_log2, mb, ls0, ls1);
       const float lsum = ls0 + ls1;
       tc_wait_st();
       l += lsum;

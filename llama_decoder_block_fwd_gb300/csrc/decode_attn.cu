@@ -205,12 +205,11 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_kernel(const __grid
           if (!mbar_wait(&s_free[sb], ((gt >> 1) & 1) ^ 1, abort_flag, p.status)) return false;
           tc_fence_after();
           const uint32_t ka = sbase + L::OFF_K + st * L::KV;
+          const uint64_t ad0 = sdesc_sw128(ka, 16, 1024), bd0 = sdesc_sw128(qa, 16, 1024);
 #pragma unroll
-          for (int k = 0; k < DA_HD / 16; ++k) {
-            const uint64_t ad = sdesc_sw128(ka + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(qa + (k >> 2) * (L::QB / 2) + (k & 3) * 32, 16, 1024);
-            tc_mma(tS + sb * 16, ad, bd, idesc_s, k > 0 ? 1u : 0u);
-          }
+          for (int k = 0; k < DA_HD / 16; ++k)   // k-step offsets added to the address field (16-byte units)
+            tc_mma(tS + sb * 16, ad0 + (uint64_t)(((k >> 2) * 16384 + (k & 3) * 32) >> 4),
+                   bd0 + (uint64_t)(((k >> 2) * (L::QB / 2) + (k & 3) * 32) >> 4), idesc_s, k > 0 ? 1u : 0u);
           tc_commit(&s_full[sb]);
           return true;
         };
@@ -225,12 +224,12 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_kernel(const __grid
           tc_fence_after();
           const uint32_t va = sbase + L::OFF_V + st * L::KV;
           const uint32_t pa = sbase + L::OFF_P + pb * L::PB;
+          const uint64_t ad0 = sdesc_sw128(va, 16384, 1024);   // V^T, MN-major
+          const uint64_t bd0 = sdesc_sw128(pa, 16, 1024);
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {     // 16 keys per step
-            const uint64_t ad = sdesc_sw128(va + k * 2048, 16384, 1024);           // V^T, MN-major
-            const uint64_t bd = sdesc_sw128(pa + (k >> 2) * (L::PB / 2) + (k & 3) * 32, 16, 1024);
-            tc_mma(tO, ad, bd, idesc_o, (j > 0 || k > 0) ? 1u : 0u);
-          }
+          for (int k = 0; k < 8; ++k)       // 16 keys per step
+            tc_mma(tO, ad0 + (uint64_t)(k * 2048 >> 4), bd0 + (uint64_t)(((k >> 2) * (L::PB / 2) + (k & 3) * 32) >> 4),
+                   idesc_o, (j > 0 || k > 0) ? 1u : 0u);
           tc_commit(&o_done[pb]);
           tc_commit(&kv_empty[st]);
           return true;

@@ -221,11 +221,11 @@ __global__ void __launch_bounds__(D8_THREADS, 1) decode_attn8_kernel(const __gri
           if (!mbar_wait(&bars[B_K16F + sb], (gt >> 1) & 1, abort_flag, p.status)) return false;
           if (!mbar_wait(&bars[B_SFREE + sb], ((gt >> 1) & 1) ^ 1, abort_flag, p.status)) return false;
           tc_fence_after();
+          const uint64_t bd0 = sdesc_sw128(qa, 16, 1024);
 #pragma unroll
-          for (int k = 0; k < D8_HD / 16; ++k) {   // A = K from tensor memory, 16 hd per step
-            const uint64_t bd = sdesc_sw128(qa + (k >> 2) * (L::QB / 2) + (k & 3) * 32, 16, 1024);
-            tc_mma_ts(tS + sb * 16, tK + sb * 64 + k * 8, bd, idesc_s, k > 0 ? 1u : 0u);
-          }
+          for (int k = 0; k < D8_HD / 16; ++k)   // A = K from tensor memory, 16 hd per step
+            tc_mma_ts(tS + sb * 16, tK + sb * 64 + k * 8,
+                      bd0 + (uint64_t)(((k >> 2) * (L::QB / 2) + (k & 3) * 32) >> 4), idesc_s, k > 0 ? 1u : 0u);
           tc_commit(&bars[B_SF + sb]);
           tc_commit(&bars[B_K16E + sb]);
           return true;
@@ -239,12 +239,12 @@ __global__ void __launch_bounds__(D8_THREADS, 1) decode_attn8_kernel(const __gri
           if (j == 0 && !mbar_wait(&bars[B_OFREE], (it & 1) ^ 1, abort_flag, p.status)) return false;
           tc_fence_after();
           const uint32_t pa = sbase + L::OFF_P + pb * L::PB;
+          const uint64_t ad0 = sdesc_sw128(va, 16384, 1024);   // V^T, MN-major
+          const uint64_t bd0 = sdesc_sw128(pa, 16, 1024);
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint64_t ad = sdesc_sw128(va + k * 2048, 16384, 1024);           // V^T, MN-major
-            const uint64_t bd = sdesc_sw128(pa + (k >> 2) * (L::PB / 2) + (k & 3) * 32, 16, 1024);
-            tc_mma(tO, ad, bd, idesc_o, (j > 0 || k > 0) ? 1u : 0u);
-          }
+          for (int k = 0; k < 8; ++k)
+            tc_mma(tO, ad0 + (uint64_t)(k * 2048 >> 4), bd0 + (uint64_t)(((k >> 2) * (L::PB / 2) + (k & 3) * 32) >> 4),
+                   idesc_o, (j > 0 || k > 0) ? 1u : 0u);
           tc_commit(&bars[B_OD + pb]);
           tc_commit(&bars[B_V16E + pb]);
           return true;

@@ -174,10 +174,10 @@ __global__ void __launch_bounds__(SK_THREADS, 1) gemm_skinny_kernel(const __grid
           tc_fence_after();
           const uint32_t sa = smem_base + stage * stage_bytes;
           const uint32_t sb = sa + SK_A_BYTES;
+          const uint64_t ad0 = sdesc_sw128(sa, 16, 1024), bd0 = sdesc_sw128(sb, 16, 1024);
 #pragma unroll
-          for (int k = 0; k < SK_TK / 16; ++k)
-            tc_mma(d, sdesc_sw128(sa + k * 32, 16, 1024), sdesc_sw128(sb + k * 32, 16, 1024), idesc,
-                   (kb != kb0 || k != 0) ? 1u : 0u);
+          for (int k = 0; k < SK_TK / 16; ++k)   // +32 bytes per k-step = +2 in the address field
+            tc_mma(d, ad0 + 2 * k, bd0 + 2 * k, idesc, (kb != kb0 || k != 0) ? 1u : 0u);
           tc_commit(&empty[stage]);
           if (++stage == p.stages) { stage = 0; phase ^= 1; }
         }

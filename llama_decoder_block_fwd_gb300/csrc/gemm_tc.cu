@@ -159,11 +159,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tc_kernel(const __grid_co
           tc_fence_after();
           const uint32_t sa = smem_base + stage * STAGE_BYTES;
           const uint32_t sb = sa + (p.dual ? 2 * A_BYTES : A_BYTES);
+          const uint64_t ad0 = sdesc_sw128(sa, 16, 1024), bd0 = sdesc_sw128(sb, 16, 1024);
+          const uint64_t ad1 = sdesc_sw128(sa + A_BYTES, 16, 1024);
 #pragma unroll
-          for (int k = 0; k < TK / 16; ++k) {
-            const uint64_t bd = sdesc_sw128(sb + k * 32, 16, 1024);
-            tc_mma(d, sdesc_sw128(sa + k * 32, 16, 1024), bd, idesc, (kb != kb0 || k != 0) ? 1u : 0u);
-            if (p.dual) tc_mma(d, sdesc_sw128(sa + A_BYTES + k * 32, 16, 1024), bd, idesc, 1u);
+          for (int k = 0; k < TK / 16; ++k) {   // +32 bytes per k-step = +2 in the address field
+            tc_mma(d, ad0 + 2 * k, bd0 + 2 * k, idesc, (kb != kb0 || k != 0) ? 1u : 0u);
+            if (p.dual) tc_mma(d, ad1 + 2 * k, bd0 + 2 * k, idesc, 1u);
           }
           tc_commit(&empty[stage]);
           if (++stage == STAGES) { stage = 0; phase ^= 1; }

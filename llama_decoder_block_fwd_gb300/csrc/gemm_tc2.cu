@@ -210,10 +210,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS2, 1)
           tc_fence_after();
           const uint32_t sa = smem_base + stage * STAGE2;
           const uint32_t sb = sa + A2_BYTES;
+          const uint64_t ad0 = sdesc_sw128(sa, 16, 1024), bd0 = sdesc_sw128(sb, 16, 1024);
 #pragma unroll
-          for (int k = 0; k < T2K / 16; ++k)
-            tc2_mma(d, sdesc_sw128(sa + k * 32, 16, 1024), sdesc_sw128(sb + k * 32, 16, 1024), idesc,
-                    (kb | k) != 0);
+          for (int k = 0; k < T2K / 16; ++k)   // +32 bytes per k-step = +2 in the address field
+            tc2_mma(d, ad0 + 2 * k, bd0 + 2 * k, idesc, (kb | k) != 0);
           tc2_commit_mc(&empty[stage], 0x3);
           if (++stage == S2) { stage = 0; phase ^= 1; }
         }
