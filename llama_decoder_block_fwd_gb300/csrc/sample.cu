@@ -8,12 +8,15 @@
 // top-k mass reaches p; the draw walks the kept tokens in increasing id and stops at the first
 // whose cumulative mass exceeds u times the kept mass (u in [0, 1) is supplied by the caller).
 //
-// One CTA per row.  The row (up to a few hundred KB of fp32) is streamed from L2 once per pass;
-// nothing is sorted.  The thresholds are found by radix selection on an order-preserving 32-bit
-// key of the logit, four 8-bit digits from the top: by count for top-k, by probability mass for
-// top-p.  Masses are exp((z - z_max) / T) in fp32, held as 2^-40 fixed point in 64-bit integers
-// so that every sum is exact and independent of the order of the atomic adds: the same logits
-// always give the same token.  Terms below 2^-40 of the largest count as zero.
+// One CTA per row.  Top-k up to 1024 (the usual case): the argmax pass over the row also keeps
+// every thread's two largest logits; the k-th largest of those bounds the k-th largest logit from
+// below, so a second pass gathers the few tokens at or above that bound into shared memory, where
+// they are ranked by a bitonic sort.  Otherwise (or when too many tokens tie near the bound) the
+// thresholds are found by radix selection on an order-preserving 32-bit key of the logit, four
+// 8-bit digits from the top: by count for top-k, by probability mass for top-p, one pass over the
+// row (from L2) per digit.  Masses are exp((z - z_max) / T) in fp32, held as 2^-40 fixed point in
+// 64-bit integers so that every sum is exact and independent of the order of the atomic adds: the
+// same logits always give the same token.  Terms below 2^-40 of the largest count as zero.
 #include <climits>
 
 #include "kernels.h"
@@ -31,9 +34,16 @@ __device__ __forceinline__ uint32_t order_key(float z) {
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
+constexpr int SP_SMALL_K = 1024;   // top-k up to this: ranked in shared memory
+constexpr int SP_CAP = 4096;       // candidates gathered into shared memory at most
+// dynamic shared memory of the small-k path: candidate keys, their logits, ranked masses
+constexpr size_t SP_DYN_SMEM = SP_CAP * 8 + SP_CAP * 4 + SP_SMALL_K * 8;
+
 struct SampleShared {
   u64 hmass[256];
   unsigned hcnt[256];
+  unsigned ccount;
+  unsigned cbin, ctotal;
   u64 wsum[SP_WARPS];
   float wval[SP_WARPS];
   int widx[SP_WARPS];
@@ -105,6 +115,31 @@ __device__ void select_digit(SampleShared& sh, u64 target) {
   }
 }
 
+// Call f(i, z_i, valid) for every element of the row: 16-byte loads, two in flight per thread,
+// the same trip count on every lane of a warp (f may use warp-collective operations); `valid` is
+// false on the padding calls.  z must be 16-byte aligned.
+template <typename F>
+__device__ __forceinline__ void row_pass4(const float* __restrict__ z, int V, F&& f) {
+  const int lane = threadIdx.x & 31;
+  const int nv4 = V >> 2;
+  const float4* z4 = reinterpret_cast<const float4*>(z);
+  for (int base = (int)(threadIdx.x & ~31u); base < nv4; base += 2 * SP_THREADS) {
+    const int q0 = base + lane, q1 = base + SP_THREADS + lane;
+    const bool ok0 = q0 < nv4, ok1 = q1 < nv4;
+    const float4 w0 = ok0 ? __ldg(z4 + q0) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 w1 = ok1 ? __ldg(z4 + q1) : make_float4(0.f, 0.f, 0.f, 0.f);
+    f(4 * q0, w0.x, ok0); f(4 * q0 + 1, w0.y, ok0); f(4 * q0 + 2, w0.z, ok0); f(4 * q0 + 3, w0.w, ok0);
+    if (base + SP_THREADS < nv4) {   // warp-uniform
+      f(4 * q1, w1.x, ok1); f(4 * q1 + 1, w1.y, ok1); f(4 * q1 + 2, w1.z, ok1); f(4 * q1 + 3, w1.w, ok1);
+    }
+  }
+  if (threadIdx.x < 32) {   // the last V % 4 elements
+    const int i = 4 * nv4 + lane;
+    const bool ok = i < V;
+    f(i, ok ? z[i] : 0.f, ok);
+  }
+}
+
 // The id of the n-th (1-based) token, in increasing id, for which pred(i, z_i) holds.
 template <typename Pred>
 __device__ int nth_index(const float* z, int V, int n, Pred pred, SampleShared& sh) {
@@ -134,12 +169,30 @@ __global__ void __launch_bounds__(SP_THREADS) sample_kernel(const float* __restr
   const float* z = logits + (int64_t)row * ld;
 
   // ---- the largest logit and its lowest id (argmax)
-  float best = -INFINITY;
+  const bool vec = (reinterpret_cast<uintptr_t>(z) & 15) == 0;
+  // small top-k: the argmax pass also keeps each thread's two largest logits; the k-th largest
+  // of those 2 x SP_THREADS values bounds the k-th largest logit from below, so one more pass
+  // gathers every token at or above it and the ranking is finished in shared memory
+  const bool small_k = vec && temperature > 0.f && top_k >= 2 && top_k <= SP_SMALL_K && top_k < V && top_p > 0.f;
+  extern __shared__ uint8_t dyn[];
+  u64* ckey = reinterpret_cast<u64*>(dyn);
+  float* cz = reinterpret_cast<float*>(dyn + SP_CAP * 8);
+  u64* cmass = reinterpret_cast<u64*>(dyn + SP_CAP * 8 + SP_CAP * 4);
+  float best = -INFINITY, second = -INFINITY;
   int bi = INT_MAX;
-  for (int i = tid; i < V; i += SP_THREADS) {
-    const float v = z[i];
-    if (v > best || (v == best && i < bi)) { best = v; bi = i; }
+  if (vec) {
+    row_pass4(z, V, [&](int i, float v, bool ok) {
+      if (!ok) return;
+      if (v > best || (v == best && i < bi)) { second = best; best = v; bi = i; }
+      else if (v > second) { second = v; }
+    });
+  } else {
+    for (int i = tid; i < V; i += SP_THREADS) {
+      const float v = z[i];
+      if (v > best || (v == best && i < bi)) { best = v; bi = i; }
+    }
   }
+  const uint32_t top2_key[2] = {order_key(best), order_key(second)};
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     const float ov = __shfl_xor_sync(0xffffffffu, best, o);
@@ -160,6 +213,133 @@ __global__ void __launch_bounds__(SP_THREADS) sample_kernel(const float* __restr
   }
   auto mass = [&](float v) -> u64 { return __float2ull_rz(expf((v - zmax) / temperature) * kMassOne); };
 
+  if (small_k) {
+    // ---- the gather threshold: the upper 16 bits of the k-th largest of the per-thread top-2
+    //      keys (radix selection, two 8-bit digits).  At least top_k tokens have a key at or
+    //      above it (a thread with fewer than two tokens holds -inf, whose key is below all others)
+    uint32_t prefix = 0u, pmask = 0u;
+    u64 remaining = (u64)top_k;
+    for (int shift = 24; shift >= 16; shift -= 8) {
+      for (int i = tid; i < 256; i += SP_THREADS) sh.hcnt[i] = 0u;
+      __syncthreads();
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const uint32_t key = top2_key[j];
+        const bool hit = (key & pmask) == prefix;
+        const unsigned hm = __ballot_sync(0xffffffffu, hit);
+        if (hit) {
+          const uint32_t bin = (key >> shift) & 255u;
+          const unsigned peers = __match_any_sync(hm, bin);
+          if (lane == __ffs(peers) - 1) atomicAdd(&sh.hcnt[bin], (unsigned)__popc(peers));
+        }
+      }
+      __syncthreads();
+      if (warp == 0) select_digit<false>(sh, remaining);
+      __syncthreads();
+      prefix |= sh.b32[0] << shift;
+      pmask |= 0xFFu << shift;
+      remaining -= sh.b64[0];
+      __syncthreads();
+    }
+    const uint32_t tau = prefix;
+    if (tid == 0) sh.ccount = 0u;
+    __syncthreads();
+    // ---- second pass (from L2): gather the tokens whose key is at least tau
+    row_pass4(z, V, [&](int i, float v, bool ok) {
+      const uint32_t key = order_key(v);
+      const bool take = ok && key >= tau;
+      const unsigned tm = __ballot_sync(0xffffffffu, take);
+      if (tm) {   // warp-uniform
+        unsigned slot0 = 0u;
+        if (lane == 0) slot0 = atomicAdd(&sh.ccount, (unsigned)__popc(tm));
+        slot0 = __shfl_sync(0xffffffffu, slot0, 0);
+        if (take) {
+          const unsigned slot = slot0 + __popc(tm & ((1u << lane) - 1u));
+          if (slot < (unsigned)SP_CAP) {
+            ckey[slot] = ((u64)key << 32) | (u64)(0xFFFFFFFFu - (uint32_t)i);
+            cz[slot] = v;
+          }
+        }
+      }
+    });
+    __syncthreads();
+    const unsigned gathered = sh.ccount;
+    if (gathered <= (unsigned)SP_CAP && gathered >= (unsigned)top_k) {
+      const int nc = (int)gathered;
+      int n2 = 1;
+      while (n2 < nc) n2 <<= 1;
+      for (int t = nc + tid; t < n2; t += SP_THREADS) ckey[t] = 0ull;   // sorts after every candidate
+      __syncthreads();
+      // bitonic sort, descending: larger key first, then lower id (its complement is larger)
+      for (int size = 2; size <= n2; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+          for (int t = tid; t < n2; t += SP_THREADS) {
+            const int o = t ^ stride;
+            if (o > t) {
+              const bool desc = (t & size) == 0;
+              const u64 a = ckey[t], c = ckey[o];
+              if (desc ? (a < c) : (a > c)) {
+                ckey[t] = c; ckey[o] = a;
+                const float fz = cz[t]; cz[t] = cz[o]; cz[o] = fz;
+              }
+            }
+          }
+          __syncthreads();
+        }
+      }
+      // the top-k set is the first top_k; masses in ranked order; the shortest prefix reaching
+      // top_p of the top-k mass
+      const int n = top_k;
+      const u64 mt = tid < n ? mass(cz[tid]) : 0ull;
+      u64 zk2;
+      const u64 excl = block_scan_excl(mt, sh, &zk2);
+      int n_p = n;
+      if (top_p < 1.f) {
+        u64 target = (u64)ceil((double)top_p * (double)zk2);
+        target = target < 1ull ? 1ull : (target > zk2 ? zk2 : target);
+        if (tid == 0) sh.bidx = n;
+        __syncthreads();
+        if (tid < n && excl < target && excl + mt >= target) sh.bidx = tid + 1;   // exactly one thread
+        __syncthreads();
+        n_p = sh.bidx;
+        __syncthreads();
+      }
+      // the draw: kept tokens in increasing id, first whose cumulative mass exceeds u * kept mass
+      const bool kept_t = tid < n_p;
+      const uint32_t id_t = kept_t ? 0xFFFFFFFFu - (uint32_t)(ckey[tid] & 0xFFFFFFFFull) : 0xFFFFFFFFu;
+      cmass[tid] = kept_t ? mt : 0ull;
+      int m2 = 1;
+      while (m2 < n_p) m2 <<= 1;
+      __syncthreads();
+      if (tid < m2) ckey[tid] = kept_t ? (((u64)id_t << 32) | (u64)tid) : ~0ull;   // (id, ranked slot)
+      __syncthreads();
+      for (int size = 2; size <= m2; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+          for (int t = tid; t < m2; t += SP_THREADS) {
+            const int o = t ^ stride;
+            if (o > t) {
+              const bool asc = (t & size) == 0;
+              const u64 a = ckey[t], c = ckey[o];
+              if (asc ? (a > c) : (a < c)) { ckey[t] = c; ckey[o] = a; }
+            }
+          }
+          __syncthreads();
+        }
+      }
+      const bool live = tid < n_p;
+      const u64 m_id = live ? cmass[(uint32_t)(ckey[tid] & 0xFFFFFFFFull)] : 0ull;
+      u64 zkept2;
+      const u64 ex2c = block_scan_excl(m_id, sh, &zkept2);
+      float uu = uniforms[row];
+      uu = (uu >= 0.f) ? fminf(uu, 0.99999994f) : 0.f;
+      u64 tg = (u64)floor((double)uu * (double)zkept2);
+      if (tg >= zkept2) tg = zkept2 - 1;
+      if (live && ex2c <= tg && tg < ex2c + m_id) tokens[row] = (int)(ckey[tid] >> 32);
+      return;
+    }
+    // more candidates than fit: the general path below
+  }
+
   // ---- top-k: the k-th largest key kk; ties at kk are kept up to id kcut
   uint32_t kk = 0u;
   int kcut = INT_MAX;
@@ -170,9 +350,24 @@ __global__ void __launch_bounds__(SP_THREADS) sample_kernel(const float* __restr
     for (int shift = 24; shift >= 0; shift -= 8) {
       for (int i = tid; i < 256; i += SP_THREADS) sh.hcnt[i] = 0u;
       __syncthreads();
-      for (int i = tid; i < V; i += SP_THREADS) {
-        const uint32_t key = order_key(z[i]);
-        if ((key & pmask) == prefix) atomicAdd(&sh.hcnt[(key >> shift) & 255u], 1u);
+      // warp-aggregated: lanes that hit the same bin add once (the top bins are crowded)
+      auto count = [&](int, float v, bool ok) {
+        const uint32_t key = order_key(v);
+        const bool hit = ok && (key & pmask) == prefix;
+        const unsigned hm = __ballot_sync(0xffffffffu, hit);
+        if (hit) {
+          const uint32_t bin = (key >> shift) & 255u;
+          const unsigned peers = __match_any_sync(hm, bin);
+          if (lane == __ffs(peers) - 1) atomicAdd(&sh.hcnt[bin], (unsigned)__popc(peers));
+        }
+      };
+      if (vec) {
+        row_pass4(z, V, count);
+      } else {
+        for (int base = warp * 32; base < V; base += SP_THREADS) {
+          const int i = base + lane;
+          count(i, i < V ? z[i] : 0.f, i < V);
+        }
       }
       __syncthreads();
       if (warp == 0) select_digit<false>(sh, remaining);
@@ -298,7 +493,16 @@ __global__ void embed_kernel(const T* __restrict__ table, int64_t V, int64_t d, 
 int launch_sample(const float* logits, int64_t B, int64_t V, int64_t ld, float temperature, int64_t top_k,
                   float top_p, const float* u, int* tokens, cudaStream_t st) {
   const int k = top_k <= 0 || top_k >= V ? 0 : (int)top_k;
-  sample_kernel<<<(unsigned)B, SP_THREADS, 0, st>>>(logits, ld, (int)V, temperature, k, top_p, u, tokens);
+  int dev = 0;
+  cudaGetDevice(&dev);
+  static bool attr_set[64] = {};
+  if (dev < 0 || dev >= 64) return -1;
+  if (!attr_set[dev]) {
+    if (cudaFuncSetAttribute(sample_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SP_DYN_SMEM) != cudaSuccess)
+      return -1;
+    attr_set[dev] = true;
+  }
+  sample_kernel<<<(unsigned)B, SP_THREADS, SP_DYN_SMEM, st>>>(logits, ld, (int)V, temperature, k, top_p, u, tokens);
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 

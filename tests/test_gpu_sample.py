@@ -122,6 +122,46 @@ def test_ties_at_the_top_k_and_top_p_cuts(k, p):
     _check(zh, 1.0, k, p, uh, got)
 
 
+@pytest.mark.parametrize("V", [5, 100, 1031, 2049, 4099, 50001])
+def test_small_top_k_over_small_and_masked_vocabularies(V):
+    """Top-k up to 1024 ranks a gathered candidate set: vocabularies below one token per thread
+    (threads holding no token), ragged rows (V % 4 != 0) and rows that are mostly -inf."""
+    import torch
+    rng = np.random.default_rng(V)
+    B = 8
+    zh = rng.normal(0, 2, (B, V))
+    zh[4:][rng.random((4, V)) < 0.97] = -np.inf                       # rows 4-7: mostly masked
+    zh[4:, 0] = rng.normal(0, 2, 4)
+    z = torch.from_numpy(zh.astype(np.float32)).cuda()
+    zh = to_f64(z)
+    for k in sorted({2, 3, 50, min(V - 1, 1024)}):
+        if k >= V or k < 2:
+            continue
+        u, uh = _uniforms(B, seed=k)
+        got = _run(z, 0.9, k, 0.97, u)
+        for b in range(B):
+            assert int(got[b]) in set(S.order_desc(zh[b])[:k].tolist())
+            assert np.isfinite(zh[b, got[b]])
+        _check(zh, 0.9, k, 0.97, uh, got)
+
+
+def test_small_top_k_when_the_gather_bound_holds_too_many_tokens():
+    """Equal logits: the gather bound admits the whole row, more than shared memory holds, and the
+    radix-selection path must take over with the same result (the lowest ids are kept)."""
+    import torch
+    B, V = 4, 128256
+    zh = np.zeros((B, V))
+    zh[1, 7::1000] = 0.5                                              # a few above an equal plateau
+    zh[2, :] = np.round(np.random.default_rng(8).normal(0, 0.3, V))
+    z = torch.from_numpy(zh.astype(np.float32)).cuda()
+    for k in (2, 700, 1024):
+        u, uh = _uniforms(B, seed=k + 5)
+        got = _run(z, 1.0, k, 1.0, u)
+        for b in range(B):
+            assert int(got[b]) in set(S.order_desc(zh[b])[:k].tolist())
+        _check(zh, 1.0, k, 1.0, uh, got)
+
+
 def test_masked_tokens_strided_rows_and_small_vocabularies():
     import torch
     rng = np.random.default_rng(2)
