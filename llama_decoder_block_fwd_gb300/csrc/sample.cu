@@ -36,8 +36,12 @@ __device__ __forceinline__ uint32_t order_key(float z) {
 
 constexpr int SP_SMALL_K = 1024;   // top-k up to this: ranked in shared memory
 constexpr int SP_CAP = 4096;       // candidates gathered into shared memory at most
-// dynamic shared memory of the small-k path: candidate keys, their logits, ranked masses
-constexpr size_t SP_DYN_SMEM = SP_CAP * 8 + SP_CAP * 4 + SP_SMALL_K * 8;
+constexpr int SP_BUCKETS = 256;    // top-p buckets of (z_max - z) / T, 1/8 wide: [0, 32) holds every nonzero mass
+// dynamic shared memory: candidate keys, their logits and ranked masses; the per-warp top-p
+// bucket mass histograms use the same bytes before any candidate is gathered
+constexpr size_t SP_CAND_SMEM = SP_CAP * 8 + SP_CAP * 4 + SP_SMALL_K * 8;
+constexpr size_t SP_BUCKET_SMEM = (size_t)SP_WARPS * SP_BUCKETS * 8;
+constexpr size_t SP_DYN_SMEM = SP_CAND_SMEM > SP_BUCKET_SMEM ? SP_CAND_SMEM : SP_BUCKET_SMEM;
 
 struct SampleShared {
   u64 hmass[256];
@@ -137,6 +141,39 @@ __device__ __forceinline__ void row_pass4(const float* __restrict__ z, int V, F&
     const int i = 4 * nv4 + lane;
     const bool ok = i < V;
     f(i, ok ? z[i] : 0.f, ok);
+  }
+}
+
+// row_pass4 on a 16-byte aligned row, else one element per thread and step (same contract).
+template <typename F>
+__device__ __forceinline__ void row_each(const float* __restrict__ z, int V, bool vec, F&& f) {
+  if (vec) {
+    row_pass4(z, V, f);
+  } else {
+    for (int base = (int)(threadIdx.x & ~31u); base < V; base += SP_THREADS) {
+      const int i = base + (int)(threadIdx.x & 31);
+      f(i, i < V ? z[i] : 0.f, i < V);
+    }
+  }
+}
+
+// Bitonic sort of ckey[0, n2) into descending order (n2 a power of two), cz moved alongside.
+__device__ void sort_desc(u64* ckey, float* cz, int n2) {
+  for (int size = 2; size <= n2; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int t = threadIdx.x; t < n2; t += SP_THREADS) {
+        const int o = t ^ stride;
+        if (o > t) {
+          const bool desc = (t & size) == 0;
+          const u64 a = ckey[t], c = ckey[o];
+          if (desc ? (a < c) : (a > c)) {
+            ckey[t] = c; ckey[o] = a;
+            const float fz = cz[t]; cz[t] = cz[o]; cz[o] = fz;
+          }
+        }
+      }
+      __syncthreads();
+    }
   }
 }
 
@@ -270,23 +307,7 @@ __global__ void __launch_bounds__(SP_THREADS) sample_kernel(const float* __restr
       while (n2 < nc) n2 <<= 1;
       for (int t = nc + tid; t < n2; t += SP_THREADS) ckey[t] = 0ull;   // sorts after every candidate
       __syncthreads();
-      // bitonic sort, descending: larger key first, then lower id (its complement is larger)
-      for (int size = 2; size <= n2; size <<= 1) {
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-          for (int t = tid; t < n2; t += SP_THREADS) {
-            const int o = t ^ stride;
-            if (o > t) {
-              const bool desc = (t & size) == 0;
-              const u64 a = ckey[t], c = ckey[o];
-              if (desc ? (a < c) : (a > c)) {
-                ckey[t] = c; ckey[o] = a;
-                const float fz = cz[t]; cz[t] = cz[o]; cz[o] = fz;
-              }
-            }
-          }
-          __syncthreads();
-        }
-      }
+      sort_desc(ckey, cz, n2);   // larger key first, then lower id (its complement is larger)
       // the top-k set is the first top_k; masses in ranked order; the shortest prefix reaching
       // top_p of the top-k mass
       const int n = top_k;
@@ -361,14 +382,7 @@ __global__ void __launch_bounds__(SP_THREADS) sample_kernel(const float* __restr
           if (lane == __ffs(peers) - 1) atomicAdd(&sh.hcnt[bin], (unsigned)__popc(peers));
         }
       };
-      if (vec) {
-        row_pass4(z, V, count);
-      } else {
-        for (int base = warp * 32; base < V; base += SP_THREADS) {
-          const int i = base + lane;
-          count(i, i < V ? z[i] : 0.f, i < V);
-        }
-      }
+      row_each(z, V, vec, count);
       __syncthreads();
       if (warp == 0) select_digit<false>(sh, remaining);
       __syncthreads();
@@ -386,86 +400,206 @@ __global__ void __launch_bounds__(SP_THREADS) sample_kernel(const float* __restr
   }
   auto in_k = [kk, kcut](int i, uint32_t key) { return key > kk || (key == kk && i <= kcut); };
 
-  // ---- mass of the top-k set
-  u64 part = 0;
-  for (int i = tid; i < V; i += SP_THREADS) {
-    const float v = z[i];
-    if (in_k(i, order_key(v))) part += mass(v);
-  }
-  u64 zk;
-  block_scan_excl(part, sh, &zk);
-
-  // ---- top-p: the kept set is key > kp, or key == kp up to id pcut
+  // ---- top-p: the kept set is key > kp, or key == kp up to id pcut (the shortest prefix of the
+  //      top-k ranking whose mass reaches ceil(p * top-k mass))
   uint32_t kp = kk;
   int pcut = kcut;
-  u64 zkept = zk;
   if (top_p < 1.f) {
+    // one pass: the top-k mass and, per bucket of d = (z_max - z) / T (1/8 wide; larger d, lower
+    // rank, so a bucket's members sit together in the ranking), its mass; per-warp copies in
+    // shared memory
+    u64* bmass = reinterpret_cast<u64*>(dyn);
+    for (int i = tid; i < SP_WARPS * SP_BUCKETS; i += SP_THREADS) bmass[i] = 0ull;
+    __syncthreads();
+    auto bucket_of = [&](float v) -> int {
+      const float d8 = (zmax - v) / temperature * 8.f;
+      return d8 < (float)SP_BUCKETS ? (int)d8 : -1;   // beyond: zero mass (or -inf)
+    };
+    u64 part = 0ull;
+    row_each(z, V, vec, [&](int i, float v, bool ok) {
+      if (!ok || !in_k(i, order_key(v))) return;
+      const u64 m = mass(v);
+      part += m;
+      const int bk = bucket_of(v);
+      if (bk >= 0 && m != 0ull) atomicAdd(&bmass[warp * SP_BUCKETS + bk], m);
+    });
+    __syncthreads();
+    for (int bk = tid; bk < SP_BUCKETS; bk += SP_THREADS) {   // digit 255 - bk: select_digit walks down
+      u64 m = 0ull;
+      for (int w = 0; w < SP_WARPS; ++w) m += bmass[w * SP_BUCKETS + bk];
+      sh.hmass[255 - bk] = m;
+    }
+    u64 zk;
+    block_scan_excl(part, sh, &zk);   // synchronises
     u64 target = (u64)ceil((double)top_p * (double)zk);
     target = target < 1ull ? 1ull : (target > zk ? zk : target);
-    uint32_t prefix = 0u, pmask = 0u;
-    u64 above = 0ull, bin_mass = 0ull;
-    unsigned bin_cnt = 0u;
-    for (int shift = 24; shift >= 0; shift -= 8) {
-      for (int i = tid; i < 256; i += SP_THREADS) { sh.hcnt[i] = 0u; sh.hmass[i] = 0ull; }
-      __syncthreads();
-      for (int i = tid; i < V; i += SP_THREADS) {
-        const float v = z[i];
-        const uint32_t key = order_key(v);
-        if (in_k(i, key) && (key & pmask) == prefix) {
-          const uint32_t dg = (key >> shift) & 255u;
-          atomicAdd(&sh.hmass[dg], mass(v));
-          atomicAdd(&sh.hcnt[dg], 1u);
+    if (warp == 0) select_digit<true>(sh, target);
+    __syncthreads();
+    const int bstar = 255 - (int)sh.b32[0];
+    const u64 above = sh.b64[0];                 // mass of the buckets before bstar
+    if (tid == 0) sh.ccount = 0u;
+    __syncthreads();
+    // gather bucket bstar (its zero-mass members too: they rank among it) into shared memory
+    u64* ckey = reinterpret_cast<u64*>(dyn);
+    float* cz = reinterpret_cast<float*>(dyn + SP_CAP * 8);
+    row_each(z, V, vec, [&](int i, float v, bool ok) {
+      const uint32_t key = order_key(v);
+      const bool take = ok && bucket_of(v) == bstar && in_k(i, key);
+      const unsigned tm = __ballot_sync(0xffffffffu, take);
+      if (tm) {
+        unsigned slot0 = 0u;
+        if (lane == 0) slot0 = atomicAdd(&sh.ccount, (unsigned)__popc(tm));
+        slot0 = __shfl_sync(0xffffffffu, slot0, 0);
+        if (take) {
+          const unsigned slot = slot0 + __popc(tm & ((1u << lane) - 1u));
+          if (slot < (unsigned)SP_CAP) {
+            ckey[slot] = ((u64)key << 32) | (u64)(0xFFFFFFFFu - (uint32_t)i);
+            cz[slot] = v;
+          }
         }
       }
+    });
+    __syncthreads();
+    const unsigned bcount = sh.ccount;
+    __syncthreads();
+    if (bcount <= (unsigned)SP_CAP) {
+      // rank bucket bstar and cut where the running mass reaches the target
+      const int nc = (int)bcount;
+      int n2 = 1;
+      while (n2 < nc) n2 <<= 1;
+      for (int t = nc + tid; t < n2; t += SP_THREADS) ckey[t] = 0ull;
       __syncthreads();
-      if (warp == 0) select_digit<true>(sh, target - above);
+      sort_desc(ckey, cz, n2);
+      // four ranked candidates per thread
+      u64 m4[4], loc = 0ull;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int j = 4 * tid + e;
+        m4[e] = j < nc ? mass(cz[j]) : 0ull;
+        loc += m4[e];
+      }
+      u64 bsum;
+      u64 run = above + block_scan_excl(loc, sh, &bsum);
+      if (tid == 0) sh.bidx = nc - 1;   // not reached only through rounding: keep the whole bucket
       __syncthreads();
-      prefix |= sh.b32[0] << shift;
-      pmask |= 0xFFu << shift;
-      above += sh.b64[0];
-      bin_cnt = sh.b32[1];
-      bin_mass = sh.b64[1];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int j = 4 * tid + e;
+        if (j < nc && run < target && run + m4[e] >= target) sh.bidx = j;   // exactly one candidate
+        run += m4[e];
+      }
       __syncthreads();
-    }
-    kp = prefix;
-    // every token at key kp has the same logit, hence the same mass
-    const u64 each = bin_mass / bin_cnt;
-    u64 need = (target - above + each - 1) / each;
-    if (need > bin_cnt) need = bin_cnt;
-    if (need < (u64)bin_cnt) {
-      const uint32_t pkey = kp;
-      pcut = nth_index(z, V, (int)need,
-                       [pkey, in_k](int i, float v) { const uint32_t k = order_key(v); return k == pkey && in_k(i, k); },
-                       sh);
+      const int jc = sh.bidx;
+      kp = (uint32_t)(ckey[jc] >> 32);
+      pcut = (int)(0xFFFFFFFFu - (uint32_t)(ckey[jc] & 0xFFFFFFFFull));
+      __syncthreads();
     } else {
-      pcut = kp == kk ? kcut : INT_MAX;
+      // a crowded bucket (many equal logits): radix selection on the key, by mass
+      uint32_t prefix = 0u, pmask = 0u;
+      u64 above_r = 0ull, bin_mass = 0ull;
+      unsigned bin_cnt = 0u;
+      for (int shift = 24; shift >= 0; shift -= 8) {
+        for (int i = tid; i < 256; i += SP_THREADS) { sh.hcnt[i] = 0u; sh.hmass[i] = 0ull; }
+        __syncthreads();
+        row_each(z, V, vec, [&](int i, float v, bool ok) {
+          const uint32_t key = order_key(v);
+          if (ok && in_k(i, key) && (key & pmask) == prefix) {
+            const uint32_t dg = (key >> shift) & 255u;
+            atomicAdd(&sh.hmass[dg], mass(v));
+            atomicAdd(&sh.hcnt[dg], 1u);
+          }
+        });
+        __syncthreads();
+        if (warp == 0) select_digit<true>(sh, target - above_r);
+        __syncthreads();
+        prefix |= sh.b32[0] << shift;
+        pmask |= 0xFFu << shift;
+        above_r += sh.b64[0];
+        bin_cnt = sh.b32[1];
+        bin_mass = sh.b64[1];
+        __syncthreads();
+      }
+      kp = prefix;
+      // every token at key kp has the same logit, hence the same mass
+      const u64 each = bin_mass / bin_cnt;
+      u64 need = (target - above_r + each - 1) / each;
+      if (need > bin_cnt) need = bin_cnt;
+      if (need < (u64)bin_cnt) {
+        const uint32_t pkey = kp;
+        pcut = nth_index(z, V, (int)need,
+                         [pkey, in_k](int i, float v) { const uint32_t k = order_key(v); return k == pkey && in_k(i, k); },
+                         sh);
+      } else {
+        pcut = kp == kk ? kcut : INT_MAX;
+      }
     }
-    zkept = above + need * each;
   }
 
-  // ---- the draw: first id (increasing) whose cumulative kept mass exceeds u * zkept
+  // ---- the draw: first id (increasing) whose cumulative kept mass exceeds u * (kept mass).
+  //      Warp w sums the kept mass of its contiguous stretch of the row (coalesced 16-byte
+  //      loads); the stretch holding the target is then scanned again by the whole block.
+  auto kept = [kp, pcut](int i, uint32_t key) { return key > kp || (key == kp && i <= pcut); };
+  const int nq = (V + 3) >> 2;
+  const int per_warp = (nq + SP_WARPS - 1) / SP_WARPS;
+  auto mass4 = [&](int q, u64 (&m)[4]) {
+    const int i0 = 4 * q;
+    float v[4];
+    if (vec && i0 + 4 <= V) {
+      const float4 w = __ldg(reinterpret_cast<const float4*>(z) + q);
+      v[0] = w.x; v[1] = w.y; v[2] = w.z; v[3] = w.w;
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) v[e] = i0 + e < V ? z[i0 + e] : -INFINITY;
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) m[e] = (i0 + e < V && kept(i0 + e, order_key(v[e]))) ? mass(v[e]) : 0ull;
+  };
+  {
+    u64 acc = 0ull;
+    const int qa = warp * per_warp, qb = min(nq, qa + per_warp);
+#pragma unroll 4
+    for (int q = qa + lane; q < qb; q += 32) {
+      u64 m[4];
+      mass4(q, m);
+      acc += m[0] + m[1] + m[2] + m[3];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) sh.wsum[warp] = acc;
+  }
+  __syncthreads();
+  u64 zkept = 0ull;
+  for (int w = 0; w < SP_WARPS; ++w) zkept += sh.wsum[w];
   float u = uniforms[row];
   u = (u >= 0.f) ? fminf(u, 0.99999994f) : 0.f;   // NaN and negatives -> 0, 1 -> largest float below 1
   u64 tgt = (u64)floor((double)u * (double)zkept);
   if (tgt >= zkept) tgt = zkept - 1;   // (double)zkept may round up
-  const int seg = (V + SP_THREADS - 1) / SP_THREADS;
-  const int lo = min(V, tid * seg), hi = min(V, lo + seg);
-  auto kept = [kp, pcut](int i, uint32_t key) { return key > kp || (key == kp && i <= pcut); };
-  u64 s = 0;
-  for (int i = lo; i < hi; ++i) {
-    const float v = z[i];
-    if (kept(i, order_key(v))) s += mass(v);
+  int wstar = SP_WARPS - 1;
+  u64 base = 0ull;
+  for (int w = 0; w < SP_WARPS; ++w) {
+    const u64 c = sh.wsum[w];
+    if (tgt < base + c) { wstar = w; break; }
+    base += c;
   }
-  u64 total;
-  const u64 before = block_scan_excl(s, sh, &total);
-  if (before <= tgt && tgt < before + s) {
-    u64 acc = before;
-    for (int i = lo; i < hi; ++i) {
-      const float v = z[i];
-      if (!kept(i, order_key(v))) continue;
-      acc += mass(v);
-      if (acc > tgt) { tokens[row] = i; break; }
+  __syncthreads();
+  const int qa = wstar * per_warp, qb = min(nq, qa + per_warp);
+  for (int c0 = qa; c0 < qb; c0 += SP_THREADS) {   // block-uniform trip count
+    const int q = c0 + tid;
+    u64 m[4] = {0ull, 0ull, 0ull, 0ull};
+    if (q < qb) mass4(q, m);
+    const u64 sq = m[0] + m[1] + m[2] + m[3];
+    u64 chunk;
+    const u64 ex = block_scan_excl(sq, sh, &chunk);
+    if (base + ex <= tgt && tgt < base + ex + sq) {
+      u64 a = base + ex;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        a += m[e];
+        if (a > tgt) { tokens[row] = 4 * q + e; break; }
+      }
     }
+    if (tgt < base + chunk) break;
+    base += chunk;
   }
 }
 

@@ -146,20 +146,37 @@ def test_small_top_k_over_small_and_masked_vocabularies(V):
 
 
 def test_small_top_k_when_the_gather_bound_holds_too_many_tokens():
-    """Equal logits: the gather bound admits the whole row, more than shared memory holds, and the
-    radix-selection path must take over with the same result (the lowest ids are kept)."""
+    """Equal logits: the gather bound (or the top-p bucket) admits more tokens than shared memory
+    holds, and the radix-selection path must take over with the same result (lowest ids kept)."""
     import torch
     B, V = 4, 128256
     zh = np.zeros((B, V))
     zh[1, 7::1000] = 0.5                                              # a few above an equal plateau
     zh[2, :] = np.round(np.random.default_rng(8).normal(0, 0.3, V))
     z = torch.from_numpy(zh.astype(np.float32)).cuda()
-    for k in (2, 700, 1024):
+    for k, p in ((2, 1.0), (700, 1.0), (1024, 1.0), (0, 0.5), (1500, 0.9)):
         u, uh = _uniforms(B, seed=k + 5)
-        got = _run(z, 1.0, k, 1.0, u)
+        got = _run(z, 1.0, k, p, u)
+        if k:
+            for b in range(B):
+                assert int(got[b]) in set(S.order_desc(zh[b])[:k].tolist())
+        _check(zh, 1.0, k, p, uh, got)
+
+
+@pytest.mark.parametrize("k,p", [(0, 0.9), (50, 0.95), (0, 1.0), (2000, 0.8)])
+def test_rows_not_16_byte_aligned(k, p):
+    """Row stride of 1001 floats: every other row starts off a 16-byte boundary (scalar loads)."""
+    import torch
+    B, V = 6, 1001
+    zh = np.random.default_rng(k + 17).normal(0, 2, (B, V))
+    z = torch.from_numpy(zh.astype(np.float32)).cuda()
+    zh = to_f64(z)
+    u, uh = _uniforms(B, seed=k + 3)
+    got = _run(z, 0.9, k, p, u)
+    if 0 < k < V:
         for b in range(B):
             assert int(got[b]) in set(S.order_desc(zh[b])[:k].tolist())
-        _check(zh, 1.0, k, 1.0, uh, got)
+    _check(zh, 0.9, k, p, uh, got)
 
 
 def test_masked_tokens_strided_rows_and_small_vocabularies():
