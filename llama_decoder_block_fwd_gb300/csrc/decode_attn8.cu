@@ -3,17 +3,19 @@
 // 8B ...", section 七 sizes the cache; section 九 has decode read all of it per token).
 //
 // Same work split as the bf16 kernel (decode_attn.cu): persistent CTAs take (sequence, KV head,
-// chunk of 128-key tiles) items, S^T = K Q^T and O^T += V^T P^T run on tcgen05 with the r query
-// heads of the group padded to N = 16, and each item leaves an unnormalised partial (m, l, O) for
-// the combine pass.  What differs:
-//   * TMA brings 128 keys x 128 codes (16 KB) per K or V tile into a 4-stage ring;
-//   * the codes are expanded to f16 (exact: every E4M3 value is an f16 value): K by four warps,
-//     one key row per thread, straight into tensor memory, where S^T = K Q^T reads its A operand;
-//     V by two warps into the 128-byte-swizzled shared-memory layout the P V MMA reads.  Both
-//     are double-buffered, so the expansion of tile j + 1 overlaps the MMAs of tile j;
-//   * the MMAs run in f16 (kind::f16 with f16 A and B): q is converted from bf16 in place when
-//     it lands, P is written as f16;
-//   * the K scale multiplies the scores, the V scale the partial O.
+// chunk of 128-key tiles) items, S^T = K Q^T and O^T += V^T P^T run on tcgen05, and each item
+// leaves an unnormalised partial (m, l, O) for the combine pass.  What differs:
+//   * the MMAs read the codes as TMA lands them (kind::f8f6f4, E4M3 A and B, K = 32 per
+//     instruction): 4 MMAs for S^T and 4 for O^T per 128-key tile, nothing expanded;
+//   * the other operand is E4M3 too, so q and P enter as hi + lo pairs: x = hi + lo with
+//     hi = e4m3(x) and lo = e4m3(x - hi), about 8 significant bits, in the N rows 0..r-1 (hi) and
+//     r..2r-1 (lo) of an operand padded to N = 16 (32 for r = 16).  An MMA with N = 16 costs as
+//     much to issue as one with N = 8, so the lo rows are free; the two column groups of S^T and
+//     O^T are summed when read;
+//   * q is scaled by a power of two per item so its largest magnitude lands in [128, 256) (E4M3
+//     saturates at 448); P is taken as exp2(s - m + 6) with a rescale threshold of 2, so it lies
+//     in [0, 256] and keeps ~8 bits down to 2^-7 of the maximum;
+//   * the K scale and the inverse q scale multiply the scores, the V scale the partial O.
 #include <algorithm>
 #include <cmath>
 #include <cstring>
@@ -25,17 +27,20 @@
 namespace llama {
 namespace {
 
-constexpr int D8_THREADS = 384;   // warp 0 TMA, 1 MMA, 2-5 softmax, 6-9 expand K, 10-11 expand V (+ q)
-constexpr int D8_STAGES = 4;
+constexpr int D8_THREADS = 224;   // warp 0 TMA, 1 MMA, 2-5 softmax, 6 q -> E4M3 hi/lo
+constexpr int D8_STAGES = 6;
 constexpr int D8_HD = 128;
-constexpr int D8_NPAD = 16;
-constexpr uint32_t D8_TMEM_COLS = 256;   // S^T 2 x 16, O^T 16, K (f16, A operand) 2 x 64
-constexpr float kD8RescaleLog2 = 8.0f;
+constexpr uint32_t D8_TMEM_COLS = 128;   // S^T 2 x NP (cols 0..63), O^T NP (cols 64..)
+// Lazy rescale: O and l keep the reference maximum until a tile's maximum exceeds it by 2 (log2
+// units), so P <= 4 before the 2^6 scale below and P * 2^6 <= 256 stays under E4M3's 448, while
+// P down to 2^-7 keeps ~8 significant bits as hi + lo (the scale cancels in O / l).
+constexpr float kD8RescaleLog2 = 2.0f;
+constexpr float kD8PScaleLog2 = 6.0f;
 
 struct __align__(64) DecodeAttn8Params {
-  CUtensorMap tmK;   // codes [B, kv_len, n_kv, hd] (bytes), box (128, 1, 128, 1)
+  CUtensorMap tmK;   // codes [B, kv_len, n_kv, hd] (bytes), box (128, 1, 128, 1), 128-byte swizzle
   CUtensorMap tmV;
-  CUtensorMap tmQ;   // bf16 [B, n_q, hd], box (64, r, 1)
+  const uint16_t* q;      // bf16 [B, n_q, hd]
   const float* k_scale;   // [n_kv]
   const float* v_scale;   // [n_kv]
   float* part_o;
@@ -46,26 +51,23 @@ struct __align__(64) DecodeAttn8Params {
 };
 
 struct D8Smem {
-  static constexpr uint32_t F8 = 128 * D8_HD;              // one code tile: 16 KB
-  static constexpr uint32_t H16 = 128 * D8_HD * 2;         // one f16 tile: 32 KB (two 64-column halves)
-  static constexpr uint32_t QB = D8_NPAD * D8_HD * 2;      // 4 KB
-  static constexpr uint32_t PB = D8_NPAD * 128 * 2;        // 4 KB
+  static constexpr uint32_t F8 = 128 * D8_HD;   // one code tile: 128 keys x 128 bytes = 16 KB
+  static constexpr uint32_t OPB = 32 * 128;     // q or P operand: up to 32 rows of 128 codes
   static constexpr uint32_t OFF_K8 = 0;
   static constexpr uint32_t OFF_V8 = OFF_K8 + D8_STAGES * F8;
-  static constexpr uint32_t OFF_V16 = OFF_V8 + D8_STAGES * F8;    // 2 buffers
-  static constexpr uint32_t OFF_Q = OFF_V16 + 2 * H16;            // 2 buffers
-  static constexpr uint32_t OFF_P = OFF_Q + 2 * QB;         // 2 buffers
-  static constexpr uint32_t OFF_RED = OFF_P + 2 * PB;       // [3][4][16] floats
-  static constexpr uint32_t OFF_BAR = OFF_RED + 3 * 4 * 16 * 4;
+  static constexpr uint32_t OFF_Q = OFF_V8 + D8_STAGES * F8;   // 2 buffers
+  static constexpr uint32_t OFF_P = OFF_Q + 2 * OPB;           // 2 buffers
+  static constexpr uint32_t OFF_RED = OFF_P + 2 * OPB;         // [3][4][16] floats
+  static constexpr uint32_t OFF_QS = OFF_RED + 3 * 4 * 16 * 4; // inverse q scale per q buffer
+  static constexpr uint32_t OFF_BAR = OFF_QS + 16;
   static constexpr uint32_t TOTAL = OFF_BAR + 512 + 1024;
 };
 static_assert(D8Smem::TOTAL <= 232448, "shared memory");
 
 // barrier slots
 enum : int {
-  B_K8F = 0, B_V8F = 4, B_K8E = 8, B_V8E = 12, B_K16F = 16, B_K16E = 18, B_V16F = 20, B_V16E = 22,
-  B_QF = 24, B_QR = 26, B_QE = 28, B_SF = 30, B_SFREE = 32, B_PF = 34, B_OD = 36, B_OFREE = 38, B_DRAIN = 39,
-  B_COUNT = 40
+  B_K8F = 0, B_V8F = 6, B_K8E = 12, B_V8E = 18, B_QR = 24, B_QE = 26, B_SF = 28, B_SFREE = 30, B_PF = 32,
+  B_OD = 34, B_OFREE = 36, B_DRAIN = 37, B_QC = 38, B_COUNT = 40
 };
 
 __device__ __forceinline__ void tma_load_4d_d8(uint32_t dst, const CUtensorMap* m, uint64_t* bar, int x, int y,
@@ -90,37 +92,45 @@ __device__ __forceinline__ float warp_max_f32_d8(float v) {
   return r;
 }
 
-// f16 instruction descriptor: D f32, A and B f16 (format 0), K-major unless stated.
-__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool b_mn_major = false, bool a_mn_major = false) {
-  return (1u << 4) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
-         ((uint32_t)(M >> 4) << 24);
+// Instruction descriptor for kind::f8f6f4 with E4M3 A and B (format 0) and an fp32 accumulator;
+// K-major unless stated.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N, bool a_mn_major = false) {
+  return (1u << 4) | ((a_mn_major ? 1u : 0u) << 15) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+// D[tmem] (+)= A[smem] * B[smem]^T on 8-bit operands (K = 32 per instruction), one thread.
+__device__ __forceinline__ void tc_mma_f8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
 }
 
-// Four E4M3 codes (one 32-bit word, lowest byte first) to four f16 values (two 32-bit words).
-__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
-      : "=r"(lo), "=r"(hi)
-      : "r"(w));
+// Two floats to two E4M3 codes (round to nearest even, saturating): a in the low byte.
+__device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
+  uint16_t c;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(c) : "f"(b), "f"(a));
+  return c;
+}
+// Two E4M3 codes (low byte first) back to floats.
+__device__ __forceinline__ float2 e4m3x2_to_f2(uint32_t c) {
+  uint32_t h;
+  asm("{\n\t.reg .b16 a;\n\tcvt.u16.u32 a, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, a;\n\t}" : "=r"(h) : "r"(c));
+  return __half22float2(*reinterpret_cast<const __half2*>(&h));
+}
+// x = hi + lo in E4M3 (both codes of each pair in one byte, a first): returns hi codes, sets lo codes.
+__device__ __forceinline__ uint32_t split_e4m3x2(float a, float b, uint32_t& lo) {
+  const uint32_t hi = e4m3x2(a, b);
+  const float2 h = e4m3x2_to_f2(hi);
+  lo = e4m3x2(a - h.x, b - h.y);
+  return hi;
 }
 
-// Expand one 128 x 128 code tile (TMA 128-byte swizzle: the 16-byte chunk c of key row k sits at
-// chunk c ^ (k & 7)) into the f16 operand layout (two 64-column halves, same swizzle), with the
-// 64 threads of the two V warps.
-__device__ __forceinline__ void expand_tile(const uint8_t* src, uint8_t* dst, int t64) {
-#pragma unroll 4
-  for (int u = t64; u < 1024; u += 64) {
-    const int k = u >> 3, c = u & 7, sw = k & 7;
-    const uint4 w = *reinterpret_cast<const uint4*>(src + k * 128 + ((c ^ sw) << 4));
-    uint4 a, b;
-    e4m3x4_to_f16x4(w.x, a.x, a.y);
-    e4m3x4_to_f16x4(w.y, a.z, a.w);
-    e4m3x4_to_f16x4(w.z, b.x, b.y);
-    e4m3x4_to_f16x4(w.w, b.z, b.w);
-    uint8_t* row = dst + (c >> 2) * 16384 + k * 128;
-    const int c0 = 2 * (c & 3);
-    *reinterpret_cast<uint4*>(row + ((c0 ^ sw) << 4)) = a;
-    *reinterpret_cast<uint4*>(row + (((c0 + 1) ^ sw) << 4)) = b;
-  }
+// Byte offset of (row n, byte c) in a K-major operand of 128-byte rows with the 128-byte swizzle.
+__device__ __forceinline__ uint32_t sw128_off(int n, int c) {
+  return (uint32_t)(n * 128 + ((((c >> 4) ^ (n & 7))) << 4) + (c & 15));
 }
 
 __device__ __forceinline__ void item_coords8(const DecodeAttn8Params& p, int item, int& b, int& g, int& t_begin,
@@ -136,22 +146,23 @@ __device__ __forceinline__ void item_coords8(const DecodeAttn8Params& p, int ite
 template <int R>
 __global__ void __launch_bounds__(D8_THREADS, 1) decode_attn8_kernel(const __grid_constant__ DecodeAttn8Params p) {
   using L = D8Smem;
+  constexpr int NP = R <= 8 ? 16 : 32;   // operand rows: hi 0..R-1, lo R..2R-1, zero padding
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::OFF_BAR);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + B_COUNT);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* red = reinterpret_cast<float*>(smem + L::OFF_RED);
+  float* qinv = reinterpret_cast<float*>(smem + L::OFF_QS);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_trigger();
   if (threadIdx.x == 0) {
     for (int i = 0; i < B_COUNT; ++i) {
       int cnt = 1;
-      if ((i >= B_V8E && i < B_V8E + D8_STAGES) || i == B_V16F || i == B_V16F + 1 || i == B_QR || i == B_QR + 1)
-        cnt = 64;
-      if ((i >= B_K8E && i < B_K8E + D8_STAGES) || i == B_K16F || i == B_K16F + 1 || i == B_SFREE ||
-          i == B_SFREE + 1 || i == B_PF || i == B_PF + 1 || i == B_OFREE)
+      if (i == B_QR || i == B_QR + 1) cnt = 32;
+      if (i == B_SFREE || i == B_SFREE + 1 || i == B_PF || i == B_PF + 1 || i == B_OFREE || i == B_QC ||
+          i == B_QC + 1)
         cnt = 128;
       mbar_init(&bars[i], cnt);
     }
@@ -159,10 +170,9 @@ __global__ void __launch_bounds__(D8_THREADS, 1) decode_attn8_kernel(const __gri
     fence_mbar_init();
     tma_prefetch_desc(&p.tmK);
     tma_prefetch_desc(&p.tmV);
-    tma_prefetch_desc(&p.tmQ);
   }
-  // Q operand rows r..15 and the padded P^T rows stay zero for the whole kernel.
-  for (int i = threadIdx.x; i < (int)(2 * L::QB + 2 * L::PB) / 16; i += D8_THREADS)
+  // the padding rows (2R..NP-1) of the q and P operands stay zero for the whole kernel
+  for (int i = threadIdx.x; i < (int)(4 * L::OPB) / 16; i += D8_THREADS)
     reinterpret_cast<uint4*>(smem + L::OFF_Q)[i] = make_uint4(0, 0, 0, 0);
   fence_proxy_async_smem();
   if (warp == 1) { tmem_alloc(tmem_slot, D8_TMEM_COLS); tmem_relinquish(); }
@@ -170,24 +180,18 @@ __global__ void __launch_bounds__(D8_THREADS, 1) decode_attn8_kernel(const __gri
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem;          // S^T buffers: columns 0..15 and 16..31
-  const uint32_t tO = tmem + 32;     // O^T: columns 32..47
-  const uint32_t tK = tmem + 64;     // K tiles (f16 pairs): columns 64..127 and 128..191
+  const uint32_t tS = tmem;          // S^T buffers: columns 0..NP-1 and NP..2NP-1
+  const uint32_t tO = tmem + 64;     // O^T: columns 64..64+NP-1
   const uint32_t sbase = smem_u32(smem);
 
   pdl_wait();
   if (warp == 0) {
     if (lane == 0) {  // ---------------------------------------------------- TMA producer
-      int tile = 0, it = 0;
+      int tile = 0;
       bool ok = true;
-      for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x, ++it) {
+      for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
         int b, g, t0, t1, chunk;
         item_coords8(p, item, b, g, t0, t1, chunk);
-        const int qb = it & 1;
-        if (!mbar_wait(&bars[B_QE + qb], ((it >> 1) & 1) ^ 1, abort_flag, p.status)) break;
-        mbar_arrive_expect_tx(&bars[B_QF + qb], 2 * 64 * p.r * 2);
-        for (int hh = 0; hh < 2; ++hh)
-          tma_load_3d(sbase + L::OFF_Q + qb * L::QB + hh * (L::QB / 2), &p.tmQ, &bars[B_QF + qb], hh * 64, g * p.r, b);
         for (int t = t0; t < t1; ++t, ++tile) {
           const int st = tile % D8_STAGES;
           const uint32_t ph = (tile / D8_STAGES) & 1;
@@ -202,9 +206,8 @@ __global__ void __launch_bounds__(D8_THREADS, 1) decode_attn8_kernel(const __gri
     }
   } else if (warp == 1) {
     if (lane == 0) {  // ---------------------------------------------------- MMA issuer
-      const uint32_t idesc_s = idesc_f16(128, D8_NPAD);
-      const uint32_t idesc_o = idesc_f16(128, D8_NPAD, /*b_mn_major=*/false, /*a_mn_major=*/true);
-      const uint32_t va0 = sbase + L::OFF_V16;
+      const uint32_t idesc_s = idesc_e4m3(128, NP);
+      const uint32_t idesc_o = idesc_e4m3(128, NP, /*a_mn_major=*/true);
       int tile = 0, it = 0;
       bool ok = true;
       for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x, ++it) {
@@ -213,40 +216,38 @@ __global__ void __launch_bounds__(D8_THREADS, 1) decode_attn8_kernel(const __gri
         const int qb = it & 1;
         if (!mbar_wait(&bars[B_QR + qb], (it >> 1) & 1, abort_flag, p.status)) break;
         tc_fence_after();
-        const uint32_t qa = sbase + L::OFF_Q + qb * L::QB;
+        const uint64_t qd0 = sdesc_sw128(sbase + L::OFF_Q + qb * L::OPB, 16, 1024);
         const int n = t1 - t0;
         auto issue_s = [&](int j) -> bool {
           const int gt = tile + j;
-          const int sb = gt & 1;
-          if (!mbar_wait(&bars[B_K16F + sb], (gt >> 1) & 1, abort_flag, p.status)) return false;
+          const int st = gt % D8_STAGES, sb = gt & 1;
+          if (!mbar_wait(&bars[B_K8F + st], (gt / D8_STAGES) & 1, abort_flag, p.status)) return false;
           if (!mbar_wait(&bars[B_SFREE + sb], ((gt >> 1) & 1) ^ 1, abort_flag, p.status)) return false;
           tc_fence_after();
-          const uint64_t bd0 = sdesc_sw128(qa, 16, 1024);
+          const uint64_t kd0 = sdesc_sw128(sbase + L::OFF_K8 + st * L::F8, 16, 1024);
 #pragma unroll
-          for (int k = 0; k < D8_HD / 16; ++k)   // A = K from tensor memory, 16 hd per step
-            tc_mma_ts(tS + sb * 16, tK + sb * 64 + k * 8,
-                      bd0 + (uint64_t)(((k >> 2) * (L::QB / 2) + (k & 3) * 32) >> 4), idesc_s, k > 0 ? 1u : 0u);
+          for (int k = 0; k < D8_HD / 32; ++k)   // 32 hd (bytes) per step
+            tc_mma_f8(tS + sb * NP, kd0 + (uint64_t)(2 * k), qd0 + (uint64_t)(2 * k), idesc_s, k > 0 ? 1u : 0u);
           tc_commit(&bars[B_SF + sb]);
-          tc_commit(&bars[B_K16E + sb]);
+          tc_commit(&bars[B_K8E + st]);
           return true;
         };
         auto issue_pv = [&](int j) -> bool {
           const int gt = tile + j;
-          const int pb = gt & 1;
+          const int st = gt % D8_STAGES, pb = gt & 1;
           if (!mbar_wait(&bars[B_PF + pb], (gt >> 1) & 1, abort_flag, p.status)) return false;
-          if (!mbar_wait(&bars[B_V16F + pb], (gt >> 1) & 1, abort_flag, p.status)) return false;
-          const uint32_t va = va0 + pb * L::H16;
+          if (!mbar_wait(&bars[B_V8F + st], (gt / D8_STAGES) & 1, abort_flag, p.status)) return false;
           if (j == 0 && !mbar_wait(&bars[B_OFREE], (it & 1) ^ 1, abort_flag, p.status)) return false;
           tc_fence_after();
-          const uint32_t pa = sbase + L::OFF_P + pb * L::PB;
-          const uint64_t ad0 = sdesc_sw128(va, 16384, 1024);   // V^T, MN-major
-          const uint64_t bd0 = sdesc_sw128(pa, 16, 1024);
+          // V^T: M = hd runs along each 128-byte key row (MN-major), 8-key groups 1024 bytes apart
+          const uint64_t vd0 = sdesc_sw128(sbase + L::OFF_V8 + st * L::F8, 16384, 1024);
+          const uint64_t pd0 = sdesc_sw128(sbase + L::OFF_P + pb * L::OPB, 16, 1024);
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            tc_mma(tO, ad0 + (uint64_t)(k * 2048 >> 4), bd0 + (uint64_t)(((k >> 2) * (L::PB / 2) + (k & 3) * 32) >> 4),
-                   idesc_o, (j > 0 || k > 0) ? 1u : 0u);
+          for (int k = 0; k < 4; ++k)   // 32 keys per step
+            tc_mma_f8(tO, vd0 + (uint64_t)(k * 4096 >> 4), pd0 + (uint64_t)(2 * k), idesc_o,
+                      (j > 0 || k > 0) ? 1u : 0u);
           tc_commit(&bars[B_OD + pb]);
-          tc_commit(&bars[B_V16E + pb]);
+          tc_commit(&bars[B_V8E + st]);
           return true;
         };
         for (int j = 0; j < n; ++j) {
@@ -262,89 +263,71 @@ __global__ void __launch_bounds__(D8_THREADS, 1) decode_attn8_kernel(const __gri
       tc_commit(&bars[B_DRAIN]);
       mbar_wait(&bars[B_DRAIN], 0, &no_abort, p.status);
     }
-  } else if (warp >= 6 && warp < 10) {  // -------------------------------- K codes -> f16 in TMEM
-    const int key = (warp & 3) * 32 + lane;          // this thread's TMEM lane = key row of the tile
-    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    int tile = 0;
-    bool ok = true;
-    for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
+  } else if (warp == 6) {  // ------------------------------------------- q -> E4M3 hi / lo operand
+    constexpr int NCH = R * D8_HD / 8;          // 8-element chunks of the group's q rows
+    constexpr int PER = (NCH + 31) / 32;
+    int it = 0;
+    for (int item = blockIdx.x; item < p.n_items; item += gridDim.x, ++it) {
       int b, g, t0, t1, chunk;
       item_coords8(p, item, b, g, t0, t1, chunk);
-      for (int tt = t0; tt < t1; ++tt, ++tile) {
-        const int st = tile % D8_STAGES;
-        const int hb = tile & 1;
-        if (!mbar_wait(&bars[B_K8F + st], (tile / D8_STAGES) & 1, abort_flag, p.status)) { ok = false; break; }
-        if (!mbar_wait(&bars[B_K16E + hb], ((tile >> 1) & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
-        tc_fence_after();
-        const uint8_t* row = smem + L::OFF_K8 + st * L::F8 + key * 128;
-        const int sw = key & 7;
+      const int qb = it & 1;
+      // the buffer is free once the MMAs of item it - 2 have read it and the softmax warps its scale
+      if (!mbar_wait(&bars[B_QE + qb], ((it >> 1) & 1) ^ 1, abort_flag, p.status)) break;
+      if (!mbar_wait(&bars[B_QC + qb], ((it >> 1) & 1) ^ 1, abort_flag, p.status)) break;
+      const uint4* src = reinterpret_cast<const uint4*>(p.q + ((int64_t)b * p.n_q + (int64_t)g * R) * D8_HD);
+      uint4 w[PER];
+      float amax = 0.f;
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t w[32];
+      for (int j = 0; j < PER; ++j) {
+        const int c = lane + 32 * j;
+        w[j] = c < NCH ? src[c] : make_uint4(0, 0, 0, 0);
+        const uint32_t e[4] = {w[j].x, w[j].y, w[j].z, w[j].w};
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
-            const int c = half * 4 + cc;
-            const uint4 v = *reinterpret_cast<const uint4*>(row + ((c ^ sw) << 4));
-            e4m3x4_to_f16x4(v.x, w[cc * 8 + 0], w[cc * 8 + 1]);
-            e4m3x4_to_f16x4(v.y, w[cc * 8 + 2], w[cc * 8 + 3]);
-            e4m3x4_to_f16x4(v.z, w[cc * 8 + 4], w[cc * 8 + 5]);
-            e4m3x4_to_f16x4(v.w, w[cc * 8 + 6], w[cc * 8 + 7]);
-          }
-          tmem_st32(tK + hb * 64 + half * 32 + lane_off, w);
+        for (int k = 0; k < 4; ++k)
+          amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(e[k] << 16)), fabsf(__uint_as_float(e[k] & 0xFFFF0000u))));
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      // power-of-two scale: amax * qs in [128, 256)
+      int ex = 0;
+      frexpf(amax, &ex);
+      ex = amax > 0.f ? min(max(ex, -100), 100) : 0;
+      const float qs = ldexpf(1.f, 8 - ex);
+      uint8_t* qop = smem + L::OFF_Q + qb * L::OPB;
+#pragma unroll
+      for (int j = 0; j < PER; ++j) {
+        const int c = lane + 32 * j;
+        if (c < NCH) {
+          const int h = c / (D8_HD / 8), d = (c % (D8_HD / 8)) * 8;
+          const uint32_t e[4] = {w[j].x, w[j].y, w[j].z, w[j].w};
+          uint32_t hi[4], lo[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            hi[k] = split_e4m3x2(__uint_as_float(e[k] << 16) * qs, __uint_as_float(e[k] & 0xFFFF0000u) * qs, lo[k]);
+          *reinterpret_cast<uint2*>(qop + sw128_off(h, d)) =
+              make_uint2(hi[0] | (hi[1] << 16), hi[2] | (hi[3] << 16));
+          *reinterpret_cast<uint2*>(qop + sw128_off(R + h, d)) =
+              make_uint2(lo[0] | (lo[1] << 16), lo[2] | (lo[3] << 16));
         }
-        tc_wait_st();
-        tc_fence_before();
-        mbar_arrive(&bars[B_K16F + hb]);
-        mbar_arrive(&bars[B_K8E + st]);
       }
+      if (lane == 0) qinv[qb] = 1.f / qs;
+      fence_proxy_async_smem();
+      __syncwarp();
+      mbar_arrive(&bars[B_QR + qb]);
     }
-  } else if (warp >= 10) {  // ------------------------------------ V codes -> f16 in shared memory; q
-    const int t64 = (warp & 1) * 32 + lane;
-    int tile = 0, it = 0;
-    bool ok = true;
-    for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x, ++it) {
-      int b, g, t0, t1, chunk;
-      item_coords8(p, item, b, g, t0, t1, chunk);
-      {   // q: bf16 -> f16 in place (same 2-byte layout)
-        const int qb = it & 1;
-        if (!mbar_wait(&bars[B_QF + qb], (it >> 1) & 1, abort_flag, p.status)) break;
-        uint4* q = reinterpret_cast<uint4*>(smem + L::OFF_Q + qb * L::QB);
-        for (int i = t64; i < (int)(L::QB / 16); i += 64) {
-          uint4 w = q[i];
-          uint32_t* e = reinterpret_cast<uint32_t*>(&w);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float lo = __uint_as_float(e[j] << 16), hi = __uint_as_float(e[j] & 0xFFFF0000u);
-            const __half2 h = __floats2half2_rn(lo, hi);
-            e[j] = *reinterpret_cast<const uint32_t*>(&h);
-          }
-          q[i] = w;
-        }
-        fence_proxy_async_smem();
-        mbar_arrive(&bars[B_QR + qb]);
-      }
-      for (int tt = t0; tt < t1; ++tt, ++tile) {
-        const int st = tile % D8_STAGES;
-        const int hb = tile & 1;
-        if (!mbar_wait(&bars[B_V8F + st], (tile / D8_STAGES) & 1, abort_flag, p.status)) { ok = false; break; }
-        if (!mbar_wait(&bars[B_V16E + hb], ((tile >> 1) & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
-        expand_tile(smem + L::OFF_V8 + st * L::F8, smem + L::OFF_V16 + hb * L::H16, t64);
-        fence_proxy_async_smem();
-        mbar_arrive(&bars[B_V16F + hb]);
-        mbar_arrive(&bars[B_V8E + st]);
-      }
-    }
-  } else {  // ------------------------------------------------------------ softmax warps 2..5
-    const int qw = warp & 3;
+  } else if (warp >= 2 && warp < 6) {  // ------------------------------------ softmax warps 2..5
+    const int qw = warp & 3;   // a warp reaches TMEM lanes 32 * (warp % 4) ..
     const int t = qw * 32 + lane;
     const uint32_t lane_off = (uint32_t)(qw * 32) << 16;
-    constexpr int r = R;
     int tile = 0, it = 0;
     bool ok = true;
     for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x, ++it) {
       int b, g, t0, t1, chunk;
       item_coords8(p, item, b, g, t0, t1, chunk);
-      const float sc = p.scale_log2 * p.k_scale[g];
+      const int qb = it & 1;
+      if (!mbar_wait(&bars[B_QR + qb], (it >> 1) & 1, abort_flag, p.status)) break;
+      const float sc = p.scale_log2 * p.k_scale[g] * qinv[qb];
+      mbar_arrive(&bars[B_QC + qb]);
       float m_ref[R], lsum[R];
 #pragma unroll
       for (int h = 0; h < R; ++h) { m_ref[h] = -INFINITY; lsum[h] = 0.f; }
@@ -352,15 +335,16 @@ __global__ void __launch_bounds__(D8_THREADS, 1) decode_attn8_kernel(const __gri
         const int sb = tile & 1;
         if (!mbar_wait(&bars[B_SF + sb], (tile >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
         tc_fence_after();
-        uint32_t sv[16];
-        tmem_ld16_d8(tS + sb * 16 + lane_off, sv);
+        uint32_t sv[NP];
+#pragma unroll
+        for (int c = 0; c < NP / 16; ++c) tmem_ld16_d8(tS + sb * NP + c * 16 + lane_off, *reinterpret_cast<uint32_t(*)[16]>(sv + 16 * c));
         tc_wait_ld();
         tc_fence_before();
         mbar_arrive(&bars[B_SFREE + sb]);
         const bool valid = tt * 128 + t < p.kv_len;
         float s[R];
 #pragma unroll
-        for (int h = 0; h < R; ++h) s[h] = valid ? __uint_as_float(sv[h]) * sc : -INFINITY;
+        for (int h = 0; h < R; ++h) s[h] = valid ? (__uint_as_float(sv[h]) + __uint_as_float(sv[R + h])) * sc : -INFINITY;
         float* rbuf = red + (tile & 1) * 64;
 #pragma unroll
         for (int h = 0; h < R; ++h) {
@@ -389,25 +373,33 @@ __global__ void __launch_bounds__(D8_THREADS, 1) decode_attn8_kernel(const __gri
         if (resc) {
           if (!mbar_wait(&bars[B_OD + ((tile - 1) & 1)], ((tile - 1) >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
           tc_fence_after();
-          uint32_t ov[16];
-          tmem_ld16_d8(tO + lane_off, ov);
-          tc_wait_ld();
 #pragma unroll
-          for (int h = 0; h < R; ++h) ov[h] = __float_as_uint(__uint_as_float(ov[h]) * alpha[h]);
-          tmem_st16(tO + lane_off, ov);
+          for (int c = 0; c < NP / 16; ++c) {
+            uint32_t ov[16];
+            tmem_ld16_d8(tO + c * 16 + lane_off, ov);
+            tc_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              const int col = c * 16 + k;
+              if (col < 2 * R) ov[k] = __float_as_uint(__uint_as_float(ov[k]) * alpha[col % R]);
+            }
+            tmem_st16(tO + c * 16 + lane_off, ov);
+          }
           tc_wait_st();
 #pragma unroll
           for (int h = 0; h < R; ++h) lsum[h] *= alpha[h];
         }
-        uint8_t* pbase = smem + L::OFF_P + pb * L::PB + (t >> 6) * (L::PB / 2);
-        const int kin = t & 63;
+        // P^T rows: h (hi) and R + h (lo), this thread's key in byte t of each row
+        uint8_t* pbase = smem + L::OFF_P + pb * L::OPB;
 #pragma unroll
         for (int h = 0; h < R; ++h) {
-          const float pv = exp2f(s[h] - m_ref[h]);
-          const __half pq = __float2half_rn(pv);
-          lsum[h] += pv;
-          const int chunk16 = (kin >> 3) ^ (h & 7);
-          *reinterpret_cast<__half*>(pbase + h * 128 + chunk16 * 16 + (kin & 7) * 2) = pq;
+          const float pv = exp2f(s[h] - (m_ref[h] - kD8PScaleLog2));
+          uint32_t lo;
+          const uint32_t hi = split_e4m3x2(pv, 0.f, lo);
+          const float2 hf = e4m3x2_to_f2(hi), lf = e4m3x2_to_f2(lo);
+          lsum[h] += hf.x + lf.x;   // the weights the MMA applies
+          pbase[sw128_off(h, t)] = (uint8_t)(hi & 0xFFu);
+          pbase[sw128_off(R + h, t)] = (uint8_t)(lo & 0xFFu);
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -416,15 +408,17 @@ __global__ void __launch_bounds__(D8_THREADS, 1) decode_attn8_kernel(const __gri
       if (!ok) break;
       if (!mbar_wait(&bars[B_OD + ((tile - 1) & 1)], ((tile - 1) >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
       tc_fence_after();
-      uint32_t ov[16];
-      tmem_ld16_d8(tO + lane_off, ov);
+      uint32_t ov[NP];
+#pragma unroll
+      for (int c = 0; c < NP / 16; ++c) tmem_ld16_d8(tO + c * 16 + lane_off, *reinterpret_cast<uint32_t(*)[16]>(ov + 16 * c));
       tc_wait_ld();
       tc_fence_before();
       mbar_arrive(&bars[B_OFREE]);
       const float vs = p.v_scale[g];
-      const int64_t base = ((int64_t)b * p.n_chunks + chunk) * p.n_q + (int64_t)g * r;
+      const int64_t base = ((int64_t)b * p.n_chunks + chunk) * p.n_q + (int64_t)g * R;
 #pragma unroll
-      for (int h = 0; h < R; ++h) p.part_o[(base + h) * D8_HD + t] = __uint_as_float(ov[h]) * vs;
+      for (int h = 0; h < R; ++h)
+        p.part_o[(base + h) * D8_HD + t] = (__uint_as_float(ov[h]) + __uint_as_float(ov[R + h])) * vs;
       float* lbuf = red + 128;
 #pragma unroll
       for (int h = 0; h < R; ++h) {
@@ -434,7 +428,7 @@ __global__ void __launch_bounds__(D8_THREADS, 1) decode_attn8_kernel(const __gri
         if (lane == h) lbuf[qw * 16 + h] = v;
       }
       softmax_sync8();
-      if (t < r) {
+      if (t < R) {
         const float l = lbuf[t] + lbuf[16 + t] + lbuf[32 + t] + lbuf[48 + t];
         float mm = -INFINITY;
 #pragma unroll
@@ -526,9 +520,7 @@ int launch_decode_attn8(const AttnDesc& a, void* ws, int num_sms, unsigned* stat
   const uint32_t box[4] = {128, 1, 128, 1};
   if (!encode_tmap_4d_u8(&p.tmK, a.k, dims, strides, box)) return -1;
   if (!encode_tmap_4d_u8(&p.tmV, a.v, dims, strides, box)) return -1;
-  if (!encode_tmap_3d_bf16(&p.tmQ, a.q, D8_HD, (uint64_t)a.n_q, (uint64_t)a.B, D8_HD * 2,
-                           (uint64_t)a.n_q * D8_HD * 2, 64, (uint32_t)r, 1))
-    return -1;
+  p.q = static_cast<const uint16_t*>(a.q);
   const size_t o_bytes = (((size_t)a.B * n_chunks * a.n_q * D8_HD * 4) + 255) & ~size_t(255);
   p.k_scale = a.k_scale;
   p.v_scale = a.v_scale;
