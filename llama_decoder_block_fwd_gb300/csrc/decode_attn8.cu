@@ -28,7 +28,10 @@ namespace llama {
 namespace {
 
 constexpr int D8_THREADS = 224;   // warp 0 TMA, 1 MMA, 2-5 softmax, 6 q -> E4M3 hi/lo
-constexpr int D8_STAGES = 6;
+// TMA rings: a V tile stays resident until P V has read it (after the scores and the softmax of
+// its tile), a K tile only until S^T has, so V gets the deeper ring
+constexpr int D8_KSTAGES = 6;
+constexpr int D8_VSTAGES = 7;
 constexpr int D8_HD = 128;
 constexpr uint32_t D8_TMEM_COLS = 128;   // S^T 2 x NP (cols 0..63), O^T NP (cols 64..)
 // Lazy rescale: O and l keep the reference maximum until a tile's maximum exceeds it by 2 (log2
@@ -54,8 +57,8 @@ struct D8Smem {
   static constexpr uint32_t F8 = 128 * D8_HD;   // one code tile: 128 keys x 128 bytes = 16 KB
   static constexpr uint32_t OPB = 32 * 128;     // q or P operand: up to 32 rows of 128 codes
   static constexpr uint32_t OFF_K8 = 0;
-  static constexpr uint32_t OFF_V8 = OFF_K8 + D8_STAGES * F8;
-  static constexpr uint32_t OFF_Q = OFF_V8 + D8_STAGES * F8;   // 2 buffers
+  static constexpr uint32_t OFF_V8 = OFF_K8 + D8_KSTAGES * F8;
+  static constexpr uint32_t OFF_Q = OFF_V8 + D8_VSTAGES * F8;  // 2 buffers
   static constexpr uint32_t OFF_P = OFF_Q + 2 * OPB;           // 2 buffers
   static constexpr uint32_t OFF_RED = OFF_P + 2 * OPB;         // [3][4][16] floats
   static constexpr uint32_t OFF_QS = OFF_RED + 3 * 4 * 16 * 4; // inverse q scale per q buffer
@@ -66,8 +69,8 @@ static_assert(D8Smem::TOTAL <= 232448, "shared memory");
 
 // barrier slots
 enum : int {
-  B_K8F = 0, B_V8F = 6, B_K8E = 12, B_V8E = 18, B_QR = 24, B_QE = 26, B_SF = 28, B_SFREE = 30, B_PF = 32,
-  B_OD = 34, B_OFREE = 36, B_DRAIN = 37, B_QC = 38, B_COUNT = 40
+  B_K8F = 0, B_V8F = 6, B_K8E = 13, B_V8E = 19, B_QR = 26, B_QE = 28, B_SF = 30, B_SFREE = 32, B_PF = 34,
+  B_OD = 36, B_OFREE = 38, B_DRAIN = 39, B_QC = 40, B_COUNT = 42
 };
 
 __device__ __forceinline__ void tma_load_4d_d8(uint32_t dst, const CUtensorMap* m, uint64_t* bar, int x, int y,
@@ -135,10 +138,12 @@ __device__ __forceinline__ uint32_t sw128_off(int n, int c) {
 
 __device__ __forceinline__ void item_coords8(const DecodeAttn8Params& p, int item, int& b, int& g, int& t_begin,
                                              int& t_end, int& chunk) {
-  chunk = item % p.n_chunks;
-  const int bg = item / p.n_chunks;
-  b = bg / p.n_kv;
-  g = bg % p.n_kv;
+  // heads innermost: the CTAs working at the same time read the n_kv heads of the same keys, so
+  // each key's n_kv * 128 contiguous code bytes are fetched together
+  g = item % p.n_kv;
+  const int bc = item / p.n_kv;
+  chunk = bc % p.n_chunks;
+  b = bc / p.n_chunks;
   t_begin = chunk * p.chunk_tiles;
   t_end = min(t_begin + p.chunk_tiles, p.kv_tiles);
 }
@@ -193,14 +198,13 @@ __global__ void __launch_bounds__(D8_THREADS, 1) decode_attn8_kernel(const __gri
         int b, g, t0, t1, chunk;
         item_coords8(p, item, b, g, t0, t1, chunk);
         for (int t = t0; t < t1; ++t, ++tile) {
-          const int st = tile % D8_STAGES;
-          const uint32_t ph = (tile / D8_STAGES) & 1;
-          if (!mbar_wait(&bars[B_K8E + st], ph ^ 1, abort_flag, p.status)) { ok = false; break; }
-          mbar_arrive_expect_tx(&bars[B_K8F + st], L::F8);
-          tma_load_4d_d8(sbase + L::OFF_K8 + st * L::F8, &p.tmK, &bars[B_K8F + st], 0, g, t * 128, b);
-          if (!mbar_wait(&bars[B_V8E + st], ph ^ 1, abort_flag, p.status)) { ok = false; break; }
-          mbar_arrive_expect_tx(&bars[B_V8F + st], L::F8);
-          tma_load_4d_d8(sbase + L::OFF_V8 + st * L::F8, &p.tmV, &bars[B_V8F + st], 0, g, t * 128, b);
+          const int ks = tile % D8_KSTAGES, vs = tile % D8_VSTAGES;
+          if (!mbar_wait(&bars[B_K8E + ks], ((tile / D8_KSTAGES) & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
+          mbar_arrive_expect_tx(&bars[B_K8F + ks], L::F8);
+          tma_load_4d_d8(sbase + L::OFF_K8 + ks * L::F8, &p.tmK, &bars[B_K8F + ks], 0, g, t * 128, b);
+          if (!mbar_wait(&bars[B_V8E + vs], ((tile / D8_VSTAGES) & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
+          mbar_arrive_expect_tx(&bars[B_V8F + vs], L::F8);
+          tma_load_4d_d8(sbase + L::OFF_V8 + vs * L::F8, &p.tmV, &bars[B_V8F + vs], 0, g, t * 128, b);
         }
       }
     }
@@ -220,8 +224,8 @@ __global__ void __launch_bounds__(D8_THREADS, 1) decode_attn8_kernel(const __gri
         const int n = t1 - t0;
         auto issue_s = [&](int j) -> bool {
           const int gt = tile + j;
-          const int st = gt % D8_STAGES, sb = gt & 1;
-          if (!mbar_wait(&bars[B_K8F + st], (gt / D8_STAGES) & 1, abort_flag, p.status)) return false;
+          const int st = gt % D8_KSTAGES, sb = gt & 1;
+          if (!mbar_wait(&bars[B_K8F + st], (gt / D8_KSTAGES) & 1, abort_flag, p.status)) return false;
           if (!mbar_wait(&bars[B_SFREE + sb], ((gt >> 1) & 1) ^ 1, abort_flag, p.status)) return false;
           tc_fence_after();
           const uint64_t kd0 = sdesc_sw128(sbase + L::OFF_K8 + st * L::F8, 16, 1024);
@@ -234,9 +238,9 @@ __global__ void __launch_bounds__(D8_THREADS, 1) decode_attn8_kernel(const __gri
         };
         auto issue_pv = [&](int j) -> bool {
           const int gt = tile + j;
-          const int st = gt % D8_STAGES, pb = gt & 1;
+          const int st = gt % D8_VSTAGES, pb = gt & 1;
           if (!mbar_wait(&bars[B_PF + pb], (gt >> 1) & 1, abort_flag, p.status)) return false;
-          if (!mbar_wait(&bars[B_V8F + st], (gt / D8_STAGES) & 1, abort_flag, p.status)) return false;
+          if (!mbar_wait(&bars[B_V8F + st], (gt / D8_VSTAGES) & 1, abort_flag, p.status)) return false;
           if (j == 0 && !mbar_wait(&bars[B_OFREE], (it & 1) ^ 1, abort_flag, p.status)) return false;
           tc_fence_after();
           // V^T: M = hd runs along each 128-byte key row (MN-major), 8-key groups 1024 bytes apart
