@@ -308,6 +308,7 @@ size_t attn_scratch_bytes(const llama_dims* d, int dtype, int64_t kv_capacity) {
 struct BlockWs {
   void *u, *q, *o, *h, *m, *k, *v;
   float *rs1, *rs2;   // per-row RMSNorm factors of the attention and FFN norms
+  float* ss;          // [T, d_model / 256] sums of squares of h per 256-column tile (fused FFN norm)
   float2* rope_tab;   // [S, hd/2] (cos, sin) of the call's positions
   void* attn;         // split-K attention scratch (one-token steps)
   size_t attn_bytes;
@@ -328,6 +329,7 @@ BlockWs plan_block(const llama_dims* d, int dtype, bool own_kv, void* base, int6
   w.v = own_kv ? c.take(T * d->n_kv * d->head_dim * es) : nullptr;
   w.rs1 = static_cast<float*>(c.take(T * 4));
   w.rs2 = static_cast<float*>(c.take(T * 4));
+  w.ss = static_cast<float*>(c.take(T * (size_t)((d->d_model + 255) / 256) * 4));
   w.rope_tab = static_cast<float2*>(c.take((size_t)d->S * (d->head_dim / 2) * sizeof(float2)));
   w.attn_bytes = attn_scratch_bytes(d, dtype, own_kv ? d->S : kv_capacity);
   w.attn = w.attn_bytes ? c.take(w.attn_bytes) : nullptr;
@@ -392,8 +394,8 @@ int run_qkv(const llama_dims* d, int dtype, const llama_block_weights* w, const 
 }
 
 // out = resid + A W^T  (W [N, K])
-int run_linear_resid(int dtype, int64_t M, const void* A, int64_t K, const void* W, int64_t N, const void* resid,
-                     int resid_f32, void* out, int out_f32, cudaStream_t st) {
+GemmDesc linear_resid_desc(int dtype, int64_t M, const void* A, int64_t K, const void* W, int64_t N,
+                           const void* resid, int resid_f32, void* out, int out_f32) {
   GemmDesc g = make_gemm(dtype, M, A, K);
   g.nseg = 1;
   g.B[0] = W; g.nB[0] = N;
@@ -402,11 +404,16 @@ int run_linear_resid(int dtype, int64_t M, const void* A, int64_t K, const void*
   g.epi.resid = resid;
   g.epi.resid_f32 = resid_f32;
   g.epi.ldr = N;
-  return run_gemm(g, nullptr, st);
+  return g;
 }
 
-int run_gate_up(int dtype, int64_t M, const void* A, int64_t K, const void* wg, const void* wu, int64_t dff,
-                void* m, cudaStream_t st, const float* row_scale = nullptr) {
+int run_linear_resid(int dtype, int64_t M, const void* A, int64_t K, const void* W, int64_t N, const void* resid,
+                     int resid_f32, void* out, int out_f32, cudaStream_t st) {
+  return run_gemm(linear_resid_desc(dtype, M, A, K, W, N, resid, resid_f32, out, out_f32), nullptr, st);
+}
+
+GemmDesc gate_up_desc(int dtype, int64_t M, const void* A, int64_t K, const void* wg, const void* wu, int64_t dff,
+                      void* m, const float* row_scale) {
   GemmDesc g = make_gemm(dtype, M, A, K);
   g.nseg = 2;
   g.B[0] = wg; g.nB[0] = dff;
@@ -414,7 +421,7 @@ int run_gate_up(int dtype, int64_t M, const void* A, int64_t K, const void* wg, 
   g.N = 2 * dff;
   g.epi = make_epi(EPI_SWIGLU, dtype == LLAMA_F32, m, dff);
   g.epi.row_scale = row_scale;
-  return run_gemm(g, nullptr, st);
+  return g;
 }
 
 AttnDesc make_attn(const llama_dims* d, int dtype, const void* q, const void* k, const void* v, void* o, int64_t cap,
@@ -465,11 +472,29 @@ int block_body(const llama_dims* d, int dtype, const llama_block_weights* w, con
   if ((rc = run_attention(a, st)) != LLAMA_OK) return rc;
   // h = x + o W_O^T, kept in fp32 (decode: the fp32 stream is updated in place)
   void* h = x_f32 ? y : ws.h;
-  if ((rc = run_linear_resid(dtype, T, ws.o, hq, w->wo, D, x, x_f32 || f32, h, 1, st)) != LLAMA_OK) return rc;
-  // RMSNorm(h; g_ffn) in the same split form (reuses u), applied inside the gate/up GEMM
-  if ((rc = run_rmsnorm(dtype, 1, f32, h, w->ffn_norm_g, ws.u, T, D, eps, st, ws.rs2)) != LLAMA_OK) return rc;
-  // m = SiLU(w W_gate^T) * (w W_up^T)
-  if ((rc = run_gate_up(dtype, T, ws.u, D, w->w_gate, w->w_up, d->d_ff, ws.m, st, ws.rs2)) != LLAMA_OK) return rc;
+  GemmDesc go = linear_resid_desc(dtype, T, ws.o, hq, w->wo, D, x, x_f32 || f32, h, 1);
+  // m = SiLU(w W_gate^T) * (w W_up^T), w = RMSNorm(h; g_ffn) in the same split form (reuses u)
+  GemmDesc gu = gate_up_desc(dtype, T, ws.u, D, w->w_gate, w->w_up, d->d_ff, ws.m, ws.rs2);
+  // On the SM-pair GEMMs the norm needs no kernel of its own: the O projection's epilogue writes
+  // h * g_ffn and the sums of squares of h per 256-column tile, and the gate/up epilogue turns
+  // the row's sums into its factor.
+  const bool fuse = ws.ss && D % 256 == 0 && gemm_tc_supported(go) && gemm_tc2_supported(go) &&
+                    gemm_tc_supported(gu) && gemm_tc2_supported(gu);
+  if (fuse) {
+    go.epi.norm_u = ws.u;
+    go.epi.norm_g = w->ffn_norm_g;
+    go.epi.ss_out = ws.ss;
+    go.epi.ss_n = (int)(D / 256);
+    gu.epi.row_scale = nullptr;
+    gu.epi.ss_in = ws.ss;
+    gu.epi.ss_n = (int)(D / 256);
+    gu.epi.ss_inv_d = 1.0f / (float)D;
+    gu.epi.ss_eps = eps;
+  }
+  if ((rc = run_gemm(go, nullptr, st)) != LLAMA_OK) return rc;
+  if (!fuse && (rc = run_rmsnorm(dtype, 1, f32, h, w->ffn_norm_g, ws.u, T, D, eps, st, ws.rs2)) != LLAMA_OK)
+    return rc;
+  if ((rc = run_gemm(gu, nullptr, st)) != LLAMA_OK) return rc;
   // y = h + m W_down^T
   return run_linear_resid(dtype, T, ws.m, d->d_ff, w->w_down, D, h, 1, y, x_f32 || f32, st);
 }
@@ -836,7 +861,8 @@ int llama_swiglu_ffn(const llama_dims* d, int dtype, const void* x, const void* 
   if (!ws || ws_bytes < need) return LLAMA_ERR_WORKSPACE;
   if (!aligned16(ws)) return LLAMA_ERR_ALIGNMENT;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if ((rc = run_gate_up(dtype, T, x, d->d_model, w_gate, w_up, d->d_ff, ws, st)) != LLAMA_OK) return rc;
+  if ((rc = run_gemm(gate_up_desc(dtype, T, x, d->d_model, w_gate, w_up, d->d_ff, ws, nullptr), nullptr, st)) != LLAMA_OK)
+    return rc;
   return run_linear_resid(dtype, T, ws, d->d_ff, w_down, d->d_model, nullptr, 0, y, dtype == LLAMA_F32, st);
 }
 
@@ -915,6 +941,7 @@ int llama_stack_decode_step(const llama_dims* d, int dtype, int n_layers, const 
   BlockWs b;
   b.u = dw.u; b.q = dw.q; b.o = dw.o; b.h = nullptr; b.m = dw.m; b.k = nullptr; b.v = nullptr; b.bytes = 0;
   b.rs1 = dw.rs1; b.rs2 = dw.rs2;
+  b.ss = nullptr;         // the SM-pair GEMMs (and the fused norm) need at least 256 rows
   b.rope_tab = nullptr;   // one position per step: computed in the epilogue
   b.attn = dw.attn; b.attn_bytes = dw.attn_bytes;
   for (int l = 0; l < n_layers; ++l) {

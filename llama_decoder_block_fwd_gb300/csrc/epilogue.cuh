@@ -121,10 +121,13 @@ __device__ __forceinline__ void rope_run(const Epi& e, int64_t c_in_seg, float p
 // Apply the epilogue to n consecutive columns c .. c+n-1 of row r (n even; for EPI_QKV the run
 // lies inside one of the Q/K/V column ranges; for EPI_SWIGLU `v` holds gate values and `u` the
 // matching up values and c indexes the d_ff output).
+// `rs_in` is the row factor when e.ss_in is set (computed once per row by the caller).  Returns
+// the sum of squares of the run's output values when e.norm_u is set (else 0).
 template <int n>
-__device__ __forceinline__ void epi_run(const Epi& e, int64_t r, int64_t c, float* v, float* u) {
-  if (e.row_scale) {   // RMSNorm's per-row factor, applied to the fp32 accumulator
-    const float rs = __ldg(e.row_scale + r);
+__device__ __forceinline__ float epi_run(const Epi& e, int64_t r, int64_t c, float* v, float* u, float rs_in = 1.f) {
+  float ssq = 0.f;
+  if (e.row_scale || e.ss_in) {   // RMSNorm's per-row factor, applied to the fp32 accumulator
+    const float rs = e.row_scale ? __ldg(e.row_scale + r) : rs_in;
 #pragma unroll
     for (int i = 0; i < n; ++i) v[i] *= rs;
     if (e.kind == EPI_SWIGLU) {
@@ -142,6 +145,17 @@ __device__ __forceinline__ void epi_run(const Epi& e, int64_t r, int64_t c, floa
 #pragma unroll
       for (int i = 0; i < n; ++i) v[i] += t[i];
       store_run<n>(e.out, e.out_f32, e.ldo, r, c, v);
+      if (e.norm_u) {   // the next RMSNorm's x * g and sum of squares, from the fp32 h
+        float gg[n], sq = 0.f;
+        load_run<n>(e.norm_g, 0, 0, 0, c, gg);
+#pragma unroll
+        for (int i = 0; i < n; ++i) {
+          sq = fmaf(v[i], v[i], sq);
+          gg[i] *= v[i];
+        }
+        store_run<n>(e.norm_u, 0, e.ldo, r, c, gg);
+        ssq = sq;
+      }
       break;
     }
     case EPI_SWIGLU: {
@@ -182,6 +196,7 @@ __device__ __forceinline__ void epi_run(const Epi& e, int64_t r, int64_t c, floa
     default:
       break;
   }
+  return ssq;
 }
 
 }  // namespace llama

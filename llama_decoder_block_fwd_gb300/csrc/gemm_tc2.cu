@@ -239,6 +239,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS2, 1)
       const bool live = r < p.M;
       const uint32_t tb = tmem + buf * 256 + lane_base;
       if (p.swiglu) {
+        float rs = 1.f;
+        if (p.epi.ss_in && live) {   // the row's RMSNorm factor from the producing GEMM's partial sums
+          float ss = 0.f;
+          for (int j = 0; j < p.epi.ss_n; ++j) ss += __ldg(p.epi.ss_in + r * p.epi.ss_n + j);
+          rs = rsqrtf(ss * p.epi.ss_inv_d + p.epi.ss_eps);
+        }
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t g[32], u[32];
@@ -249,10 +255,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS2, 1)
             float gv[32], uv[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) { gv[i] = __uint_as_float(g[i]); uv[i] = __uint_as_float(u[i]); }
-            epi_run<32>(p.epi, r, (int64_t)nb * 128 + c * 32, gv, uv);
+            epi_run<32>(p.epi, r, (int64_t)nb * 128 + c * 32, gv, uv, rs);
           }
         }
       } else {
+        float ssq = 0.f;
 #pragma unroll 1
         for (int c = 0; c < 8; ++c) {
           uint32_t v[32];
@@ -262,9 +269,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS2, 1)
             float fv[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) fv[i] = __uint_as_float(v[i]);
-            epi_run<32>(p.epi, r, (int64_t)nb * T2N + c * 32, fv, fv);
+            ssq += epi_run<32>(p.epi, r, (int64_t)nb * T2N + c * 32, fv, fv);
           }
         }
+        if (p.epi.ss_out && live) p.epi.ss_out[r * p.epi.ss_n + nb] = ssq;
       }
       tc_fence_before();
       mbar_arrive_cluster(map_to_rank(smem_u32(&acc_empty[buf]), 0));

@@ -40,6 +40,16 @@ struct Epi {
   int hd;
   const float2* rope_tab;   // optional [S, hd/2] (cos, sin) for positions pos0 .. pos0+S-1
   RopeFreq freq[kMaxRopePairs];
+  // RMSNorm of the GEMM's output, split across two GEMMs (SM-pair kernel only):
+  //   EPI_RESID with norm_u: also writes norm_u[r, c] = bf16(h[r, c] * norm_g[c]) (ld ldo) and the
+  //   sum of squares of h over each 256-column tile to ss_out[r * ss_n + tile];
+  //   any kind with ss_in: the row factor is rsqrt(sum_j ss_in[r * ss_n + j] * ss_inv_d + ss_eps).
+  void* norm_u;
+  const void* norm_g;   // bf16 [N]
+  float* ss_out;
+  const float* ss_in;
+  int ss_n;
+  float ss_inv_d, ss_eps;
 };
 
 // D[M, N] = A[M, K] * B[N, K]^T with B the row-concatenation of nseg segments
