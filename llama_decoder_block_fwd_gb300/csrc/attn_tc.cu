@@ -92,17 +92,36 @@ __device__ __forceinline__ void tmem_ld16_at(uint32_t taddr, uint32_t (&v)[16]) 
       : "r"(taddr));
 }
 
+// Packed pairs of fp32 (sm_100 and later): (d0, d1) = (a0 b0 + c0, a1 b1 + c1) in one instruction,
+// and (s0, s1) += (a0, a1).
+__device__ __forceinline__ void fma_f32x2(float& d0, float& d1, float a0, float a1, float b0, float b1, float c0,
+                                          float c1) {
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+__device__ __forceinline__ void add_f32x2(float& s0, float& s1, float a0, float a1) {
+  asm("{\n\t.reg .b64 ra, rs;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rs, {%0, %1};\n\t"
+      "add.rn.f32x2 rs, rs, ra;\n\tmov.b64 {%0, %1}, rs;\n\t}"
+      : "+f"(s0), "+f"(s1)
+      : "f"(a0), "f"(a1));
+}
+
 // 32 scores of a row -> 16 bf16 pairs of P = 2^(s * scale - m) stored at TMEM column `col`; the
-// fp32 values are added to the row sums.
+// fp32 values are added to the row sums.  The scaling and the sums run on packed pairs.
 __device__ __forceinline__ void exp_chunk(const uint32_t (&v)[32], uint32_t col, float scale, float m, float& ls0,
                                           float& ls1) {
   uint32_t w[16];
 #pragma unroll
   for (int e = 0; e < 16; ++e) {
-    const float p0 = ex2(fmaf(__uint_as_float(v[2 * e]), scale, -m));
-    const float p1 = ex2(fmaf(__uint_as_float(v[2 * e + 1]), scale, -m));
-    ls0 += p0;
-    ls1 += p1;
+    float a0, a1;
+    fma_f32x2(a0, a1, __uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]), scale, scale, -m, -m);
+    const float p0 = ex2(a0);
+    const float p1 = ex2(a1);
+    add_f32x2(ls0, ls1, p0, p1);
     w[e] = pack_bf16x2(p0, p1);
   }
   tmem_st16(col, w);
