@@ -297,9 +297,10 @@ def bench_prefill(args, world, rank):
     barrier(world)
     if L.llama_get_device_status() != 0:
         raise RuntimeError("device status word set during warm-up")
+    # the step time comes from K steps with nothing between the launches; the per-kernel durations
+    # (roofline, kernel shares) from a second pass of K steps with an event pair around each launch,
+    # which adds small gaps of its own
     clocks = ClockSampler(torch.cuda.current_device())
-    L.llama_profile_read()            # clear
-    L.llama_profile_enable(True)
     barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
@@ -307,34 +308,67 @@ def bench_prefill(args, world, rank):
         step()
     e1.record(stream)
     barrier(world)
-    L.llama_profile_enable(False)
     clk = clocks.stop()
     ms_total = max_over_ranks(world, e0.elapsed_time(e1))
+    L.llama_profile_read()            # clear
+    L.llama_profile_enable(True)
+    barrier(world)
+    for _ in range(args.steps):
+        step()
+    barrier(world)
+    L.llama_profile_enable(False)
     prof = L.llama_profile_read()
     if L.llama_get_device_status() != 0:
         raise RuntimeError("device status word set during the timed region")
 
-    # end to end: pinned host x -> device, block, device y -> pinned host, every step
+    # end to end: pinned host x -> device, block, device y -> pinned host, every step.  The copies
+    # run on their own streams with two device buffers each, so step i+1's input copy and step
+    # i-1's output copy overlap step i's block; the timed region still holds every step's copies.
     xh = torch.empty(x.shape, dtype=x.dtype, pin_memory=True)
     xh.copy_(x)
-    yh = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
-    xd = torch.empty_like(x)
+    yh = [torch.empty(y.shape, dtype=y.dtype, pin_memory=True) for _ in range(2)]
+    xd = [torch.empty_like(x) for _ in range(2)]
+    yd = [torch.empty_like(y) for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    in_done = [torch.cuda.Event() for _ in range(2)]
+    comp_done = [torch.cuda.Event() for _ in range(2)]
+    out_done = [torch.cuda.Event() for _ in range(2)]
 
-    def e2e_step():
-        xd.copy_(xh, non_blocking=True)
-        L.llama_block_forward(wl.dims, wl.dtype, bw, xd, y, 0, None, None, 0, ws, stream)
-        yh.copy_(y, non_blocking=True)
+    def e2e_run(n, start_ev=None, end_ev=None):
+        if start_ev is not None:
+            start_ev.record(stream)
+            s_in.wait_event(start_ev)
+        for i in range(n):
+            k = i & 1
+            if i >= 2:
+                s_in.wait_event(comp_done[k])      # step i-2 has read xd[k]
+            with torch.cuda.stream(s_in):
+                xd[k].copy_(xh, non_blocking=True)
+                in_done[k].record(s_in)
+            stream.wait_event(in_done[k])
+            if i >= 2:
+                stream.wait_event(out_done[k])     # step i-2's result has left yd[k]
+            L.llama_block_forward(wl.dims, wl.dtype, bw, xd[k], yd[k], 0, None, None, 0, ws, stream)
+            comp_done[k].record(stream)
+            s_out.wait_event(comp_done[k])
+            with torch.cuda.stream(s_out):
+                yh[k].copy_(yd[k], non_blocking=True)
+                out_done[k].record(s_out)
+        stream.wait_event(out_done[(n - 1) & 1])
+        if n >= 2:
+            stream.wait_event(out_done[(n - 2) & 1])
+        if end_ev is not None:
+            end_ev.record(stream)
 
-    for _ in range(2):
-        e2e_step()
+    e2e_run(2)
+    torch.cuda.synchronize()
     barrier(world)
     f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    f0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    f1.record(stream)
+    e2e_run(args.steps, f0, f1)
+    torch.cuda.synchronize()
     barrier(world)
     e2e_ms = max_over_ranks(world, f0.elapsed_time(f1))
+    e2e_same = bool(torch.equal(yh[(args.steps - 1) & 1], y.cpu()))   # bit-identical to the resident step
 
     pk, pk_src = peaks()
     flops = prefill_flops(wl)
@@ -358,7 +392,10 @@ def bench_prefill(args, world, rank):
         "clocks": clk,
         "e2e": {"value": aggregate_rate(world, T, e2e_ms / args.steps), "unit": "tokens/s",
                 "h2d_bytes_per_step": x.numel() * x.element_size(),
-                "d2h_bytes_per_step": y.numel() * y.element_size()},
+                "d2h_bytes_per_step": y.numel() * y.element_size(),
+                "copies": "pinned host buffers; H2D and D2H on their own streams, double-buffered, overlapping "
+                          "the neighbouring steps' blocks",
+                "result_equals_resident_step": e2e_same},
         "gpu_launches": launches,
         "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
                      "frac": achieved / peak_tf, "traffic": kernel_traffic(dom) if wl.S == 8192 else None,
