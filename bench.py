@@ -526,6 +526,150 @@ def bench_decode(args, world, rank, kv8=False):
     return out
 
 
+def bench_chunked_prefill(args, world):
+    """Chunked prefill: the 8B block on 2048 new tokens at positions 6144..8191 of one sequence
+    whose first 6144 positions are already in the cache (the call attends to them and appends its
+    own K/V).  Each step rewrites the same cache rows with the same values."""
+    import dataclasses
+
+    import torch
+
+    import llama_decoder_block_fwd_gb300 as L
+    from synth import BF16, TID_KCACHE, TID_VCACHE
+    from synth import configs as C
+    from synth import workloads as W
+
+    pos0, cap = 6144, 8192
+    wl = dataclasses.replace(C.LLAMA3_8B_PREFILL, S=2048, name="llama3-8b-block-chunk-S2048-after-6144")
+    T = wl.B * wl.S
+    w = W.device_layer(wl)
+    bw = L.block_weights(w)
+    x = W.device_x(wl).reshape(T, wl.d_model)
+    y = torch.empty_like(x)
+    kc = W.device_tensor(BF16, (wl.B, cap, wl.n_kv, wl.head_dim), wl.seed, TID_KCACHE, 0.0, 1.0)
+    vc = W.device_tensor(BF16, (wl.B, cap, wl.n_kv, wl.head_dim), wl.seed, TID_VCACHE, 0.0, 1.0)
+    ws = torch.empty(L.llama_workspace_bytes(L.OP_BLOCK_FORWARD, wl.dims, wl.dtype), dtype=torch.uint8,
+                     device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        L.llama_block_forward(wl.dims, wl.dtype, bw, x, y, pos0, kc, vc, cap, ws, stream)
+
+    for _ in range(args.warmup):
+        step()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    barrier(world)
+    if L.llama_get_device_status() != 0:
+        raise RuntimeError("device status word set during the chunked prefill")
+    ms = max_over_ranks(world, e0.elapsed_time(e1)) / args.steps
+    fl = prefill_flops(wl)
+    fl["attn"] = 4.0 * wl.n_q * wl.head_dim * wl.B * (wl.S * pos0 + wl.S * (wl.S + 1) / 2)
+    flops = sum(fl.values())
+    pk, pk_src = peaks()
+    out = {"workload": wl.name, "value": aggregate_rate(world, T, ms), "unit": "tokens/s", "ms_per_step": ms,
+           "pos0": pos0, "flops_per_step": flops, "block_tflops": flops / (ms / 1e3) / 1e12,
+           "block_tc_frac": flops / (ms / 1e3) / 1e12 / pk["bf16_tflops"], "peak_source": f"{pk_src} bf16 burst"}
+    del w, bw, x, y, kc, vc, ws
+    torch.cuda.empty_cache()
+    return out
+
+
+def bench_decode_paged(args, world):
+    """The 32-layer decode step of the main decode workload through the paged cache: every
+    sequence's 8193 positions sit in 128-position pages spread over one pool in a random order."""
+    import dataclasses
+
+    import numpy as np
+    import torch
+
+    import llama_decoder_block_fwd_gb300 as L
+    from synth import BF16, TID_KCACHE, TID_VCACHE
+    from synth import configs as C
+    from synth import workloads as W
+
+    wl = C.LLAMA3_8B_DECODE
+    if args.decode_layers != wl.n_layers:
+        wl = dataclasses.replace(wl, n_layers=args.decode_layers, name=f"{wl.name}-L{args.decode_layers}")
+    max_pos = wl.t_cache                      # the new token's position; 8193 keys
+    per_seq = (max_pos + 1 + 127) // 128
+    n_pages = wl.B * per_seq + 1
+    perm = np.random.default_rng(wl.seed).permutation(n_pages).astype(np.int32)
+    table = torch.from_numpy(perm[:wl.B * per_seq].reshape(wl.B, per_seq).copy()).cuda()
+    pos = torch.full((wl.B,), max_pos, dtype=torch.int32, device="cuda")
+    tensors = [W.device_layer(wl, l) for l in range(wl.n_layers)]
+    layers = [L.block_weights(t) for t in tensors]
+    kp = torch.empty((wl.n_layers, n_pages, 128, wl.n_kv, wl.head_dim), dtype=torch.bfloat16, device="cuda")
+    vp = torch.empty_like(kp)
+    for l in range(wl.n_layers):
+        for tid, dst in ((TID_KCACHE, kp), (TID_VCACHE, vp)):
+            dst[l].copy_(W.device_tensor(BF16, (n_pages, 128, wl.n_kv, wl.head_dim), wl.seed + l, tid, 0.0, 1.0))
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    final_g, w_lm = W.device_final(wl)
+    x = W.device_x_emb(wl)
+    logits = torch.empty((wl.B, wl.vocab), dtype=torch.float32, device="cuda")
+    ws = torch.empty(L.llama_workspace_bytes(L.OP_STACK_DECODE_STEP, wl.dims, wl.dtype, wl.n_layers, wl.vocab,
+                                             max_pos + 1), dtype=torch.uint8, device="cuda")
+
+    def step():
+        L.llama_stack_decode_step_paged(wl.dims, layers, final_g, w_lm, wl.vocab, x, kp, vp, table, pos, max_pos,
+                                        logits, ws)
+
+    step()
+    L.llama_profile_read()
+    L.llama_profile_enable(True)
+    nprof = max(2, min(args.steps, 5))
+    for _ in range(nprof):
+        step()
+    L.llama_profile_enable(False)
+    prof = L.llama_profile_read()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step()
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for _ in range(args.warmup):
+        g.replay()
+    barrier(world)
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        g.replay()
+    e1.record(stream)
+    barrier(world)
+    if L.llama_get_device_status() != 0:
+        raise RuntimeError("device status word set during the paged decode")
+    ms = max_over_ranks(world, e0.elapsed_time(e1)) / args.steps
+    pk, pk_src = peaks()
+    nb = decode_bytes(wl, kv_elem_bytes=2)
+    step_bytes = sum(nb.values())
+    out = {"workload": wl.name + "-paged", "value": aggregate_rate(world, wl.B, ms), "unit": "tokens/s",
+           "ms_per_step": ms, "bytes_per_step": step_bytes,
+           "hbm_frac_step": step_bytes / (ms / 1e3) / 1e9 / pk["hbm_gbs"],
+           "pages": f"{n_pages} pages of 128 positions, random order; block table [{wl.B}, {per_seq}]",
+           "graph": "CUDA graph replay of one decode step"}
+    attn = [k for k in prof if k.startswith("attn")]
+    if attn:
+        n, t = prof[attn[0]]
+        per_launch = nb["kv_read"] / wl.n_layers
+        ach = per_launch / (t / n / 1e3) / 1e9
+        out["roofline"] = {"bound": "hbm", "kernel": attn[0], "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                           "frac": ach / pk["hbm_gbs"], "traffic": None, "peak_source": f"{pk_src} hbm",
+                           "algorithmic_bytes_per_launch": per_launch}
+    del tensors, layers, kp, vp, final_g, w_lm, x, logits, ws, g, table, pos
+    torch.cuda.empty_cache()
+    return out
+
+
 # ----------------------------------------------------------------------------- oracle legs
 def oracle_prefill_sample(S_sample: int):
     """Time the fp64 oracle on one sequence of S_sample tokens of the 8B block (weights drawn
@@ -582,6 +726,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-mha", action="store_true", help="skip the LLaMA-7B MHA block prefill")
     ap.add_argument("--no-kv8", action="store_true", help="skip the decode step over an 8-bit KV cache")
+    ap.add_argument("--no-chunked", action="store_true", help="skip the chunked-prefill line")
+    ap.add_argument("--no-paged", action="store_true", help="skip the paged-cache decode line")
     ap.add_argument("--prefill-seq", type=int, default=8192, help="tokens of the prefill workload (default 8192)")
     ap.add_argument("--decode-layers", type=int, default=32, help="layers of the decode stack (default 32)")
     args = ap.parse_args()
@@ -599,6 +745,8 @@ def main():
     dec = None if args.no_decode else bench_decode(args, world, rank)
     dec8 = None if (args.no_decode or args.no_kv8) else bench_decode(args, world, rank, kv8=True)
     smp = None if args.no_decode else bench_sample(args, world)
+    chk = None if args.no_chunked else bench_chunked_prefill(args, world)
+    pgd = None if (args.no_decode or args.no_paged) else bench_decode_paged(args, world)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         S_sample, n_seq, total = 1024, 0, 0.0
@@ -616,7 +764,7 @@ def main():
             "config": pre["config"], "roofline": pre["roofline"], "cpu_baseline": cpu, "e2e": pre["e2e"],
             "gpu_launches": pre["gpu_launches"], "clocks": pre["clocks"], "block_tc_frac": pre["block_tc_frac"],
             "block_tflops": pre["block_tflops"], "kernels": pre["kernels"], "decode": dec, "mha_prefill": mha,
-            "decode_kv8": dec8, "sample": smp,
+            "decode_kv8": dec8, "sample": smp, "chunked_prefill": chk, "decode_paged": pgd,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
