@@ -507,12 +507,25 @@ int block_body(const llama_dims* d, int dtype, const llama_block_weights* w, con
 // parts (two MMAs per k-step into one accumulator): the weights are still read once, and the
 // activations keep ~16 mantissa bits, which holds the 32-layer drift of a bf16-only data flow.
 // ------------------------------------------------------------------------------------------
-constexpr int kDecodeUnits = 320;
+// K splits of a weight-streaming projection with fixed units (128-column tile, K range): the count
+// (1..16) that minimises the k-blocks the busiest SM streams when the units are dealt out over
+// the 152 SMs of the part; ties go to fewer splits (fewer partials for the finisher).  The 8B QKV
+// projection (48 tiles x 64 k-blocks) gets 3 splits: 22 k-blocks on the busiest SM against an
+// even share of 20.2 (7 splits, 336 units, would give 30).
+constexpr int64_t kDecodeSms = 152;
 
 int decode_splits(int64_t n_cols, int64_t K) {
   const int64_t tiles = (n_cols + 127) / 128;
-  const int want = (int)std::max<int64_t>(1, (kDecodeUnits + tiles - 1) / tiles);
-  return gemm_skinny_splits(K, want);
+  const int64_t nkb = (K + 63) / 64;
+  int best = 1;
+  int64_t best_cost = INT64_MAX;
+  for (int want = 1; want <= 16; ++want) {
+    const int sp = gemm_skinny_splits(K, want);
+    const int64_t kbps = (nkb + sp - 1) / sp;
+    const int64_t cost = ((tiles * sp + kDecodeSms - 1) / kDecodeSms) * kbps;
+    if (cost < best_cost) { best_cost = cost; best = sp; }
+  }
+  return best;
 }
 
 bool decode_tc_path(const llama_dims* d, int dtype) {
