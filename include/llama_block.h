@@ -193,7 +193,10 @@ int llama_kv_quantize(const void* x, int64_t n_tokens, int64_t n_kv, int64_t hea
  * codes [B, kv_capacity, n_kv, head_dim] holding positions 0..pos0 (the new token's K/V already
  * written), k_scale / v_scale [n_kv] fp32 (device); q and o bf16 [B, n_q, head_dim].
  * Needs head_dim 128, n_q / n_kv in {1, 2, 4, 8, 16} (else LLAMA_ERR_UNSUPPORTED) and the
- * workspace llama_workspace_bytes(LLAMA_OP_GQA_ATTENTION, ...) gives for this shape.          */
+ * workspace llama_workspace_bytes(LLAMA_OP_GQA_ATTENTION, ...) gives for this shape.
+ * Numerics: the products run on 8-bit tensor-core MMAs, so q and the softmax weights enter as
+ * sums of two E4M3 values (about 8 significant bits, as in bf16); the result is attention over
+ * the decoded cache (code * scale) to within the bf16 tolerance, accumulated in fp32.          */
 int llama_gqa_attention_decode_kv8(const llama_dims* dims, const void* q, const void* k,
                                    const void* v, const float* k_scale, const float* v_scale,
                                    int64_t kv_capacity, int64_t pos0, void* o, void* ws,
