@@ -2,21 +2,25 @@
 // to every cached key plus its own ("LLaMA-3 8B ...", section 九: the 8193rd token sees the 8192
 // cached keys and itself; "Llama Architecture ...", Mathematical Foundations 4 for GQA).
 //
-//   phase 1 (decode_attn_kernel): persistent CTAs take work items (b, g, chunk of 128-key
-//     tiles).  Per tile, tcgen05 computes S^T = K Q^T (M = 128 keys, N = 16: the r <= 16 query
+//   phase 1 (decode_attn_kernel): the 128-key tiles of all (sequence b, KV group g) pairs, in
+//     (b, g, tile) order, are cut into one equal contiguous range per CTA, so every CTA streams
+//     the same number of tiles; a pair is split only where a range ends, and the CTA c's piece of
+//     pair q leaves its partial in slot q + c (unique: along the sequence q and c never decrease
+//     and one of them grows at each new piece, so B n_kv + grid slots suffice).  Per tile, tcgen05 computes S^T = K Q^T (M = 128 keys, N = 16: the r <= 16 query
 //     heads of KV group g, zero-padded; K = hd) and O^T += V^T P^T (M = hd, N = 16, K = 128 keys;
 //     V is read as the MN-major A operand straight from the TMA tile).  One thread per key does
 //     the softmax for the r heads; the running max is shared per head through shared memory and
-//     O^T is rescaled in TMEM only when a head's max grows by more than 2^8.  Each item writes its
+//     O^T is rescaled in TMEM only when a head's max grows by more than 2^8.  Each piece writes its
 //     unnormalised partial (m, l, O) to the workspace.
-//   phase 2 (decode_combine_kernel): o = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c.
+//   phase 2 (decode_combine_seg_kernel): o = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c over the
+//     pieces of the pair, found from the same range arithmetic.
 // The result equals softmax(q K^T / sqrt(hd)) V up to the order of additions.
 //
 // Paged cache (block_table set): K and V live in a pool of 128-position pages [n_pages, 128, n_kv,
 // hd]; sequence b's tile t is page block_table[b * max_pages + t], and b holds seq_pos[b] + 1
-// keys, so sequences may have different lengths (items past a sequence's end are empty and
-// leave m = -inf, l = 0).  Positions past a sequence's last key in its last page are not read:
-// their V rows are zeroed in shared memory before the P V MMA (P is 0 there).
+// keys, so sequences may have different lengths (a pair has ceil((seq_pos[b] + 1) / 128) tiles).
+// Positions past a sequence's last key in its last page are not read: their V rows are zeroed
+// in shared memory before the P V MMA (P is 0 there).
 #include <algorithm>
 #include <cmath>
 #include <cstring>
@@ -33,13 +37,15 @@ constexpr int DA_NPAD = 16;              // MMA N: query heads of the group, zer
 constexpr uint32_t DA_TMEM_COLS = 64;
 constexpr float kDaRescaleLog2 = 8.0f;
 
+constexpr int DA_MAX_GRID = 256;         // CTAs at most (sizes the partial slots)
+
 struct __align__(64) DecodeAttnParams {
   CUtensorMap tmK;   // [B, kv_len, n_kv, hd], box (64, 1, 128, 1)
   CUtensorMap tmV;
   CUtensorMap tmQ;   // [B, n_q, hd], box (64, r, 1)
-  float* part_o;     // [B, n_chunks, n_q, hd]
-  float* part_ml;    // [B, n_chunks, n_q, 2]  (m in log2 units, l)
-  int B, n_q, n_kv, r, kv_len, kv_tiles, chunk_tiles, n_chunks, n_items;
+  float* part_o;     // [B n_kv + grid slots, r, hd]
+  float* part_ml;    // [B n_kv + grid slots, r, 2]  (m in log2 units, l)
+  int B, n_q, n_kv, r, kv_len, kv_tiles;
   float scale_log2;
   unsigned* status;
   const int* block_table;   // paged cache: [B, max_pages] page ids; null: dense [B, cap, n_kv, hd]
@@ -84,16 +90,87 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
 // Named barrier over the 128 softmax threads (warps 2..5).
 __device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
-__device__ __forceinline__ void item_coords(const DecodeAttnParams& p, int item, int& b, int& g, int& t_begin,
-                                            int& t_end, int& chunk, int& kv_len) {
-  chunk = item % p.n_chunks;
-  const int bg = item / p.n_chunks;
-  b = bg / p.n_kv;
-  g = bg % p.n_kv;
+// ---- the work split: one contiguous range of the (b, g, tile) sequence per CTA
+__device__ __forceinline__ int seq_tiles(const int* seq_pos, int kv_tiles, int b) {
+  return seq_pos ? (__ldg(seq_pos + b) + 1 + 127) / 128 : kv_tiles;
+}
+__device__ __forceinline__ int64_t all_tiles(const int* seq_pos, int kv_tiles, int B, int n_kv) {
+  if (!seq_pos) return (int64_t)B * n_kv * kv_tiles;
+  int64_t s = 0;
+  for (int b = 0; b < B; ++b) s += seq_tiles(seq_pos, kv_tiles, b);
+  return s * n_kv;
+}
+__device__ __forceinline__ int64_t range_begin(int64_t T, int G, int c) { return (int64_t)c * T / G; }
+// The CTA whose range holds tile x (the last of several with the same start: ranges may be empty
+// when there are fewer tiles than CTAs).
+__device__ __forceinline__ int cta_of(int64_t T, int G, int64_t x) {
+  int c = (int)min((int64_t)G - 1, x * G / T);
+  while (c + 1 < G && range_begin(T, G, c + 1) <= x) ++c;
+  while (c > 0 && range_begin(T, G, c) > x) --c;
+  return c;
+}
+// First tile of pair (b, g) in the sequence and its tile count.
+__device__ __forceinline__ void pair_span(const int* seq_pos, int kv_tiles, int n_kv, int b, int g, int64_t& off,
+                                          int& nt) {
+  if (!seq_pos) {
+    off = ((int64_t)b * n_kv + g) * kv_tiles;
+    nt = kv_tiles;
+    return;
+  }
+  int64_t s = 0;
+  for (int bb = 0; bb < b; ++bb) s += seq_tiles(seq_pos, kv_tiles, bb);
+  nt = seq_tiles(seq_pos, kv_tiles, b);
+  off = s * n_kv + (int64_t)g * nt;
+}
+
+// The pieces of this CTA's range, one pair at a time, in order.
+struct SegIter {
+  int64_t x, end, pair_off;
+  int b, g, nt;
+};
+__device__ __forceinline__ void seg_begin(const DecodeAttnParams& p, int64_t T, SegIter& s) {
+  s.x = range_begin(T, gridDim.x, blockIdx.x);
+  s.end = range_begin(T, gridDim.x, blockIdx.x + 1);
+  if (s.x >= s.end) return;
+  if (!p.seq_pos) {
+    const int64_t pair = s.x / p.kv_tiles;
+    s.b = (int)(pair / p.n_kv);
+    s.g = (int)(pair % p.n_kv);
+    s.nt = p.kv_tiles;
+    s.pair_off = pair * p.kv_tiles;
+  } else {
+    int64_t off = 0;
+    int b = 0, nt = 0;
+    for (;; ++b) {
+      nt = seq_tiles(p.seq_pos, p.kv_tiles, b);
+      if (s.x < off + (int64_t)p.n_kv * nt) break;
+      off += (int64_t)p.n_kv * nt;
+    }
+    s.b = b;
+    s.nt = nt;
+    s.g = (int)((s.x - off) / nt);
+    s.pair_off = off + (int64_t)s.g * nt;
+  }
+}
+// Next piece: pair (b, g), its tiles [t0, t1), the pair's key count and its partial slot.
+__device__ __forceinline__ bool seg_next(const DecodeAttnParams& p, SegIter& s, int& b, int& g, int& t0, int& t1,
+                                         int& kv_len, int64_t& slot) {
+  if (s.x >= s.end) return false;
+  b = s.b;
+  g = s.g;
+  t0 = (int)(s.x - s.pair_off);
+  t1 = (int)min((int64_t)s.nt, s.end - s.pair_off);
   kv_len = p.seq_pos ? __ldg(p.seq_pos + b) + 1 : p.kv_len;
-  const int tiles = p.seq_pos ? (kv_len + 127) / 128 : p.kv_tiles;
-  t_begin = chunk * p.chunk_tiles;
-  t_end = min(t_begin + p.chunk_tiles, tiles);
+  slot = (int64_t)b * p.n_kv + g + blockIdx.x;
+  s.x = s.pair_off + t1;
+  if (t1 == s.nt) {   // the pair is done: the next one starts here
+    s.pair_off += s.nt;
+    if (++s.g == p.n_kv) {
+      s.g = 0;
+      if (++s.b < p.B) s.nt = seq_tiles(p.seq_pos, p.kv_tiles, s.b);
+    }
+  }
+  return true;
 }
 
 // Warp-wide maximum of a float (one instruction).
@@ -153,14 +230,16 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_kernel(const __grid
   const uint32_t sbase = smem_u32(smem);
 
   pdl_wait();   // q and the newest K/V come from the previous kernel; the partials may still be read
+  const int64_t T = all_tiles(p.seq_pos, p.kv_tiles, p.B, p.n_kv);
   if (warp == 0) {
     if (lane == 0) {  // ---------------------------------------------------- TMA producer
       int tile = 0, it = 0;
       bool ok = true;
-      for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
-        int b, g, t0, t1, chunk, kv_len;
-        item_coords(p, item, b, g, t0, t1, chunk, kv_len);
-        if (t1 <= t0) continue;   // past this sequence's end
+      SegIter si;
+      seg_begin(p, T, si);
+      int b, g, t0, t1, kv_len;
+      int64_t slot;
+      while (ok && seg_next(p, si, b, g, t0, t1, kv_len, slot)) {
         const int qb = it & 1;
         ++it;
         if (!mbar_wait(&q_empty[qb], (((it - 1) >> 1) & 1) ^ 1, abort_flag, p.status)) break;
@@ -188,10 +267,11 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_kernel(const __grid
       const uint32_t idesc_o = idesc_bf16(128, DA_NPAD, /*b_mn_major=*/false, /*a_mn_major=*/true);
       int tile = 0, it = 0;
       bool ok = true;
-      for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x, ++it) {
-        int b, g, t0, t1, chunk, kv_len;
-        item_coords(p, item, b, g, t0, t1, chunk, kv_len);
-        if (t1 <= t0) { --it; continue; }   // past this sequence's end
+      SegIter si;
+      seg_begin(p, T, si);
+      int b, g, t0, t1, kv_len;
+      int64_t slot;
+      for (; ok && seg_next(p, si, b, g, t0, t1, kv_len, slot); ++it) {
         const int qb = it & 1;
         if (!mbar_wait(&q_full[qb], (it >> 1) & 1, abort_flag, p.status)) break;
         tc_fence_after();
@@ -219,7 +299,7 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_kernel(const __grid
           const int pb = gt & 1;
           if (!mbar_wait(&p_full[pb], (gt >> 1) & 1, abort_flag, p.status)) return false;
           if (!mbar_wait(&v_full[st], (gt / DA_STAGES) & 1, abort_flag, p.status)) return false;
-          // the first P V of an item overwrites O^T: the previous item's O^T must have been read
+          // the first P V of a piece overwrites O^T: the previous piece's O^T must have been read
           if (j == 0 && !mbar_wait(o_free, (it & 1) ^ 1, abort_flag, p.status)) return false;
           tc_fence_after();
           const uint32_t va = sbase + L::OFF_V + st * L::KV;
@@ -254,20 +334,11 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_kernel(const __grid
     constexpr int r = R;
     int tile = 0, it = 0;
     bool ok = true;
-    for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x, ++it) {
-      int b, g, t0, t1, chunk, kv_len;
-      item_coords(p, item, b, g, t0, t1, chunk, kv_len);
-      if (t1 <= t0) {   // past this sequence's end: an empty partial
-        const int64_t base = ((int64_t)b * p.n_chunks + chunk) * p.n_q + (int64_t)g * r;
-#pragma unroll
-        for (int h = 0; h < R; ++h) p.part_o[(base + h) * DA_HD + t] = 0.f;
-        if (t < r) {
-          p.part_ml[(base + t) * 2 + 0] = -INFINITY;
-          p.part_ml[(base + t) * 2 + 1] = 0.f;
-        }
-        --it;
-        continue;
-      }
+    SegIter si;
+    seg_begin(p, T, si);
+    int b, g, t0, t1, kv_len;
+    int64_t slot;
+    for (; ok && seg_next(p, si, b, g, t0, t1, kv_len, slot); ++it) {
       float m_ref[R], lsum[R];
 #pragma unroll
       for (int h = 0; h < R; ++h) { m_ref[h] = -INFINITY; lsum[h] = 0.f; }
@@ -357,7 +428,7 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_kernel(const __grid
         mbar_arrive(&p_full[pb]);
       }
       if (!ok) break;
-      // ---- item done: write the unnormalised partial (m, l, O)
+      // ---- piece done: write the unnormalised partial (m, l, O) to its slot
       if (!mbar_wait(&o_done[(tile - 1) & 1], ((tile - 1) >> 1) & 1, abort_flag, p.status)) { ok = false; break; }
       tc_fence_after();
       uint32_t ov[16];
@@ -365,7 +436,7 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_kernel(const __grid
       tc_wait_ld();
       tc_fence_before();
       mbar_arrive(o_free);
-      const int64_t base = ((int64_t)b * p.n_chunks + chunk) * p.n_q + (int64_t)g * r;
+      const int64_t base = slot * r;
 #pragma unroll
       for (int h = 0; h < R; ++h) p.part_o[(base + h) * DA_HD + t] = __uint_as_float(ov[h]);
       // l: sum the per-thread partial sums over the 128 keys of each head
@@ -386,7 +457,7 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_kernel(const __grid
         p.part_ml[(base + t) * 2 + 0] = mm;
         p.part_ml[(base + t) * 2 + 1] = l;
       }
-      // lbuf is written again only after the next item's first tile barrier, which every thread
+      // lbuf is written again only after the next piece's first tile barrier, which every thread
       // passes after reading it here
     }
   }
@@ -435,6 +506,69 @@ __global__ void decode_combine_kernel(const float* __restrict__ part_o, const fl
     lo.y = pack_bf2(r[2] - __uint_as_float(out.y << 16), r[3] - __uint_as_float(out.y & 0xFFFF0000u));
     *reinterpret_cast<uint2*>(o_lo + off) = lo;
   }
+}
+
+// The same merge over the pieces of pair (b, g = h / r): the CTAs c0..c1 whose ranges hold the
+// pair's first and last tiles (a CTA with an empty range wrote nothing and is skipped).
+__global__ void decode_combine_seg_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml,
+                                          uint16_t* __restrict__ o, uint16_t* __restrict__ o_lo, int B, int n_q,
+                                          int n_kv, int kv_tiles, const int* __restrict__ seq_pos, int G) {
+  pdl_trigger();
+  pdl_wait();
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (warp >= B * n_q) return;
+  const int b = warp / n_q, h = warp % n_q;
+  const int r = n_q / n_kv, g = h / r, hh = h % r;
+  const int64_t T = all_tiles(seq_pos, kv_tiles, B, n_kv);
+  int64_t off;
+  int nt;
+  pair_span(seq_pos, kv_tiles, n_kv, b, g, off, nt);
+  const int c0 = cta_of(T, G, off), c1 = cta_of(T, G, off + nt - 1);
+  const int64_t pair = (int64_t)b * n_kv + g;
+  float M = -INFINITY;
+  for (int c = c0; c <= c1; ++c)
+    if (range_begin(T, G, c) < range_begin(T, G, c + 1)) M = fmaxf(M, part_ml[((pair + c) * r + hh) * 2]);
+  float l = 0.f, acc[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int c = c0; c <= c1; ++c) {
+    if (range_begin(T, G, c) >= range_begin(T, G, c + 1)) continue;
+    const int64_t idx = (pair + c) * r + hh;
+    const float w = exp2f(part_ml[idx * 2] - M);
+    l += w * part_ml[idx * 2 + 1];
+    const float4 v = *reinterpret_cast<const float4*>(part_o + idx * DA_HD + lane * 4);
+    acc[0] += w * v.x; acc[1] += w * v.y; acc[2] += w * v.z; acc[3] += w * v.w;
+  }
+  const float inv = 1.f / l;
+  float rr[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) rr[i] = acc[i] * inv;
+  uint2 out;
+  out.x = pack_bf2(rr[0], rr[1]);
+  out.y = pack_bf2(rr[2], rr[3]);
+  const int64_t o_off = ((int64_t)b * n_q + h) * DA_HD + lane * 4;
+  *reinterpret_cast<uint2*>(o + o_off) = out;
+  if (o_lo) {
+    uint2 lo;
+    lo.x = pack_bf2(rr[0] - __uint_as_float(out.x << 16), rr[1] - __uint_as_float(out.x & 0xFFFF0000u));
+    lo.y = pack_bf2(rr[2] - __uint_as_float(out.y << 16), rr[3] - __uint_as_float(out.y & 0xFFFF0000u));
+    *reinterpret_cast<uint2*>(o_lo + o_off) = lo;
+  }
+}
+
+int launch_combine_seg(const DecodeAttnParams& p, void* o, void* o_lo, int G, cudaStream_t st) {
+  const int warps = p.B * p.n_q;
+  return launch_k(decode_combine_seg_kernel, dim3((warps * 32 + 255) / 256), dim3(256), 0, st, (const float*)p.part_o,
+                  (const float*)p.part_ml, static_cast<uint16_t*>(o), static_cast<uint16_t*>(o_lo), p.B, p.n_q,
+                  p.n_kv, p.kv_tiles, p.seq_pos, G) == cudaSuccess
+             ? 0
+             : -1;
+}
+
+size_t round256(size_t b) { return (b + 255) & ~size_t(255); }
+
+// Partial slots of the range split: B n_kv + grid, each r x (hd + 2) floats.
+size_t seg_ws_bytes(int64_t B, int64_t n_kv, int64_t r, int64_t grid) {
+  const size_t slots = (size_t)(B * n_kv + grid);
+  return round256(slots * r * DA_HD * 4) + round256(slots * r * 2 * 4);
 }
 
 // Launch phase 1 for the params' head ratio (attributes set once per device).
@@ -490,10 +624,13 @@ bool decode_attn_supported(const AttnDesc& a) {
 }
 
 size_t decode_attn_ws_bytes(const AttnDesc& a) {
+  if (a.n_kv <= 0 || a.n_q % a.n_kv != 0) return 0;
+  const size_t seg = seg_ws_bytes(a.B, a.n_kv, a.n_q / a.n_kv, DA_MAX_GRID);
+  // the 8-bit kernel keeps fixed chunks of up to 8 tiles per (b, g) and uses the same workspace
   const DecodePlan d = plan(a.B, a.n_kv, a.pos0 + 1);
-  const size_t o = (size_t)a.B * d.n_chunks * a.n_q * DA_HD * 4;
-  const size_t ml = (size_t)a.B * d.n_chunks * a.n_q * 2 * 4;
-  return ((o + 255) & ~size_t(255)) + ((ml + 255) & ~size_t(255));
+  const size_t chunked = round256((size_t)a.B * d.n_chunks * a.n_q * DA_HD * 4) +
+                         round256((size_t)a.B * d.n_chunks * a.n_q * 2 * 4);
+  return std::max(seg, chunked);
 }
 
 int launch_decode_attn(const AttnDesc& a, void* ws, int num_sms, unsigned* status, cudaStream_t st) {
@@ -516,20 +653,21 @@ int launch_decode_attn(const AttnDesc& a, void* ws, int num_sms, unsigned* statu
   if (!encode_tmap_3d_bf16(&p.tmQ, a.q, DA_HD, (uint64_t)a.n_q, (uint64_t)a.B, DA_HD * 2,
                            (uint64_t)a.n_q * DA_HD * 2, 64, (uint32_t)r, 1))
     return -1;
-  const size_t o_bytes = (((size_t)a.B * d.n_chunks * a.n_q * DA_HD * 4) + 255) & ~size_t(255);
+  const int64_t slots = a.B * a.n_kv + DA_MAX_GRID;
   p.part_o = static_cast<float*>(ws);
-  p.part_ml = reinterpret_cast<float*>(static_cast<char*>(ws) + o_bytes);
+  p.part_ml = reinterpret_cast<float*>(static_cast<char*>(ws) + round256((size_t)slots * r * DA_HD * 4));
   p.B = (int)a.B; p.n_q = (int)a.n_q; p.n_kv = (int)a.n_kv; p.r = r;
   p.kv_len = (int)kv_len;
   p.kv_tiles = d.kv_tiles;
-  p.chunk_tiles = d.chunk_tiles;
-  p.n_chunks = d.n_chunks;
-  p.n_items = (int)(a.B * a.n_kv * d.n_chunks);
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.status = status;
-  const int grid = std::max(1, std::min(p.n_items, num_sms));
+  // one CTA per SM; with a dense cache no more CTAs than tiles (a paged cache's tile count is on
+  // the device: CTAs past it get empty ranges)
+  int grid = std::min(num_sms, DA_MAX_GRID);
+  if (!paged) grid = (int)std::min<int64_t>(grid, a.B * a.n_kv * d.kv_tiles);
+  grid = std::max(1, grid);
   if (launch_decode_kernel(p, grid, st) != 0) return -1;
-  return launch_decode_combine(p.part_o, p.part_ml, a.o, a.o_lo, a.B, a.n_q, d.n_chunks, st);
+  return launch_combine_seg(p, a.o, a.o_lo, grid, st);
 }
 
 void decode_attn_plan(int64_t kv_len, int& kv_tiles, int& chunk_tiles, int& n_chunks) {
@@ -576,21 +714,6 @@ void* noalloc_scratch_ptr() {
   return cached[dev];
 }
 
-size_t round256(size_t b) { return (b + 255) & ~size_t(255); }
-
-// The default chunking, with fewer (longer) chunks when the partials would not fit in `cap`.
-bool plan_within(int64_t B, int64_t n_q, int64_t n_kv, int64_t kv_len, size_t cap, DecodePlan& d) {
-  d = plan(B, n_kv, kv_len);
-  auto bytes = [&](int chunks) {
-    return round256((size_t)B * chunks * n_q * DA_HD * 4) + round256((size_t)B * chunks * n_q * 2 * 4);
-  };
-  if (bytes(1) > cap) return false;
-  while (bytes(d.n_chunks) > cap) {
-    d.chunk_tiles += 1;
-    d.n_chunks = (d.kv_tiles + d.chunk_tiles - 1) / d.chunk_tiles;
-  }
-  return true;
-}
 
 }  // namespace
 
@@ -614,9 +737,12 @@ extern "C" int llama_gqa_attention_decode_noalloc(const llama_dims* dims, int dt
   const uintptr_t al = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
                        reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o);
   if (al & 15) return LLAMA_ERR_ALIGNMENT;
-  DecodePlan d;
-  if (!plan_within(dims->B, dims->n_q, dims->n_kv, pos0 + 1, kNoAllocScratchBytes, d))
-    return LLAMA_ERR_WORKSPACE;   // B * n_q too large for the fixed scratch, even as one chunk
+  const DecodePlan d = plan(dims->B, dims->n_kv, pos0 + 1);
+  const int grid = std::max(1, (int)std::min<int64_t>(std::min(num_sms(), DA_MAX_GRID),
+                                                      dims->B * dims->n_kv * d.kv_tiles));
+  const int64_t rr = dims->n_q / dims->n_kv;
+  if (seg_ws_bytes(dims->B, dims->n_kv, rr, grid) > kNoAllocScratchBytes)
+    return LLAMA_ERR_WORKSPACE;   // B * n_q too large for the fixed scratch
   void* scratch = noalloc_scratch_ptr();
   unsigned* status = status_ptr();
   if (!scratch || !status) return LLAMA_ERR_CUDA;
@@ -633,23 +759,17 @@ extern "C" int llama_gqa_attention_decode_noalloc(const llama_dims* dims, int dt
       !encode_tmap_3d_bf16(&p.tmQ, q, DA_HD, (uint64_t)dims->n_q, (uint64_t)dims->B, DA_HD * 2,
                            (uint64_t)dims->n_q * DA_HD * 2, 64, (uint32_t)r, 1))
     return LLAMA_ERR_CUDA;
-  // Every partial a work item owns is overwritten by that item: nothing has to start at zero.
+  // Every partial slot the combine reads is written by its piece: nothing has to start at zero.
   p.part_o = static_cast<float*>(scratch);
   p.part_ml = reinterpret_cast<float*>(static_cast<char*>(scratch) +
-                                       round256((size_t)dims->B * d.n_chunks * dims->n_q * DA_HD * 4));
+                                       round256((size_t)(dims->B * dims->n_kv + grid) * rr * DA_HD * 4));
   p.B = (int)dims->B; p.n_q = (int)dims->n_q; p.n_kv = (int)dims->n_kv; p.r = r;
   p.kv_len = (int)kv_len;
   p.kv_tiles = d.kv_tiles;
-  p.chunk_tiles = d.chunk_tiles;
-  p.n_chunks = d.n_chunks;
-  p.n_items = (int)(dims->B * dims->n_kv * d.n_chunks);
   p.scale_log2 = (float)(1.0 / std::sqrt((double)DA_HD)) * 1.4426950408889634f;
   p.status = status;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int grid = std::max(1, std::min(p.n_items, num_sms()));
   if (launch_decode_kernel(p, grid, st) != 0) return LLAMA_ERR_CUDA;
-  const int warps = (int)(dims->B * dims->n_q);
-  decode_combine_kernel<<<(warps * 32 + 255) / 256, 256, 0, st>>>(p.part_o, p.part_ml, static_cast<uint16_t*>(o),
-                                                                   nullptr, (int)dims->B, (int)dims->n_q, d.n_chunks);
+  if (launch_combine_seg(p, o, nullptr, grid, st) != 0) return LLAMA_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? LLAMA_OK : LLAMA_ERR_CUDA;
 }
