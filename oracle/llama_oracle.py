@@ -36,9 +36,11 @@ Readings taken where the pages are silent or disagree (each is listed in DESIGN.
   * No intermediate rounding: the oracle is exact fp64 arithmetic on the
     (already rounded) stored inputs.
 
-Parity pins for each function are in tests/test_oracle_pins.py.  The end-to-end
-block and stack values are "parity unpinned" beyond those pins: no page prints
-a block output, so they are pinned only by composition of pinned parts.
+Parity pins for each function are in tests/test_oracle_pins.py.  No page prints
+a block output; the whole block is pinned against an independent formulation from
+library routines (attention, RMSNorm and SiLU routines of torch in float64, RoPE as
+complex multiplication) in tests/test_oracle_block_library.py, and the stack by
+composition (a stack is the chain of its blocks).
 """
 from __future__ import annotations
 
