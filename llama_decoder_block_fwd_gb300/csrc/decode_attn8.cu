@@ -192,21 +192,31 @@ __global__ void __launch_bounds__(D8_THREADS, 1) decode_attn8_kernel(const __gri
   pdl_wait();
   if (warp == 0) {
     if (lane == 0) {  // ---------------------------------------------------- TMA producer
+      // V(j) is requested one tile after K(j): P V needs it only after S^T and the softmax of
+      // its tile, so it spends less time resident in its stage and more in flight
       int tile = 0;
       bool ok = true;
+      int vb = 0, vg = 0, vt = 0;   // the V tile still to be requested
+      auto issue_v = [&](int gt) -> bool {
+        const int vs = gt % D8_VSTAGES;
+        if (!mbar_wait(&bars[B_V8E + vs], ((gt / D8_VSTAGES) & 1) ^ 1, abort_flag, p.status)) return false;
+        mbar_arrive_expect_tx(&bars[B_V8F + vs], L::F8);
+        tma_load_4d_d8(sbase + L::OFF_V8 + vs * L::F8, &p.tmV, &bars[B_V8F + vs], 0, vg, vt * 128, vb);
+        return true;
+      };
       for (int item = blockIdx.x; ok && item < p.n_items; item += gridDim.x) {
         int b, g, t0, t1, chunk;
         item_coords8(p, item, b, g, t0, t1, chunk);
         for (int t = t0; t < t1; ++t, ++tile) {
-          const int ks = tile % D8_KSTAGES, vs = tile % D8_VSTAGES;
+          const int ks = tile % D8_KSTAGES;
           if (!mbar_wait(&bars[B_K8E + ks], ((tile / D8_KSTAGES) & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
           mbar_arrive_expect_tx(&bars[B_K8F + ks], L::F8);
           tma_load_4d_d8(sbase + L::OFF_K8 + ks * L::F8, &p.tmK, &bars[B_K8F + ks], 0, g, t * 128, b);
-          if (!mbar_wait(&bars[B_V8E + vs], ((tile / D8_VSTAGES) & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
-          mbar_arrive_expect_tx(&bars[B_V8F + vs], L::F8);
-          tma_load_4d_d8(sbase + L::OFF_V8 + vs * L::F8, &p.tmV, &bars[B_V8F + vs], 0, g, t * 128, b);
+          if (tile > 0 && !issue_v(tile - 1)) { ok = false; break; }
+          vb = b; vg = g; vt = t;
         }
       }
+      if (ok && tile > 0) issue_v(tile - 1);
     }
   } else if (warp == 1) {
     if (lane == 0) {  // ---------------------------------------------------- MMA issuer
