@@ -284,6 +284,14 @@ int llama_embed(int dtype, const void* table, int64_t vocab, int64_t d_model, co
  * Returns LLAMA_OK, or LLAMA_ERR_CUDA if the synchronisation or the copy failed.             */
 int llama_get_device_status(int* out, void* stream);
 
+/* Self-test of the device-side failure path: one small kernel whose threads wait, through the
+ * same bounded mbarrier wait every pipelined kernel uses, on phases that nothing completes.  The
+ * waits give up after their limit (2 s of %globaltimer), latch LLAMA_ERR_TIMEOUT in the device
+ * status word and the kernel exits: llama_get_device_status then reports LLAMA_ERR_TIMEOUT and
+ * the context stays usable.  Asynchronous on `stream`; returns LLAMA_OK, or LLAMA_ERR_CUDA if the
+ * launch failed.                                                                              */
+int llama_selftest_bounded_wait(void* stream);
+
 /* Benchmark timing.  While enabled, every kernel the library launches is bracketed by two CUDA
  * events recorded on the launching stream (the events are created on first use and reused;
  * no device memory is allocated).  Do not enable it while a stream is being captured. */

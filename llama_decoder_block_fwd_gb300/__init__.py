@@ -19,6 +19,7 @@ __all__ = [
     "llama_sample", "llama_embed", "llama_kv_quantize", "llama_gqa_attention_decode_kv8",
     "llama_stack_decode_step_kv8", "llama_stack_decode_step_paged", "llama_gqa_attention_decode_paged",
     "llama_get_device_status", "llama_status_string", "llama_profile_enable", "llama_profile_read",
+    "llama_selftest_bounded_wait",
     "OP_RMSNORM", "OP_ROPE", "OP_GQA_ATTENTION", "OP_SWIGLU_FFN", "OP_BLOCK_FORWARD",
     "OP_STACK_DECODE_STEP",
 ]
@@ -77,6 +78,7 @@ def lib() -> ctypes.CDLL:
                 "llama_stack_decode_step": [pd, i32, i32, ctypes.POINTER(BlockWeights), vp, vp, i64, vp,
                                             vp, vp, i64, i64, vp, vp, sz, vp],
                 "llama_get_device_status": [ctypes.POINTER(ctypes.c_int), vp],
+                "llama_selftest_bounded_wait": [vp],
                 "llama_gqa_attention_decode_noalloc": [pd, i32, vp, vp, vp, i64, i64, vp, vp],
                 "llama_sample": [vp, i64, i64, i64, ctypes.c_float, i64, ctypes.c_float, vp, vp, vp],
                 "llama_embed": [i32, vp, i64, i64, vp, i64, vp, vp],
@@ -260,6 +262,12 @@ def llama_get_device_status(stream=None) -> int:
     out = ctypes.c_int(-1)
     _check(lib().llama_get_device_status(ctypes.byref(out), _s(stream)), "llama_get_device_status")
     return out.value
+
+
+def llama_selftest_bounded_wait(stream=None) -> None:
+    """Launch the kernel whose bounded waits run out on purpose (the device status word then holds
+    LLAMA_ERR_TIMEOUT; read it with llama_get_device_status)."""
+    _check(lib().llama_selftest_bounded_wait(_s(stream)), "llama_selftest_bounded_wait")
 
 
 def llama_profile_enable(on: bool = True) -> None:

@@ -16,7 +16,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libllama_block.so")
-SOURCES = ["api.cu", "kernels_simt.cu", "gemm_tc.cu", "gemm_tc2.cu", "gemm_skinny.cu", "attn_tc.cu", "decode_attn.cu", "decode_fin.cu", "sample.cu", "decode_attn8.cu"]
+SOURCES = ["api.cu", "kernels_simt.cu", "gemm_tc.cu", "gemm_tc2.cu", "gemm_skinny.cu", "attn_tc.cu", "decode_attn.cu", "decode_fin.cu", "sample.cu", "decode_attn8.cu", "selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
               "-Xptxas", "-v"]

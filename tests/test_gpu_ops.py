@@ -131,3 +131,25 @@ def test_empty_calls_are_no_ops():
     L.llama_rmsnorm((0, 4, 16, 1, 1, 2, 1, 1e4, 1e-5), L.F32, None, None, None)
     L.llama_block_forward((2, 0, 16, 8, 2, 2, 48, 1e4, 1e-5), L.F32, L.BlockWeights(*[16] * 9), 16, 32)
     _sync()
+
+
+def test_bounded_wait_times_out_cleanly_and_the_context_survives():
+    """A kernel's mbarrier wait on a phase that nothing completes gives up after its limit: the host
+    reads LLAMA_ERR_TIMEOUT (and the word is cleared), and the next call still computes correctly."""
+    import time
+
+    import torch
+    t0 = time.perf_counter()
+    L.llama_selftest_bounded_wait()
+    assert L.llama_get_device_status() == 6                       # LLAMA_ERR_TIMEOUT
+    assert 1.0 < time.perf_counter() - t0 < 30.0                  # the 2 s limit, not a hang
+    assert L.llama_get_device_status() == 0                       # read-and-clear
+    rows, d = 7, 64
+    x = torch.randn(rows, d, dtype=torch.float32, device="cuda")
+    g = torch.randn(d, dtype=torch.float32, device="cuda")
+    y = torch.empty_like(x)
+    L.llama_rmsnorm(L.dims_of(1, rows, d, 1, 1, 64, 128, 1e4, 1e-5), L.F32, x, g, y)
+    torch.cuda.synchronize()
+    ref = x * torch.rsqrt((x * x).mean(-1, keepdim=True) + 1e-5) * g
+    assert torch.allclose(y, ref, rtol=1e-5, atol=1e-5)
+    assert L.llama_get_device_status() == 0
