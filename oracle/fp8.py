@@ -5,7 +5,7 @@ TEST INFRASTRUCTURE ONLY (the same rule as llama_oracle.py).
 
 The pages size the KV cache in bf16 and note that it dominates decode memory ("Llama
 Architecture ...", Mathematical Foundations 4, KV cache scaling; "LLaMA-3 8B ...", section 七); they
-give no 8-bit format.  Readings taken (each listed in the design doc):
+give no 8-bit format.  Readings taken:
   * the format is OCP 8-bit floating point E4M3 ("e4m3fn"): sign, 4 exponent bits with bias 7,
     3 mantissa bits; exponent field 0 holds subnormals 2^-6 * m/8; S.1111.111 is NaN; there are
     no infinities; the largest finite magnitude is 448;

@@ -22,7 +22,7 @@ Sources (page title, section):
   [P4] "LLaMA Architecture > Model Architecture" (mbrenndoerfer.com):
        "The Transformer Block" (block equations), "Key Architectural Choices".
 
-Readings taken where the pages are silent or disagree (each is listed in the design doc):
+Readings taken where the pages are silent or disagree:
   * eps sits inside the square root (P2 "How it works", P4, P1 Step 1 code);
     P1 section 1's displayed equation puts it outside.
   * RoPE frequency theta_k = theta_base^(-2k/head_dim), interleaved pairs

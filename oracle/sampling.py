@@ -10,7 +10,7 @@ Sources (page title, section):
        sampling shaped by temperature, top-k and top-p; the sampled token goes back to the
        embedding for the next step).
 
-The page names the four rules without formulas.  Readings taken (each listed in the design doc):
+The page names the four rules without formulas.  Readings taken:
   * temperature T > 0 divides the logits before the softmax; T <= 0 means argmax.
   * argmax and every "most probable" ordering rank tokens by logit, larger first, and break
     ties by the lower token id (the order is total, so every set below is unique).
