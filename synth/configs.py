@@ -1,8 +1,8 @@
 """Workload shapes and the seeded input recipe for each of them.
 
 Shapes follow the Llama configurations the pages describe: the toy 8Q/2KV
-block, a small 512-wide block, the Llama-3-8B block (P3 section 一 table), the
-original LLaMA-7B MHA block (P4 configuration table), and a 32-layer
+block, a small 512-wide block, the Llama-3-8B block ("LLaMA-3 8B ..." page, section 一 table), the
+original LLaMA-7B MHA block ("LLaMA Architecture > Model Architecture" page, configuration table), and a 32-layer
 Llama-3-8B stack decoding one token per sequence against 8192 cached positions.
 
 Recipe (all draws from synth's counter-based generator):

@@ -125,7 +125,8 @@ def test_rope_composes():
 
 
 # ---------------------------------------------------------------- RMSNorm
-# P2 "How it works": x * (mean(x^2) + eps)^(-1/2), gain g; P4: outputs have RMS near 1.
+# "RMSNorm" study note, "How it works": x * (mean(x^2) + eps)^(-1/2), gain g; "LLaMA Architecture >
+# Model Architecture", "Key Architectural Choices": outputs have RMS near 1.
 def test_rmsnorm_unit_gain_rms():
     x = rng.standard_normal((5, 4096)) * 3.0
     y = O.rmsnorm(x, np.ones(4096), 1e-5)
@@ -277,7 +278,7 @@ def test_block_rows_subset_matches_full():
 
 def test_prefill_then_decode_equals_longer_prefill():
     # A decode step at position S against the cache of an S-token prefill gives the same output
-    # as the last row of an (S+1)-token prefill (P3 section 九: KV cache reuse).
+    # as the last row of an (S+1)-token prefill ("LLaMA-3 8B ..." page, section 九: KV cache reuse).
     dims1 = O.Dims(2, 7, 16, 4, 2, 4, 24, 1e4, 1e-5)
     w = _rand_weights(16, 4, 2, 4, 24)
     x = rng.standard_normal((2, 7, 16))
@@ -306,7 +307,7 @@ def test_stack_decode_two_layers_matches_manual_chain():
 
 
 # ---------------------------------------------------------------- sizes
-# P3 section 六 (parameter counts) and section 七 (KV cache per token).
+# "LLaMA-3 8B ..." page, section 六 (parameter counts) and section 七 (KV cache per token).
 def test_parameter_counts():
     assert O.block_param_count(4096, 32, 8, 128, 14336) == 218_112_000
     assert O.model_param_count(32, 4096, 32, 8, 128, 14336, 128256) == 8_030_261_248
@@ -320,4 +321,4 @@ def test_kv_cache_bytes():
     assert O.kv_bytes_per_token(1, 8, 128, 2) == 4096
     assert O.kv_bytes_per_token(32, 8, 128, 2) == 128 * 1024
     assert O.kv_bytes_per_token(32, 8, 128, 2) * 8192 == 1 << 30
-    assert O.kv_bytes_per_token(32, 32, 128, 2) == 512 * 1024     # MHA: 4x (P1 section 4: g/h = 1/r)
+    assert O.kv_bytes_per_token(32, 32, 128, 2) == 512 * 1024     # MHA: 4x ("Llama Architecture ..." page, Mathematical Foundations 4: g/h = 1/r)
