@@ -414,10 +414,10 @@ def bench_prefill(args, world, rank):
     return out
 
 
-def bench_decode(args, world, rank, kv8=False):
-    """One 32-layer decode step for 64 sequences holding 8192 cached positions.  kv8: the cache
-    holds E4M3 codes with per-head scales (made from the same synthetic values by
-    llama_kv_quantize) instead of bf16."""
+def bench_decode(args, world, rank, kv8=False, seqs=None, cached=None):
+    """One 32-layer decode step for 64 sequences holding 8192 cached positions (or `seqs`
+    sequences holding `cached` positions).  kv8: the cache holds E4M3 codes with per-head scales
+    (made from the same synthetic values by llama_kv_quantize) instead of bf16."""
     import numpy as np
     import torch
 
@@ -429,6 +429,9 @@ def bench_decode(args, world, rank, kv8=False):
     if args.decode_layers != wl.n_layers:   # fewer layers for sizing profiler captures
         import dataclasses
         wl = dataclasses.replace(wl, n_layers=args.decode_layers, name=f"{wl.name}-L{args.decode_layers}")
+    if seqs is not None:
+        import dataclasses
+        wl = dataclasses.replace(wl, B=seqs, t_cache=cached, name=f"llama3-8b-{wl.n_layers}L-decode-B{seqs}-T{cached}")
     cap = wl.t_cache + 1
     tensors = []
     layers = []
@@ -575,6 +578,53 @@ def bench_chunked_prefill(args, world):
            "pos0": pos0, "flops_per_step": flops, "block_tflops": flops / (ms / 1e3) / 1e12,
            "block_tc_frac": flops / (ms / 1e3) / 1e12 / pk["bf16_tflops"], "peak_source": f"{pk_src} bf16 burst"}
     del w, bw, x, y, kc, vc, ws
+    torch.cuda.empty_cache()
+    return out
+
+
+def bench_prefill_long(args, world):
+    """The 8B block over one 32768-token sequence (RoPE base 5e5): causal attention is 38% of the
+    FLOPs at this length."""
+    import dataclasses
+
+    import torch
+
+    import llama_decoder_block_fwd_gb300 as L
+    from synth import configs as C
+    from synth import workloads as W
+
+    wl = dataclasses.replace(C.LLAMA3_8B_PREFILL, S=32768, name="llama3-8b-block-prefill-B1-S32768")
+    T = wl.B * wl.S
+    w = W.device_layer(wl)
+    bw = L.block_weights(w)
+    x = W.device_x(wl).reshape(T, wl.d_model)
+    y = torch.empty_like(x)
+    ws = torch.empty(L.llama_workspace_bytes(L.OP_BLOCK_FORWARD, wl.dims, wl.dtype), dtype=torch.uint8,
+                     device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        L.llama_block_forward(wl.dims, wl.dtype, bw, x, y, 0, None, None, 0, ws, stream)
+
+    for _ in range(args.warmup):
+        step()
+    barrier(world)
+    n = max(2, min(args.steps, 5))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        step()
+    e1.record(stream)
+    barrier(world)
+    if L.llama_get_device_status() != 0:
+        raise RuntimeError("device status word set during the long prefill")
+    ms = max_over_ranks(world, e0.elapsed_time(e1)) / n
+    fl = sum(prefill_flops(wl).values())
+    pk, pk_src = peaks()
+    out = {"workload": wl.name, "value": aggregate_rate(world, T, ms), "unit": "tokens/s", "ms_per_step": ms,
+           "steps": n, "flops_per_step": fl, "block_tflops": fl / (ms / 1e3) / 1e12,
+           "block_tc_frac": fl / (ms / 1e3) / 1e12 / pk["bf16_tflops"], "peak_source": f"{pk_src} bf16 burst"}
+    del w, bw, x, y, ws
     torch.cuda.empty_cache()
     return out
 
@@ -728,6 +778,7 @@ def main():
     ap.add_argument("--no-kv8", action="store_true", help="skip the decode step over an 8-bit KV cache")
     ap.add_argument("--no-chunked", action="store_true", help="skip the chunked-prefill line")
     ap.add_argument("--no-paged", action="store_true", help="skip the paged-cache decode line")
+    ap.add_argument("--no-long", action="store_true", help="skip the 32K-context prefill and decode lines")
     ap.add_argument("--prefill-seq", type=int, default=8192, help="tokens of the prefill workload (default 8192)")
     ap.add_argument("--decode-layers", type=int, default=32, help="layers of the decode stack (default 32)")
     args = ap.parse_args()
@@ -747,6 +798,8 @@ def main():
     smp = None if args.no_decode else bench_sample(args, world)
     chk = None if args.no_chunked else bench_chunked_prefill(args, world)
     pgd = None if (args.no_decode or args.no_paged) else bench_decode_paged(args, world)
+    lpre = None if args.no_long else bench_prefill_long(args, world)
+    ldec = None if (args.no_decode or args.no_long) else bench_decode(args, world, rank, seqs=16, cached=32768)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         S_sample, n_seq, total = 1024, 0, 0.0
@@ -765,6 +818,7 @@ def main():
             "gpu_launches": pre["gpu_launches"], "clocks": pre["clocks"], "block_tc_frac": pre["block_tc_frac"],
             "block_tflops": pre["block_tflops"], "kernels": pre["kernels"], "decode": dec, "mha_prefill": mha,
             "decode_kv8": dec8, "sample": smp, "chunked_prefill": chk, "decode_paged": pgd,
+            "prefill_32k": lpre, "decode_32k": ldec,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
