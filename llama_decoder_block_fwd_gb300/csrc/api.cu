@@ -329,7 +329,7 @@ BlockWs plan_block(const llama_dims* d, int dtype, bool own_kv, void* base, int6
   w.v = own_kv ? c.take(T * d->n_kv * d->head_dim * es) : nullptr;
   w.rs1 = static_cast<float*>(c.take(T * 4));
   w.rs2 = static_cast<float*>(c.take(T * 4));
-  w.ss = static_cast<float*>(c.take(T * (size_t)((d->d_model + 255) / 256) * 4));
+  w.ss = static_cast<float*>(c.take(T * (size_t)((d->d_model + 127) / 128) * 4));
   w.rope_tab = static_cast<float2*>(c.take((size_t)d->S * (d->head_dim / 2) * sizeof(float2)));
   w.attn_bytes = attn_scratch_bytes(d, dtype, own_kv ? d->S : kv_capacity);
   w.attn = w.attn_bytes ? c.take(w.attn_bytes) : nullptr;
@@ -476,7 +476,7 @@ int block_body(const llama_dims* d, int dtype, const llama_block_weights* w, con
   // m = SiLU(w W_gate^T) * (w W_up^T), w = RMSNorm(h; g_ffn) in the same split form (reuses u)
   GemmDesc gu = gate_up_desc(dtype, T, ws.u, D, w->w_gate, w->w_up, d->d_ff, ws.m, ws.rs2);
   // On the SM-pair GEMMs the norm needs no kernel of its own: the O projection's epilogue writes
-  // h * g_ffn and the sums of squares of h per 256-column tile, and the gate/up epilogue turns
+  // h * g_ffn and the sums of squares of h per 128 columns, and the gate/up epilogue turns
   // the row's sums into its factor.
   const bool fuse = ws.ss && D % 256 == 0 && gemm_tc_supported(go) && gemm_tc2_supported(go) &&
                     gemm_tc_supported(gu) && gemm_tc2_supported(gu);
@@ -484,10 +484,10 @@ int block_body(const llama_dims* d, int dtype, const llama_block_weights* w, con
     go.epi.norm_u = ws.u;
     go.epi.norm_g = w->ffn_norm_g;
     go.epi.ss_out = ws.ss;
-    go.epi.ss_n = (int)(D / 256);
+    go.epi.ss_n = (int)(D / 128);
     gu.epi.row_scale = nullptr;
     gu.epi.ss_in = ws.ss;
-    gu.epi.ss_n = (int)(D / 256);
+    gu.epi.ss_n = (int)(D / 128);
     gu.epi.ss_inv_d = 1.0f / (float)D;
     gu.epi.ss_eps = eps;
   }

@@ -26,7 +26,7 @@ constexpr uint32_t A2_BYTES = 128 * T2K * 2;    // this CTA's 128 rows of A: 16 
 constexpr uint32_t B2_BYTES = 128 * T2K * 2;    // this CTA's 128-row half of B: 16 KB
 constexpr uint32_t STAGE2 = A2_BYTES + B2_BYTES;
 constexpr uint32_t SMEM2 = S2 * STAGE2 + 1024 + 256;
-constexpr int THREADS2 = 192;
+constexpr int THREADS2 = 320;   // TMA warp, MMA warp, 8 epilogue warps
 constexpr uint32_t TMEM2_COLS = 512;
 
 struct __align__(64) Tc2Params {
@@ -151,7 +151,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS2, 1)
   const int cluster_id = (int)(blockIdx.x >> 1), n_clusters = (int)(gridDim.x >> 1);
   if (threadIdx.x == 0) {
     for (int s = 0; s < S2; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
-    for (int b = 0; b < 2; ++b) { mbar_init(&acc_full[b], 1); mbar_init(&acc_empty[b], 2 * 128); }
+    for (int b = 0; b < 2; ++b) { mbar_init(&acc_full[b], 1); mbar_init(&acc_empty[b], 2 * 256); }
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -224,8 +224,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS2, 1)
       tc2_commit_mc(drain, 0x1);
       mbar_wait(drain, 0, &no_abort, p.status);
     }
-  } else {  // ---------------- epilogue warps 2..5 (both CTAs)
+  } else {  // ---------------- epilogue warps 2..9 (both CTAs)
+    // Warp w reads TMEM lanes 32 (w % 4) .. +31 (the lane quarter a warp may access) and column
+    // half (w - 2) / 4 of the tile: two warps per lane quarter halve each warp's serial chain of
+    // TMEM loads, global loads and stores per tile.
     const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     int it = 0;
     for (int t = cluster_id; t < p.num_tiles; t += n_clusters, ++it) {
@@ -242,11 +246,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS2, 1)
         float rs = 1.f;
         if (p.epi.ss_in && live) {   // the row's RMSNorm factor from the producing GEMM's partial sums
           float ss = 0.f;
-          for (int j = 0; j < p.epi.ss_n; ++j) ss += __ldg(p.epi.ss_in + r * p.epi.ss_n + j);
+          const float* sp = p.epi.ss_in + r * p.epi.ss_n;
+          if ((p.epi.ss_n & 3) == 0) {
+            for (int j = 0; j < p.epi.ss_n; j += 4) {
+              const float4 t4 = __ldg(reinterpret_cast<const float4*>(sp + j));
+              ss += (t4.x + t4.y) + (t4.z + t4.w);
+            }
+          } else {
+            for (int j = 0; j < p.epi.ss_n; ++j) ss += __ldg(sp + j);
+          }
           rs = rsqrtf(ss * p.epi.ss_inv_d + p.epi.ss_eps);
         }
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 2 * half; c < 2 * half + 2; ++c) {
           uint32_t g[32], u[32];
           tmem_ld32(tb + c * 32, g);
           tmem_ld32(tb + 128 + c * 32, u);
@@ -261,7 +273,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS2, 1)
       } else {
         float ssq = 0.f;
 #pragma unroll 1
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 4 * half; c < 4 * half + 4; ++c) {
           uint32_t v[32];
           tmem_ld32(tb + c * 32, v);
           tc_wait_ld();
@@ -272,7 +284,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS2, 1)
             ssq += epi_run<32>(p.epi, r, (int64_t)nb * T2N + c * 32, fv, fv);
           }
         }
-        if (p.epi.ss_out && live) p.epi.ss_out[r * p.epi.ss_n + nb] = ssq;
+        if (p.epi.ss_out && live) p.epi.ss_out[r * p.epi.ss_n + 2 * nb + half] = ssq;
       }
       tc_fence_before();
       mbar_arrive_cluster(map_to_rank(smem_u32(&acc_empty[buf]), 0));

@@ -42,7 +42,7 @@ struct Epi {
   RopeFreq freq[kMaxRopePairs];
   // RMSNorm of the GEMM's output, split across two GEMMs (SM-pair kernel only):
   //   EPI_RESID with norm_u: also writes norm_u[r, c] = bf16(h[r, c] * norm_g[c]) (ld ldo) and the
-  //   sum of squares of h over each 256-column tile to ss_out[r * ss_n + tile];
+  //   sum of squares of h over each 128-column half of a 256-column tile to ss_out[r * ss_n + half];
   //   any kind with ss_in: the row factor is rsqrt(sum_j ss_in[r * ss_n + j] * ss_inv_d + ss_eps).
   void* norm_u;
   const void* norm_g;   // bf16 [N]
