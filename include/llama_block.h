@@ -149,7 +149,7 @@ int llama_stack_decode_step(const llama_dims* dims, int dtype, int n_layers,
                             void* v_cache, int64_t cache_capacity, int64_t t_cache, float* logits,
                             void* ws, size_t ws_bytes, void* stream);
 
-/* Allocation-free one-token GQA attention (the paper has no counterpart: this is a library entry
+/* Allocation-free one-token GQA attention (no counterpart in the method itself: this is a library entry
  * point for callers that cannot allocate device memory at the call site, e.g. code running under
  * an allocator that owns all of device memory, or loops where cudaMalloc/cudaFree would
  * synchronise the device).  Same arguments and result as llama_gqa_attention with dims->S == 1,
