@@ -63,6 +63,14 @@ __device__ __forceinline__ void rope_sincos(float m, RopeFreq f, float& s, float
   sincosf(r, &s, &c);
 }
 
+// Copy the per-pair frequencies of a launch's parameters into shared memory (whole block, ends with
+// a barrier).  Threads of a warp that index a kernel-parameter array with different indices are
+// served one address at a time, so kernels whose lanes take different pairs read the copy instead.
+__device__ __forceinline__ void stage_freq(const RopeFreq* src, int half, RopeFreq* dst) {
+  for (int i = threadIdx.x + threadIdx.y * blockDim.x; i < half; i += blockDim.x * blockDim.y) dst[i] = src[i];
+  __syncthreads();
+}
+
 // ---------------------------------------------------------------- shared memory / mbarrier
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);

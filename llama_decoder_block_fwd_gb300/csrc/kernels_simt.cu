@@ -180,6 +180,8 @@ struct RopeParams {
 
 template <typename T>
 __global__ void rope_kernel(const __grid_constant__ RopeParams p) {
+  __shared__ RopeFreq freq[kMaxRopePairs];
+  stage_freq(p.freq, p.hd / 2, freq);
   const int64_t half = p.hd / 2;
   const int64_t nq_pairs = p.B * p.S * p.n_q * half;
   const int64_t nk_pairs = p.B * p.S * p.n_kv * half;
@@ -194,7 +196,7 @@ __global__ void rope_kernel(const __grid_constant__ RopeParams p) {
     const int64_t token = idx / half / heads;
     const float pos = (float)(p.pos0 + token % p.S);
     float s, c;
-    rope_sincos(pos, p.freq[kk], s, c);
+    rope_sincos(pos, freq[kk], s, c);
     T* e = base + 2 * idx;
     const float x0 = Elt<T>::ld(e), x1 = Elt<T>::ld(e + 1);
     Elt<T>::st(e, x0 * c - x1 * s);
@@ -283,14 +285,17 @@ __global__ void __launch_bounds__(256) gemm_simt_kernel(const __grid_constant__ 
 // Generic causal GQA attention: one warp per (b, s, h) query row, 32 keys per step (one per
 // lane), online softmax (running max and sum), output dims split across lanes.
 // ------------------------------------------------------------------------------------------
+// Block (half, rows): thread (k, y) writes pair k of position blockIdx.x * rows + y.
 __global__ void rope_table_kernel(float2* __restrict__ tab, int64_t S, int half, int64_t pos0,
                                   const __grid_constant__ RopeParams p) {
-  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= S * half) return;
-  const int k = (int)(i % half);
-  float s, c;
-  rope_sincos((float)(pos0 + i / half), p.freq[k], s, c);
-  tab[i] = make_float2(c, s);
+  __shared__ RopeFreq freq[kMaxRopePairs];
+  stage_freq(p.freq, half, freq);
+  const int k = threadIdx.x;
+  const int64_t s = (int64_t)blockIdx.x * blockDim.y + threadIdx.y;
+  if (s >= S) return;
+  float sn, cs;
+  rope_sincos((float)(pos0 + s), freq[k], sn, cs);
+  tab[s * half + k] = make_float2(cs, sn);
 }
 
 __global__ void widen_bf16_kernel(const uint16_t* __restrict__ src, float* __restrict__ dst, int64_t n) {
@@ -407,9 +412,10 @@ int launch_rope_table(float2* tab, int64_t S, int hd, int64_t pos0, const RopeFr
   memset(&p, 0, sizeof(p));
   p.hd = hd;
   for (int i = 0; i < hd / 2; ++i) p.freq[i] = freq[i];
-  const int64_t n = S * (hd / 2);
-  if (n <= 0) return 0;
-  rope_table_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(tab, S, hd / 2, pos0, p);
+  const int half = hd / 2;
+  if (S <= 0 || half <= 0) return 0;
+  const int rows = std::max(1, 256 / half);
+  rope_table_kernel<<<(unsigned)((S + rows - 1) / rows), dim3(half, rows), 0, st>>>(tab, S, half, pos0, p);
   return 0;
 }
 
