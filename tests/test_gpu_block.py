@@ -65,6 +65,23 @@ def test_block_full_size_sampled_rows(wl):
         assert_sublayer_parity(got, ref[0], xb[0][rows], wl.dtype, f"{wl.name} seq {b} y-x")
 
 
+@pytest.mark.parametrize("wl", [
+    # on 76 SM pairs: QKV 96 tile pairs, gate/up 320, O and down 64 (several rounds, short last rounds)
+    C.Workload("mid-B2-S2048-d1024", 12, C.BF16, 2, 2048, 1024, 8, 2, 128, 2560, 5e5, 1e-5, gain_std=0.1),
+    # O and down 80 tile pairs with the fused FFN norm, gate/up 400, QKV 120
+    C.Workload("mid-B2-S2560-d1024", 13, C.BF16, 2, 2560, 1024, 8, 2, 128, 2560, 5e5, 1e-5, gain_std=0.1),
+], ids=lambda w: w.name)
+def test_block_mid_size_every_row(wl):
+    """Mid-size blocks whose SM-pair GEMMs run several rounds of tiles, head_dim 128 with GQA 4:1
+    and RoPE base 5e5: every row of both sequences against the oracle, and a second call
+    bit-identical to the first."""
+    x = W.device_x(wl).reshape(wl.B * wl.S, wl.d_model)
+    y = _run_block(wl, x, W.device_layer(wl)).reshape(wl.B, wl.S, wl.d_model)
+    _check(wl, y)
+    y2 = _run_block(wl, x, W.device_layer(wl)).reshape(wl.B, wl.S, wl.d_model)
+    assert bool((y2 == y).all())
+
+
 def test_block_chunked_prefill_against_cache():
     """A 3-chunk prefill (pos0 = 0, 100, 229) through the cache equals one 300-token prefill."""
     import torch
