@@ -365,7 +365,8 @@ DecodeWs plan_decode(const llama_dims* d, int dtype, void* base, int64_t kv_capa
 
 // The Q/K/V projection with RoPE on Q and K and the K/V write into [B, cap, n_kv*hd] caches.
 int run_qkv(const llama_dims* d, int dtype, const llama_block_weights* w, const void* u, const float* row_scale,
-            void* q, void* kc, void* vc, int64_t cap, int64_t pos0, cudaStream_t st, float2* rope_tab = nullptr) {
+            void* q, void* kc, void* vc, int64_t cap, int64_t pos0, cudaStream_t st, float2* rope_tab = nullptr,
+            bool tab_ready = false) {
   const int64_t T = d->B * d->S, hq = d->n_q * d->head_dim, hkv = d->n_kv * d->head_dim;
   GemmDesc g = make_gemm(dtype, T, u, d->d_model);
   g.nseg = 3;
@@ -384,12 +385,12 @@ int run_qkv(const llama_dims* d, int dtype, const llama_block_weights* w, const 
   g.epi.hd = (int)d->head_dim;
   g.epi.row_scale = row_scale;
   rope_freqs(d, g.epi.freq);
-  if (rope_tab) {   // one (cos, sin) per position and frequency, shared by every head of the token
+  if (rope_tab && !tab_ready) {   // one (cos, sin) per position and frequency, shared by every head
     prof::begin("rope_table", st);
     if (launch_rope_table(rope_tab, d->S, (int)d->head_dim, pos0, g.epi.freq, st) != 0) return LLAMA_ERR_CUDA;
     prof::end(st);
-    g.epi.rope_tab = rope_tab;
   }
+  g.epi.rope_tab = rope_tab;
   return run_gemm(g, nullptr, st);
 }
 
@@ -461,10 +462,25 @@ int block_body(const llama_dims* d, int dtype, const llama_block_weights* w, con
   int rc;
   // RMSNorm(x; g_attn) = rs1 * (x * g_attn): the GEMM takes a = x * g_attn (exact in bf16 when the
   // gain is one) and multiplies its fp32 accumulator by rs1[row] before RoPE.
-  if ((rc = run_rmsnorm(dtype, x_f32 || f32, f32, x, w->attn_norm_g, ws.u, T, D, eps, st, ws.rs1)) != LLAMA_OK)
+  // bf16 rows: the norm and the RoPE table of the call's positions in one launch
+  const bool fused_tab = !x_f32 && !f32 && ws.rope_tab &&
+                         rmsnorm_rope_table_ok(x, w->attn_norm_g, ws.u, T, D, d->S, (int)d->head_dim);
+  if (fused_tab) {
+    RopeFreq freq[kMaxRopePairs];
+    rope_freqs(d, freq);
+    prof::begin("rmsnorm", st);
+    if (launch_rmsnorm_rope_table(x, w->attn_norm_g, ws.u, ws.rs1, T, D, eps, ws.rope_tab, d->S, (int)d->head_dim,
+                                  pos0, freq, st) != 0)
+      return LLAMA_ERR_UNSUPPORTED;
+    prof::end(st);
+    if ((rc = launch_status()) != LLAMA_OK) return rc;
+  } else if ((rc = run_rmsnorm(dtype, x_f32 || f32, f32, x, w->attn_norm_g, ws.u, T, D, eps, st, ws.rs1)) !=
+             LLAMA_OK) {
     return rc;
+  }
   // q, k, v with RoPE; k, v written into the cache at pos0..pos0+S-1
-  if ((rc = run_qkv(d, dtype, w, ws.u, ws.rs1, ws.q, kc, vc, cap, pos0, st, ws.rope_tab)) != LLAMA_OK) return rc;
+  if ((rc = run_qkv(d, dtype, w, ws.u, ws.rs1, ws.q, kc, vc, cap, pos0, st, ws.rope_tab, fused_tab)) != LLAMA_OK)
+    return rc;
   // o = causal GQA attention
   AttnDesc a = make_attn(d, dtype, ws.q, kc, vc, ws.o, cap, pos0);
   a.ws = ws.attn;

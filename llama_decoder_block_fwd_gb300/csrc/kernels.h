@@ -98,6 +98,11 @@ int launch_attn_simt(const AttnDesc& a, cudaStream_t st);
 int launch_widen_bf16(const void* src, float* dst, int64_t n, cudaStream_t st);
 // tab[s, k] = (cos, sin)((pos0 + s) * theta_k) for s < S, k < hd/2.
 int launch_rope_table(float2* tab, int64_t S, int hd, int64_t pos0, const RopeFreq* freq, cudaStream_t st);
+// Both of the above in one launch, for bf16 rows in the split form (rs_out set) whose width takes
+// the register path (16-byte aligned, d % 8 == 0, d <= 4096); returns -1 (nothing launched) otherwise.
+bool rmsnorm_rope_table_ok(const void* x, const void* g, const void* y, int64_t rows, int64_t d, int64_t S, int hd);
+int launch_rmsnorm_rope_table(const void* x, const void* g, void* y, float* rs, int64_t rows, int64_t d, float eps,
+                              float2* tab, int64_t S, int hd, int64_t pos0, const RopeFreq* freq, cudaStream_t st);
 
 // tensor-core paths (bf16 only)
 bool gemm_tc_supported(const GemmDesc& g);

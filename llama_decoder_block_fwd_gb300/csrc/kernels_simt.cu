@@ -79,13 +79,14 @@ __device__ __forceinline__ void unpack16(const uint4& w, float* f, uint16_t) {
 // One warp per row; the row is held in registers (CH 16-byte chunks per lane) between the
 // sum of squares and the scaling pass.  SPLIT: write a = x * g and rs[row] = rsqrt(mean(x^2)+eps)
 // instead of y = x * rs * g, for a consumer GEMM that applies rs to its fp32 accumulator.
+// (rows 8 * bid .. 8 * bid + 7 for a block of 256 threads)
 template <typename TX, typename TG, typename TY, int CH, bool SPLIT>
-__global__ void __launch_bounds__(256) rmsnorm_reg_kernel(const TX* __restrict__ x, const TG* __restrict__ g,
-                                                          TY* __restrict__ y, float* __restrict__ rs_out,
-                                                          int64_t rows, int d, float eps) {
+__device__ __forceinline__ void rmsnorm_reg_rows(const TX* __restrict__ x, const TG* __restrict__ g,
+                                                 TY* __restrict__ y, float* __restrict__ rs_out, int64_t rows, int d,
+                                                 float eps, int64_t bid) {
   constexpr int N = 16 / (int)sizeof(TX);
   const int lane = threadIdx.x & 31;
-  const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int64_t row = bid * 8 + (threadIdx.x >> 5);
   if (row >= rows) return;
   const int nch = d / N;
   const uint4* xr = reinterpret_cast<const uint4*>(x + row * d);
@@ -119,6 +120,13 @@ __global__ void __launch_bounds__(256) rmsnorm_reg_kernel(const TX* __restrict__
       VecIO<TY, N>::st(yr + c * N, f);
     }
   }
+}
+
+template <typename TX, typename TG, typename TY, int CH, bool SPLIT>
+__global__ void __launch_bounds__(256) rmsnorm_reg_kernel(const TX* __restrict__ x, const TG* __restrict__ g,
+                                                          TY* __restrict__ y, float* __restrict__ rs_out,
+                                                          int64_t rows, int d, float eps) {
+  rmsnorm_reg_rows<TX, TG, TY, CH, SPLIT>(x, g, y, rs_out, rows, d, eps, blockIdx.x);
 }
 
 // Any width, any alignment.  Two passes over the row.
@@ -298,6 +306,47 @@ __global__ void rope_table_kernel(float2* __restrict__ tab, int64_t S, int half,
   tab[s * half + k] = make_float2(cs, sn);
 }
 
+// The split-form RMSNorm of bf16 rows (CH 16-byte chunks per lane) and the RoPE table of the
+// same call in one launch, so that the table's arithmetic runs beside the norm's memory traffic
+// instead of in a launch of its own.  Blocks come in groups of K norm blocks (8 rows each, as in
+// rmsnorm_reg_kernel) and one table block (kTabPasses x 256 / half positions), so table blocks
+// are dispatched throughout the norm; the norm blocks left over follow the groups.
+constexpr int kTabPasses = 8;
+template <int CH>
+__global__ void __launch_bounds__(256) rmsnorm_rope_table_kernel(const uint16_t* __restrict__ x,
+                                                                 const uint16_t* __restrict__ g,
+                                                                 uint16_t* __restrict__ y, float* __restrict__ rs_out,
+                                                                 int64_t rows, int d, float eps, int K, int tab_blocks,
+                                                                 float2* __restrict__ tab, int64_t S, int half,
+                                                                 int64_t pos0, const __grid_constant__ RopeParams p) {
+  const int b = blockIdx.x;
+  const int lead = tab_blocks * (K + 1);
+  int norm_idx = -1, tab_idx = -1;
+  if (b < lead) {
+    const int grp = b / (K + 1), pos = b - grp * (K + 1);
+    if (pos == K) tab_idx = grp;
+    else norm_idx = grp * K + pos;
+  } else {
+    norm_idx = tab_blocks * K + (b - lead);
+  }
+  if (norm_idx >= 0) {   // block-uniform
+    rmsnorm_reg_rows<uint16_t, uint16_t, uint16_t, CH, true>(x, g, y, rs_out, rows, d, eps, norm_idx);
+    return;
+  }
+  __shared__ RopeFreq freq[kMaxRopePairs];
+  stage_freq(p.freq, half, freq);
+  const int per = 256 / half;
+  const int k = (int)threadIdx.x % half, j = (int)threadIdx.x / half;
+  if (j >= per) return;
+  for (int pass = 0; pass < kTabPasses; ++pass) {
+    const int64_t s = ((int64_t)tab_idx * kTabPasses + pass) * per + j;
+    if (s >= S) return;
+    float sn, cs;
+    rope_sincos((float)(pos0 + s), freq[k], sn, cs);
+    tab[s * half + k] = make_float2(cs, sn);
+  }
+}
+
 __global__ void widen_bf16_kernel(const uint16_t* __restrict__ src, float* __restrict__ dst, int64_t n) {
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
     dst[i] = bf2f(src[i]);
@@ -404,6 +453,41 @@ int launch_gemm_simt(const GemmDesc& g, cudaStream_t st) {
     if (sw) gemm_simt_kernel<uint16_t, true><<<grid, 256, 0, st>>>(g);
     else gemm_simt_kernel<uint16_t, false><<<grid, 256, 0, st>>>(g);
   }
+  return 0;
+}
+
+bool rmsnorm_rope_table_ok(const void* x, const void* g, const void* y, int64_t rows, int64_t d, int64_t S, int hd) {
+  const int half = hd / 2;
+  const bool aligned = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(g) |
+                         reinterpret_cast<uintptr_t>(y)) & 15) == 0;
+  const int64_t per_lane = (d / 8 + 31) / 32;   // 16-byte chunks (8 bf16) per lane
+  return aligned && d % 8 == 0 && per_lane >= 1 && per_lane <= 16 && rows > 0 && S > 0 && half >= 1 &&
+         half <= kMaxRopePairs && (rows + 7) / 8 + S < INT32_MAX;
+}
+
+int launch_rmsnorm_rope_table(const void* x, const void* g, void* y, float* rs, int64_t rows, int64_t d, float eps,
+                              float2* tab, int64_t S, int hd, int64_t pos0, const RopeFreq* freq, cudaStream_t st) {
+  if (!rmsnorm_rope_table_ok(x, g, y, rows, d, S, hd)) return -1;
+  const int half = hd / 2;
+  const int64_t per_lane = (d / 8 + 31) / 32;
+  RopeParams p;
+  memset(&p, 0, sizeof(p));
+  p.hd = hd;
+  for (int i = 0; i < half; ++i) p.freq[i] = freq[i];
+  const int norm_blocks = (int)((rows + 7) / 8);
+  const int per = 256 / half;
+  const int tab_blocks = (int)((S + (int64_t)per * kTabPasses - 1) / ((int64_t)per * kTabPasses));
+  const int K = norm_blocks / tab_blocks;   // 0: the table blocks come first
+  const dim3 grid((unsigned)(norm_blocks + tab_blocks));
+  const uint16_t* xb = static_cast<const uint16_t*>(x);
+  const uint16_t* gb = static_cast<const uint16_t*>(g);
+  uint16_t* yb = static_cast<uint16_t*>(y);
+  if (per_lane <= 4)
+    rmsnorm_rope_table_kernel<4><<<grid, 256, 0, st>>>(xb, gb, yb, rs, rows, (int)d, eps, K, tab_blocks, tab, S, half, pos0, p);
+  else if (per_lane <= 8)
+    rmsnorm_rope_table_kernel<8><<<grid, 256, 0, st>>>(xb, gb, yb, rs, rows, (int)d, eps, K, tab_blocks, tab, S, half, pos0, p);
+  else
+    rmsnorm_rope_table_kernel<16><<<grid, 256, 0, st>>>(xb, gb, yb, rs, rows, (int)d, eps, K, tab_blocks, tab, S, half, pos0, p);
   return 0;
 }
 
