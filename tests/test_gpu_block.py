@@ -107,6 +107,38 @@ def test_block_chunked_prefill_against_cache():
     assert float(kc[:, 300:].abs().max()) == 0.0        # nothing written past the last token
 
 
+def test_block_chunked_prefill_full_size_sampled_rows():
+    """The chunked-prefill bench line: the 8B block on 2048 new tokens at positions 6144..8191 of a
+    sequence whose first 6144 positions are already cached (seeded N(0, 1) K/V drawn as the bench
+    draws them), in the bench's launch configuration.  64 sampled rows of y against the oracle
+    (which takes the same cached K/V), and every K/V row the call appended."""
+    import dataclasses
+
+    import torch
+
+    from synth import BF16, TID_KCACHE, TID_VCACHE, host_f64
+    pos0, cap = 6144, 8192
+    wl = dataclasses.replace(C.LLAMA3_8B_PREFILL, S=2048, name="llama3-8b-block-chunk-S2048-after-6144")
+    shape = (1, cap, wl.n_kv, wl.head_dim)
+    kc = W.device_tensor(BF16, shape, wl.seed, TID_KCACHE, 0.0, 1.0)
+    vc = W.device_tensor(BF16, shape, wl.seed, TID_VCACHE, 0.0, 1.0)
+    x = W.device_x(wl).reshape(wl.S, wl.d_model)
+    y = _run_block(wl, x, W.device_layer(wl), pos0, kc, vc, cap)
+    rows = sample_rows(wl.S)
+    past = (1, pos0, wl.n_kv, wl.head_dim)
+    kp = host_f64(BF16, past, wl.seed, TID_KCACHE, 0.0, 1.0)
+    vp = host_f64(BF16, past, wl.seed, TID_VCACHE, 0.0, 1.0)
+    xb = W.host_x(wl, 0)[None]
+    ref, kn, vn = O.block_forward(xb, O.BlockWeights(**W.host_layer(wl)), oracle_dims(wl, B=1), pos0=pos0,
+                                  k_past=kp, v_past=vp, rows=rows)
+    got = to_f64(y[rows])
+    assert_parity(got, ref[0], wl.dtype, "chunk after 6144 cached: y")
+    assert_sublayer_parity(got, ref[0], xb[0][rows], wl.dtype, "chunk after 6144 cached: y-x")
+    assert_parity(to_f64(kc[0, pos0:pos0 + wl.S]), kn[0], wl.dtype, "appended k rows")
+    assert_parity(to_f64(vc[0, pos0:pos0 + wl.S]), vn[0], wl.dtype, "appended v rows")
+    assert torch.equal(kc[0, :pos0].cpu(), W.device_tensor(BF16, shape, wl.seed, TID_KCACHE, 0.0, 1.0)[0, :pos0].cpu())
+
+
 def test_block_identity_zero_sublayers():
     """W_O = 0 and W_down = 0 leave the input unchanged (the residual paths)."""
     import torch

@@ -164,6 +164,55 @@ def test_paged_decode_stack_variable_lengths():
             assert torch.isnan(kp[0, page, row + 1:]).all()
 
 
+def test_llama3_8b_32_layers_paged_sampled_sequences():
+    """The paged decode bench line: the 32-layer 8B stack, batch 64, each sequence's 8193 positions in
+    128-position pages spread over one pool in a random order, the pool drawn per page as the bench
+    draws it.  Logits of sequences 0, 31 and 63 against the oracle, which reads each sequence's
+    positions back from the pages its block table names."""
+    import torch
+    wl = C.LLAMA3_8B_DECODE
+    max_pos = wl.t_cache
+    per_seq = (max_pos + 1 + 127) // 128
+    n_pages = wl.B * per_seq + 1
+    perm = np.random.default_rng(wl.seed).permutation(n_pages).astype(np.int32)
+    table = perm[:wl.B * per_seq].reshape(wl.B, per_seq).copy()
+    page_shape = (128, wl.n_kv, wl.head_dim)
+    kp = torch.empty((wl.n_layers, n_pages) + page_shape, dtype=torch.bfloat16, device="cuda")
+    vp = torch.empty_like(kp)
+    for l in range(wl.n_layers):
+        W.device_tensor(BF16, (n_pages,) + page_shape, wl.seed + l, TID_KCACHE, 0.0, 1.0, out=kp[l])
+        W.device_tensor(BF16, (n_pages,) + page_shape, wl.seed + l, TID_VCACHE, 0.0, 1.0, out=vp[l])
+    layers = [W.device_layer(wl, l) for l in range(wl.n_layers)]
+    final_g, w_lm = W.device_final(wl)
+    x = W.device_x_emb(wl)
+    logits = torch.empty((wl.B, wl.vocab), dtype=torch.float32, device="cuda")
+    ws = torch.empty(L.llama_workspace_bytes(L.OP_STACK_DECODE_STEP, wl.dims, wl.dtype, wl.n_layers, wl.vocab,
+                                             max_pos + 1), dtype=torch.uint8, device="cuda")
+    pos = torch.full((wl.B,), max_pos, dtype=torch.int32, device="cuda")
+    L.llama_stack_decode_step_paged(wl.dims, layers, final_g, w_lm, wl.vocab, x, kp, vp,
+                                    torch.from_numpy(table).cuda(), pos, max_pos, logits, ws)
+    torch.cuda.synchronize()
+    assert L.llama_get_device_status() == 0
+    got = to_f64(logits)
+    del kp, vp, layers, ws
+    torch.cuda.empty_cache()
+    rows = [0, 31, 63]
+    page_elems = 128 * wl.n_kv * wl.head_dim
+    n_full = max_pos // 128                # pages 0 .. n_full-1 hold positions 0 .. max_pos-1
+
+    def seq_cache(l, tid, b):
+        return np.concatenate([host_f64(BF16, page_shape, wl.seed + l, tid, 0.0, 1.0,
+                                        offset=int(table[b, j]) * page_elems) for j in range(n_full)])
+
+    fg, wlm = W.host_final(wl)
+    ref = O.stack_decode_step(W.host_x_emb(wl, rows), lambda l: O.BlockWeights(**W.host_layer(wl, l)), wl.n_layers,
+                              oracle_dims(wl, B=len(rows)), max_pos,
+                              lambda l: (np.stack([seq_cache(l, TID_KCACHE, b) for b in rows]),
+                                         np.stack([seq_cache(l, TID_VCACHE, b) for b in rows])),
+                              fg, wlm)
+    assert_parity(got[rows], ref, wl.dtype, "llama3-8b paged decode logits")
+
+
 @pytest.mark.slow
 def test_llama3_8b_block_prefill_32k_tokens():
     """The 8B block over one 32768-token sequence (RoPE theta 5e5), 48 sampled rows."""
