@@ -84,3 +84,18 @@ def test_decode_llama3_8b_32_layers_sampled_sequences():
     rows = [0, 31, 63]
     ref = _oracle(wl, rows, cap)
     assert_parity(to_f64(logits[rows]), ref, wl.dtype, "llama3-8b decode logits")
+
+
+def test_decode_llama3_8b_32_layers_32k_context_sampled_sequences():
+    """The long-context decode bench line: the 32-layer 8B stack for 16 sequences holding 32768 cached
+    positions each (RoPE base 5e5, a new token at position 32768); sequences 0 and 15 against the
+    oracle."""
+    import dataclasses
+    wl = dataclasses.replace(C.LLAMA3_8B_DECODE, B=16, t_cache=32768, name="llama3-8b-32L-decode-B16-T32768")
+    cap = wl.t_cache + 1
+    logits, kc, vc = _decode(wl, cap)
+    got = to_f64(logits)
+    del kc, vc
+    rows = [0, 15]
+    ref = _oracle(wl, rows, cap)
+    assert_parity(got[rows], ref, wl.dtype, "llama3-8b decode logits, 32768 cached")
