@@ -113,18 +113,16 @@ struct FinQkvParams {
 };
 
 // One thread per (row, column pair).
-// (B * pairs < 2^31, checked at launch)
 __global__ void fin_qkv_kernel(const __grid_constant__ FinQkvParams p) {
   pdl_trigger();
-  __shared__ RopeFreq freq[kMaxRopePairs];
-  stage_freq(p.freq, p.hd / 2, freq);   // kernel parameters only: before the dependency wait
   pdl_wait();
   const int n_cols = p.nq_cols + 2 * p.nkv_cols;
   const int pairs = n_cols / 2;
-  const int total = p.B * pairs;
-  for (int idx = blockIdx.x * blockDim.x + threadIdx.x; idx < total; idx += gridDim.x * blockDim.x) {
-  const int r = idx / pairs;
-  const int c = (idx - r * pairs) * 2;
+  const int64_t total = (int64_t)p.B * pairs;
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+  const int r = (int)(idx / pairs);
+  const int c = (int)(idx % pairs) * 2;
   float v0 = 0.f, v1 = 0.f;
   for (int s = 0; s < p.n_split; ++s) {
     const float2 w = *reinterpret_cast<const float2*>(p.part + ((int64_t)s * p.B + r) * n_cols + c);
@@ -139,7 +137,7 @@ __global__ void fin_qkv_kernel(const __grid_constant__ FinQkvParams p) {
   if (c < p.nq_cols + p.nkv_cols) {       // RoPE on q and k
     const int cc = c < p.nq_cols ? c : c - p.nq_cols;
     float sn, cs;
-    rope_sincos(pos, freq[(cc % p.hd) >> 1], sn, cs);
+    rope_sincos(pos, p.freq[(cc % p.hd) >> 1], sn, cs);
     const float x0 = v0, x1 = v1;
     v0 = x0 * cs - x1 * sn;
     v1 = x0 * sn + x1 * cs;
@@ -216,7 +214,6 @@ int launch_fin_qkv(const float* part, int n_split, const float* rs, void* q, voi
   p.n_split = n_split; p.B = B; p.nq_cols = nq_cols; p.nkv_cols = nkv_cols; p.hd = hd; p.cap = cap; p.t = t;
   for (int i = 0; i < hd / 2; ++i) p.freq[i] = freq[i];
   const int64_t n = (int64_t)B * (nq_cols + 2 * nkv_cols) / 2;
-  if (n >= INT32_MAX) return -1;
   // one thread per pair: B * 3 * 1024 threads at most for the shapes of the decode path, which
   // are resident at once (the next kernel of the stream can launch early)
   return launch_k(fin_qkv_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st, p) == cudaSuccess ? 0 : -1;
