@@ -122,10 +122,14 @@ def _d(dims) -> Dims:
 
 
 def _p(t) -> int | None:
+    """The device address of a tensor (an int passes through as an address).  Every pointer of the
+    C ABI is device memory: a tensor that lives on the host is refused here, not handed to a kernel."""
     if t is None:
         return None
     if isinstance(t, int):
         return t
+    if not getattr(t, "is_cuda", False):
+        raise ValueError(f"expected a CUDA tensor, got one on {getattr(t, 'device', type(t).__name__)}")
     return t.data_ptr()
 
 

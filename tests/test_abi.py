@@ -137,3 +137,14 @@ def test_kv8_calls_reject_bad_arguments():
     dd = _dims(B=4, S=1, n_q=32, n_kv=8, head_dim=128, d_model=4096, d_ff=14336)
     assert lib.llama_stack_decode_step_kv8(ctypes.byref(dd), 1, w, fake, fake, 128, fake, fake, fake, None, 100, 10,
                                            fake, fake, 1 << 30, None) == 1
+
+
+def test_host_tensors_are_refused_before_the_library_is_called():
+    """Every pointer of the ABI is device memory; the binding refuses a host tensor up front."""
+    torch = pytest.importorskip("torch")
+    d = _dims()
+    x = torch.zeros(4, 16)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        L.llama_rmsnorm(d, L.F32, x, torch.ones(16), torch.empty_like(x), stream=0)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        L.llama_sample(torch.zeros(2, 10), 1.0, 0, 1.0, torch.zeros(2), torch.zeros(2, dtype=torch.int32), stream=0)
