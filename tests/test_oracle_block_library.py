@@ -87,3 +87,28 @@ def test_block_against_a_cache_matches_library_formulation(S1):
     _, k0, v0 = O.block_forward(x0, w, d0)
     y, _, _ = O.block_forward(x1, w, d1, pos0=S0, k_past=k0, v_past=v0)
     np.testing.assert_allclose(y, y_ref.numpy(), rtol=0, atol=1e-10)
+
+
+def test_stack_decode_matches_library_formulation():
+    """The decode stack ("LLaMA-3 8B ...", sections 二, 九 and 十: blocks, then the final RMSNorm and
+    the untied LM head) in the library formulation: two layers of one-token decode after 5 cached
+    positions per layer (the same cached K/V on both sides), torch's rms_norm for the final norm and
+    a plain product with the head.  A wrong layer order, a skipped final norm or a transposed head
+    moves the logits far past the tolerance."""
+    rng = np.random.default_rng(5)
+    B, S0, d, n_q, n_kv, hd, d_ff, vocab, eps = 2, 5, 32, 4, 2, 8, 40, 13, 1e-6
+    ws = [_weights(rng, d, n_q, n_kv, hd, d_ff) for _ in range(2)]
+    caches = [(rng.normal(0.0, 1.0, (B, S0, n_kv, hd)), rng.normal(0.0, 1.0, (B, S0, n_kv, hd))) for _ in range(2)]
+    fg = rng.normal(1.0, 0.2, d)
+    wlm = rng.normal(0.0, 1.0 / np.sqrt(d), (vocab, d))
+    x_emb = rng.normal(0.0, 1.0, (B, d))
+    dims = O.Dims(B, 1, d, n_q, n_kv, hd, d_ff, 5e5, eps)
+    logits = O.stack_decode_step(x_emb, lambda l: ws[l], 2, dims, S0, lambda l: caches[l], fg, wlm)
+    t = lambda a: torch.from_numpy(np.asarray(a, dtype=np.float64))
+    h = x_emb[:, None, :]
+    for l in range(2):
+        y, _, _ = _torch_block(h, ws[l], dims, pos0=S0, k_past=t(caches[l][0]), v_past=t(caches[l][1]))
+        h = y.numpy()
+    ref = F.rms_norm(t(h[:, 0, :]), (d,), weight=t(fg), eps=eps) @ t(wlm).T
+    np.testing.assert_allclose(logits, ref.numpy(), rtol=0, atol=1e-10)
+    assert logits.shape == (B, vocab)
