@@ -91,24 +91,31 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
             out = ""
-        sm, smax, reasons = [], [], set()
-        for line in out.strip().splitlines():
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
-            except ValueError:
-                continue
-            for name, val in zip(self.NAMES, parts[5:9]):
-                if val.lower() == "active":
-                    reasons.add(name)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        hi = [s for s in sm if s >= 0.5 * max(sm)]   # samples under load
-        return {"sm_mhz": statistics.median(hi), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        return parse_clocks(out)
+
+
+def parse_clocks(out: str) -> dict:
+    """The clocks record of the timed region from nvidia-smi's CSV lines (ClockSampler.FIELDS, no
+    header, no units): median SM clock of the samples under load (at least half the highest), the
+    maximum SM clock, and every throttle reason seen active in any sample."""
+    sm, smax, reasons = [], [], set()
+    for line in out.strip().splitlines():
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) < 9:
+            continue
+        try:
+            sm.append(float(parts[1]))
+            smax.append(float(parts[2]))
+        except ValueError:
+            continue
+        for name, val in zip(ClockSampler.NAMES, parts[5:9]):
+            if val.lower() == "active":
+                reasons.add(name)
+    if not sm:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+    hi = [s for s in sm if s >= 0.5 * max(sm)]   # samples under load
+    return {"sm_mhz": statistics.median(hi), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+            "samples": len(sm)}
 
 
 # ----------------------------------------------------------------------------- helpers
