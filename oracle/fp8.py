@@ -1,69 +1,78 @@
-"""fp64 CPU oracle for an 8-bit KV cache: the E4M3 encoding and the per-head scaling that store
-K and V in one byte per element.
+"""Python face of the C++ oracle's 8-bit KV cache format (``e4m3.cpp``): OCP E4M3 codes with one
+fp32 scale per (layer, K or V, KV head).
 
-TEST INFRASTRUCTURE ONLY (the same rule as llama_oracle.py).
-
-The pages size the KV cache in bf16 and note that it dominates decode memory ("Llama
-Architecture ...", Mathematical Foundations 4, KV cache scaling; "LLaMA-3 8B ...", section 七); they
-give no 8-bit format.  Readings taken:
-  * the format is OCP 8-bit floating point E4M3 ("e4m3fn"): sign, 4 exponent bits with bias 7,
-    3 mantissa bits; exponent field 0 holds subnormals 2^-6 * m/8; S.1111.111 is NaN; there are
-    no infinities; the largest finite magnitude is 448;
-  * a cached element is x ~= code * s with one fp32 scale s per (layer, K or V, KV head);
-  * encoding holds x in fp32 and divides in fp32 (q = fl32(fl32(x) / s)), rounds q to the nearest
-    E4M3 value with ties to the even code, and saturates at +-448 -- so the integer decision is
-    taken in the precision a GPU kernel takes it;
-  * attention reads the decoded values code * s, including for the token being decoded, whose
-    K and V are encoded before it attends to them.
+TEST INFRASTRUCTURE ONLY (the same rule as llama_oracle.py).  The readings taken where the pages
+give no 8-bit format are stated in ``e4m3.cpp``: E4M3 as OCP defines it, x ~= code * s, the
+quotient x / s taken in fp32 and rounded to the nearest code (ties to the even code), saturating at
++-448; attention reads the decoded values, the new token's own K/V included.
 """
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+
 import numpy as np
+
+from ._lib import check, lib
+
+
+def _p(a):
+    return ctypes.c_void_p(a.ctypes.data)
 
 
 def e4m3_decode(code) -> np.ndarray:
     """Value of each E4M3 code (uint8 array) as fp64."""
-    c = np.asarray(code, dtype=np.uint8).astype(np.int64)
-    sign = np.where(c & 0x80, -1.0, 1.0)
-    e = (c >> 3) & 0xF
-    m = c & 0x7
-    val = np.where(e == 0, np.ldexp(m / 8.0, -6), np.ldexp(1.0 + m / 8.0, e - 7))
-    val = np.where((e == 15) & (m == 7), np.nan, val)
-    return sign * val
-
-
-_POS_CODES = np.arange(0, 127, dtype=np.uint8)          # 0x00 .. 0x7E: every finite non-negative value
-_POS_VALS = e4m3_decode(_POS_CODES)                      # increasing
+    c = np.ascontiguousarray(code, dtype=np.uint8)
+    out = np.empty(c.shape, dtype=np.float64)
+    check(lib().oracle_e4m3_decode(_p(c), c.size, _p(out)), "e4m3_decode")
+    return out
 
 
 def e4m3_encode(q) -> np.ndarray:
     """Nearest E4M3 code to each value of q (ties to the even code), saturating at +-448."""
-    q = np.asarray(q, dtype=np.float64)
-    a = np.minimum(np.abs(q), 448.0)
-    hi = np.searchsorted(_POS_VALS, a, side="left")      # first value >= a
-    hi = np.minimum(hi, 126)
-    lo = np.maximum(hi - 1, 0)
-    d_lo = a - _POS_VALS[lo]
-    d_hi = _POS_VALS[hi] - a
-    take_hi = (d_hi < d_lo) | ((d_hi == d_lo) & ((_POS_CODES[hi] & 1) == 0))
-    code = np.where(take_hi, _POS_CODES[hi], _POS_CODES[lo]).astype(np.uint8)
-    code = np.where(np.signbit(q), code | 0x80, code)
-    return np.where(np.isnan(q), np.uint8(0x7F), code).astype(np.uint8)
+    q = np.ascontiguousarray(q, dtype=np.float64)
+    out = np.empty(q.shape, dtype=np.uint8)
+    check(lib().oracle_e4m3_encode(_p(q), q.size, _p(out)), "e4m3_encode")
+    return out
+
+
+def _heads(x, scale):
+    s = np.ascontiguousarray(np.asarray(scale).reshape(-1), dtype=np.float32)
+    n_kv, hd = x.shape[-2], x.shape[-1]
+    assert s.shape == (n_kv,), (s.shape, n_kv)
+    return s, x.size // (n_kv * hd) if n_kv * hd else 0, n_kv, hd
 
 
 def quantize(x, scale) -> np.ndarray:
-    """Codes of x [..., n_kv, hd] with one scale per KV head (scale [n_kv]): the quotient is
-    taken in fp32, then encoded."""
-    x32 = np.asarray(x, dtype=np.float32)
-    s32 = np.asarray(scale, dtype=np.float32)[:, None]
-    return e4m3_encode((x32 / s32).astype(np.float64))
+    """Codes of x [..., n_kv, hd] with one scale per KV head (scale [n_kv]), quotient in fp32."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    s, n, n_kv, hd = _heads(x, scale)
+    out = np.empty(x.shape, dtype=np.uint8)
+    check(lib().oracle_kv_quantize(_p(x), n, n_kv, hd, _p(s), _p(out)), "kv_quantize")
+    return out
 
 
 def dequantize(code, scale) -> np.ndarray:
     """code * s in fp64 for codes [..., n_kv, hd] and scale [n_kv]."""
-    return e4m3_decode(code) * np.asarray(scale, dtype=np.float32).astype(np.float64)[:, None]
+    c = np.ascontiguousarray(code, dtype=np.uint8)
+    s, n, n_kv, hd = _heads(c, scale)
+    out = np.empty(c.shape, dtype=np.float64)
+    check(lib().oracle_kv_dequantize(_p(c), n, n_kv, hd, _p(s), _p(out)), "kv_dequantize")
+    return out
 
 
-def kv_quant_fn(k_scale, v_scale):
-    """(k_new, v_new) -> their stored values, for block_forward / stack_decode_step."""
-    def f(k_new, v_new):
-        return dequantize(quantize(k_new, k_scale), k_scale), dequantize(quantize(v_new, v_scale), v_scale)
-    return f
+@dataclass
+class KVStore:
+    """An 8-bit cache's per-head scales for K and V; block_forward / stack_decode_step replace the
+    new tokens' K and V by the values the cache stores.  Calling it applies that map directly."""
+    k_scale: np.ndarray
+    v_scale: np.ndarray
+
+    def __call__(self, k_new, v_new):
+        return (dequantize(quantize(k_new, self.k_scale), self.k_scale),
+                dequantize(quantize(v_new, self.v_scale), self.v_scale))
+
+
+def kv_quant_fn(k_scale, v_scale) -> KVStore:
+    """The store of an 8-bit cache with these per-head scales."""
+    return KVStore(np.asarray(k_scale, dtype=np.float32), np.asarray(v_scale, dtype=np.float32))
