@@ -737,12 +737,15 @@ extern "C" int llama_gqa_attention_decode_noalloc(const llama_dims* dims, int dt
   const uintptr_t al = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
                        reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(o);
   if (al & 15) return LLAMA_ERR_ALIGNMENT;
+  const int64_t rr = dims->n_q / dims->n_kv;
+  // The partials need B n_kv + grid slots of r (hd + 2) floats, whatever the number of keys.  The
+  // size rule takes the largest grid (DA_MAX_GRID), so whether a shape fits does not depend on the
+  // device's SM count.
+  if (seg_ws_bytes(dims->B, dims->n_kv, rr, DA_MAX_GRID) > kNoAllocScratchBytes)
+    return LLAMA_ERR_WORKSPACE;
   const DecodePlan d = plan(dims->B, dims->n_kv, pos0 + 1);
   const int grid = std::max(1, (int)std::min<int64_t>(std::min(num_sms(), DA_MAX_GRID),
                                                       dims->B * dims->n_kv * d.kv_tiles));
-  const int64_t rr = dims->n_q / dims->n_kv;
-  if (seg_ws_bytes(dims->B, dims->n_kv, rr, grid) > kNoAllocScratchBytes)
-    return LLAMA_ERR_WORKSPACE;   // B * n_q too large for the fixed scratch
   void* scratch = noalloc_scratch_ptr();
   unsigned* status = status_ptr();
   if (!scratch || !status) return LLAMA_ERR_CUDA;

@@ -148,3 +148,46 @@ def test_host_tensors_are_refused_before_the_library_is_called():
         L.llama_rmsnorm(d, L.F32, x, torch.ones(16), torch.empty_like(x), stream=0)
     with pytest.raises(ValueError, match="CUDA tensor"):
         L.llama_sample(torch.zeros(2, 10), 1.0, 0, 1.0, torch.zeros(2), torch.zeros(2, dtype=torch.int32), stream=0)
+
+
+def _noalloc_scratch_bytes(B, n_kv, r):
+    """The allocation-free decode attention's size rule as its header states it: B*n_kv + 256
+    slots of r rows of 130 floats, as two arrays each rounded up to 256 bytes."""
+    r256 = lambda b: (b + 255) // 256 * 256
+    slots = B * n_kv + 256
+    return r256(slots * r * 512) + r256(slots * r * 8)
+
+
+@pytest.mark.parametrize("n_q,n_kv", [(32, 8), (64, 4)])   # r = 4 and r = 16
+def test_noalloc_size_rule_at_its_boundary(n_q, n_kv):
+    """Just under the 12 MiB rule the call gets past the size check (and, with no GPU visible in
+    the child process, stops at its first CUDA call: LLAMA_ERR_CUDA); just over it returns
+    LLAMA_ERR_WORKSPACE.  The number of keys does not enter the rule."""
+    import subprocess
+    import sys
+    r = n_q // n_kv
+    B = 1
+    while _noalloc_scratch_bytes(B + 1, n_kv, r) <= 12 << 20:
+        B += 1
+    code = f"""
+import ctypes, sys
+sys.path.insert(0, {ROOT!r})
+import llama_decoder_block_fwd_gb300 as L
+lib = L.lib()
+fake = 0x10000
+out = []
+for B in ({B}, {B + 1}):
+    for keys in (1, 100000):
+        d = L.dims_of(B, 1, {n_q} * 128, {n_q}, {n_kv}, 128, 1, 5e5, 1e-5)
+        out.append(lib.llama_gqa_attention_decode_noalloc(ctypes.byref(d), L.BF16, fake, fake, fake, keys, keys - 1,
+                                                          fake, None))
+print(out)
+"""
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    res = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=300)
+    assert res.returncode == 0, res.stderr[-2000:]
+    rcs = eval(res.stdout.strip().splitlines()[-1])
+    assert rcs[:2] == [5, 5], rcs      # under: past the size check, no device to reach
+    assert rcs[2:] == [4, 4], rcs      # over: LLAMA_ERR_WORKSPACE
+    if (n_q, n_kv) == (32, 8):
+        assert B == 724                # the largest batch the header names for 32/8 heads
