@@ -276,6 +276,48 @@ def bench_sample(args, world):
     return out
 
 
+def bench_rmsnorm(args, world):
+    """Standalone llama_rmsnorm on the 8B block's prefill activations: 8192 x 4096 bf16 rows in,
+    bf16 rows out, bf16 gains.  L2 is flushed (a 256 MB write) before every timed call."""
+    import torch
+
+    import llama_decoder_block_fwd_gb300 as L
+    from synth import configs as C
+    from synth import workloads as W
+
+    wl = C.LLAMA3_8B_PREFILL
+    T = wl.B * wl.S
+    x = W.device_x(wl).reshape(T, wl.d_model)
+    g = W.device_layer(wl)["attn_norm_g"]
+    y = torch.empty_like(x)
+    dims = (wl.B, wl.S, wl.d_model, wl.n_q, wl.n_kv, wl.head_dim, wl.d_ff, wl.theta_base, wl.eps)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        L.llama_rmsnorm(dims, wl.dtype, x, g, y, stream)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier(world)
+    for a, b in ev:
+        flush.fill_(1)
+        a.record(stream)
+        L.llama_rmsnorm(dims, wl.dtype, x, g, y, stream)
+        b.record(stream)
+    barrier(world)
+    if L.llama_get_device_status() != 0:
+        raise RuntimeError("device status word set during the RMSNorm line")
+    ms = max_over_ranks(world, sum(a.elapsed_time(b) for a, b in ev) / args.steps)
+    pk, pk_src = peaks()
+    nbytes = x.numel() * 2 + y.numel() * 2 + g.numel() * 2
+    gbs = nbytes / (ms / 1e3) / 1e9
+    out = {"workload": f"llama_rmsnorm {T} x {wl.d_model} bf16", "us_per_call": ms * 1e3, "bytes_per_call": nbytes,
+           "roofline": {"bound": "hbm", "kernel": "rmsnorm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                        "frac": gbs / pk["hbm_gbs"], "peak_source": f"{pk_src} hbm"},
+           "l2": "flushed before every call"}
+    del x, g, y, flush
+    torch.cuda.empty_cache()
+    return out
+
+
 def bench_prefill(args, world, rank):
     import torch
 
@@ -317,6 +359,17 @@ def bench_prefill(args, world, rank):
     barrier(world)
     clk = clocks.stop()
     ms_total = max_over_ranks(world, e0.elapsed_time(e1))
+    # a second, longer region (about one second of back-to-back steps) for the rate under the
+    # power cap, reported beside the headline against the sustained bf16 peak
+    n_sus = max(args.steps, int(1000.0 / max(ms_total / args.steps, 1e-3)) + 1)
+    barrier(world)
+    s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record(stream)
+    for _ in range(n_sus):
+        step()
+    s1.record(stream)
+    barrier(world)
+    ms_sus = max_over_ranks(world, s0.elapsed_time(s1)) / n_sus
     L.llama_profile_read()            # clear
     L.llama_profile_enable(True)
     barrier(world)
@@ -411,6 +464,10 @@ def bench_prefill(args, world, rank):
         "block_tflops": step_flops / (ms_step / 1e3) / 1e12,
         "kernels": kernels,
         "config": prefill_config(wl, world, step_flops),
+        "sustained": {"steps": n_sus, "timed_s": n_sus * ms_sus / 1e3, "ms_per_step": ms_sus,
+                      "value": aggregate_rate(world, T, ms_sus), "block_tflops": step_flops / (ms_sus / 1e3) / 1e12,
+                      "block_tc_frac": step_flops / (ms_sus / 1e3) / 1e12 / pk["bf16_tflops_sustained"],
+                      "peak_source": f"{pk_src} bf16 sustained"},
     }
     del w, x, y, ws, xh, yh, xd
     torch.cuda.empty_cache()
@@ -505,7 +562,7 @@ def bench_decode(args, world, rank, kv8=False, seqs=None, cached=None):
     pk, pk_src = peaks()
     nb = decode_bytes(wl, kv_elem_bytes=1 if kv8 else 2)
     step_bytes = sum(nb.values())
-    kernels = {k: {"launches": n // nprof, "ms_per_step": t / nprof} for k, (n, t) in prof.items()}
+    kernels = {k: [n // nprof, round(t / nprof, 4)] for k, (n, t) in prof.items()}   # [launches, ms per step]
     attn = [k for k in prof if k.startswith("attn")]
     dom = max(prof.items(), key=lambda kv: kv[1][1])[0]
     out = {
@@ -723,6 +780,16 @@ def bench_decode_paged(args, world):
     return out
 
 
+def decode_summary(d):
+    """The dense decode step's headline figures, without its per-kernel record."""
+    if d is None:
+        return None
+    r = d.get("roofline", {})
+    return {"workload": d["workload"], "value": d["value"], "unit": d["unit"], "ms_per_step": d["ms_per_step"],
+            "bytes_per_step": d["bytes_per_step"], "hbm_frac_step": d["hbm_frac_step"],
+            "roofline": {k: r.get(k) for k in ("bound", "kernel", "achieved", "peak", "unit", "frac", "traffic")}}
+
+
 # ----------------------------------------------------------------------------- oracle legs
 ORACLE_SLICE = 128          # tokens per oracle step: 64 slices make up the S = 8192 sequence
 
@@ -826,6 +893,7 @@ def main():
     ap.add_argument("--no-chunked", action="store_true", help="skip the chunked-prefill line")
     ap.add_argument("--no-paged", action="store_true", help="skip the paged-cache decode line")
     ap.add_argument("--no-long", action="store_true", help="skip the 32K-context prefill and decode lines")
+    ap.add_argument("--no-rmsnorm", action="store_true", help="skip the standalone RMSNorm line")
     ap.add_argument("--prefill-seq", type=int, default=8192, help="tokens of the prefill workload (default 8192)")
     ap.add_argument("--decode-layers", type=int, default=32, help="layers of the decode stack (default 32)")
     args = ap.parse_args()
@@ -847,6 +915,7 @@ def main():
     pgd = None if (args.no_decode or args.no_paged) else bench_decode_paged(args, world)
     lpre = None if args.no_long else bench_prefill_long(args, world)
     ldec = None if (args.no_decode or args.no_long) else bench_decode(args, world, rank, seqs=16, cached=32768)
+    rms = None if args.no_rmsnorm else bench_rmsnorm(args, world)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline()
@@ -857,9 +926,11 @@ def main():
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,0.02) weights, N(0,1) inputs)",
             "config": pre["config"], "roofline": pre["roofline"], "cpu_baseline": cpu, "e2e": pre["e2e"],
             "gpu_launches": pre["gpu_launches"], "clocks": pre["clocks"], "block_tc_frac": pre["block_tc_frac"],
-            "block_tflops": pre["block_tflops"], "kernels": pre["kernels"], "decode": dec, "mha_prefill": mha,
-            "decode_kv8": dec8, "sample": smp, "chunked_prefill": chk, "decode_paged": pgd,
-            "prefill_32k": lpre, "decode_32k": ldec,
+            "block_tflops": pre["block_tflops"], "kernels": pre["kernels"], "prefill_sustained": pre["sustained"],
+            "decode_detail": dec, "mha_prefill": mha, "decode_kv8": dec8, "sample": smp, "chunked_prefill": chk,
+            "decode_paged": pgd, "prefill_32k": lpre, "decode_32k": ldec, "rmsnorm": rms,
+            # last, so that a reader of the line's tail sees it: the 32-layer B64 x 8192 dense decode step
+            "decode": decode_summary(dec),
         }
         print(json.dumps(line), flush=True)
     if world > 1:
