@@ -5,7 +5,8 @@
 
 Headline workload: one Llama-3-8B-shaped block prefill, B=1, S=8192 (bf16, fp32 accumulation).
 A step is one llama_block_forward call over the 8192 tokens (RMSNorm, fused QKV+RoPE+KV write,
-causal GQA attention, O projection + residual, RMSNorm, gate/up + SiLU*mul, down + residual).
+causal GQA attention, O projection + residual, RMSNorm, gate/up + SiLU*mul, down + residual), bf16
+input and weights, output in fp32 (LLAMA_Y_F32: the residual stream a stack hands on).
 `decode` reports the 32-layer batch-64 decode step against 8192 cached positions
 (llama_stack_decode_step, replayed as a CUDA graph).  Under torchrun every rank runs its own
 replica (the block has no exchange step); value = all ranks' tokens / max rank time.
@@ -210,18 +211,18 @@ def bench_mha_prefill(args, world):
     T = wl.B * wl.S
     w = W.device_layer(wl)
     x = W.device_x(wl).reshape(T, wl.d_model)
-    y = torch.empty_like(x)
+    y = torch.empty(x.shape, dtype=torch.float32, device="cuda")   # fp32 residual stream out
     ws = torch.empty(L.llama_workspace_bytes(L.OP_BLOCK_FORWARD, wl.dims, wl.dtype), dtype=torch.uint8,
                      device="cuda")
     bw = L.block_weights(w)
     stream = torch.cuda.current_stream()
     for _ in range(args.warmup):
-        L.llama_block_forward(wl.dims, wl.dtype, bw, x, y, 0, None, None, 0, ws, stream)
+        L.llama_block_forward(wl.dims, wl.dtype | L.Y_F32, bw, x, y, 0, None, None, 0, ws, stream)
     barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
-        L.llama_block_forward(wl.dims, wl.dtype, bw, x, y, 0, None, None, 0, ws, stream)
+        L.llama_block_forward(wl.dims, wl.dtype | L.Y_F32, bw, x, y, 0, None, None, 0, ws, stream)
     e1.record(stream)
     barrier(world)
     if L.llama_get_device_status() != 0:
@@ -332,14 +333,14 @@ def bench_prefill(args, world, rank):
     T = wl.B * wl.S
     w = W.device_layer(wl)
     x = W.device_x(wl).reshape(T, wl.d_model)
-    y = torch.empty_like(x)
+    y = torch.empty(x.shape, dtype=torch.float32, device="cuda")   # fp32 residual stream out
     ws = torch.empty(L.llama_workspace_bytes(L.OP_BLOCK_FORWARD, wl.dims, wl.dtype), dtype=torch.uint8,
                      device="cuda")
     bw = L.block_weights(w)
     stream = torch.cuda.current_stream()
 
     def step():
-        L.llama_block_forward(wl.dims, wl.dtype, bw, x, y, 0, None, None, 0, ws, stream)
+        L.llama_block_forward(wl.dims, wl.dtype | L.Y_F32, bw, x, y, 0, None, None, 0, ws, stream)
 
     for _ in range(args.warmup):
         step()
@@ -408,7 +409,7 @@ def bench_prefill(args, world, rank):
             stream.wait_event(in_done[k])
             if i >= 2:
                 stream.wait_event(out_done[k])     # step i-2's result has left yd[k]
-            L.llama_block_forward(wl.dims, wl.dtype, bw, xd[k], yd[k], 0, None, None, 0, ws, stream)
+            L.llama_block_forward(wl.dims, wl.dtype | L.Y_F32, bw, xd[k], yd[k], 0, None, None, 0, ws, stream)
             comp_done[k].record(stream)
             s_out.wait_event(comp_done[k])
             with torch.cuda.stream(s_out):
@@ -608,7 +609,7 @@ def bench_chunked_prefill(args, world):
     w = W.device_layer(wl)
     bw = L.block_weights(w)
     x = W.device_x(wl).reshape(T, wl.d_model)
-    y = torch.empty_like(x)
+    y = torch.empty(x.shape, dtype=torch.float32, device="cuda")   # fp32 residual stream out
     kc = W.device_tensor(BF16, (wl.B, cap, wl.n_kv, wl.head_dim), wl.seed, TID_KCACHE, 0.0, 1.0)
     vc = W.device_tensor(BF16, (wl.B, cap, wl.n_kv, wl.head_dim), wl.seed, TID_VCACHE, 0.0, 1.0)
     ws = torch.empty(L.llama_workspace_bytes(L.OP_BLOCK_FORWARD, wl.dims, wl.dtype), dtype=torch.uint8,
@@ -616,7 +617,7 @@ def bench_chunked_prefill(args, world):
     stream = torch.cuda.current_stream()
 
     def step():
-        L.llama_block_forward(wl.dims, wl.dtype, bw, x, y, pos0, kc, vc, cap, ws, stream)
+        L.llama_block_forward(wl.dims, wl.dtype | L.Y_F32, bw, x, y, pos0, kc, vc, cap, ws, stream)
 
     for _ in range(args.warmup):
         step()
@@ -658,13 +659,13 @@ def bench_prefill_long(args, world):
     w = W.device_layer(wl)
     bw = L.block_weights(w)
     x = W.device_x(wl).reshape(T, wl.d_model)
-    y = torch.empty_like(x)
+    y = torch.empty(x.shape, dtype=torch.float32, device="cuda")   # fp32 residual stream out
     ws = torch.empty(L.llama_workspace_bytes(L.OP_BLOCK_FORWARD, wl.dims, wl.dtype), dtype=torch.uint8,
                      device="cuda")
     stream = torch.cuda.current_stream()
 
     def step():
-        L.llama_block_forward(wl.dims, wl.dtype, bw, x, y, 0, None, None, 0, ws, stream)
+        L.llama_block_forward(wl.dims, wl.dtype | L.Y_F32, bw, x, y, 0, None, None, 0, ws, stream)
 
     for _ in range(args.warmup):
         step()

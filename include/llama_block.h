@@ -131,9 +131,20 @@ int llama_swiglu_ffn(const llama_dims* dims, int dtype, const void* x, const voi
                      const void* w_up, const void* w_down, void* y, void* ws, size_t ws_bytes,
                      void* stream);
 
+/* Residual-stream flags, OR-ed into the dtype argument of llama_block_forward only.  The
+ * residual stream is what one block hands to the next (x in, y out); a stack of prefill blocks
+ * keeps it in fp32 (as llama_stack_decode_step does) by giving its first block LLAMA_BF16 |
+ * LLAMA_Y_F32 and every later block LLAMA_BF16 | LLAMA_X_F32 | LLAMA_Y_F32.  The GEMM and
+ * attention operands, the weights and the KV cache keep the dtype; only x and y change.  With
+ * LLAMA_Y_F32 the call computes the same values and skips the final bf16 rounding of y, which
+ * alone is up to 2^-8 |y| (1.3e-2 of a row's RMS on the worst rows of the 4096-wide blocks).
+ * Both flags are ignored for LLAMA_F32, where x and y are fp32 already.                      */
+enum { LLAMA_X_F32 = 0x100, LLAMA_Y_F32 = 0x200 };
+
 /* One decoder block over B sequences of S new tokens at positions pos0 .. pos0+S-1
  * ("Llama Architecture ...", Step 2 LlamaTransformerBlock; "LLaMA Architecture > Model
  * Architecture", The Transformer Block).  x, y: [B*S, d_model]; y must not alias x.
+ * dtype: LLAMA_F32 or LLAMA_BF16, optionally OR-ed with LLAMA_X_F32 and LLAMA_Y_F32.
  * k_cache, v_cache: [B, cache_capacity, n_kv, hd]; on entry they hold positions 0..pos0-1,
  * and the call writes the rotated keys and the values of the new tokens at pos0..pos0+S-1.
  * Both NULL: pos0 must be 0 and the block's K/V live in the workspace.                       */

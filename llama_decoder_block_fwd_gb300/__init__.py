@@ -13,7 +13,7 @@ import threading
 from typing import Sequence
 
 __all__ = [
-    "F32", "BF16", "LlamaError", "Dims", "BlockWeights", "lib", "dims_of",
+    "F32", "BF16", "X_F32", "Y_F32", "LlamaError", "Dims", "BlockWeights", "lib", "dims_of",
     "llama_rmsnorm", "llama_rope", "llama_gqa_attention", "llama_gqa_attention_decode_noalloc", "llama_swiglu_ffn",
     "llama_block_forward", "llama_stack_decode_step", "llama_workspace_bytes",
     "llama_sample", "llama_embed", "llama_kv_quantize", "llama_gqa_attention_decode_kv8",
@@ -25,6 +25,7 @@ __all__ = [
 ]
 
 F32, BF16 = 0, 1
+X_F32, Y_F32 = 0x100, 0x200   # residual-stream flags for llama_block_forward's dtype (x fp32, y fp32)
 (OP_RMSNORM, OP_ROPE, OP_GQA_ATTENTION, OP_SWIGLU_FFN, OP_BLOCK_FORWARD,
  OP_STACK_DECODE_STEP) = range(6)
 STATUS_NAMES = {0: "LLAMA_OK", 1: "LLAMA_ERR_INVALID_ARG", 2: "LLAMA_ERR_UNSUPPORTED",

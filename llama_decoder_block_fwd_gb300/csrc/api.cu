@@ -454,8 +454,9 @@ bool block_weights_aligned(const llama_block_weights* w) {
 
 // One block on already-validated arguments (shared by block_forward and the decode stack).
 // x/y: dtype rows unless x_f32 (decode residual stream in fp32, updated in place: y == x).
+// x_f32: x is fp32; y is fp32 when x_f32 or y_f32 is set (the residual stream of a stack).
 int block_body(const llama_dims* d, int dtype, const llama_block_weights* w, const void* x, int x_f32, void* y,
-               int64_t pos0, void* kc, void* vc, int64_t cap, const BlockWs& ws, cudaStream_t st) {
+               int64_t pos0, void* kc, void* vc, int64_t cap, const BlockWs& ws, cudaStream_t st, int y_f32 = 0) {
   const int64_t T = d->B * d->S, D = d->d_model, hq = d->n_q * d->head_dim;
   const int f32 = dtype == LLAMA_F32;
   const float eps = (float)d->eps;
@@ -486,8 +487,9 @@ int block_body(const llama_dims* d, int dtype, const llama_block_weights* w, con
   a.ws = ws.attn;
   a.ws_bytes = ws.attn_bytes;
   if ((rc = run_attention(a, st)) != LLAMA_OK) return rc;
-  // h = x + o W_O^T, kept in fp32 (decode: the fp32 stream is updated in place)
-  void* h = x_f32 ? y : ws.h;
+  // h = x + o W_O^T, kept in fp32; an fp32 y holds it (the down projection then adds in place)
+  y_f32 = y_f32 || x_f32 || f32;
+  void* h = y_f32 ? y : ws.h;
   GemmDesc go = linear_resid_desc(dtype, T, ws.o, hq, w->wo, D, x, x_f32 || f32, h, 1);
   // m = SiLU(w W_gate^T) * (w W_up^T), w = RMSNorm(h; g_ffn) in the same split form (reuses u)
   GemmDesc gu = gate_up_desc(dtype, T, ws.u, D, w->w_gate, w->w_up, d->d_ff, ws.m, ws.rs2);
@@ -512,7 +514,7 @@ int block_body(const llama_dims* d, int dtype, const llama_block_weights* w, con
     return rc;
   if ((rc = run_gemm(gu, nullptr, st)) != LLAMA_OK) return rc;
   // y = h + m W_down^T
-  return run_linear_resid(dtype, T, ws.m, d->d_ff, w->w_down, D, h, 1, y, x_f32 || f32, st);
+  return run_linear_resid(dtype, T, ws.m, d->d_ff, w->w_down, D, h, 1, y, y_f32, st);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -895,11 +897,13 @@ int llama_swiglu_ffn(const llama_dims* d, int dtype, const void* x, const void* 
   return run_linear_resid(dtype, T, ws, d->d_ff, w_down, d->d_model, nullptr, 0, y, dtype == LLAMA_F32, st);
 }
 
-int llama_block_forward(const llama_dims* d, int dtype, const llama_block_weights* w, const void* x, void* y,
+int llama_block_forward(const llama_dims* d, int dtype_flags, const llama_block_weights* w, const void* x, void* y,
                         int64_t pos0, void* k_cache, void* v_cache, int64_t cache_capacity, void* ws, size_t ws_bytes,
                         void* stream) {
   int rc;
+  const int dtype = dtype_flags & ~(LLAMA_X_F32 | LLAMA_Y_F32);
   if ((rc = check_dtype(dtype)) != LLAMA_OK) return rc;
+  const int x_f32 = (dtype_flags & LLAMA_X_F32) ? 1 : 0, y_f32 = (dtype_flags & LLAMA_Y_F32) ? 1 : 0;
   if ((rc = check_dims(d, NEED_D | NEED_HEADS | NEED_FF)) != LLAMA_OK) return rc;
   if (!block_weights_ok(w) || !x || !y || x == y) return LLAMA_ERR_INVALID_ARG;
   const bool own_kv = !k_cache && !v_cache;
@@ -919,7 +923,8 @@ int llama_block_forward(const llama_dims* d, int dtype, const llama_block_weight
   BlockWs b = plan_block(d, dtype, own_kv, ws, cache_capacity);
   void* kc = own_kv ? b.k : k_cache;
   void* vc = own_kv ? b.v : v_cache;
-  return block_body(d, dtype, w, x, 0, y, pos0, kc, vc, cache_capacity, b, static_cast<cudaStream_t>(stream));
+  return block_body(d, dtype, w, x, x_f32, y, pos0, kc, vc, cache_capacity, b, static_cast<cudaStream_t>(stream),
+                    y_f32);
 }
 
 int llama_stack_decode_step(const llama_dims* d, int dtype, int n_layers, const llama_block_weights* layers,

@@ -222,9 +222,9 @@ def test_llama3_8b_block_prefill_32k_tokens():
     T = wl.B * wl.S
     w = W.device_layer(wl)
     x = W.device_x(wl).reshape(T, wl.d_model)
-    y = torch.empty_like(x)
+    y = torch.empty(x.shape, dtype=torch.float32, device="cuda")       # fp32 output, as the bench runs it
     ws = torch.empty(L.llama_workspace_bytes(L.OP_BLOCK_FORWARD, wl.dims, wl.dtype), dtype=torch.uint8, device="cuda")
-    L.llama_block_forward(wl.dims, wl.dtype, L.block_weights(w), x, y, 0, None, None, 0, ws)
+    L.llama_block_forward(wl.dims, wl.dtype | L.Y_F32, L.block_weights(w), x, y, 0, None, None, 0, ws)
     torch.cuda.synchronize()
     assert L.llama_get_device_status() == 0
     rows = sample_rows(wl.S, 48)
