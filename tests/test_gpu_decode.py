@@ -68,6 +68,18 @@ def test_decode_small_stack_full(hd, vocab):
             assert not np.array_equal(got[wl.t_cache], before[wl.t_cache])
 
 
+def test_decode_stack_narrow_model():
+    """d_model 128 with 4 query heads and 1 KV head of 128 (so n_q * head_dim = 512 != d_model, a
+    general W_O) and d_ff 256: every weight-streaming projection is one or a few 128-row tiles with
+    short K ranges, and the LM head 256 rows; three layers against the oracle."""
+    wl = C.Workload("tiny-stack", 8, C.BF16, 5, 1, 128, 4, 1, 128, 256, 1e4, 1e-5, gain_std=0.1, n_layers=3,
+                    t_cache=200, vocab=256)
+    cap = 256
+    logits, _, _ = _decode(wl, cap)
+    ref = _oracle(wl, list(range(wl.B)), cap)
+    assert_parity(to_f64(logits), ref, wl.dtype, "tiny stack logits")
+
+
 def test_decode_fp32_toy_stack():
     wl = C.Workload("toy-stack", 7, C.F32, 2, 1, 16, 8, 2, 2, 48, 1e4, 1e-5, n_layers=2, t_cache=5, vocab=11)
     cap = 8
