@@ -14,6 +14,7 @@ replica (the block has no exchange step); value = all ranks' tokens / max rank t
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -240,9 +241,25 @@ def bench_mha_prefill(args, world):
     return out
 
 
+class L2Flush:
+    """Evicts L2 between timed calls: a 256 MB write, then a 256 MB read, so that L2 (129 MB)
+    holds neither the timed call's inputs nor dirty lines whose write-back would land inside the
+    timed call.  The ~80 us of device work also covers the host's launch latency of the call."""
+    what = "flushed before every call (256 MB written, then 256 MB read)"
+
+    def __init__(self):
+        import torch
+        self.w = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+        self.r = torch.ones(64 << 20, dtype=torch.int32, device="cuda")
+
+    def __call__(self):
+        self.w.fill_(1)
+        self.r.sum()
+
+
 def bench_sample(args, world):
     """Next-token choice for the decode batch: 64 rows of 128256 fp32 logits, temperature 0.8,
-    top-k 50, top-p 0.95.  L2 is flushed (a 256 MB write) before every timed call."""
+    top-k 50, top-p 0.95.  L2 is flushed (L2Flush) before every timed call."""
     import numpy as np
     import torch
 
@@ -255,14 +272,14 @@ def bench_sample(args, world):
     z = W.device_tensor(F32, (wl.B, wl.vocab), wl.seed, TID_LOGITS, 0.0, 2.5)
     u = torch.from_numpy(np.random.default_rng(wl.seed).random(wl.B).astype(np.float32)).cuda()
     tok = torch.empty(wl.B, dtype=torch.int32, device="cuda")
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    flush = L2Flush()
     stream = torch.cuda.current_stream()
     for _ in range(args.warmup):
         L.llama_sample(z, 0.8, 50, 0.95, u, tok)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     barrier(world)
     for a, b in ev:
-        flush.fill_(1)
+        flush()
         a.record(stream)
         L.llama_sample(z, 0.8, 50, 0.95, u, tok)
         b.record(stream)
@@ -271,7 +288,7 @@ def bench_sample(args, world):
     nbytes = z.numel() * 4
     out = {"workload": f"{wl.B} x {wl.vocab} fp32 logits, T 0.8, top-k 50, top-p 0.95", "us_per_call": ms * 1e3,
            "rows_per_s": aggregate_rate(world, wl.B, ms), "logits_gbs": nbytes / (ms / 1e3) / 1e9,
-           "l2": "flushed before every call"}
+           "l2": L2Flush.what}
     del z, u, tok, flush
     torch.cuda.empty_cache()
     return out
@@ -279,7 +296,7 @@ def bench_sample(args, world):
 
 def bench_rmsnorm(args, world):
     """Standalone llama_rmsnorm on the 8B block's prefill activations: 8192 x 4096 bf16 rows in,
-    bf16 rows out, bf16 gains.  L2 is flushed (a 256 MB write) before every timed call."""
+    bf16 rows out, bf16 gains.  L2 is flushed (L2Flush) before every timed call."""
     import torch
 
     import llama_decoder_block_fwd_gb300 as L
@@ -287,33 +304,43 @@ def bench_rmsnorm(args, world):
     from synth import workloads as W
 
     wl = C.LLAMA3_8B_PREFILL
+    if args.rmsnorm_rows != wl.S:
+        wl = dataclasses.replace(wl, S=args.rmsnorm_rows, name=f"{wl.name}-rows{args.rmsnorm_rows}")
     T = wl.B * wl.S
     x = W.device_x(wl).reshape(T, wl.d_model)
     g = W.device_layer(wl)["attn_norm_g"]
     y = torch.empty_like(x)
     dims = (wl.B, wl.S, wl.d_model, wl.n_q, wl.n_kv, wl.head_dim, wl.d_ff, wl.theta_base, wl.eps)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    flush = L2Flush()
     stream = torch.cuda.current_stream()
-    for _ in range(args.warmup):
+    # warm-up: at least W calls and a quarter second of them (a GPU fresh from idle ran its first
+    # few milliseconds of calls up to 20% slower)
+    t0, n = time.perf_counter(), 0
+    while n < args.warmup or time.perf_counter() - t0 < 0.25:
+        flush()
         L.llama_rmsnorm(dims, wl.dtype, x, g, y, stream)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        n += 1
+    steps = max(args.steps, 100)   # ~40 ms of calls with their flushes
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     barrier(world)
     for a, b in ev:
-        flush.fill_(1)
+        flush()
         a.record(stream)
         L.llama_rmsnorm(dims, wl.dtype, x, g, y, stream)
         b.record(stream)
     barrier(world)
     if L.llama_get_device_status() != 0:
         raise RuntimeError("device status word set during the RMSNorm line")
-    ms = max_over_ranks(world, sum(a.elapsed_time(b) for a, b in ev) / args.steps)
+    ms = max_over_ranks(world, sum(a.elapsed_time(b) for a, b in ev) / steps)
     pk, pk_src = peaks()
     nbytes = x.numel() * 2 + y.numel() * 2 + g.numel() * 2
     gbs = nbytes / (ms / 1e3) / 1e9
     out = {"workload": f"llama_rmsnorm {T} x {wl.d_model} bf16", "us_per_call": ms * 1e3, "bytes_per_call": nbytes,
-           "roofline": {"bound": "hbm", "kernel": "rmsnorm", "achieved": gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                        "frac": gbs / pk["hbm_gbs"], "peak_source": f"{pk_src} hbm"},
-           "l2": "flushed before every call"}
+           "calls_timed": steps, "warmup_calls": n,
+           "roofline": {"bound": "hbm", "kernel": "rmsnorm_stream", "achieved": gbs, "peak": pk["hbm_gbs"],
+                        "unit": "GB/s", "frac": gbs / pk["hbm_gbs"], "peak_source": f"{pk_src} hbm",
+                        "traffic": kernel_traffic("rmsnorm_stream") if T == 8192 else None},
+           "l2": L2Flush.what}
     del x, g, y, flush
     torch.cuda.empty_cache()
     return out
@@ -895,6 +922,9 @@ def main():
     ap.add_argument("--no-paged", action="store_true", help="skip the paged-cache decode line")
     ap.add_argument("--no-long", action="store_true", help="skip the 32K-context prefill and decode lines")
     ap.add_argument("--no-rmsnorm", action="store_true", help="skip the standalone RMSNorm line")
+    ap.add_argument("--rmsnorm-rows", type=int, default=8192, help="rows of the standalone RMSNorm line")
+    ap.add_argument("--only", choices=["prefill", "decode", "decode_kv8", "rmsnorm"],
+                    help="run this one line alone and print its record (for profiler captures)")
     ap.add_argument("--prefill-seq", type=int, default=8192, help="tokens of the prefill workload (default 8192)")
     ap.add_argument("--decode-layers", type=int, default=32, help="layers of the decode stack (default 32)")
     args = ap.parse_args()
@@ -907,6 +937,14 @@ def main():
         return
 
     world, rank, local = dist_setup()
+    if args.only:   # a profiling aid: one line alone
+        rec = {"prefill": lambda: bench_prefill(args, world, rank),
+               "decode": lambda: bench_decode(args, world, rank),
+               "decode_kv8": lambda: bench_decode(args, world, rank, kv8=True),
+               "rmsnorm": lambda: bench_rmsnorm(args, world)}[args.only]()
+        if rank == 0:
+            print(json.dumps({args.only: rec}), flush=True)
+        return
     pre = bench_prefill(args, world, rank)
     mha = None if args.no_mha else bench_mha_prefill(args, world)
     dec = None if args.no_decode else bench_decode(args, world, rank)

@@ -35,7 +35,12 @@ def test_synth_device_matches_host_bitwise():
 
 
 @pytest.mark.parametrize("dtype,rows,d", [(synth.F32, 4, 16), (synth.BF16, 512, 512), (synth.BF16, 37, 4096),
-                                          (synth.F32, 9, 4096), (synth.BF16, 3, 520), (synth.F32, 5, 12)])
+                                          (synth.F32, 9, 4096), (synth.BF16, 3, 520), (synth.F32, 5, 12),
+                                          # the streaming kernel (bf16, >= 304 rows of 1024..4096): ragged
+                                          # last round over the SMs, the narrowest and widest rows, and the
+                                          # 8B block's 8192 x 4096 activations
+                                          (synth.BF16, 305, 1024), (synth.BF16, 1001, 2056),
+                                          (synth.BF16, 2000, 4096), (synth.BF16, 8192, 4096)])
 def test_rmsnorm(dtype, rows, d):
     import torch
     x = dev_tensor(dtype, (rows, d), SEED, 1, 0.0, 1.0)
