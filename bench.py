@@ -923,7 +923,7 @@ def main():
     ap.add_argument("--no-long", action="store_true", help="skip the 32K-context prefill and decode lines")
     ap.add_argument("--no-rmsnorm", action="store_true", help="skip the standalone RMSNorm line")
     ap.add_argument("--rmsnorm-rows", type=int, default=8192, help="rows of the standalone RMSNorm line")
-    ap.add_argument("--only", choices=["prefill", "decode", "decode_kv8", "rmsnorm"],
+    ap.add_argument("--only", choices=["prefill", "decode", "decode_kv8", "rmsnorm", "sample"],
                     help="run this one line alone and print its record (for profiler captures)")
     ap.add_argument("--prefill-seq", type=int, default=8192, help="tokens of the prefill workload (default 8192)")
     ap.add_argument("--decode-layers", type=int, default=32, help="layers of the decode stack (default 32)")
@@ -941,7 +941,8 @@ def main():
         rec = {"prefill": lambda: bench_prefill(args, world, rank),
                "decode": lambda: bench_decode(args, world, rank),
                "decode_kv8": lambda: bench_decode(args, world, rank, kv8=True),
-               "rmsnorm": lambda: bench_rmsnorm(args, world)}[args.only]()
+               "rmsnorm": lambda: bench_rmsnorm(args, world),
+               "sample": lambda: bench_sample(args, world)}[args.only]()
         if rank == 0:
             print(json.dumps({args.only: rec}), flush=True)
         return

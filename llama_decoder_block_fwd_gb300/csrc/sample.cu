@@ -8,15 +8,22 @@
 // top-k mass reaches p; the draw walks the kept tokens in increasing id and stops at the first
 // whose cumulative mass exceeds u times the kept mass (u in [0, 1) is supplied by the caller).
 //
-// One CTA per row.  Top-k up to 1024 (the usual case): the argmax pass over the row also keeps
-// every thread's two largest logits; the k-th largest of those bounds the k-th largest logit from
-// below, so a second pass gathers the few tokens at or above that bound into shared memory, where
-// they are ranked by a bitonic sort.  Otherwise (or when too many tokens tie near the bound) the
+// A cluster of P CTAs per row (P up to 8, chosen so that the B x P CTAs cover the SMs; P = 1 for
+// rows that are not 16-byte aligned or for the general path below).  Each CTA takes 1/P of the row
+// for the argmax pass; the partial maxima are exchanged through distributed shared memory.
+// Top-k up to 1024 (the usual case): the argmax pass also keeps every thread's two largest logits;
+// the k-th largest of those bounds the k-th largest logit of the CTA's part of the row from below,
+// so a second pass over that part (from L2) gathers the few tokens at or above the bound into the
+// CTA's shared memory.  Every token of the row's top k is among the top k of its own part, hence
+// gathered; the cluster's leader CTA copies the other CTAs' candidates into its own shared memory
+// and ranks them all by a bitonic sort.  Otherwise (or when too many tokens tie near the bound) the
 // thresholds are found by radix selection on an order-preserving 32-bit key of the logit, four
 // 8-bit digits from the top: by count for top-k, by probability mass for top-p, one pass over the
 // row (from L2) per digit.  Masses are exp((z - z_max) / T) in fp32, held as 2^-40 fixed point in
 // 64-bit integers so that every sum is exact and independent of the order of the atomic adds: the
 // same logits always give the same token.  Terms below 2^-40 of the largest count as zero.
+#include <cooperative_groups.h>
+
 #include <climits>
 
 #include "kernels.h"
@@ -54,6 +61,8 @@ struct SampleShared {
   u64 b64[4];
   unsigned b32[4];
   int bidx;
+  float cval;   // this CTA's part of the row: its largest logit and that logit's lowest id
+  int cidx;
 };
 
 // Exclusive prefix sum of v over the threads in id order; *total gets the block's sum.
@@ -119,36 +128,63 @@ __device__ void select_digit(SampleShared& sh, u64 target) {
   }
 }
 
-// Call f(i, z_i, valid) for every element of the row: 16-byte loads, two in flight per thread,
-// the same trip count on every lane of a warp (f may use warp-collective operations); `valid` is
-// false on the padding calls.  z must be 16-byte aligned.
+// Call f(i, z_i, valid) for every element of the float4 units [q_lo, q_hi) of the row, and, when
+// `tail`, for its last V % 4 elements: 16-byte loads, two in flight per thread, the same trip count
+// on every lane of a warp (f may use warp-collective operations); `valid` is false on the padding
+// calls.  z must be 16-byte aligned.
 template <typename F>
-__device__ __forceinline__ void row_pass4(const float* __restrict__ z, int V, F&& f) {
+__device__ __forceinline__ void row_pass4(const float* __restrict__ z, int V, int q_lo, int q_hi, bool tail, F&& f) {
   const int lane = threadIdx.x & 31;
   const int nv4 = V >> 2;
   const float4* z4 = reinterpret_cast<const float4*>(z);
-  for (int base = (int)(threadIdx.x & ~31u); base < nv4; base += 2 * SP_THREADS) {
+  for (int base = q_lo + (int)(threadIdx.x & ~31u); base < q_hi; base += 2 * SP_THREADS) {
     const int q0 = base + lane, q1 = base + SP_THREADS + lane;
-    const bool ok0 = q0 < nv4, ok1 = q1 < nv4;
+    const bool ok0 = q0 < q_hi, ok1 = q1 < q_hi;
     const float4 w0 = ok0 ? __ldg(z4 + q0) : make_float4(0.f, 0.f, 0.f, 0.f);
     const float4 w1 = ok1 ? __ldg(z4 + q1) : make_float4(0.f, 0.f, 0.f, 0.f);
     f(4 * q0, w0.x, ok0); f(4 * q0 + 1, w0.y, ok0); f(4 * q0 + 2, w0.z, ok0); f(4 * q0 + 3, w0.w, ok0);
-    if (base + SP_THREADS < nv4) {   // warp-uniform
+    if (base + SP_THREADS < q_hi) {   // warp-uniform
       f(4 * q1, w1.x, ok1); f(4 * q1 + 1, w1.y, ok1); f(4 * q1 + 2, w1.z, ok1); f(4 * q1 + 3, w1.w, ok1);
     }
   }
-  if (threadIdx.x < 32) {   // the last V % 4 elements
+  if (tail && threadIdx.x < 32) {   // the last V % 4 elements
     const int i = 4 * nv4 + lane;
     const bool ok = i < V;
     f(i, ok ? z[i] : 0.f, ok);
   }
 }
 
-// row_pass4 on a 16-byte aligned row, else one element per thread and step (same contract).
+// A walk over the float4 units [q_lo, q_hi) with U loads in flight per thread: one call
+// f4(q, w, valid) per unit q, a thread's units in increasing q, the same calls on every lane of a
+// warp (f4 may use warp-collective operations).  U x 16 KB per CTA in flight keeps a pass from being
+// bound by load latency (a row part is only a few such rounds).
+template <int U, typename F4>
+__device__ __forceinline__ void row_pass_f4(const float* __restrict__ z, int q_lo, int q_hi, F4&& f4) {
+  const int lane = threadIdx.x & 31;
+  const float4* z4 = reinterpret_cast<const float4*>(z);
+  for (int base = q_lo + (int)(threadIdx.x & ~31u); base < q_hi; base += U * SP_THREADS) {
+    float4 w[U];
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+      const int q = base + j * SP_THREADS + lane;
+      w[j] = q < q_hi ? __ldg(z4 + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int j = 0; j < U; ++j) {
+      const int q = base + j * SP_THREADS + lane;
+      if (base + j * SP_THREADS < q_hi) f4(q, w[j], q < q_hi);   // warp-uniform
+    }
+  }
+}
+
+__device__ __forceinline__ float max4(const float4& w) { return fmaxf(fmaxf(w.x, w.y), fmaxf(w.z, w.w)); }
+
+// row_pass4 over the whole of a 16-byte aligned row, else one element per thread and step (same
+// contract).
 template <typename F>
 __device__ __forceinline__ void row_each(const float* __restrict__ z, int V, bool vec, F&& f) {
   if (vec) {
-    row_pass4(z, V, f);
+    row_pass4(z, V, 0, V >> 2, true, f);
   } else {
     for (int base = (int)(threadIdx.x & ~31u); base < V; base += SP_THREADS) {
       const int i = base + (int)(threadIdx.x & 31);
@@ -177,6 +213,27 @@ __device__ void sort_desc(u64* ckey, float* cz, int n2) {
   }
 }
 
+// Sort of n <= SP_THREADS distinct keys by rank: thread t counts the keys that go before its own and
+// moves its entry there (one barrier, against a bitonic network's log^2 n).  Worth it for short
+// lists only, since every thread reads all n keys.  DESC: larger keys first.  cz (may be null) moves
+// alongside.
+template <bool DESC>
+__device__ void sort_by_rank(u64* ckey, float* cz, int n) {
+  const int t = threadIdx.x;
+  const u64 mine = t < n ? ckey[t] : 0ull;
+  const float mz = (cz && t < n) ? cz[t] : 0.f;
+  int r = 0;
+  if (t < n)
+    for (int j = 0; j < n; ++j) r += DESC ? (ckey[j] > mine) : (ckey[j] < mine);
+  __syncthreads();
+  if (t < n) {
+    ckey[r] = mine;
+    if (cz) cz[r] = mz;
+  }
+  __syncthreads();
+}
+constexpr int SP_RANK_SORT_MAX = 256;
+
 // The id of the n-th (1-based) token, in increasing id, for which pred(i, z_i) holds.
 template <typename Pred>
 __device__ int nth_index(const float* z, int V, int n, Pred pred, SampleShared& sh) {
@@ -202,11 +259,19 @@ __global__ void __launch_bounds__(SP_THREADS) sample_kernel(const float* __restr
                                                             float temperature, int top_k, float top_p,
                                                             const float* __restrict__ uniforms, int* __restrict__ tokens) {
   __shared__ SampleShared sh;
-  const int row = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  namespace cg = cooperative_groups;
+  const cg::cluster_group cl = cg::this_cluster();
+  const int P = (int)cl.num_blocks(), cr = (int)cl.block_rank();   // P = 1 without a cluster launch
+  const int row = blockIdx.x / P, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const float* z = logits + (int64_t)row * ld;
 
-  // ---- the largest logit and its lowest id (argmax)
+  // ---- the largest logit and its lowest id (argmax); CTA cr of the cluster takes the float4
+  //      units [q_lo, q_hi) and, the last one, the V % 4 tail (P > 1 only for aligned rows)
   const bool vec = (reinterpret_cast<uintptr_t>(z) & 15) == 0;
+  const int nv4 = V >> 2, per_cta = (nv4 + P - 1) / P;
+  const int q_lo = min(nv4, cr * per_cta), q_hi = min(nv4, q_lo + per_cta);
+  const bool tail = cr == P - 1;
+
   // small top-k: the argmax pass also keeps each thread's two largest logits; the k-th largest
   // of those 2 x SP_THREADS values bounds the k-th largest logit from below, so one more pass
   // gathers every token at or above it and the ranking is finished in shared memory
@@ -218,11 +283,18 @@ __global__ void __launch_bounds__(SP_THREADS) sample_kernel(const float* __restr
   float best = -INFINITY, second = -INFINITY;
   int bi = INT_MAX;
   if (vec) {
-    row_pass4(z, V, [&](int i, float v, bool ok) {
+    auto upd = [&](int i, float v, bool ok) {
       if (!ok) return;
       if (v > best || (v == best && i < bi)) { second = best; best = v; bi = i; }
       else if (v > second) { second = v; }
+    };
+    // a unit whose largest value is not above the thread's second largest changes nothing (the
+    // thread visits ids in increasing order, so an equal maximum found later keeps the lower id)
+    row_pass_f4<8>(z, q_lo, q_hi, [&](int q, const float4& w, bool ok) {
+      if (!ok || !(max4(w) > second)) return;
+      upd(4 * q, w.x, true); upd(4 * q + 1, w.y, true); upd(4 * q + 2, w.z, true); upd(4 * q + 3, w.w, true);
     });
+    row_pass4(z, V, q_hi, q_hi, tail, upd);   // the V % 4 tail
   } else {
     for (int i = tid; i < V; i += SP_THREADS) {
       const float v = z[i];
@@ -243,9 +315,19 @@ __global__ void __launch_bounds__(SP_THREADS) sample_kernel(const float* __restr
   for (int w = 1; w < SP_WARPS; ++w) {
     if (sh.wval[w] > best || (sh.wval[w] == best && sh.widx[w] < bi)) { best = sh.wval[w]; bi = sh.widx[w]; }
   }
+  if (P > 1) {   // the row's maximum from the CTAs' maxima (each CTA reads them all)
+    if (tid == 0) { sh.cval = best; sh.cidx = bi; }
+    cl.sync();
+    for (int r = 0; r < P; ++r) {
+      const float ov = *cl.map_shared_rank(&sh.cval, r);
+      const int oi = *cl.map_shared_rank(&sh.cidx, r);
+      if (ov > best || (ov == best && oi < bi)) { best = ov; bi = oi; }
+    }
+    cl.sync();   // no CTA leaves, or overwrites sh, while another still reads it
+  }
   const float zmax = best;
   if (!(temperature > 0.f) || top_k == 1 || !(top_p > 0.f) || !isfinite(zmax) || V == 1) {
-    if (tid == 0) tokens[row] = bi == INT_MAX ? 0 : bi;
+    if (tid == 0 && cr == 0) tokens[row] = bi == INT_MAX ? 0 : bi;
     return;
   }
   auto mass = [&](float v) -> u64 { return __float2ull_rz(expf((v - zmax) / temperature) * kMassOne); };
@@ -281,8 +363,8 @@ __global__ void __launch_bounds__(SP_THREADS) sample_kernel(const float* __restr
     const uint32_t tau = prefix;
     if (tid == 0) sh.ccount = 0u;
     __syncthreads();
-    // ---- second pass (from L2): gather the tokens whose key is at least tau
-    row_pass4(z, V, [&](int i, float v, bool ok) {
+    // ---- second pass (from L2): gather the tokens of this CTA's part whose key is at least tau
+    auto gather = [&](int i, float v, bool ok) {
       const uint32_t key = order_key(v);
       const bool take = ok && key >= tau;
       const unsigned tm = __ballot_sync(0xffffffffu, take);
@@ -298,8 +380,35 @@ __global__ void __launch_bounds__(SP_THREADS) sample_kernel(const float* __restr
           }
         }
       }
+    };
+    row_pass_f4<8>(z, q_lo, q_hi, [&](int q, const float4& w, bool ok) {
+      if (!__any_sync(0xffffffffu, ok && order_key(max4(w)) >= tau)) return;   // most units: nothing to take
+      gather(4 * q, w.x, ok); gather(4 * q + 1, w.y, ok); gather(4 * q + 2, w.z, ok); gather(4 * q + 3, w.w, ok);
     });
+    row_pass4(z, V, q_hi, q_hi, tail, gather);   // the V % 4 tail
     __syncthreads();
+    if (P > 1) {   // the leader appends the other CTAs' candidates to its own
+      cl.sync();
+      if (cr == 0) {
+        unsigned total = sh.ccount;
+        for (int r = 1; r < P; ++r) total += *cl.map_shared_rank(&sh.ccount, r);
+        if (total <= (unsigned)SP_CAP) {
+          unsigned at = sh.ccount;
+          for (int r = 1; r < P; ++r) {
+            const unsigned n_r = *cl.map_shared_rank(&sh.ccount, r);
+            const u64* rk = cl.map_shared_rank(ckey, r);
+            const float* rz = cl.map_shared_rank(cz, r);
+            for (unsigned t = tid; t < n_r; t += SP_THREADS) { ckey[at + t] = rk[t]; cz[at + t] = rz[t]; }
+            at += n_r;
+          }
+        }
+        __syncthreads();
+        if (tid == 0) sh.ccount = total;   // > SP_CAP: too many to rank here, the general path below
+      }
+      cl.sync();   // the others' shared memory stays until the leader has read it
+      if (cr != 0) return;
+      __syncthreads();
+    }
     const unsigned gathered = sh.ccount;
     if (gathered <= (unsigned)SP_CAP && gathered >= (unsigned)top_k) {
       const int nc = (int)gathered;
@@ -307,7 +416,9 @@ __global__ void __launch_bounds__(SP_THREADS) sample_kernel(const float* __restr
       while (n2 < nc) n2 <<= 1;
       for (int t = nc + tid; t < n2; t += SP_THREADS) ckey[t] = 0ull;   // sorts after every candidate
       __syncthreads();
-      sort_desc(ckey, cz, n2);   // larger key first, then lower id (its complement is larger)
+      // larger key first, then lower id (its complement is larger)
+      if (nc <= SP_RANK_SORT_MAX) sort_by_rank<true>(ckey, cz, nc);
+      else sort_desc(ckey, cz, n2);
       // the top-k set is the first top_k; masses in ranked order; the shortest prefix reaching
       // top_p of the top-k mass
       const int n = top_k;
@@ -334,6 +445,7 @@ __global__ void __launch_bounds__(SP_THREADS) sample_kernel(const float* __restr
       __syncthreads();
       if (tid < m2) ckey[tid] = kept_t ? (((u64)id_t << 32) | (u64)tid) : ~0ull;   // (id, ranked slot)
       __syncthreads();
+      if (n_p <= SP_RANK_SORT_MAX) { sort_by_rank<false>(ckey, nullptr, n_p); m2 = 0; }
       for (int size = 2; size <= m2; size <<= 1) {
         for (int stride = size >> 1; stride > 0; stride >>= 1) {
           for (int t = tid; t < m2; t += SP_THREADS) {
@@ -361,6 +473,8 @@ __global__ void __launch_bounds__(SP_THREADS) sample_kernel(const float* __restr
     // more candidates than fit: the general path below
   }
 
+  // ---- the general path: one CTA over the whole row (with P > 1 only the leader gets here)
+  if (cr != 0) return;
   // ---- top-k: the k-th largest key kk; ties at kk are kept up to id kcut
   uint32_t kk = 0u;
   int kcut = INT_MAX;
@@ -636,7 +750,30 @@ int launch_sample(const float* logits, int64_t B, int64_t V, int64_t ld, float t
       return -1;
     attr_set[dev] = true;
   }
-  sample_kernel<<<(unsigned)B, SP_THREADS, SP_DYN_SMEM, st>>>(logits, ld, (int)V, temperature, k, top_p, u, tokens);
+  // CTAs per row: a power of two up to 8 such that B x P CTAs (one per SM) still fit on the GPU, each
+  // taking at least 4096 logits; only for 16-byte aligned rows on the argmax and small top-k paths
+  // (the general path runs on one CTA per row)
+  const bool argmax = !(temperature > 0.f) || k == 1 || !(top_p > 0.f) || V == 1;
+  const bool small_k = temperature > 0.f && k >= 2 && k <= SP_SMALL_K && top_p > 0.f;
+  const bool aligned = (reinterpret_cast<uintptr_t>(logits) & 15) == 0 && ld % 4 == 0;
+  int P = 1;
+  if (aligned && (argmax || small_k))
+    while (P < 8 && B * (2 * P) <= num_sms() && V / (2 * P) >= 4096) P *= 2;
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3((unsigned)(B * P));
+  cfg.blockDim = dim3(SP_THREADS);
+  cfg.dynamicSmemBytes = SP_DYN_SMEM;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)P;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = P > 1 ? 1 : 0;
+  if (cudaLaunchKernelEx(&cfg, sample_kernel, logits, ld, (int)V, temperature, k, top_p, u, tokens) != cudaSuccess)
+    return -1;
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 

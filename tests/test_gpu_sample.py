@@ -94,6 +94,31 @@ def test_argmax_ties_go_to_the_lowest_id():
     np.testing.assert_array_equal(got, [int(np.flatnonzero(zh[b] == zh[b].max())[0]) for b in range(B)])
 
 
+def test_rows_split_over_a_cluster_ties_across_parts():
+    """Few rows over a large vocabulary: each row is split over a cluster of up to eight CTAs.  Equal
+    maxima that sit in different CTAs' parts still go to the lowest id, and small top-k draws
+    (candidates gathered by every CTA, ranked by the leader) match the oracle."""
+    import torch
+    B, V = 8, 65536
+    zh = np.round(np.random.default_rng(21).normal(0, 1, (B, V)))     # integers: equal maxima far apart
+    zh[3, 5] = zh[3, V - 3] = zh[3].max() + 1.0                       # first and last part
+    z = torch.from_numpy(zh.astype(np.float32)).cuda()
+    u, uh = _uniforms(B, seed=21)
+    got = _run(z, 0.0, 0, 1.0, u)
+    np.testing.assert_array_equal(got, [int(np.flatnonzero(zh[b] == zh[b].max())[0]) for b in range(B)])
+    for k, p in ((50, 0.95), (1024, 0.9), (2, 1.0)):
+        got = _run(z, 1.0, k, p, u)
+        for b in range(B):
+            assert int(got[b]) in set(S.order_desc(zh[b])[:k].tolist())
+        _check(zh, 1.0, k, p, uh, got)
+    z1, z1h = _logits(1, 128256, 2.5)                                 # one row: eight CTAs
+    u1, u1h = _uniforms(1, seed=3)
+    for T, k, p in ((0.8, 50, 0.95), (0.0, 0, 1.0)):
+        got = _run(z1, T, k, p, u1)
+        want = S.argmax(z1h[0]) if T == 0.0 else S.sample(z1h[0], T, k, p, min(u1h[0], 0.99999994))
+        assert int(got[0]) == want or (T > 0 and _valid(z1h[0], T, k, p, u1h[0], int(got[0])))
+
+
 @pytest.mark.parametrize("T,k,p", [(1.0, 0, 1.0), (0.7, 50, 1.0), (1.0, 0, 0.9), (0.8, 40, 0.95),
                                    (1.3, 1000, 0.5), (2.0, 0, 0.99), (0.5, 0, 1e-4)])
 def test_draws_match_the_oracle_llama3_vocab(T, k, p):
