@@ -71,7 +71,9 @@ typedef enum llama_status {
   LLAMA_ERR_ALIGNMENT = 3,     /* pointer not 16-byte aligned */
   LLAMA_ERR_WORKSPACE = 4,     /* workspace missing or smaller than llama_workspace_bytes() */
   LLAMA_ERR_CUDA = 5,          /* a CUDA runtime call or launch failed */
-  LLAMA_ERR_TIMEOUT = 6        /* device side: a bounded wait ran out (kernel gave up cleanly) */
+  LLAMA_ERR_TIMEOUT = 6,       /* device side: a bounded wait ran out (kernel gave up cleanly) */
+  LLAMA_ERR_BOUNDS = 7         /* device side, bounds-checking builds only: a kernel found a store
+                                  or TMA box start outside its tensor, skipped it and returned */
 } llama_status;
 
 /* One block's parameters (device pointers, dtype of the call):
@@ -298,10 +300,31 @@ int llama_embed(int dtype, const void* table, int64_t vocab, int64_t d_model, co
                 int64_t n, void* x, void* stream);
 
 /* Synchronises `stream`, then reads and clears the device status word of the current device.
- * *out receives LLAMA_OK, LLAMA_ERR_TIMEOUT (a kernel's bounded wait ran out and it exited) or
- * LLAMA_ERR_INVALID_ARG (llama_embed met a token id outside the table).
+ * *out receives LLAMA_OK, LLAMA_ERR_TIMEOUT (a kernel's bounded wait ran out and it exited),
+ * LLAMA_ERR_BOUNDS (bounds-checking builds: a kernel met an index outside its tensor) or
+ * LLAMA_ERR_INVALID_ARG (llama_embed met a token id outside the table), in that order of
+ * precedence when several were latched.
  * Returns LLAMA_OK, or LLAMA_ERR_CUDA if the synchronisation or the copy failed.             */
 int llama_get_device_status(int* out, void* stream);
+
+/* Build information: bit LLAMA_BUILD_BOUNDS_CHECKS is set when the library was compiled with
+ * -DLLAMA_DEBUG.  In that build every kernel checks each global store's index range and each
+ * TMA box (or tile) start against the extent of its tensor before issuing it.  A failed check
+ * latches LLAMA_ERR_BOUNDS (read with llama_get_device_status) and skips the access; a TMA
+ * producer that skips a load also raises its CTA's abort flag, so that the kernel's other roles
+ * leave through their bounded waits.  No trap and no assert: the context stays usable.  Release
+ * builds compile the checks away.  There is no counterpart on the source pages: it is a
+ * debugging aid of this library, standing in for a memory checker.                           */
+enum { LLAMA_BUILD_BOUNDS_CHECKS = 1 };
+int llama_build_info(void);
+
+/* Self-test of the bounds checks: one small kernel stores to element 40 of `scratch` (64 fp32
+ * elements, device, 16-byte aligned) through the checked store path, declaring the tensor's
+ * extent as 32 elements.  A bounds-checking build skips the store and latches LLAMA_ERR_BOUNDS;
+ * a release build performs it (inside the 64 elements).  Asynchronous on `stream`; returns
+ * LLAMA_OK, LLAMA_ERR_INVALID_ARG for a NULL or unaligned scratch, or LLAMA_ERR_CUDA if the
+ * launch failed.                                                                              */
+int llama_selftest_bounds(float* scratch, void* stream);
 
 /* Self-test of the device-side failure path: one small kernel whose threads wait, through the
  * same bounded mbarrier wait every pipelined kernel uses, on phases that nothing completes.  The

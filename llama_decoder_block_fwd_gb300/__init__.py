@@ -19,7 +19,7 @@ __all__ = [
     "llama_sample", "llama_embed", "llama_kv_quantize", "llama_gqa_attention_decode_kv8",
     "llama_stack_decode_step_kv8", "llama_stack_decode_step_paged", "llama_gqa_attention_decode_paged",
     "llama_get_device_status", "llama_status_string", "llama_profile_enable", "llama_profile_read",
-    "llama_selftest_bounded_wait",
+    "llama_selftest_bounded_wait", "llama_selftest_bounds", "llama_build_info", "BUILD_BOUNDS_CHECKS", "DEBUG_BUILD",
     "OP_RMSNORM", "OP_ROPE", "OP_GQA_ATTENTION", "OP_SWIGLU_FFN", "OP_BLOCK_FORWARD",
     "OP_STACK_DECODE_STEP",
 ]
@@ -30,10 +30,12 @@ X_F32, Y_F32 = 0x100, 0x200   # residual-stream flags for llama_block_forward's 
  OP_STACK_DECODE_STEP) = range(6)
 STATUS_NAMES = {0: "LLAMA_OK", 1: "LLAMA_ERR_INVALID_ARG", 2: "LLAMA_ERR_UNSUPPORTED",
                 3: "LLAMA_ERR_ALIGNMENT", 4: "LLAMA_ERR_WORKSPACE", 5: "LLAMA_ERR_CUDA",
-                6: "LLAMA_ERR_TIMEOUT"}
+                6: "LLAMA_ERR_TIMEOUT", 7: "LLAMA_ERR_BOUNDS"}
 
 _DIR = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_DIR, "libllama_block.so")
+# LLAMA_BLOCK_DEBUG=1 selects the bounds-checking build (built by _build.build(debug=True))
+DEBUG_BUILD = os.environ.get("LLAMA_BLOCK_DEBUG", "0") not in ("", "0")
+LIB_PATH = os.path.join(_DIR, "libllama_block_debug.so" if DEBUG_BUILD else "libllama_block.so")
 
 
 class Dims(ctypes.Structure):
@@ -80,6 +82,7 @@ def lib() -> ctypes.CDLL:
                                             vp, vp, i64, i64, vp, vp, sz, vp],
                 "llama_get_device_status": [ctypes.POINTER(ctypes.c_int), vp],
                 "llama_selftest_bounded_wait": [vp],
+                "llama_selftest_bounds": [vp, vp],
                 "llama_gqa_attention_decode_noalloc": [pd, i32, vp, vp, vp, i64, i64, vp, vp],
                 "llama_sample": [vp, i64, i64, i64, ctypes.c_float, i64, ctypes.c_float, vp, vp, vp],
                 "llama_embed": [i32, vp, i64, i64, vp, i64, vp, vp],
@@ -102,6 +105,8 @@ def lib() -> ctypes.CDLL:
             L.llama_profile_read.argtypes = [i32, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_int),
                                              ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int)]
             L.llama_profile_read.restype = ctypes.c_int
+            L.llama_build_info.argtypes = []
+            L.llama_build_info.restype = ctypes.c_int
             L.llama_status_string.argtypes = [i32]
             L.llama_status_string.restype = ctypes.c_char_p
             _lib = L
@@ -273,6 +278,20 @@ def llama_selftest_bounded_wait(stream=None) -> None:
     """Launch the kernel whose bounded waits run out on purpose (the device status word then holds
     LLAMA_ERR_TIMEOUT; read it with llama_get_device_status)."""
     _check(lib().llama_selftest_bounded_wait(_s(stream)), "llama_selftest_bounded_wait")
+
+
+def llama_selftest_bounds(scratch, stream=None) -> None:
+    """Store through the checked path to element 40 of `scratch` (64 fp32) declared 32 long: a
+    bounds-checking build skips it and latches LLAMA_ERR_BOUNDS, a release build performs it."""
+    _check(lib().llama_selftest_bounds(_p(scratch), _s(stream)), "llama_selftest_bounds")
+
+
+def llama_build_info() -> int:
+    """Bit 1 (LLAMA_BUILD_BOUNDS_CHECKS): the loaded library checks bounds (-DLLAMA_DEBUG)."""
+    return int(lib().llama_build_info())
+
+
+BUILD_BOUNDS_CHECKS = 1
 
 
 def llama_profile_enable(on: bool = True) -> None:

@@ -661,7 +661,7 @@ int decode_stack_tc(const llama_dims* d, int n_layers, const llama_block_weights
       return rc;
     prof::begin("fin_qkv", st);
     rc = launch_fin_qkv(w.part, w.s_qkv, w.rs1, w.q, kc, vc, B, (int)hq, (int)hkv, (int)d->head_dim, cap, t_cache, freq,
-                        ks, vs, pc.block_table, (int)pc.max_pages, pc.seq_pos, st);
+                        ks, vs, pc.block_table, (int)pc.max_pages, pc.seq_pos, pc.n_pages, st);
     prof::end(st);
     if ((rc = run_fin("fin_qkv", rc, st)) != LLAMA_OK) return rc;
     // attention over t_cache + 1 keys; o as hi + lo into the activation buffers
@@ -724,11 +724,15 @@ int decode_stack_tc(const llama_dims* d, int n_layers, const llama_block_weights
 }
 
 }  // namespace
+LLAMA_DEFINE_BOUNDS_READER(api)
+
 }  // namespace llama
 
 using namespace llama;
 
 extern "C" {
+
+int llama_build_info(void) { return kBoundsChecks ? LLAMA_BUILD_BOUNDS_CHECKS : 0; }
 
 const char* llama_status_string(int status) {
   switch (status) {
@@ -739,6 +743,7 @@ const char* llama_status_string(int status) {
     case LLAMA_ERR_WORKSPACE: return "workspace missing or too small";
     case LLAMA_ERR_CUDA: return "CUDA error";
     case LLAMA_ERR_TIMEOUT: return "device wait timed out";
+    case LLAMA_ERR_BOUNDS: return "device index outside its tensor (bounds-checking build)";
     default: return "unknown status";
   }
 }
@@ -784,7 +789,16 @@ int llama_get_device_status(int* out, void* stream) {
     const unsigned zero = 0;
     if (cudaMemcpy(p, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return LLAMA_ERR_CUDA;
   }
-  *out = (v & STATUS_TIMEOUT) ? LLAMA_ERR_TIMEOUT : (v & STATUS_BAD_TOKEN) ? LLAMA_ERR_INVALID_ARG : LLAMA_OK;
+  unsigned bounds = 0;
+  if (kBoundsChecks)
+    bounds = bounds_read_clear_api() | bounds_read_clear_kernels_simt() | bounds_read_clear_gemm_tc() |
+             bounds_read_clear_gemm_tc2() | bounds_read_clear_gemm_skinny() | bounds_read_clear_attn_tc() |
+             bounds_read_clear_decode_attn() | bounds_read_clear_decode_attn8() | bounds_read_clear_decode_fin() |
+             bounds_read_clear_sample() | bounds_read_clear_selftest();
+  *out = (v & STATUS_TIMEOUT) ? LLAMA_ERR_TIMEOUT
+         : bounds             ? LLAMA_ERR_BOUNDS
+         : (v & STATUS_BAD_TOKEN) ? LLAMA_ERR_INVALID_ARG
+                                  : LLAMA_OK;
   return LLAMA_OK;
 }
 

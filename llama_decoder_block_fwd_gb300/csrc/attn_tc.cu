@@ -182,16 +182,22 @@ __global__ void __launch_bounds__(AT_THREADS, 1) attn_tc_kernel(const __grid_con
 
   if (warp == 0) {
     if (lane == 0) {  // ------------------------------------------------ TMA producer
-      mbar_arrive_expect_tx(q_full, nq_tiles * L::QT);
-      for (int x = 0; x < 2; ++x) {
+      // bounds-checking builds: every box start inside Q [B*S, n_q, hd] and K/V [B, kv_len, n_kv, hd]
+      bool inb = true;
+      for (int x = 0; x < 2; ++x)
+        if (ntile[x] > 0) inb = inb && box_in(0, HD, (int64_t)g * p.r, p.n_q, (int64_t)b * p.S + t0[x], (int64_t)p.B * p.S);
+      if (!inb) *abort_flag = 1;
+      if (inb) mbar_arrive_expect_tx(q_full, nq_tiles * L::QT);
+      for (int x = 0; x < 2 && inb; ++x) {
         if (ntile[x] == 0) continue;
         for (int hh = 0; hh < HALVES; ++hh)
           tma_load_3d(sbase + L::OFF_Q + x * L::QT + hh * 16384, &p.tmQ, q_full, hh * 64, g * p.r, b * p.S + t0[x]);
       }
-      for (int j = 0; j < nmax; ++j) {
+      for (int j = 0; j < nmax && inb; ++j) {
         const int st = j & 1;
         const uint32_t ph = (j >> 1) & 1;
         if (!mbar_wait(&kv_empty[st], ph ^ 1, abort_flag, p.status)) break;
+        if (!box_in(0, HD, g, p.n_kv, (int64_t)j * 128, (int64_t)p.pos0 + p.S, b, p.B)) { *abort_flag = 1; break; }
         mbar_arrive_expect_tx(&k_full[st], L::KV);
         for (int hh = 0; hh < HALVES; ++hh)
           tma_load_4d(sbase + L::OFF_K + st * L::KV + hh * 16384, &p.tmK, &k_full[st], hh * 64, g, j * 128, b);
@@ -343,7 +349,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1) attn_tc_kernel(const __grid_con
         uint32_t v[32];
         tmem_ld32(tO + c * 32, v);
         tc_wait_ld();
-        if (live) {
+        if (live && in_extent((((int64_t)b * p.S + tok) * p.n_q + h) * HD + c * 32, 32, (int64_t)p.B * p.S * p.n_q * HD)) {
 #pragma unroll
           for (int i = 0; i < 32; i += 8) {
             uint4 w;
@@ -422,5 +428,7 @@ bool attn_tc_supported(const AttnDesc& a) {
 int launch_attn_tc(const AttnDesc& a, int, unsigned* status, cudaStream_t st) {
   return a.hd == 128 ? launch_hd<128>(a, status, st) : launch_hd<64>(a, status, st);
 }
+
+LLAMA_DEFINE_BOUNDS_READER(attn_tc)
 
 }  // namespace llama

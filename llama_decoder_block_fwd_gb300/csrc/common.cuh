@@ -16,6 +16,55 @@ namespace llama {
 // Bit flags latched by kernels; read and cleared by llama_get_device_status().
 enum : unsigned { STATUS_TIMEOUT = 1u, STATUS_BAD_TOKEN = 2u };
 
+// ---------------------------------------------------------------- bounds checks (-DLLAMA_DEBUG)
+// Built with -DLLAMA_DEBUG, the kernels check every global store's index range and every TMA box
+// start against the extent of its tensor before issuing it.  A failed check latches this
+// translation unit's bounds word (read and cleared on the host by its bounds_read_clear_* reader,
+// which llama_get_device_status calls) and returns false: the caller skips the access and returns.
+// Release builds compile every check to `true`.
+#ifdef LLAMA_DEBUG
+constexpr bool kBoundsChecks = true;
+static __device__ unsigned g_bounds_fail;   // one per translation unit
+#else
+constexpr bool kBoundsChecks = false;
+#endif
+
+__device__ __forceinline__ bool bounds_fail() {
+#ifdef LLAMA_DEBUG
+  atomicOr(&g_bounds_fail, 1u);
+#endif
+  return false;
+}
+// [i, i + n) lies inside [0, extent)
+__device__ __forceinline__ bool in_extent(int64_t i, int64_t n, int64_t extent) {
+  if (!kBoundsChecks) return true;
+  return (i >= 0 && n >= 0 && i <= extent - n) || bounds_fail();
+}
+// A TMA box start inside its tensor: 0 <= coordinate < extent on each dimension given.
+__device__ __forceinline__ bool box_in(int64_t x, int64_t ex, int64_t y = 0, int64_t ey = 1, int64_t z = 0,
+                                       int64_t ez = 1, int64_t w = 0, int64_t ew = 1) {
+  if (!kBoundsChecks) return true;
+  return (x >= 0 && x < ex && y >= 0 && y < ey && z >= 0 && z < ez && w >= 0 && w < ew) || bounds_fail();
+}
+
+// The host-side reader of a translation unit's bounds word (0 in release builds); each .cu file
+// defines its own with LLAMA_DEFINE_BOUNDS_READER(file name).
+#ifdef LLAMA_DEBUG
+#define LLAMA_DEFINE_BOUNDS_READER(name)                                                  \
+  unsigned bounds_read_clear_##name() {                                                  \
+    unsigned v = 0;                                                                      \
+    if (cudaMemcpyFromSymbol(&v, g_bounds_fail, sizeof(v)) != cudaSuccess) return 0u;    \
+    if (v) {                                                                             \
+      const unsigned zero = 0;                                                           \
+      cudaMemcpyToSymbol(g_bounds_fail, &zero, sizeof(zero));                            \
+    }                                                                                    \
+    return v;                                                                            \
+  }
+#else
+#define LLAMA_DEFINE_BOUNDS_READER(name) \
+  unsigned bounds_read_clear_##name() { return 0u; }
+#endif
+
 // A bounded wait gives up after this many nanoseconds of %globaltimer.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 

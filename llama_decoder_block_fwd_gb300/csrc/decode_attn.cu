@@ -51,6 +51,8 @@ struct __align__(64) DecodeAttnParams {
   const int* block_table;   // paged cache: [B, max_pages] page ids; null: dense [B, cap, n_kv, hd]
   const int* seq_pos;       // paged cache: [B] position of the new token (keys 0..seq_pos[b])
   int max_pages;
+  int n_pages;              // paged cache: pages in each pool (bounds checks)
+  int64_t n_slots;          // partial slots part_o / part_ml hold (bounds checks)
 };
 
 struct DaSmem {
@@ -243,6 +245,7 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_kernel(const __grid
         const int qb = it & 1;
         ++it;
         if (!mbar_wait(&q_empty[qb], (((it - 1) >> 1) & 1) ^ 1, abort_flag, p.status)) break;
+        if (!box_in(0, DA_HD, (int64_t)g * p.r, p.n_q, b, p.B)) { *abort_flag = 1; break; }   // checking builds
         mbar_arrive_expect_tx(&q_full[qb], 2 * 64 * p.r * 2);
         for (int hh = 0; hh < 2; ++hh)
           tma_load_3d(sbase + L::OFF_Q + qb * L::QB + hh * (L::QB / 2), &p.tmQ, &q_full[qb], hh * 64, g * p.r, b);
@@ -252,6 +255,11 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_kernel(const __grid
           if (!mbar_wait(&kv_empty[st], ph ^ 1, abort_flag, p.status)) { ok = false; break; }
           const int zc = p.block_table ? 0 : t * 128;
           const int wc = p.block_table ? __ldg(p.block_table + (int64_t)b * p.max_pages + t) : b;
+          if (!box_in(0, DA_HD, g, p.n_kv, zc, p.block_table ? 128 : p.kv_len, wc, p.block_table ? p.n_pages : p.B)) {
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
           mbar_arrive_expect_tx(&k_full[st], L::KV);
           for (int hh = 0; hh < 2; ++hh)
             tma_load_4d_da(sbase + L::OFF_K + st * L::KV + hh * 16384, &p.tmK, &k_full[st], hh * 64, g, zc, wc);
@@ -437,8 +445,10 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_kernel(const __grid
       tc_fence_before();
       mbar_arrive(o_free);
       const int64_t base = slot * r;
+      const bool slot_in = in_extent(base, r, p.n_slots * r);   // checking builds: the slot exists
 #pragma unroll
-      for (int h = 0; h < R; ++h) p.part_o[(base + h) * DA_HD + t] = __uint_as_float(ov[h]);
+      for (int h = 0; h < R; ++h)
+        if (slot_in) p.part_o[(base + h) * DA_HD + t] = __uint_as_float(ov[h]);
       // l: sum the per-thread partial sums over the 128 keys of each head
       float* lbuf = red + 128;
 #pragma unroll
@@ -449,7 +459,7 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_kernel(const __grid
         if (lane == h) lbuf[qw * 16 + h] = v;
       }
       softmax_sync();
-      if (t < r) {
+      if (t < r && slot_in) {
         const float l = lbuf[t] + lbuf[16 + t] + lbuf[32 + t] + lbuf[48 + t];
         float mm = -INFINITY;
 #pragma unroll
@@ -499,6 +509,7 @@ __global__ void decode_combine_kernel(const float* __restrict__ part_o, const fl
   out.x = pack_bf2(r[0], r[1]);
   out.y = pack_bf2(r[2], r[3]);
   const int64_t off = ((int64_t)b * n_q + h) * DA_HD + lane * 4;
+  if (!in_extent(off, 4, (int64_t)B * n_q * DA_HD)) return;
   *reinterpret_cast<uint2*>(o + off) = out;
   if (o_lo) {
     uint2 lo;
@@ -545,6 +556,7 @@ __global__ void decode_combine_seg_kernel(const float* __restrict__ part_o, cons
   out.x = pack_bf2(rr[0], rr[1]);
   out.y = pack_bf2(rr[2], rr[3]);
   const int64_t o_off = ((int64_t)b * n_q + h) * DA_HD + lane * 4;
+  if (!in_extent(o_off, 4, (int64_t)B * n_q * DA_HD)) return;
   *reinterpret_cast<uint2*>(o + o_off) = out;
   if (o_lo) {
     uint2 lo;
@@ -650,10 +662,12 @@ int launch_decode_attn(const AttnDesc& a, void* ws, int num_sms, unsigned* statu
   p.block_table = a.block_table;
   p.seq_pos = a.seq_pos;
   p.max_pages = (int)a.max_pages;
+  p.n_pages = (int)a.n_pages;
   if (!encode_tmap_3d_bf16(&p.tmQ, a.q, DA_HD, (uint64_t)a.n_q, (uint64_t)a.B, DA_HD * 2,
                            (uint64_t)a.n_q * DA_HD * 2, 64, (uint32_t)r, 1))
     return -1;
   const int64_t slots = a.B * a.n_kv + DA_MAX_GRID;
+  p.n_slots = slots;
   p.part_o = static_cast<float*>(ws);
   p.part_ml = reinterpret_cast<float*>(static_cast<char*>(ws) + round256((size_t)slots * r * DA_HD * 4));
   p.B = (int)a.B; p.n_q = (int)a.n_q; p.n_kv = (int)a.n_kv; p.r = r;
@@ -717,6 +731,8 @@ void* noalloc_scratch_ptr() {
 
 }  // namespace
 
+LLAMA_DEFINE_BOUNDS_READER(decode_attn)
+
 }  // namespace llama
 
 using namespace llama;
@@ -763,6 +779,7 @@ extern "C" int llama_gqa_attention_decode_noalloc(const llama_dims* dims, int dt
                            (uint64_t)dims->n_q * DA_HD * 2, 64, (uint32_t)r, 1))
     return LLAMA_ERR_CUDA;
   // Every partial slot the combine reads is written by its piece: nothing has to start at zero.
+  p.n_slots = dims->B * dims->n_kv + grid;
   p.part_o = static_cast<float*>(scratch);
   p.part_ml = reinterpret_cast<float*>(static_cast<char*>(scratch) +
                                        round256((size_t)(dims->B * dims->n_kv + grid) * rr * DA_HD * 4));

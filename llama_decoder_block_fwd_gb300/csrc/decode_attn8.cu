@@ -204,6 +204,7 @@ __global__ void __launch_bounds__(D8_THREADS, D8_CTAS_PER_SM) decode_attn8_kerne
       auto issue_v = [&](int gt) -> bool {
         const int vs = gt % D8_VSTAGES;
         if (!mbar_wait(&bars[B_V8E + vs], ((gt / D8_VSTAGES) & 1) ^ 1, abort_flag, p.status)) return false;
+        if (!box_in(0, D8_HD, vg, p.n_kv, (int64_t)vt * 128, p.kv_len, vb, p.B)) { *abort_flag = 1; return false; }
         mbar_arrive_expect_tx(&bars[B_V8F + vs], L::F8);
         tma_load_4d_d8(sbase + L::OFF_V8 + vs * L::F8, &p.tmV, &bars[B_V8F + vs], 0, vg, vt * 128, vb);
         return true;
@@ -214,6 +215,7 @@ __global__ void __launch_bounds__(D8_THREADS, D8_CTAS_PER_SM) decode_attn8_kerne
         for (int t = t0; t < t1; ++t, ++tile) {
           const int ks = tile % D8_KSTAGES;
           if (!mbar_wait(&bars[B_K8E + ks], ((tile / D8_KSTAGES) & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
+          if (!box_in(0, D8_HD, g, p.n_kv, (int64_t)t * 128, p.kv_len, b, p.B)) { *abort_flag = 1; ok = false; break; }
           mbar_arrive_expect_tx(&bars[B_K8F + ks], L::F8);
           tma_load_4d_d8(sbase + L::OFF_K8 + ks * L::F8, &p.tmK, &bars[B_K8F + ks], 0, g, t * 128, b);
           if (tile > 0 && !issue_v(tile - 1)) { ok = false; break; }
@@ -434,9 +436,10 @@ __global__ void __launch_bounds__(D8_THREADS, D8_CTAS_PER_SM) decode_attn8_kerne
       mbar_arrive(&bars[B_OFREE]);
       const float vs = p.v_scale[g];
       const int64_t base = ((int64_t)b * p.n_chunks + chunk) * p.n_q + (int64_t)g * R;
+      const bool slot_in = in_extent(base, R, (int64_t)p.B * p.n_chunks * p.n_q);   // checking builds
 #pragma unroll
       for (int h = 0; h < R; ++h)
-        p.part_o[(base + h) * D8_HD + t] = (__uint_as_float(ov[h]) + __uint_as_float(ov[R + h])) * vs;
+        if (slot_in) p.part_o[(base + h) * D8_HD + t] = (__uint_as_float(ov[h]) + __uint_as_float(ov[R + h])) * vs;
       float* lbuf = red + 128;
 #pragma unroll
       for (int h = 0; h < R; ++h) {
@@ -446,7 +449,7 @@ __global__ void __launch_bounds__(D8_THREADS, D8_CTAS_PER_SM) decode_attn8_kerne
         if (lane == h) lbuf[qw * 16 + h] = v;
       }
       softmax_sync8();
-      if (t < R) {
+      if (t < R && slot_in) {
         const float l = lbuf[t] + lbuf[16 + t] + lbuf[32 + t] + lbuf[48 + t];
         float mm = -INFINITY;
 #pragma unroll
@@ -493,7 +496,7 @@ int launch_decode8_kernel(const DecodeAttn8Params& p, int grid, cudaStream_t st)
 __global__ void kv_quantize_kernel(const uint16_t* __restrict__ x, const float* __restrict__ scale, uint8_t* __restrict__ out,
                                    int64_t n8, int n_kv, int hd) {
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;   // one group of 8 elements
-  if (i >= n8) return;
+  if (i >= n8 || !in_extent(i * 8, 8, n8 * 8)) return;
   const int64_t e0 = i * 8;
   const int head = (int)((e0 / hd) % n_kv);
   const float s = scale[head];
@@ -564,5 +567,7 @@ int launch_kv_quantize(const void* x, const float* scale, void* codes, int64_t n
                                                                    static_cast<uint8_t*>(codes), n8, n_kv, hd);
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
+
+LLAMA_DEFINE_BOUNDS_READER(decode_attn8)
 
 }  // namespace llama

@@ -62,7 +62,8 @@ __global__ void __launch_bounds__(FN_THREADS) fin_norm_kernel(float* __restrict_
         const float4 w = *reinterpret_cast<const float4*>(part + ((int64_t)s * B + r) * d + 4 * i);
         v[j].x += w.x; v[j].y += w.y; v[j].z += w.z; v[j].w += w.w;
       }
-      if (write_x) *reinterpret_cast<float4*>(x + (int64_t)r * d + 4 * i) = v[j];
+      if (write_x && in_extent((int64_t)r * d + 4 * i, 4, (int64_t)B * d))
+        *reinterpret_cast<float4*>(x + (int64_t)r * d + 4 * i) = v[j];
       ss = fmaf(v[j].x, v[j].x, ss);
       ss = fmaf(v[j].y, v[j].y, ss);
       ss = fmaf(v[j].z, v[j].z, ss);
@@ -77,7 +78,7 @@ __global__ void __launch_bounds__(FN_THREADS) fin_norm_kernel(float* __restrict_
 #pragma unroll
   for (int w = 0; w < FN_THREADS / 32; ++w) tot += red[w];
   const float rs = rsqrtf(tot / (float)d + eps);
-  if (threadIdx.x == 0) rs_out[r] = rs;
+  if (threadIdx.x == 0 && in_extent(r, 1, B)) rs_out[r] = rs;
 #pragma unroll
   for (int j = 0; j < FN_MAX_VEC; ++j) {
     const int i = threadIdx.x + j * FN_THREADS;
@@ -88,6 +89,7 @@ __global__ void __launch_bounds__(FN_THREADS) fin_norm_kernel(float* __restrict_
       uint16_t hi[4], lo[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) split_bf16(y[k], hi[k], lo[k]);
+      if (!in_extent((int64_t)r * d + 4 * i, 4, (int64_t)B * d)) continue;   // a_hi, a_lo: [B, d] each
       *reinterpret_cast<uint2*>(a_hi + (int64_t)r * d + 4 * i) =
           make_uint2((uint32_t)hi[0] | ((uint32_t)hi[1] << 16), (uint32_t)hi[2] | ((uint32_t)hi[3] << 16));
       *reinterpret_cast<uint2*>(a_lo + (int64_t)r * d + 4 * i) =
@@ -109,6 +111,7 @@ struct FinQkvParams {
   int max_pages;
   int n_split, B, nq_cols, nkv_cols, hd;
   int64_t cap, t;
+  int64_t cache_rows;      // rows of each cache: B * cap, or n_pages * 128 (bounds checks)
   RopeFreq freq[kMaxRopePairs];
 };
 
@@ -143,7 +146,8 @@ __global__ void fin_qkv_kernel(const __grid_constant__ FinQkvParams p) {
     v1 = x0 * sn + x1 * cs;
   }
   if (c < p.nq_cols) {
-    *reinterpret_cast<uint32_t*>(p.q + (int64_t)r * p.nq_cols + c) = pack_bf2(v0, v1);
+    if (in_extent((int64_t)r * p.nq_cols + c, 2, (int64_t)p.B * p.nq_cols))
+      *reinterpret_cast<uint32_t*>(p.q + (int64_t)r * p.nq_cols + c) = pack_bf2(v0, v1);
     continue;
   }
   const bool is_k = c < p.nq_cols + p.nkv_cols;
@@ -151,6 +155,7 @@ __global__ void fin_qkv_kernel(const __grid_constant__ FinQkvParams p) {
   const int64_t slot = p.block_table ? (int64_t)__ldg(p.block_table + (int64_t)r * p.max_pages + tpos / 128) * 128 + tpos % 128
                                      : (int64_t)r * p.cap + tpos;
   const int64_t off = slot * p.nkv_cols + cc;
+  if (!in_extent(off, 2, p.cache_rows * p.nkv_cols)) continue;
   if (p.k_scale) {   // 8-bit cache: code = E4M3(fl32(x) / scale), rounded to nearest even, saturating
     const float s = (is_k ? p.k_scale : p.v_scale)[cc / p.hd];
     uint16_t code;
@@ -187,6 +192,7 @@ __global__ void fin_swiglu_kernel(const float* __restrict__ part, const float* _
     split_bf16(silu_f(gs.z * sc) * (us.z * sc), h2, l2);
     split_bf16(silu_f(gs.w * sc) * (us.w * sc), h3, l3);
     const int64_t o = (int64_t)r * dff + j;
+    if (!in_extent(o, 4, (int64_t)B * dff)) continue;   // m_hi, m_lo: [B, d_ff] each
     *reinterpret_cast<uint2*>(m_hi + o) = make_uint2((uint32_t)h0 | ((uint32_t)h1 << 16), (uint32_t)h2 | ((uint32_t)h3 << 16));
     *reinterpret_cast<uint2*>(m_lo + o) = make_uint2((uint32_t)l0 | ((uint32_t)l1 << 16), (uint32_t)l2 | ((uint32_t)l3 << 16));
   }
@@ -205,13 +211,14 @@ int launch_fin_norm(float* x, const void* init_bf16, const float* part, int n_sp
 int launch_fin_qkv(const float* part, int n_split, const float* rs, void* q, void* kc, void* vc, int B, int nq_cols,
                    int nkv_cols, int hd, int64_t cap, int64_t t, const RopeFreq* freq, const float* k_scale,
                    const float* v_scale, const int* block_table, int max_pages, const int* seq_pos,
-                   cudaStream_t st) {
+                   int64_t n_pages, cudaStream_t st) {
   FinQkvParams p;
   p.part = part; p.rs = rs;
   p.q = static_cast<uint16_t*>(q); p.kc = kc; p.vc = vc;
   p.k_scale = k_scale; p.v_scale = v_scale;
   p.block_table = block_table; p.max_pages = max_pages; p.seq_pos = seq_pos;
   p.n_split = n_split; p.B = B; p.nq_cols = nq_cols; p.nkv_cols = nkv_cols; p.hd = hd; p.cap = cap; p.t = t;
+  p.cache_rows = block_table ? n_pages * 128 : (int64_t)B * cap;
   for (int i = 0; i < hd / 2; ++i) p.freq[i] = freq[i];
   const int64_t n = (int64_t)B * (nq_cols + 2 * nkv_cols) / 2;
   // one thread per pair: B * 3 * 1024 threads at most for the shapes of the decode path, which
@@ -227,5 +234,7 @@ int launch_fin_swiglu(const float* part, int n_split, const float* rs, void* m_h
   return launch_k(fin_swiglu_kernel, dim3(grid), dim3(256), 0, st, part, rs,
                   static_cast<uint16_t*>(m_hi), static_cast<uint16_t*>(m_lo), n_split, B, dff) == cudaSuccess ? 0 : -1;
 }
+
+LLAMA_DEFINE_BOUNDS_READER(decode_fin)
 
 }  // namespace llama

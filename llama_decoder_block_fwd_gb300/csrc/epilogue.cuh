@@ -11,10 +11,12 @@ namespace llama {
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
 
-// Store n consecutive values (c % n == 0 for vector paths) of row r into a [*, ld] matrix.
+// Store n consecutive values (c % n == 0 for vector paths) of row r into a [*, ld] matrix of
+// `extent` elements (checked in -DLLAMA_DEBUG builds: a run outside it is skipped).
 template <int n>
 __device__ __forceinline__ void store_run(void* base, int is_f32, int64_t ld, int64_t r, int64_t c,
-                                          const float* v) {
+                                          const float* v, int64_t extent) {
+  if (!in_extent(r * ld + c, n, extent)) return;
   if (is_f32) {
     float* p = static_cast<float*>(base) + r * ld + c;
     if constexpr (n % 4 == 0) {
@@ -137,14 +139,14 @@ __device__ __forceinline__ float epi_run(const Epi& e, int64_t r, int64_t c, flo
   }
   switch (e.kind) {
     case EPI_STORE:
-      store_run<n>(e.out, e.out_f32, e.ldo, r, c, v);
+      store_run<n>(e.out, e.out_f32, e.ldo, r, c, v, e.out_rows * e.ldo);
       break;
     case EPI_RESID: {
       float t[n];
       load_run<n>(e.resid, e.resid_f32, e.ldr, r, c, t);
 #pragma unroll
       for (int i = 0; i < n; ++i) v[i] += t[i];
-      store_run<n>(e.out, e.out_f32, e.ldo, r, c, v);
+      store_run<n>(e.out, e.out_f32, e.ldo, r, c, v, e.out_rows * e.ldo);
       if (e.norm_u) {   // the next RMSNorm's x * g and sum of squares, from the fp32 h
         float gg[n], sq = 0.f;
         load_run<n>(e.norm_g, 0, 0, 0, c, gg);
@@ -153,7 +155,7 @@ __device__ __forceinline__ float epi_run(const Epi& e, int64_t r, int64_t c, flo
           sq = fmaf(v[i], v[i], sq);
           gg[i] *= v[i];
         }
-        store_run<n>(e.norm_u, 0, e.ldo, r, c, gg);
+        store_run<n>(e.norm_u, 0, e.ldo, r, c, gg, e.M * e.ldo);
         ssq = sq;
       }
       break;
@@ -161,10 +163,11 @@ __device__ __forceinline__ float epi_run(const Epi& e, int64_t r, int64_t c, flo
     case EPI_SWIGLU: {
 #pragma unroll
       for (int i = 0; i < n; ++i) v[i] = silu_f(v[i]) * u[i];
-      store_run<n>(e.out, e.out_f32, e.ldo, r, c, v);
+      store_run<n>(e.out, e.out_f32, e.ldo, r, c, v, e.out_rows * e.ldo);
       break;
     }
     case EPI_ATOMIC: {   // partial sums of a split K range, added into an fp32 buffer
+      if (!in_extent(r * e.ldo + c, n, e.out_rows * e.ldo)) break;
       float* p = static_cast<float*>(e.out) + r * e.ldo + c;
       if constexpr (n % 4 == 0) {
 #pragma unroll
@@ -180,15 +183,16 @@ __device__ __forceinline__ float epi_run(const Epi& e, int64_t r, int64_t c, flo
       const float pos = (float)(e.pos0 + s);
       if (c < e.nq_cols) {
         rope_run<n>(e, c, pos, s, v);
-        store_run<n>(e.out, e.out_f32, e.nq_cols, r, c, v);
+        store_run<n>(e.out, e.out_f32, e.nq_cols, r, c, v, e.M * e.nq_cols);
       } else {
         const int64_t krow = (r / e.S) * e.cap + e.pos0 + s;
         if (c < e.nq_cols + e.nkv_cols) {
           const int64_t cc = c - e.nq_cols;
           rope_run<n>(e, cc, pos, s, v);
-          store_run<n>(e.k_out, e.out_f32, e.nkv_cols, krow, cc, v);
+          store_run<n>(e.k_out, e.out_f32, e.nkv_cols, krow, cc, v, (e.M / e.S) * e.cap * e.nkv_cols);
         } else {
-          store_run<n>(e.v_out, e.out_f32, e.nkv_cols, krow, c - e.nq_cols - e.nkv_cols, v);
+          store_run<n>(e.v_out, e.out_f32, e.nkv_cols, krow, c - e.nq_cols - e.nkv_cols, v,
+                       (e.M / e.S) * e.cap * e.nkv_cols);
         }
       }
       break;

@@ -54,6 +54,11 @@ __device__ __forceinline__ void sk_seg(const SkParams& p, int nt, int& seg, int&
   row = (nt - start) * 128;
 }
 
+// Rows of weight segment s.
+__device__ __forceinline__ int sk_seg_rows(const SkParams& p, int s) {
+  return (p.seg_tile_end[s] - (s ? p.seg_tile_end[s - 1] : 0)) * 128;
+}
+
 // The units of this CTA, in order.
 struct UnitIter {
   int64_t pos, end;   // stream-K: the CTA's range of (tile, k-block) items, tile-major
@@ -121,12 +126,14 @@ __global__ void __launch_bounds__(SK_THREADS, 1) gemm_skinny_kernel(const __grid
       // The weights are never written by an earlier kernel: the first unit's first stages are
       // loaded before waiting for the kernel that produced the activations.
       int pre = 0;
+      bool bad = false;   // bounds-checking builds: a box start outside its tensor
       UnitIter first = unit_begin(p);
       int nt, split, kb0, kb1, seg, row;
       if (unit_next(p, first, nkb, nt, split, kb0, kb1)) {
         sk_seg(p, nt, seg, row);
         pre = min(p.stages, kb1 - kb0);
         for (int i = 0; i < pre; ++i) {
+          if (!box_in((kb0 + i) * SK_TK, p.K, row, sk_seg_rows(p, seg))) { *abort_flag = 1; bad = true; break; }
           mbar_arrive_expect_tx(&full[i], stage_bytes);
           tma_load_2d(smem_base + i * stage_bytes, &p.tmW[seg], &full[i], (kb0 + i) * SK_TK, row);
         }
@@ -136,11 +143,12 @@ __global__ void __launch_bounds__(SK_THREADS, 1) gemm_skinny_kernel(const __grid
       uint32_t phase = 0;
       bool first_unit = true;
       UnitIter ui = unit_begin(p);
-      while (unit_next(p, ui, nkb, nt, split, kb0, kb1)) {
+      while (!bad && unit_next(p, ui, nkb, nt, split, kb0, kb1)) {
         sk_seg(p, nt, seg, row);
         bool ok = true;
         for (int kb = kb0; kb < kb1; ++kb) {
           const uint32_t sa = smem_base + stage * stage_bytes;
+          if (!box_in(kb * SK_TK, p.K, row, sk_seg_rows(p, seg))) { *abort_flag = 1; ok = false; break; }
           if (first_unit && kb - kb0 < pre) {   // weights already on their way
             tma_load_2d(sa + SK_A_BYTES, &p.tmX, &full[stage], kb * SK_TK, 0);
           } else {
@@ -216,7 +224,9 @@ __global__ void __launch_bounds__(SK_THREADS, 1) gemm_skinny_kernel(const __grid
             const int64_t c = c0 + i;
             const float v = __uint_as_float(hi[i]) + __uint_as_float(lo[i]);
             if (p.mode == 0) {
-              p.out[((int64_t)split * p.M + c) * p.ldo + n] = v;
+              const int64_t at = ((int64_t)split * p.M + c) * p.ldo + n;
+              if (in_extent(at, 1, (int64_t)p.k_splits * p.M * p.ldo)) p.out[at] = v;
+            } else if (!in_extent(c * p.ldo + n, 1, (int64_t)p.M * p.ldo)) {
             } else if (p.mode == 1) {
               atomicAdd(p.out + c * p.ldo + n, v);
             } else {
@@ -298,5 +308,7 @@ int launch_gemm_skinny(const SkinnyDesc& g, int num_sms, unsigned* status, cudaS
                              : std::max(1, std::min(p.num_units, num_sms));
   return launch_k(gemm_skinny_kernel, dim3(grid), dim3(SK_THREADS), smem, st, p) == cudaSuccess ? 0 : -1;
 }
+
+LLAMA_DEFINE_BOUNDS_READER(gemm_skinny)
 
 }  // namespace llama

@@ -72,6 +72,11 @@ __device__ __forceinline__ void unit_coords(const TcParams& p, int u, int nkb, i
   kb1 = min(nkb, kb0 + p.kb_per_split);
 }
 
+// Rows of B segment s.
+__device__ __forceinline__ int seg_rows(const TcParams& p, int s) {
+  return (p.seg_half_end[s] - (s ? p.seg_half_end[s - 1] : 0)) * 128;
+}
+
 // Which B segment, and which row of it, supplies half hh of column tile nb.
 __device__ __forceinline__ void half_source(const TcParams& p, int nb, int hh, int& seg, int& row) {
   if (p.swiglu) { seg = hh; row = nb * 128; return; }
@@ -127,6 +132,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) gemm_tc_kernel(const __grid_co
         bool ok = true;
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) { ok = false; break; }
+          bool inb = box_in(kb * TK, p.K, (int64_t)mb * TM, p.M);   // bounds-checking builds only
+          for (int hh = 0; hh < nvh; ++hh) inb = inb && box_in(kb * TK, p.K, row[hh], seg_rows(p, seg[hh]));
+          if (!inb) { *abort_flag = 1; ok = false; break; }
           mbar_arrive_expect_tx(&full[stage], bytes);
           const uint32_t sa = smem_base + stage * STAGE_BYTES;
           tma_load_2d(sa, &p.tmA, &full[stage], kb * TK, mb * TM);
@@ -299,6 +307,7 @@ int launch_gemm_tc(const GemmDesc& g, int num_sms, unsigned* status, cudaStream_
   p.split_rows = (p.k_splits > 1 && g.epi.kind == EPI_STORE) ? 1 : 0;
   p.status = status;
   p.epi = g.epi;
+  epi_set_extents(p.epi, g.M, p.split_rows ? g.M * p.k_splits : g.M);
   int dev = 0;
   cudaGetDevice(&dev);
   static bool attr_set[64] = {};
@@ -312,5 +321,7 @@ int launch_gemm_tc(const GemmDesc& g, int num_sms, unsigned* status, cudaStream_
   gemm_tc_kernel<<<grid, NUM_THREADS, SMEM_BYTES, st>>>(p);
   return 0;
 }
+
+LLAMA_DEFINE_BOUNDS_READER(gemm_tc)
 
 }  // namespace llama

@@ -182,6 +182,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS2, 1)
         bool ok = true;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) { ok = false; break; }
+          // bounds-checking builds: the tile's start in A (the second CTA's 128-row half of a ragged
+          // last tile may lie past M by design: the load fills zeros) and this CTA's B half
+          if (!box_in(kb * T2K, p.K, (int64_t)mb * T2M, p.M) ||
+              !box_in(kb * T2K, p.K, row, (p.seg_half_end[seg] - (seg ? p.seg_half_end[seg - 1] : 0)) * 128)) {
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
           const uint32_t lbar = map_to_rank(smem_u32(&full[stage]), 0);
           if (leader) mbar_arrive_expect_tx(&full[stage], 2 * STAGE2);   // both CTAs' bytes
           const uint32_t sa = smem_base + stage * STAGE2;
@@ -284,7 +292,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS2, 1)
             ssq += epi_run<32>(p.epi, r, (int64_t)nb * T2N + c * 32, fv, fv);
           }
         }
-        if (p.epi.ss_out && live) p.epi.ss_out[r * p.epi.ss_n + 2 * nb + half] = ssq;
+        if (p.epi.ss_out && live && in_extent(r * p.epi.ss_n + 2 * nb + half, 1, p.epi.M * p.epi.ss_n))
+          p.epi.ss_out[r * p.epi.ss_n + 2 * nb + half] = ssq;
       }
       tc_fence_before();
       mbar_arrive_cluster(map_to_rank(smem_u32(&acc_empty[buf]), 0));
@@ -332,6 +341,7 @@ int launch_gemm_tc2(const GemmDesc& g, unsigned* status, cudaStream_t st) {
   p.num_tiles = p.m_tiles * p.n_tiles;
   p.status = status;
   p.epi = g.epi;
+  epi_set_extents(p.epi, g.M, g.M);
   int dev = 0;
   cudaGetDevice(&dev);
   static int max_clusters[64] = {};
@@ -352,5 +362,7 @@ int launch_gemm_tc2(const GemmDesc& g, unsigned* status, cudaStream_t st) {
   gemm_tc2_kernel<<<2 * clusters, THREADS2, SMEM2, st>>>(p);
   return 0;
 }
+
+LLAMA_DEFINE_BOUNDS_READER(gemm_tc2)
 
 }  // namespace llama

@@ -13,6 +13,19 @@ namespace llama {
 
 constexpr int kMaxRopePairs = 128;   // head_dim <= 256
 
+// Bounds words of the translation units (see LLAMA_DEFINE_BOUNDS_READER in common.cuh).
+unsigned bounds_read_clear_api();
+unsigned bounds_read_clear_kernels_simt();
+unsigned bounds_read_clear_gemm_tc();
+unsigned bounds_read_clear_gemm_tc2();
+unsigned bounds_read_clear_gemm_skinny();
+unsigned bounds_read_clear_attn_tc();
+unsigned bounds_read_clear_decode_attn();
+unsigned bounds_read_clear_decode_attn8();
+unsigned bounds_read_clear_decode_fin();
+unsigned bounds_read_clear_sample();
+unsigned bounds_read_clear_selftest();
+
 // What a GEMM does with its fp32 result D[r, c] (r < M, c < N).
 enum EpiKind : int {
   EPI_STORE = 0,   // out[r, c] = D
@@ -50,7 +63,14 @@ struct Epi {
   const float* ss_in;
   int ss_n;
   float ss_inv_d, ss_eps;
+  // extents for the bounds checks of -DLLAMA_DEBUG builds, set by the GEMM launchers
+  // (epi_set_extents): rows of D, and rows of `out` (k_splits * M for split-K partials)
+  int64_t M, out_rows;
 };
+inline void epi_set_extents(Epi& e, int64_t M, int64_t out_rows) {
+  e.M = M;
+  e.out_rows = out_rows;
+}
 
 // D[M, N] = A[M, K] * B[N, K]^T with B the row-concatenation of nseg segments
 // (the returned split count can be lower than asked: see launch_gemm_tc)
@@ -150,7 +170,7 @@ int launch_fin_norm(float* x, const void* init_bf16, const float* part, int n_sp
 int launch_fin_qkv(const float* part, int n_split, const float* rs, void* q, void* kc, void* vc, int B, int nq_cols,
                    int nkv_cols, int hd, int64_t cap, int64_t t, const RopeFreq* freq, const float* k_scale,
                    const float* v_scale, const int* block_table, int max_pages, const int* seq_pos,
-                   cudaStream_t st);
+                   int64_t n_pages, cudaStream_t st);
 int launch_fin_swiglu(const float* part, int n_split, const float* rs, void* m_hi, void* m_lo, int B, int dff,
                       cudaStream_t st);
 

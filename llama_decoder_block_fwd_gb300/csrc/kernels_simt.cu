@@ -105,13 +105,13 @@ __device__ __forceinline__ void rmsnorm_reg_rows(const TX* __restrict__ x, const
   }
   ss = warp_sum(ss);
   const float rs = rsqrtf(ss / (float)d + eps);
-  if (SPLIT && lane == 0) rs_out[row] = rs;
+  if (SPLIT && lane == 0 && in_extent(row, 1, rows)) rs_out[row] = rs;
   const float mul = SPLIT ? 1.f : rs;
   TY* yr = y + row * d;
 #pragma unroll
   for (int i = 0; i < CH; ++i) {
     const int c = lane + 32 * i;
-    if (c < nch) {
+    if (c < nch && in_extent(row * d + c * N, N, rows * d)) {
       float f[N], w[N];
       unpack16(buf[i], f, TX());
       VecIO<TG, N>::ld(g + c * N, w);
@@ -145,10 +145,11 @@ __global__ void __launch_bounds__(256) rmsnorm_generic_kernel(const TX* __restri
   }
   ss = warp_sum(ss);
   const float rs = rsqrtf(ss / (float)d + eps);
-  if (SPLIT && lane == 0) rs_out[row] = rs;
+  if (SPLIT && lane == 0 && in_extent(row, 1, rows)) rs_out[row] = rs;
   const float mul = SPLIT ? 1.f : rs;
   TY* yr = y + row * d;
-  for (int64_t c = lane; c < d; c += 32) Elt<TY>::st(yr + c, Elt<TX>::ld(xr + c) * mul * Elt<TG>::ld(g + c));
+  for (int64_t c = lane; c < d; c += 32)
+    if (in_extent(row * d + c, 1, rows * d)) Elt<TY>::st(yr + c, Elt<TX>::ld(xr + c) * mul * Elt<TG>::ld(g + c));
 }
 
 // Streaming RMSNorm for bf16 rows of 1024..4096 elements (multiples of 8): two CTAs per SM, CTA b
@@ -205,6 +206,7 @@ __global__ void __launch_bounds__(kRnThreads, 2) rmsnorm_stream_kernel(const uin
         const int s = (int)(issued % nbuf);
         const uint32_t ph = (uint32_t)((issued / nbuf) & 1);
         if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, status)) break;
+        if (!in_extent((b + issued * G) * (int64_t)d, d, rows * (int64_t)d)) { *abort_flag = 1; break; }
         mbar_arrive_expect_tx(&full[s], row_bytes);
         bulk_load_row(smem_u32(rn_smem + (size_t)s * row_bytes), x + (b + issued * G) * (int64_t)d, row_bytes,
                       &full[s]);
@@ -241,14 +243,14 @@ __global__ void __launch_bounds__(kRnThreads, 2) rmsnorm_stream_kernel(const uin
     const float ss = warp_sum(acc.x + acc.y);
     const float rs = rsqrtf(ss / (float)d + eps);
     const int64_t row = b + i * G;
-    if (SPLIT && lane == 0) rs_out[row] = rs;
+    if (SPLIT && lane == 0 && in_extent(row, 1, rows)) rs_out[row] = rs;
     const float mul = SPLIT ? 1.f : rs;
     const float2 mul2 = make_float2(mul, mul);
     uint16_t* yr = y + row * (int64_t)d;
 #pragma unroll
     for (int k = 0; k < CH; ++k) {
       const int c = lane + 32 * k;
-      if (c < nch) {
+      if (c < nch && in_extent(row * d + c * 8, 8, rows * (int64_t)d)) {
         const uint4 v = srow[c], w = gs[c];
         const uint32_t u[4] = {v.x, v.y, v.z, v.w}, gw[4] = {w.x, w.y, w.z, w.w};
         uint32_t o[4];
@@ -341,9 +343,9 @@ __global__ void rope_kernel(const __grid_constant__ RopeParams p) {
   const int64_t total = nq_pairs + (p.k ? nk_pairs : 0);
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
     T* base;
-    int64_t idx, heads;
-    if (i < nq_pairs && p.q) { base = static_cast<T*>(p.q); idx = i; heads = p.n_q; }
-    else if (i >= nq_pairs) { base = static_cast<T*>(p.k); idx = i - nq_pairs; heads = p.n_kv; }
+    int64_t idx, heads, pairs;
+    if (i < nq_pairs && p.q) { base = static_cast<T*>(p.q); idx = i; heads = p.n_q; pairs = nq_pairs; }
+    else if (i >= nq_pairs) { base = static_cast<T*>(p.k); idx = i - nq_pairs; heads = p.n_kv; pairs = nk_pairs; }
     else continue;
     const int kk = (int)(idx % half);
     const int64_t token = idx / half / heads;
@@ -351,6 +353,7 @@ __global__ void rope_kernel(const __grid_constant__ RopeParams p) {
     float s, c;
     rope_sincos(pos, freq[kk], s, c);
     T* e = base + 2 * idx;
+    if (!in_extent(2 * idx, 2, 2 * pairs)) continue;
     const float x0 = Elt<T>::ld(e), x1 = Elt<T>::ld(e + 1);
     Elt<T>::st(e, x0 * c - x1 * s);
     Elt<T>::st(e + 1, x0 * s + x1 * c);
@@ -448,7 +451,7 @@ __global__ void rope_table_kernel(float2* __restrict__ tab, int64_t S, int half,
   if (s >= S) return;
   float sn, cs;
   rope_sincos((float)(pos0 + s), freq[k], sn, cs);
-  tab[s * half + k] = make_float2(cs, sn);
+  if (in_extent(s * half + k, 1, S * half)) tab[s * half + k] = make_float2(cs, sn);
 }
 
 // The split-form RMSNorm of bf16 rows (CH 16-byte chunks per lane) and the RoPE table of the
@@ -488,13 +491,13 @@ __global__ void __launch_bounds__(256) rmsnorm_rope_table_kernel(const uint16_t*
     if (s >= S) return;
     float sn, cs;
     rope_sincos((float)(pos0 + s), freq[k], sn, cs);
-    tab[s * half + k] = make_float2(cs, sn);
+    if (in_extent(s * half + k, 1, S * half)) tab[s * half + k] = make_float2(cs, sn);
   }
 }
 
 __global__ void widen_bf16_kernel(const uint16_t* __restrict__ src, float* __restrict__ dst, int64_t n) {
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
-    dst[i] = bf2f(src[i]);
+    if (in_extent(i, 1, n)) dst[i] = bf2f(src[i]);
 }
 
 template <typename T>
@@ -549,7 +552,7 @@ __global__ void __launch_bounds__(128) attn_simt_kernel(const __grid_constant__ 
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const int t = lane + 32 * i;
-    if (t < hd) Elt<T>::st(orow + t, o[i] * inv);
+    if (t < hd && in_extent(row * hd + t, 1, rows * hd)) Elt<T>::st(orow + t, o[i] * inv);
   }
 }
 
@@ -597,12 +600,14 @@ int launch_gemm_simt(const GemmDesc& g, cudaStream_t st) {
   if (g.M <= 0 || nout <= 0) return 0;
   dim3 grid((unsigned)((nout + SB - 1) / SB), (unsigned)((g.M + SB - 1) / SB));
   const bool sw = g.epi.kind == EPI_SWIGLU;
+  GemmDesc gd = g;
+  epi_set_extents(gd.epi, g.M, g.M);
   if (g.dtype == LLAMA_F32) {
-    if (sw) gemm_simt_kernel<float, true><<<grid, 256, 0, st>>>(g);
-    else gemm_simt_kernel<float, false><<<grid, 256, 0, st>>>(g);
+    if (sw) gemm_simt_kernel<float, true><<<grid, 256, 0, st>>>(gd);
+    else gemm_simt_kernel<float, false><<<grid, 256, 0, st>>>(gd);
   } else {
-    if (sw) gemm_simt_kernel<uint16_t, true><<<grid, 256, 0, st>>>(g);
-    else gemm_simt_kernel<uint16_t, false><<<grid, 256, 0, st>>>(g);
+    if (sw) gemm_simt_kernel<uint16_t, true><<<grid, 256, 0, st>>>(gd);
+    else gemm_simt_kernel<uint16_t, false><<<grid, 256, 0, st>>>(gd);
   }
   return 0;
 }
@@ -670,5 +675,7 @@ int launch_attn_simt(const AttnDesc& a, cudaStream_t st) {
   else attn_simt_kernel<uint16_t><<<grid, 128, smem, st>>>(a);
   return 0;
 }
+
+LLAMA_DEFINE_BOUNDS_READER(kernels_simt)
 
 }  // namespace llama

@@ -327,7 +327,7 @@ __global__ void __launch_bounds__(SP_THREADS) sample_kernel(const float* __restr
   }
   const float zmax = best;
   if (!(temperature > 0.f) || top_k == 1 || !(top_p > 0.f) || !isfinite(zmax) || V == 1) {
-    if (tid == 0 && cr == 0) tokens[row] = bi == INT_MAX ? 0 : bi;
+    if (tid == 0 && cr == 0 && in_extent(row, 1, gridDim.x / P)) tokens[row] = bi == INT_MAX ? 0 : bi;
     return;
   }
   auto mass = [&](float v) -> u64 { return __float2ull_rz(expf((v - zmax) / temperature) * kMassOne); };
@@ -467,7 +467,7 @@ __global__ void __launch_bounds__(SP_THREADS) sample_kernel(const float* __restr
       uu = (uu >= 0.f) ? fminf(uu, 0.99999994f) : 0.f;
       u64 tg = (u64)floor((double)uu * (double)zkept2);
       if (tg >= zkept2) tg = zkept2 - 1;
-      if (live && ex2c <= tg && tg < ex2c + m_id) tokens[row] = (int)(ckey[tid] >> 32);
+      if (live && ex2c <= tg && tg < ex2c + m_id && in_extent(row, 1, gridDim.x / P)) tokens[row] = (int)(ckey[tid] >> 32);
       return;
     }
     // more candidates than fit: the general path below
@@ -709,7 +709,10 @@ __global__ void __launch_bounds__(SP_THREADS) sample_kernel(const float* __restr
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         a += m[e];
-        if (a > tgt) { tokens[row] = 4 * q + e; break; }
+        if (a > tgt) {
+          if (in_extent(row, 1, gridDim.x / P)) tokens[row] = 4 * q + e;
+          break;
+        }
       }
     }
     if (tgt < base + chunk) break;
@@ -729,10 +732,12 @@ __global__ void embed_kernel(const T* __restrict__ table, int64_t V, int64_t d, 
     const int64_t n16 = d * (int64_t)sizeof(T) / 16;
     const uint4* src = reinterpret_cast<const uint4*>(table + (ok ? (int64_t)tok : 0) * d);
     uint4* out = reinterpret_cast<uint4*>(dst);
-    for (int64_t i = threadIdx.x; i < n16; i += blockDim.x) out[i] = ok ? __ldg(src + i) : make_uint4(0, 0, 0, 0);
+    for (int64_t i = threadIdx.x; i < n16; i += blockDim.x)   // x: [gridDim.x rows, d]
+      if (in_extent(row * n16 + i, 1, (int64_t)gridDim.x * n16)) out[i] = ok ? __ldg(src + i) : make_uint4(0, 0, 0, 0);
   } else {
     const T* src = table + (ok ? (int64_t)tok : 0) * d;
-    for (int64_t i = threadIdx.x; i < d; i += blockDim.x) dst[i] = ok ? src[i] : T(0);
+    for (int64_t i = threadIdx.x; i < d; i += blockDim.x)
+      if (in_extent(row * d + i, 1, (int64_t)gridDim.x * d)) dst[i] = ok ? src[i] : T(0);
   }
 }
 
@@ -791,5 +796,7 @@ int launch_embed(int dtype, const void* table, int64_t V, int64_t d, const int* 
   }
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
+
+LLAMA_DEFINE_BOUNDS_READER(sample)
 
 }  // namespace llama

@@ -30,9 +30,36 @@ def test_library_exports_every_declared_symbol():
 
 
 def test_status_strings():
-    for code in range(7):
+    for code in range(8):
         assert L.llama_status_string(code) != "unknown status"
     assert L.llama_status_string(99) == "unknown status"
+
+
+def test_bounds_checking_build_flag_plumbing():
+    """The -DLLAMA_DEBUG build: _build.build(debug=True) compiles every source with the flag into
+    its own library; that library reports the bounds checks in llama_build_info() and the release
+    library does not; every translation unit defines the reader of its bounds word, which
+    llama_get_device_status collects; the bounds status code has its name.  (No kernel runs here.)"""
+    import subprocess
+
+    from llama_decoder_block_fwd_gb300 import _build
+    path = _build.build(debug=True)
+    assert path == _build.LIB_DEBUG and os.path.exists(path)
+    log = open(os.path.join(_build.BUILD_DEBUG, "ptxas.log")).read()
+    assert all(f"== {src}" in log for src in _build.SOURCES)
+    dbg = ctypes.CDLL(path)
+    dbg.llama_build_info.restype = ctypes.c_int
+    assert dbg.llama_build_info() == L.BUILD_BOUNDS_CHECKS
+    if not L.DEBUG_BUILD:
+        assert L.llama_build_info() == 0                      # the release library has no checks
+    dbg.llama_status_string.restype = ctypes.c_char_p
+    assert b"bounds" in dbg.llama_status_string(7)
+    assert L.STATUS_NAMES[7] == "LLAMA_ERR_BOUNDS"
+    syms = subprocess.run(["nm", "-C", "-D", "--defined-only", path], capture_output=True, text=True).stdout
+    for src in _build.SOURCES:
+        assert f"llama::bounds_read_clear_{src[:-3]}()" in syms, src
+    for name in declared_functions():                       # the same C ABI in both builds
+        assert hasattr(dbg, name), name
 
 
 def _dims(**kw):
