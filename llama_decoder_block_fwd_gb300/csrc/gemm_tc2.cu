@@ -10,7 +10,7 @@
 //   * TMA loads of both CTAs complete on the leader's stage barrier (.cta_group::2 form);
 //   * the leader's commits are multicast to the stage and accumulator barriers of both CTAs;
 //   * both CTAs' epilogue threads release an accumulator on the leader's barrier.
-// Tiles are walked in bands of 8 column tiles as in gemm_tc.cu; the grid holds as many clusters
+// Tiles are walked in bands of column tiles (kBandBytes below); the grid holds as many clusters
 // as can be resident at once (persistent).
 #include <algorithm>
 #include <cstring>
@@ -21,7 +21,18 @@
 namespace llama {
 namespace {
 
-constexpr int T2M = 256, T2N = 256, T2K = 64, S2 = 6, BAND2 = 8;
+constexpr int T2M = 256, T2N = 256, T2K = 64, S2 = 6;
+// Tile order.  Tiles are walked in bands so that one operand's band stays in L2 while the other
+// operand streams past it once per band:
+//   * column bands (the default): a band of column tiles, row tiles inside it; the weight rows of
+//     the band stay resident and the activations are read once per band.  The band is as wide as
+//     kBandBytes of weights allows, and at least 8 tiles.
+//   * row bands, when the weights are more than twice the activations (the gate/up projection):
+//     a band of row tiles whose activation rows stay resident, column tiles inside it (the row
+//     tiles of the band take each column tile together, so its weights come from DRAM once per
+//     band); the weights are read once per band of kRowBandBytes of activations.
+constexpr int64_t kBandBytes = 48ll << 20;
+constexpr int64_t kRowBandBytes = 32ll << 20;
 constexpr uint32_t A2_BYTES = 128 * T2K * 2;    // this CTA's 128 rows of A: 16 KB
 constexpr uint32_t B2_BYTES = 128 * T2K * 2;    // this CTA's 128-row half of B: 16 KB
 constexpr uint32_t STAGE2 = A2_BYTES + B2_BYTES;
@@ -38,16 +49,27 @@ struct __align__(64) Tc2Params {
   int nseg;
   int swiglu;
   int m_tiles, n_tiles, num_tiles;
+  int band;             // column tiles per band (column bands)
+  int row_band;         // > 0: row tiles per band (row bands)
   unsigned* status;
   Epi epi;
 };
 
 __device__ __forceinline__ void tile2_coords(const Tc2Params& p, int t, int& mb, int& nb) {
-  const int band_tiles = p.m_tiles * BAND2;
+  if (p.row_band > 0) {
+    const int band_tiles = p.n_tiles * p.row_band;
+    const int band = t / band_tiles;
+    const int rem = t - band * band_tiles;
+    const int gh = min(p.row_band, p.m_tiles - band * p.row_band);
+    mb = band * p.row_band + rem % gh;
+    nb = rem / gh;
+    return;
+  }
+  const int band_tiles = p.m_tiles * p.band;
   const int band = t / band_tiles;
   const int rem = t - band * band_tiles;
-  const int gw = min(BAND2, p.n_tiles - band * BAND2);
-  nb = band * BAND2 + rem % gw;
+  const int gw = min(p.band, p.n_tiles - band * p.band);
+  nb = band * p.band + rem % gw;
   mb = rem / gw;
 }
 
@@ -339,6 +361,12 @@ int launch_gemm_tc2(const GemmDesc& g, unsigned* status, cudaStream_t st) {
   p.m_tiles = (int)((g.M + T2M - 1) / T2M);
   p.n_tiles = p.swiglu ? (int)(g.nB[0] / 128) : (int)(halves / 2);
   p.num_tiles = p.m_tiles * p.n_tiles;
+  // bytes of one column tile's weights (256 rows; gate and up: 128 rows of each) and of one row
+  // tile's activations (256 rows), both K bf16
+  const int64_t tile_bytes = 256 * g.K * 2;
+  const int64_t w_bytes = (int64_t)p.n_tiles * tile_bytes, a_bytes = (int64_t)p.m_tiles * tile_bytes;
+  p.band = (int)std::min<int64_t>(p.n_tiles, std::max<int64_t>(8, kBandBytes / tile_bytes));
+  p.row_band = w_bytes > 2 * a_bytes ? (int)std::max<int64_t>(1, std::min<int64_t>(p.m_tiles, kRowBandBytes / tile_bytes)) : 0;
   p.status = status;
   p.epi = g.epi;
   epi_set_extents(p.epi, g.M, g.M);
