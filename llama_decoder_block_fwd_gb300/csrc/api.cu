@@ -937,8 +937,14 @@ int llama_block_forward(const llama_dims* d, int dtype_flags, const llama_block_
   BlockWs b = plan_block(d, dtype, own_kv, ws, cache_capacity);
   void* kc = own_kv ? b.k : k_cache;
   void* vc = own_kv ? b.v : v_cache;
-  return block_body(d, dtype, w, x, x_f32, y, pos0, kc, vc, cache_capacity, b, static_cast<cudaStream_t>(stream),
-                    y_f32);
+  // the block's kernels that are made for it (the fused norm, the SM-pair GEMMs, the prefill
+  // attention) go out with programmatic dependent launch: each one's set-up overlaps its
+  // predecessor's tail, and each waits in griddepcontrol.wait before touching its inputs
+  set_pdl(true);
+  const int body_rc = block_body(d, dtype, w, x, x_f32, y, pos0, kc, vc, cache_capacity, b, static_cast<cudaStream_t>(stream),
+                                 y_f32);
+  set_pdl(false);
+  return body_rc;
 }
 
 int llama_stack_decode_step(const llama_dims* d, int dtype, int n_layers, const llama_block_weights* layers,

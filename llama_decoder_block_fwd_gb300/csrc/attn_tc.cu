@@ -164,6 +164,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1) attn_tc_kernel(const __grid_con
   const int nmax = max(ntile[0], ntile[1]);
   const int nq_tiles = (ntile[0] > 0) + (ntile[1] > 0);
 
+  pdl_trigger();   // the next kernel may be scheduled once every CTA of this one has started
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int i = 0; i < 14; ++i) mbar_init(&bars[i], (i == 9 || i == 10) ? 128 : 1);
@@ -179,6 +180,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1) attn_tc_kernel(const __grid_con
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint32_t sbase = smem_u32(smem);
+  pdl_wait();   // q, K and V come from the previous kernel
 
   if (warp == 0) {
     if (lane == 0) {  // ------------------------------------------------ TMA producer
@@ -407,7 +409,8 @@ int launch_hd(const AttnDesc& a, unsigned* status, cudaStream_t st) {
     attr_set[dev] = true;
   }
   const int64_t grid = (int64_t)p.pairs * a.B * a.n_kv;
-  attn_tc_kernel<HD><<<(unsigned)grid, AT_THREADS, Smem<HD>::TOTAL, st>>>(p);
+  if (launch_k(attn_tc_kernel<HD>, dim3((unsigned)grid), dim3(AT_THREADS), Smem<HD>::TOTAL, st, p) != cudaSuccess)
+    return -1;
   return 0;
 }
 

@@ -167,6 +167,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS2, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
+  // programmatic dependent launch: the next kernel may be scheduled as soon as every CTA of this
+  // one has started (it waits in its own pdl_wait until this grid has completed)
+  pdl_trigger();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
   const bool leader = rank == 0;
@@ -192,17 +195,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS2, 1)
   const uint32_t tmem = *tmem_slot;
   const int nkb = (p.K + T2K - 1) / T2K;
   const uint32_t smem_base = smem_u32(smem);
+  // The set-up above overlapped the previous kernel's tail; past pdl_wait its outputs are visible.
+  // The producer first issues the weight halves of its first stages (no kernel writes weights),
+  // then waits.
+  if (warp != 0 || lane != 0) pdl_wait();
 
   if (warp == 0) {
     if (lane == 0) {  // ---------------- TMA producer (both CTAs)
       int stage = 0;
       uint32_t phase = 0;
+      int pre = 0;   // stages of the first tile whose weights went out before pdl_wait
+      if (cluster_id < p.num_tiles) {
+        int mb, nb, seg, row;
+        tile2_coords(p, cluster_id, mb, nb);
+        half2_source(p, nb, (int)rank, seg, row);
+        const int seg_rows = (p.seg_half_end[seg] - (seg ? p.seg_half_end[seg - 1] : 0)) * 128;
+        for (; pre < min(S2, nkb); ++pre) {   // fresh stages: nothing to wait for
+          if (!box_in(pre * T2K, p.K, row, seg_rows)) break;   // bounds-checking builds
+          if (leader) mbar_arrive_expect_tx(&full[pre], 2 * STAGE2);   // both CTAs' bytes
+          tma_load_2d_pair(smem_base + pre * STAGE2 + A2_BYTES, &p.tmB[seg], map_to_rank(smem_u32(&full[pre]), 0),
+                           pre * T2K, row);
+        }
+      }
+      pdl_wait();
+      bool first_tile = true;
       for (int t = cluster_id; t < p.num_tiles; t += n_clusters) {
         int mb, nb, seg, row;
         tile2_coords(p, t, mb, nb);
         half2_source(p, nb, (int)rank, seg, row);
         bool ok = true;
         for (int kb = 0; kb < nkb; ++kb) {
+          if (first_tile && kb < pre) {   // its weights are on their way: the activations only
+            if (!box_in(kb * T2K, p.K, (int64_t)mb * T2M, p.M)) { *abort_flag = 1; ok = false; break; }
+            tma_load_2d_pair(smem_base + stage * STAGE2, &p.tmA, map_to_rank(smem_u32(&full[stage]), 0), kb * T2K,
+                             mb * T2M + (int)rank * 128);
+            if (++stage == S2) { stage = 0; phase ^= 1; }
+            continue;
+          }
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.status)) { ok = false; break; }
           // bounds-checking builds: the tile's start in A (the second CTA's 128-row half of a ragged
           // last tile may lie past M by design: the load fills zeros) and this CTA's B half
@@ -219,6 +248,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS2, 1)
           tma_load_2d_pair(sa + A2_BYTES, &p.tmB[seg], lbar, kb * T2K, row);
           if (++stage == S2) { stage = 0; phase ^= 1; }
         }
+        first_tile = false;
         if (!ok) break;
       }
     }
@@ -387,8 +417,7 @@ int launch_gemm_tc2(const GemmDesc& g, unsigned* status, cudaStream_t st) {
     max_clusters[dev] = n;
   }
   const int clusters = std::max(1, std::min(p.num_tiles, max_clusters[dev]));
-  gemm_tc2_kernel<<<2 * clusters, THREADS2, SMEM2, st>>>(p);
-  return 0;
+  return launch_k(gemm_tc2_kernel, dim3(2 * clusters), dim3(THREADS2), SMEM2, st, p) == cudaSuccess ? 0 : -1;
 }
 
 LLAMA_DEFINE_BOUNDS_READER(gemm_tc2)

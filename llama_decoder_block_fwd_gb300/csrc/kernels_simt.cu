@@ -467,6 +467,8 @@ __global__ void __launch_bounds__(256) rmsnorm_rope_table_kernel(const uint16_t*
                                                                  int64_t rows, int d, float eps, int K, int tab_blocks,
                                                                  float2* __restrict__ tab, int64_t S, int half,
                                                                  int64_t pos0, const __grid_constant__ RopeParams p) {
+  pdl_trigger();
+  pdl_wait();   // x may come from the previous kernel; the table is read by the previous call's GEMM
   const int b = blockIdx.x;
   const int lead = tab_blocks * (K + 1);
   int norm_idx = -1, tab_idx = -1;
@@ -639,11 +641,14 @@ int launch_rmsnorm_rope_table(const void* x, const void* g, void* y, float* rs, 
   const uint16_t* gb = static_cast<const uint16_t*>(g);
   uint16_t* yb = static_cast<uint16_t*>(y);
   if (per_lane <= 4)
-    rmsnorm_rope_table_kernel<4><<<grid, 256, 0, st>>>(xb, gb, yb, rs, rows, (int)d, eps, K, tab_blocks, tab, S, half, pos0, p);
+    return launch_k(rmsnorm_rope_table_kernel<4>, grid, dim3(256), 0, st, xb, gb, yb, rs, rows, (int)d, eps, K,
+                    tab_blocks, tab, S, half, pos0, p) == cudaSuccess ? 0 : -1;
   else if (per_lane <= 8)
-    rmsnorm_rope_table_kernel<8><<<grid, 256, 0, st>>>(xb, gb, yb, rs, rows, (int)d, eps, K, tab_blocks, tab, S, half, pos0, p);
+    return launch_k(rmsnorm_rope_table_kernel<8>, grid, dim3(256), 0, st, xb, gb, yb, rs, rows, (int)d, eps, K,
+                    tab_blocks, tab, S, half, pos0, p) == cudaSuccess ? 0 : -1;
   else
-    rmsnorm_rope_table_kernel<16><<<grid, 256, 0, st>>>(xb, gb, yb, rs, rows, (int)d, eps, K, tab_blocks, tab, S, half, pos0, p);
+    return launch_k(rmsnorm_rope_table_kernel<16>, grid, dim3(256), 0, st, xb, gb, yb, rs, rows, (int)d, eps, K,
+                    tab_blocks, tab, S, half, pos0, p) == cudaSuccess ? 0 : -1;
   return 0;
 }
 
