@@ -470,9 +470,14 @@ int block_body(const llama_dims* d, int dtype, const llama_block_weights* w, con
     RopeFreq freq[kMaxRopePairs];
     rope_freqs(d, freq);
     prof::begin("rmsnorm", st);
-    if (launch_rmsnorm_rope_table(x, w->attn_norm_g, ws.u, ws.rs1, T, D, eps, ws.rope_tab, d->S, (int)d->head_dim,
-                                  pos0, freq, st) != 0)
-      return LLAMA_ERR_UNSUPPORTED;
+    // the block's first kernel goes out without programmatic launch: what precedes it in the stream
+    // may be a wait on another stream (a copy of x), which it must not overlap
+    const bool pdl = pdl_enabled();
+    set_pdl(false);
+    const int lrc = launch_rmsnorm_rope_table(x, w->attn_norm_g, ws.u, ws.rs1, T, D, eps, ws.rope_tab, d->S,
+                                              (int)d->head_dim, pos0, freq, st);
+    set_pdl(pdl);
+    if (lrc != 0) return LLAMA_ERR_UNSUPPORTED;
     prof::end(st);
     if ((rc = launch_status()) != LLAMA_OK) return rc;
   } else if ((rc = run_rmsnorm(dtype, x_f32 || f32, f32, x, w->attn_norm_g, ws.u, T, D, eps, st, ws.rs1)) !=
