@@ -34,7 +34,7 @@ constexpr int AT_THREADS = 320;
 constexpr uint32_t TMEM_COLS_ATTN = 512;
 constexpr float kRescaleLog2 = 8.0f;
 
-struct __align__(64) AttnParams {
+struct AttnParams {   // 128-byte aligned by its tensor maps
   CUtensorMap tmQ;   // [B*S, n_q, hd], box (64, r, 128/r)
   CUtensorMap tmK;   // [B, kv_len, n_kv, hd], box (64, 1, 128, 1)
   CUtensorMap tmV;

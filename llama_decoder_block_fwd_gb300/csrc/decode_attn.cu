@@ -39,7 +39,7 @@ constexpr float kDaRescaleLog2 = 8.0f;
 
 constexpr int DA_MAX_GRID = 256;         // CTAs at most (sizes the partial slots)
 
-struct __align__(64) DecodeAttnParams {
+struct DecodeAttnParams {   // 128-byte aligned by its tensor maps
   CUtensorMap tmK;   // [B, kv_len, n_kv, hd], box (64, 1, 128, 1)
   CUtensorMap tmV;
   CUtensorMap tmQ;   // [B, n_q, hd], box (64, r, 1)
@@ -77,11 +77,6 @@ __device__ __forceinline__ void tma_load_4d_da(uint32_t dst, const CUtensorMap* 
       : "memory");
 }
 
-__device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t (&v)[4]) {
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3])
-               : "r"(taddr));
-}
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"

@@ -42,7 +42,7 @@ constexpr uint32_t D8_TMEM_COLS = 128;   // S^T 2 x NP (cols 0..63), O^T NP (col
 constexpr float kD8RescaleLog2 = 2.0f;
 constexpr float kD8PScaleLog2 = 6.0f;
 
-struct __align__(64) DecodeAttn8Params {
+struct DecodeAttn8Params {   // 128-byte aligned by its tensor maps
   CUtensorMap tmK;   // codes [B, kv_len, n_kv, hd] (bytes), box (128, 1, 128, 1), 128-byte swizzle
   CUtensorMap tmV;
   const uint16_t* q;      // bf16 [B, n_q, hd]

@@ -24,7 +24,7 @@ constexpr int SK_TK = 64, SK_THREADS = 192;
 constexpr uint32_t SK_A_BYTES = 128 * SK_TK * 2;     // 128 weight rows x 64: 16 KB
 constexpr uint32_t SK_TMEM_COLS = 512;
 
-struct __align__(64) SkParams {
+struct SkParams {   // 128-byte aligned by its tensor maps
   CUtensorMap tmW[3];   // weight segments [n_i, K], box (64, 128)
   CUtensorMap tmX;      // stacked activations [2 Mp, K], box (64, 2 Mp)
   int M, Mp, K, N;

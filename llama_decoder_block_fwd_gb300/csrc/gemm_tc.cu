@@ -23,7 +23,7 @@
 namespace llama {
 namespace {
 
-constexpr int TM = 128, TN = 256, TK = 64, STAGES = 4, BAND = 8;
+constexpr int TM = 128, TK = 64, STAGES = 4, BAND = 8;   // tiles of 128 rows x 256 columns
 constexpr uint32_t A_BYTES = TM * TK * 2;        // 16 KB
 constexpr uint32_t BH_BYTES = 128 * TK * 2;      // 16 KB per 128-row half of B
 constexpr uint32_t STAGE_BYTES = A_BYTES + 2 * BH_BYTES;
@@ -31,7 +31,7 @@ constexpr uint32_t SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
 constexpr int NUM_THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
 
-struct __align__(64) TcParams {
+struct TcParams {   // 128-byte aligned by its tensor maps
   CUtensorMap tmA;
   CUtensorMap tmA_lo;    // dual: low bf16 part of A (A = hi + lo)
   CUtensorMap tmB[3];

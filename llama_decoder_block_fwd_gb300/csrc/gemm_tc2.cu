@@ -40,7 +40,7 @@ constexpr uint32_t SMEM2 = S2 * STAGE2 + 1024 + 256;
 constexpr int THREADS2 = 320;   // TMA warp, MMA warp, 8 epilogue warps
 constexpr uint32_t TMEM2_COLS = 512;
 
-struct __align__(64) Tc2Params {
+struct Tc2Params {   // 128-byte aligned by its tensor maps
   CUtensorMap tmA;
   CUtensorMap tmB[3];
   int M, K;

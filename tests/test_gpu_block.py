@@ -182,3 +182,30 @@ def test_two_blocks_with_an_fp32_residual_stream():
         h, _, _ = O.block_forward(W.host_x(wl, b)[None], hw[0], d1)
         ref, _, _ = O.block_forward(h, hw[1], d1)
         assert_parity(to_f64(y2[b]), ref[0], wl.dtype, f"two blocks, seq {b}")
+
+
+def test_back_to_back_calls_share_a_workspace():
+    """Two block forwards on different inputs, queued back to back on one stream with one workspace
+    and no synchronisation between them, give bit for bit what each gives alone.  Inside a call the
+    kernels overlap their set-up with their predecessor's tail (programmatic dependent launch); this
+    checks that no kernel reads or writes a buffer early, within a call or across the two."""
+    import torch
+
+    from synth import BF16
+    wl = C.Workload("mid-b2b", 15, C.BF16, 1, 1024, 1024, 8, 2, 128, 2560, 5e5, 1e-5, gain_std=0.1)
+    w = W.device_layer(wl)
+    x1 = W.device_x(wl).reshape(-1, wl.d_model)
+    x2 = W.device_tensor(BF16, tuple(x1.shape), wl.seed + 1, 7, 0.0, 1.0)
+    bw = L.block_weights(w)
+    ws = torch.empty(L.llama_workspace_bytes(L.OP_BLOCK_FORWARD, wl.dims, wl.dtype), dtype=torch.uint8, device="cuda")
+    ya = torch.empty(x1.shape, dtype=torch.float32, device="cuda")
+    yb = torch.empty_like(ya)
+    for _ in range(3):
+        L.llama_block_forward(wl.dims, wl.dtype | L.Y_F32, bw, x1, ya, 0, None, None, 0, ws)
+        L.llama_block_forward(wl.dims, wl.dtype | L.Y_F32, bw, x2, yb, 0, None, None, 0, ws)
+    torch.cuda.synchronize()
+    assert L.llama_get_device_status() == 0
+    y1 = _run_block(wl, x1, w, flags=L.Y_F32)
+    y2 = _run_block(wl, x2, w, flags=L.Y_F32)
+    assert torch.equal(ya, y1) and torch.equal(yb, y2)
+    assert not torch.equal(y1, y2)
