@@ -88,6 +88,7 @@ __device__ __forceinline__ bool unit_next(const SkParams& p, UnitIter& it, int n
   return true;
 }
 
+template <int MODE>   // 0: split-K partials; 1: atomic add; 2: store (x row scale)
 __global__ void __launch_bounds__(SK_THREADS, 1) gemm_skinny_kernel(const __grid_constant__ SkParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -210,28 +211,27 @@ __global__ void __launch_bounds__(SK_THREADS, 1) gemm_skinny_kernel(const __grid
       const int64_t n = (int64_t)nt * 128 + q * 32 + lane;     // output column (virtual N)
       const bool live = n < p.N;
       const uint32_t tb = tmem + buf * 256 + lane_base;
+      // Four token rows per step, rolled: this code runs once per unit, at the end of the CTA's
+      // weight stream, and a short loop keeps its instruction fetches few while the memory system
+      // is still saturated by the other SMs' streams.
 #pragma unroll 1
-      for (int c0 = 0; c0 < p.M; c0 += 32) {
-        uint32_t hi[32], lo[32];
-        tmem_ld32(tb + c0, hi);
-        tmem_ld32(tb + p.Mp + c0, lo);
+      for (int c0 = 0; c0 < p.M; c0 += 4) {
+        uint32_t hi[4], lo[4];
+        tmem_ld4(tb + c0, hi);
+        tmem_ld4(tb + p.Mp + c0, lo);
         tc_wait_ld();
-        if (live) {
-          const int cn = min(32, p.M - c0);
+        if (!live) continue;
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            if (i >= cn) break;
-            const int64_t c = c0 + i;
-            const float v = __uint_as_float(hi[i]) + __uint_as_float(lo[i]);
-            if (p.mode == 0) {
-              const int64_t at = ((int64_t)split * p.M + c) * p.ldo + n;
-              if (in_extent(at, 1, (int64_t)p.k_splits * p.M * p.ldo)) p.out[at] = v;
-            } else if (!in_extent(c * p.ldo + n, 1, (int64_t)p.M * p.ldo)) {
-            } else if (p.mode == 1) {
-              atomicAdd(p.out + c * p.ldo + n, v);
-            } else {
-              p.out[c * p.ldo + n] = p.row_scale ? v * __ldg(p.row_scale + c) : v;
-            }
+        for (int i = 0; i < 4; ++i) {
+          const int64_t c = c0 + i;
+          if (c >= p.M) break;
+          const float v = __uint_as_float(hi[i]) + __uint_as_float(lo[i]);
+          if (MODE == 0) {
+            const int64_t at = ((int64_t)split * p.M + c) * p.ldo + n;
+            if (in_extent(at, 1, (int64_t)p.k_splits * p.M * p.ldo)) p.out[at] = v;
+          } else if (in_extent(c * p.ldo + n, 1, (int64_t)p.M * p.ldo)) {
+            if (MODE == 1) atomicAdd(p.out + c * p.ldo + n, v);
+            else p.out[c * p.ldo + n] = p.row_scale ? v * __ldg(p.row_scale + c) : v;
           }
         }
       }
@@ -299,14 +299,22 @@ int launch_gemm_skinny(const SkinnyDesc& g, int num_sms, unsigned* status, cudaS
   static bool attr_set[64] = {};
   if (dev < 0 || dev >= 64) return -1;
   if (!attr_set[dev]) {
-    if (cudaFuncSetAttribute(gemm_skinny_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, budget + 1280) !=
-        cudaSuccess)
-      return -1;
+    const void* fns[3] = {(const void*)gemm_skinny_kernel<0>, (const void*)gemm_skinny_kernel<1>,
+                          (const void*)gemm_skinny_kernel<2>};
+    for (const void* f : fns)
+      if (cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, budget + 1280) != cudaSuccess) return -1;
     attr_set[dev] = true;
   }
   const int grid = p.streamk ? (int)std::max<int64_t>(1, std::min<int64_t>(p.total_items, num_sms))
                              : std::max(1, std::min(p.num_units, num_sms));
-  return launch_k(gemm_skinny_kernel, dim3(grid), dim3(SK_THREADS), smem, st, p) == cudaSuccess ? 0 : -1;
+  cudaError_t e;
+  switch (p.mode) {
+    case 0: e = launch_k(gemm_skinny_kernel<0>, dim3(grid), dim3(SK_THREADS), smem, st, p); break;
+    case 1: e = launch_k(gemm_skinny_kernel<1>, dim3(grid), dim3(SK_THREADS), smem, st, p); break;
+    case 2: e = launch_k(gemm_skinny_kernel<2>, dim3(grid), dim3(SK_THREADS), smem, st, p); break;
+    default: return -1;
+  }
+  return e == cudaSuccess ? 0 : -1;
 }
 
 LLAMA_DEFINE_BOUNDS_READER(gemm_skinny)
