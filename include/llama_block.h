@@ -245,7 +245,9 @@ int llama_stack_decode_step_kv8(const llama_dims* dims, int n_layers,
  * upper bound of seq_pos over the batch (host value: it sizes the work split and the workspace,
  * llama_workspace_bytes(..., kv_capacity = max_pos + 1)).  block_table and seq_pos are int32
  * device arrays; every page that a sequence uses up to its new position must be listed.  Rows of
- * a sequence's last page past its new position are never used (their contents do not matter).  */
+ * a sequence's last page past its new position are never used (their contents do not matter).
+ * The page that receives a sequence's new K/V belongs to that sequence alone: the step writes it
+ * while other sequences' attention may already be reading their earlier pages.                  */
 
 /* llama_stack_decode_step over a paged cache: writes each sequence's new K/V into its page at
  * seq_pos[b] and runs RoPE at that position.  Same shapes as the tensor-core dense call (else

@@ -158,9 +158,14 @@ def _nbytes(t) -> int:
 
 
 def block_weights(w) -> BlockWeights:
-    """BlockWeights from a mapping (or object) holding the nine device tensors."""
+    """BlockWeights from a mapping (or object) holding the nine device tensors.  The struct keeps
+    references to the tensors, so their memory stays allocated while the struct is alive (the
+    library reads it through the raw pointers)."""
     get = (lambda n: w[n]) if isinstance(w, dict) else (lambda n: getattr(w, n))
-    return BlockWeights(*[_p(get(n)) for n in _WEIGHT_FIELDS])
+    tensors = [get(n) for n in _WEIGHT_FIELDS]
+    bw = BlockWeights(*[_p(t) for t in tensors])
+    bw._tensors = tensors
+    return bw
 
 
 def llama_rmsnorm(dims, dtype, x, g, y, stream=None):

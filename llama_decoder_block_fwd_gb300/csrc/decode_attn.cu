@@ -226,10 +226,45 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_kernel(const __grid
   const uint32_t tO = tmem + 32;     // O^T: columns 32..47
   const uint32_t sbase = smem_u32(smem);
 
-  pdl_wait();   // q and the newest K/V come from the previous kernel; the partials may still be read
   const int64_t T = all_tiles(p.seq_pos, p.kv_tiles, p.B, p.n_kv);
+  // K and V of tile t of pair (b, g) into ring stage st (false: a box outside the cache, which
+  // bounds-checking builds report)
+  auto load_kv = [&](int b, int g, int t, int st) -> bool {
+    const int zc = p.block_table ? 0 : t * 128;
+    const int wc = p.block_table ? __ldg(p.block_table + (int64_t)b * p.max_pages + t) : b;
+    if (!box_in(0, DA_HD, g, p.n_kv, zc, p.block_table ? 128 : p.kv_len, wc, p.block_table ? p.n_pages : p.B))
+      return false;
+    mbar_arrive_expect_tx(&k_full[st], L::KV);
+    for (int hh = 0; hh < 2; ++hh)
+      tma_load_4d_da(sbase + L::OFF_K + st * L::KV + hh * 16384, &p.tmK, &k_full[st], hh * 64, g, zc, wc);
+    mbar_arrive_expect_tx(&v_full[st], L::KV);
+    for (int hh = 0; hh < 2; ++hh)
+      tma_load_4d_da(sbase + L::OFF_V + st * L::KV + hh * 16384, &p.tmV, &v_full[st], hh * 64, g, zc, wc);
+    return true;
+  };
+  // Before the dependency wait the producer starts on the first ring stages: the cached keys and
+  // values of a pair's tiles before its last are not written by the kernel before this one (the
+  // decode step writes only the new position, which lies in the pair's last tile).
+  int pre = 0;
+  bool pre_ok = true;
+  if (warp == 0 && lane == 0) {
+    SegIter si;
+    seg_begin(p, T, si);
+    int b, g, t0, t1, kv_len;
+    int64_t slot;
+    bool stop = false;
+    while (!stop && pre < DA_STAGES && seg_next(p, si, b, g, t0, t1, kv_len, slot)) {
+      const int nt = seq_tiles(p.seq_pos, p.kv_tiles, b);
+      for (int t = t0; t < t1 && pre < DA_STAGES; ++t) {
+        if (t >= nt - 1) { stop = true; break; }
+        if (!load_kv(b, g, t, pre)) { *abort_flag = 1; pre_ok = false; stop = true; break; }
+        ++pre;
+      }
+    }
+  }
+  pdl_wait();   // q and the newest K/V come from the previous kernel; the partials may still be read
   if (warp == 0) {
-    if (lane == 0) {  // ---------------------------------------------------- TMA producer
+    if (lane == 0 && pre_ok) {  // ---------------------------------------------------- TMA producer
       int tile = 0, it = 0;
       bool ok = true;
       SegIter si;
@@ -245,22 +280,11 @@ __global__ void __launch_bounds__(DA_THREADS, 1) decode_attn_kernel(const __grid
         for (int hh = 0; hh < 2; ++hh)
           tma_load_3d(sbase + L::OFF_Q + qb * L::QB + hh * (L::QB / 2), &p.tmQ, &q_full[qb], hh * 64, g * p.r, b);
         for (int t = t0; t < t1; ++t, ++tile) {
+          if (tile < pre) continue;   // issued before the dependency wait
           const int st = tile % DA_STAGES;
           const uint32_t ph = (tile / DA_STAGES) & 1;
           if (!mbar_wait(&kv_empty[st], ph ^ 1, abort_flag, p.status)) { ok = false; break; }
-          const int zc = p.block_table ? 0 : t * 128;
-          const int wc = p.block_table ? __ldg(p.block_table + (int64_t)b * p.max_pages + t) : b;
-          if (!box_in(0, DA_HD, g, p.n_kv, zc, p.block_table ? 128 : p.kv_len, wc, p.block_table ? p.n_pages : p.B)) {
-            *abort_flag = 1;
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&k_full[st], L::KV);
-          for (int hh = 0; hh < 2; ++hh)
-            tma_load_4d_da(sbase + L::OFF_K + st * L::KV + hh * 16384, &p.tmK, &k_full[st], hh * 64, g, zc, wc);
-          mbar_arrive_expect_tx(&v_full[st], L::KV);
-          for (int hh = 0; hh < 2; ++hh)
-            tma_load_4d_da(sbase + L::OFF_V + st * L::KV + hh * 16384, &p.tmV, &v_full[st], hh * 64, g, zc, wc);
+          if (!load_kv(b, g, t, st)) { *abort_flag = 1; ok = false; break; }
         }
       }
     }
