@@ -177,6 +177,33 @@ def test_host_tensors_are_refused_before_the_library_is_called():
         L.llama_sample(torch.zeros(2, 10), 1.0, 0, 1.0, torch.zeros(2), torch.zeros(2, dtype=torch.int32), stream=0)
 
 
+def test_block_weights_keep_their_tensors_alive():
+    """The weight struct holds raw addresses; it also keeps references to the tensors it was built
+    from, so dropping the caller's dict does not free memory the library still reads."""
+    import gc
+    import weakref
+
+    class FakeDeviceTensor:   # what _p needs: is_cuda and data_ptr
+        is_cuda = True
+
+        def __init__(self, addr):
+            self.addr = addr
+
+        def data_ptr(self):
+            return self.addr
+
+    w = {n: FakeDeviceTensor(0x1000 * (i + 1)) for i, n in enumerate(L._WEIGHT_FIELDS)}
+    refs = [weakref.ref(t) for t in w.values()]
+    bw = L.block_weights(w)
+    del w
+    gc.collect()
+    assert all(r() is not None for r in refs)
+    assert [getattr(bw, n) for n in L._WEIGHT_FIELDS] == [0x1000 * (i + 1) for i in range(len(L._WEIGHT_FIELDS))]
+    del bw
+    gc.collect()
+    assert all(r() is None for r in refs)
+
+
 def _noalloc_scratch_bytes(B, n_kv, r):
     """The allocation-free decode attention's size rule as its header states it: B*n_kv + 256
     slots of r rows of 130 floats, as two arrays each rounded up to 256 bytes."""
