@@ -193,6 +193,24 @@ __global__ void __launch_bounds__(D8_THREADS, D8_CTAS_PER_SM) decode_attn8_kerne
   const uint32_t tO = tmem + 64;     // O^T: columns 64..64+NP-1
   const uint32_t sbase = smem_u32(smem);
 
+  // Before the dependency wait the producer starts on the first K stages: the codes of a
+  // sequence's tiles before its last are not written by the kernel before this one (the decode
+  // step writes only the new position, which lies in the last tile).
+  int pre = 0;
+  if (warp == 0 && lane == 0) {
+    bool stop = false;
+    for (int item = blockIdx.x; !stop && pre < D8_KSTAGES && item < p.n_items; item += gridDim.x) {
+      int b, g, t0, t1, chunk;
+      item_coords8(p, item, b, g, t0, t1, chunk);
+      for (int t = t0; t < t1 && pre < D8_KSTAGES; ++t) {
+        if (t >= p.kv_tiles - 1) { stop = true; break; }
+        if (!box_in(0, D8_HD, g, p.n_kv, (int64_t)t * 128, p.kv_len, b, p.B)) { *abort_flag = 1; stop = true; break; }
+        mbar_arrive_expect_tx(&bars[B_K8F + pre], L::F8);
+        tma_load_4d_d8(sbase + L::OFF_K8 + pre * L::F8, &p.tmK, &bars[B_K8F + pre], 0, g, t * 128, b);
+        ++pre;
+      }
+    }
+  }
   pdl_wait();
   if (warp == 0) {
     if (lane == 0) {  // ---------------------------------------------------- TMA producer
@@ -213,11 +231,13 @@ __global__ void __launch_bounds__(D8_THREADS, D8_CTAS_PER_SM) decode_attn8_kerne
         int b, g, t0, t1, chunk;
         item_coords8(p, item, b, g, t0, t1, chunk);
         for (int t = t0; t < t1; ++t, ++tile) {
-          const int ks = tile % D8_KSTAGES;
-          if (!mbar_wait(&bars[B_K8E + ks], ((tile / D8_KSTAGES) & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
-          if (!box_in(0, D8_HD, g, p.n_kv, (int64_t)t * 128, p.kv_len, b, p.B)) { *abort_flag = 1; ok = false; break; }
-          mbar_arrive_expect_tx(&bars[B_K8F + ks], L::F8);
-          tma_load_4d_d8(sbase + L::OFF_K8 + ks * L::F8, &p.tmK, &bars[B_K8F + ks], 0, g, t * 128, b);
+          if (tile >= pre) {   // (tiles below pre were issued before the dependency wait)
+            const int ks = tile % D8_KSTAGES;
+            if (!mbar_wait(&bars[B_K8E + ks], ((tile / D8_KSTAGES) & 1) ^ 1, abort_flag, p.status)) { ok = false; break; }
+            if (!box_in(0, D8_HD, g, p.n_kv, (int64_t)t * 128, p.kv_len, b, p.B)) { *abort_flag = 1; ok = false; break; }
+            mbar_arrive_expect_tx(&bars[B_K8F + ks], L::F8);
+            tma_load_4d_d8(sbase + L::OFF_K8 + ks * L::F8, &p.tmK, &bars[B_K8F + ks], 0, g, t * 128, b);
+          }
           if (tile > 0 && !issue_v(tile - 1)) { ok = false; break; }
           vb = b; vg = g; vt = t;
         }
