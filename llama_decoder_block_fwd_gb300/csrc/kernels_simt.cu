@@ -178,13 +178,25 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float2 v) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-template <int CH, bool SPLIT>
-__global__ void __launch_bounds__(kRnThreads, 2) rmsnorm_stream_kernel(const uint16_t* __restrict__ x,
-                                                                      const uint16_t* __restrict__ g,
-                                                                      uint16_t* __restrict__ y, float* __restrict__ rs_out,
-                                                                      int64_t rows, int d, float eps, int nbuf,
-                                                                      unsigned* status) {
+// The RoPE table of a block's positions, written by one extra warp of the block's first norm
+// (TAB): tab[s][k] = (cos, sin) of (pos0 + s) * theta_k for s < S, k < half.
+struct RnTab {
+  float2* tab;
+  int64_t S, pos0;
+  int half;
+  RopeFreq freq[kMaxRopePairs];
+};
+
+template <int CH, bool SPLIT, bool TAB>
+__global__ void __launch_bounds__(kRnThreads + 32, 2) rmsnorm_stream_kernel(const uint16_t* __restrict__ x,
+                                                                           const uint16_t* __restrict__ g,
+                                                                           uint16_t* __restrict__ y,
+                                                                           float* __restrict__ rs_out, int64_t rows,
+                                                                           int d, float eps, int nbuf, unsigned* status,
+                                                                           const __grid_constant__ RnTab tp) {
   extern __shared__ __align__(128) uint8_t rn_smem[];
+  pdl_trigger();
+  pdl_wait();   // x may come from the previous kernel; the table is read by the previous call's GEMM
   const uint32_t row_bytes = (uint32_t)d * 2;
   uint4* gs = reinterpret_cast<uint4*>(rn_smem + (size_t)nbuf * row_bytes);   // the gain, d bf16
   uint64_t* full = reinterpret_cast<uint64_t*>(rn_smem + (size_t)(nbuf + 1) * row_bytes);
@@ -199,6 +211,20 @@ __global__ void __launch_bounds__(kRnThreads, 2) rmsnorm_stream_kernel(const uin
     fence_mbar_init();
   }
   __syncthreads();
+  if (TAB && warp == kRnWarps + 1) {   // the RoPE table, beside the norm's memory traffic
+    __shared__ RopeFreq fq[kMaxRopePairs];
+    for (int k = lane; k < tp.half; k += 32) fq[k] = tp.freq[k];
+    __syncwarp();
+    const int64_t total = tp.S * tp.half;
+    for (int64_t i = (int64_t)blockIdx.x * 32 + lane; i < total; i += (int64_t)gridDim.x * 32) {
+      const int64_t sp = i / tp.half;
+      const int k = (int)(i - sp * tp.half);
+      float sn, cs;
+      rope_sincos((float)(tp.pos0 + sp), fq[k], sn, cs);
+      if (in_extent(i, 1, total)) tp.tab[i] = make_float2(cs, sn);
+    }
+    return;
+  }
   if (warp == kRnWarps) {
     if (lane == 0) {   // producer
       int64_t issued = 0;
@@ -264,9 +290,9 @@ __global__ void __launch_bounds__(kRnThreads, 2) rmsnorm_stream_kernel(const uin
   }
 }
 
-template <bool SPLIT>
+template <bool SPLIT, bool TAB>
 int rmsnorm_stream_launch(const void* x, const void* g, void* y, float* rs, int64_t rows, int d, float eps,
-                          cudaStream_t st) {
+                          cudaStream_t st, const RnTab& tp) {
   unsigned* status = status_ptr();
   if (!status) return -1;
   const uint32_t row_bytes = (uint32_t)d * 2;
@@ -280,7 +306,7 @@ int rmsnorm_stream_launch(const void* x, const void* g, void* y, float* rs, int6
   const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(rows, 2 * (int64_t)num_sms()));
   int dev = 0;
   cudaGetDevice(&dev);
-  static bool attr_set[64][5] = {};
+  static bool attr_set[64][3] = {};
   auto go = [&](auto kernel, int idx) -> int {
     if (dev < 0 || dev >= 64) return -1;
     if (!attr_set[dev][idx]) {
@@ -288,14 +314,21 @@ int rmsnorm_stream_launch(const void* x, const void* g, void* y, float* rs, int6
         return -1;
       attr_set[dev][idx] = true;
     }
-    kernel<<<grid, kRnThreads, smem, st>>>(static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(g),
-                                           static_cast<uint16_t*>(y), rs, rows, d, eps, nbuf, status);
-    return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+    return launch_k(kernel, dim3(grid), dim3(kRnThreads + (TAB ? 32 : 0)), smem, st,
+                    static_cast<const uint16_t*>(x), static_cast<const uint16_t*>(g), static_cast<uint16_t*>(y), rs,
+                    rows, d, eps, nbuf, status, tp) == cudaSuccess ? 0 : -1;
   };
   const int ch = (d / 8 + 31) / 32;
-  if (ch <= 4) return go(rmsnorm_stream_kernel<4, SPLIT>, 0);
-  if (ch <= 8) return go(rmsnorm_stream_kernel<8, SPLIT>, 1);
-  return go(rmsnorm_stream_kernel<16, SPLIT>, 2);
+  if (ch <= 4) return go(rmsnorm_stream_kernel<4, SPLIT, TAB>, 0);
+  if (ch <= 8) return go(rmsnorm_stream_kernel<8, SPLIT, TAB>, 1);
+  return go(rmsnorm_stream_kernel<16, SPLIT, TAB>, 2);
+}
+
+// bf16 rows the streaming kernel takes: 16-byte aligned, 1024..4096 wide, at least two per SM
+bool rmsnorm_stream_ok(const void* x, const void* g, const void* y, int64_t rows, int64_t d) {
+  const bool aligned = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(g) |
+                         reinterpret_cast<uintptr_t>(y)) & 15) == 0;
+  return aligned && d % 8 == 0 && d >= 1024 && d <= 4096 && rows >= 2 * 152;
 }
 
 template <typename TX, typename TG, typename TY, bool SPLIT>
@@ -575,11 +608,12 @@ int launch_rmsnorm(int dtype, int x_f32, int y_f32, const void* x, const void* g
     return split ? rmsnorm_dispatch<float, bf, bf, true>(x, g, y, rs_out, rows, d, eps, st)
                  : rmsnorm_dispatch<float, bf, bf, false>(x, g, y, rs_out, rows, d, eps, st);
   // bf16 rows of 1024..4096 elements with 16-byte aligned rows: the streaming kernel
-  const bool aligned = ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(g) |
-                         reinterpret_cast<uintptr_t>(y)) & 15) == 0;
-  if (aligned && d % 8 == 0 && d >= 1024 && d <= 4096 && rows >= 2 * 152)
-    return split ? rmsnorm_stream_launch<true>(x, g, y, rs_out, rows, (int)d, eps, st)
-                 : rmsnorm_stream_launch<false>(x, g, y, rs_out, rows, (int)d, eps, st);
+  if (rmsnorm_stream_ok(x, g, y, rows, d)) {
+    RnTab none;
+    memset(&none, 0, sizeof(none));
+    return split ? rmsnorm_stream_launch<true, false>(x, g, y, rs_out, rows, (int)d, eps, st, none)
+                 : rmsnorm_stream_launch<false, false>(x, g, y, rs_out, rows, (int)d, eps, st, none);
+  }
   return split ? rmsnorm_dispatch<bf, bf, bf, true>(x, g, y, rs_out, rows, d, eps, st)
                : rmsnorm_dispatch<bf, bf, bf, false>(x, g, y, rs_out, rows, d, eps, st);
 }
@@ -626,6 +660,16 @@ bool rmsnorm_rope_table_ok(const void* x, const void* g, const void* y, int64_t 
 int launch_rmsnorm_rope_table(const void* x, const void* g, void* y, float* rs, int64_t rows, int64_t d, float eps,
                               float2* tab, int64_t S, int hd, int64_t pos0, const RopeFreq* freq, cudaStream_t st) {
   if (!rmsnorm_rope_table_ok(x, g, y, rows, d, S, hd)) return -1;
+  if (rmsnorm_stream_ok(x, g, y, rows, d)) {   // rows streamed through shared memory, table by a 10th warp
+    RnTab tp;
+    memset(&tp, 0, sizeof(tp));
+    tp.tab = tab;
+    tp.S = S;
+    tp.pos0 = pos0;
+    tp.half = hd / 2;
+    for (int i = 0; i < tp.half; ++i) tp.freq[i] = freq[i];
+    return rmsnorm_stream_launch<true, true>(x, g, y, rs, rows, (int)d, eps, st, tp);
+  }
   const int half = hd / 2;
   const int64_t per_lane = (d / 8 + 31) / 32;
   RopeParams p;
