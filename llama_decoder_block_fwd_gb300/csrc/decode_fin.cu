@@ -34,9 +34,16 @@ __global__ void __launch_bounds__(FN_THREADS) fin_norm_kernel(float* __restrict_
                                                               int B, int d, float eps) {
   __shared__ float red[FN_THREADS / 32];
   pdl_trigger();
-  pdl_wait();
   const int r = blockIdx.x;
   const int nv = d / 4;
+  // the gain is a weight (no kernel writes it): loaded before the dependency wait
+  uint2 gw[FN_MAX_VEC];
+#pragma unroll
+  for (int j = 0; j < FN_MAX_VEC; ++j) {
+    const int i = threadIdx.x + j * FN_THREADS;
+    gw[j] = i < nv ? *reinterpret_cast<const uint2*>(g + 4 * i) : make_uint2(0, 0);
+  }
+  pdl_wait();
   float4 v[FN_MAX_VEC];
 #pragma unroll
   for (int j = 0; j < FN_MAX_VEC; ++j) {
@@ -83,9 +90,8 @@ __global__ void __launch_bounds__(FN_THREADS) fin_norm_kernel(float* __restrict_
   for (int j = 0; j < FN_MAX_VEC; ++j) {
     const int i = threadIdx.x + j * FN_THREADS;
     if (i < nv) {
-      const uint2 gw = *reinterpret_cast<const uint2*>(g + 4 * i);
-      const float y[4] = {v[j].x * __uint_as_float(gw.x << 16), v[j].y * __uint_as_float(gw.x & 0xFFFF0000u),
-                          v[j].z * __uint_as_float(gw.y << 16), v[j].w * __uint_as_float(gw.y & 0xFFFF0000u)};
+      const float y[4] = {v[j].x * __uint_as_float(gw[j].x << 16), v[j].y * __uint_as_float(gw[j].x & 0xFFFF0000u),
+                          v[j].z * __uint_as_float(gw[j].y << 16), v[j].w * __uint_as_float(gw[j].y & 0xFFFF0000u)};
       uint16_t hi[4], lo[4];
 #pragma unroll
       for (int k = 0; k < 4; ++k) split_bf16(y[k], hi[k], lo[k]);
